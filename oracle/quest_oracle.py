@@ -1,0 +1,371 @@
+"""Plain, slow, fp64 CPU oracle for Quest-style query-aware page selection.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import it.
+The product path (``query_aware_sparse_gb300``) never imports, calls or links
+anything here, and nothing here imports the product path: the two share no
+code, headers, tables or helpers.
+
+Sources. "Quest page" is the PaperTrace chapter
+"3.1.1 · Quest：用 min/max 上界筛选 KV 页"; "PageWeaver notes" is the reading
+notes page "PageWeaver: KV-Guided Query Unions for Sparse Attention".
+Each function names the section / equation it restates.
+
+Conventions (all readings are listed in DESIGN.md's "Readings" section):
+
+* Arrays are numpy. Keys/values/queries arrive in their stored dtype (float16
+  or float32). Every floating-point *arithmetic* step runs in float64 on the
+  exact fp64 image of the stored values. Min/max are selections, not
+  arithmetic: the summary keeps the stored dtype and is exact.
+* min/max use the total order of IEEE 754-2019 ``minimum``/``maximum`` on
+  finite values, in which -0 < +0 (the pages are silent on signed zero).
+* Layouts (one layer):
+    k_pool, v_pool  [n_phys, h_kv, page_size, head_dim]
+    summary         [n_phys, h_kv, 2, head_dim]   (index 0 = min m, 1 = max M)
+    page_indptr     [batch + 1]   CSR row pointer into page_indices
+    page_indices    [nnz]         physical page of logical page i of a request
+    seq_lens        [batch]       valid tokens of each request
+    q               [batch, h_kv * group, head_dim]
+* parity unpinned: ``score_pages`` with group > 1 (the group-max rule is a
+  reading of Quest page §2.1; only its group == 1 reduction is pinned).
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+F64 = np.float64
+
+
+# ---------------------------------------------------------------------------
+# Signed-zero-aware min/max (the fold of Quest page §1.2 eq (8) / §3 eq (14))
+# ---------------------------------------------------------------------------
+
+def total_less(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Elementwise a < b in the order where -0 < +0 (finite inputs)."""
+    a = np.asarray(a)
+    b = np.asarray(b)
+    return (a < b) | ((a == b) & np.signbit(a) & ~np.signbit(b))
+
+
+def fold_min(cur: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """m <- min(m, k) of Quest page §1.2 eq (8), in the stored dtype."""
+    return np.where(total_less(k, cur), k, cur).astype(cur.dtype)
+
+
+def fold_max(cur: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """M <- max(M, k) of Quest page §1.2 eq (8), in the stored dtype."""
+    return np.where(total_less(cur, k), k, cur).astype(cur.dtype)
+
+
+def page_summary(keys: np.ndarray):
+    """Per-dimension (m, M) of one page's valid keys, Quest page §1.1 eq (1).
+
+    ``keys`` is [n_valid, head_dim] (n_valid >= 1). The box starts empty
+    (min = +inf, max = -inf, Quest page §1.2) and folds each key in token order.
+    """
+    keys = np.asarray(keys)
+    if keys.shape[0] < 1:
+        raise ValueError("a page summary needs at least one valid key")
+    m = np.full(keys.shape[1:], np.inf, dtype=keys.dtype)
+    M = np.full(keys.shape[1:], -np.inf, dtype=keys.dtype)
+    for r in range(keys.shape[0]):
+        m = fold_min(m, keys[r])
+        M = fold_max(M, keys[r])
+    return m, M
+
+
+# ---------------------------------------------------------------------------
+# a1: cache append + incremental summary (Quest page §1.2 eq (8), §3 eq (14))
+# ---------------------------------------------------------------------------
+
+def append_kv(k_pool, v_pool, summary, page_indptr, page_indices,
+              seq_lens_before, append_indptr, k_new, v_new):
+    """Write new tokens into their pages and update the page summaries, in place.
+
+    Token i of request r (append_indptr[r] <= i < append_indptr[r+1]) lands at
+    position pos = seq_lens_before[r] + (i - append_indptr[r]), logical page
+    pos // S, slot pos % S, physical page page_indices[page_indptr[r] + pos//S].
+    Writing slot 0 opens the page: its summary restarts from the empty box
+    (+inf min, -inf max), which is the same as m = M = k on the first write
+    (Quest page §3) and makes a reused physical slot start fresh (Quest page
+    §3, page recycling). Every other write folds the key in with eq (8).
+    Slots that are never written are never read.
+    """
+    S = k_pool.shape[2]
+    batch = len(seq_lens_before)
+    for r in range(batch):
+        for i in range(int(append_indptr[r]), int(append_indptr[r + 1])):
+            pos = int(seq_lens_before[r]) + (i - int(append_indptr[r]))
+            lp, slot = divmod(pos, S)
+            if lp >= int(page_indptr[r + 1]) - int(page_indptr[r]):
+                raise IndexError("append beyond the request's page table")
+            pp = int(page_indices[int(page_indptr[r]) + lp])
+            k_pool[pp, :, slot, :] = k_new[i]
+            v_pool[pp, :, slot, :] = v_new[i]
+            if slot == 0:
+                summary[pp, :, 0, :] = np.inf
+                summary[pp, :, 1, :] = -np.inf
+            summary[pp, :, 0, :] = fold_min(summary[pp, :, 0, :], k_new[i])
+            summary[pp, :, 1, :] = fold_max(summary[pp, :, 1, :], k_new[i])
+
+
+def build_summary(k_pool, page_indptr, page_indices, seq_lens, summary=None,
+                  requests=None):
+    """Summaries of every page of the listed requests from the pool's valid keys.
+
+    Eq (1) of Quest page §1.1 over each page's valid tokens only (the tail page
+    holds min(S, L - p*S) of them, Quest page §1.2). Vectorised over pages and
+    heads; the fold over slots is the same eq (8) fold as ``append_kv``.
+    """
+    n_phys, h_kv, S, d = k_pool.shape
+    if summary is None:
+        summary = np.zeros((n_phys, h_kv, 2, d), dtype=k_pool.dtype)
+    reqs = range(len(seq_lens)) if requests is None else requests
+    for r in reqs:
+        lo, hi = int(page_indptr[r]), int(page_indptr[r + 1])
+        L = int(seq_lens[r])
+        n_pages = -(-L // S)
+        if n_pages > hi - lo:
+            raise ValueError("seq_len exceeds the request's page table")
+        if n_pages == 0:
+            continue
+        phys = np.asarray(page_indices[lo:lo + n_pages], dtype=np.int64)
+        valid = np.minimum(S, L - np.arange(n_pages) * S)          # [n_pages]
+        m = np.full((n_pages, h_kv, d), np.inf, dtype=k_pool.dtype)
+        M = np.full((n_pages, h_kv, d), -np.inf, dtype=k_pool.dtype)
+        for slot in range(S):
+            live = valid > slot
+            if not live.any():
+                break
+            k = k_pool[phys[live], :, slot, :]
+            m[live] = fold_min(m[live], k)
+            M[live] = fold_max(M[live], k)
+        summary[phys, :, 0, :] = m
+        summary[phys, :, 1, :] = M
+    return summary
+
+
+# ---------------------------------------------------------------------------
+# a2: page upper bound U_p(q) (Quest page §1.1 eq (2)-(3)); GQA group max (§2.1)
+# ---------------------------------------------------------------------------
+
+def page_bound(q, m, M):
+    """U_p(q) = sum_j max(q_j m_j, q_j M_j) in fp64 (Quest page §1.1 eq (2)-(3)).
+
+    q is [d]; m, M are [..., d]. Returns [...].
+    """
+    q = np.asarray(q, dtype=F64)
+    m = np.asarray(m, dtype=F64)
+    M = np.asarray(M, dtype=F64)
+    return np.maximum(q * m, q * M).sum(axis=-1)
+
+
+def score_pages(q, summary, page_indptr, page_indices, group, requests=None,
+                heads=None):
+    """Scores [h_kv, nnz] (fp64) for every page of every request.
+
+    For KV head g the score of a page is U of that page under each query head
+    h in g*group .. g*group+group-1; with group > 1 the group shares one page
+    set and its score is max_h U_{h,p} (Quest page §2.1, the "group max" of
+    the GQA discussion: a reading, see module docstring). Pages outside the
+    listed requests / heads are left NaN.
+    """
+    n_phys, h_kv, _, d = summary.shape
+    batch = len(page_indptr) - 1
+    nnz = int(page_indptr[batch])
+    scores = np.full((h_kv, nnz), np.nan, dtype=F64)
+    reqs = range(batch) if requests is None else requests
+    hs = range(h_kv) if heads is None else heads
+    for r in reqs:
+        lo, hi = int(page_indptr[r]), int(page_indptr[r + 1])
+        if hi == lo:
+            continue
+        phys = np.asarray(page_indices[lo:hi], dtype=np.int64)
+        for g in hs:
+            m = summary[phys, g, 0, :]
+            M = summary[phys, g, 1, :]
+            best = np.full(hi - lo, -np.inf)
+            for h in range(g * group, (g + 1) * group):
+                best = np.maximum(best, page_bound(q[r, h], m, M))
+            scores[g, lo:hi] = best
+    return scores
+
+
+# ---------------------------------------------------------------------------
+# a3: fixed-budget Top-K pages (Quest page Fig. 1, §1.1 four-page example)
+# ---------------------------------------------------------------------------
+
+def topk_pages(U, k):
+    """Logical indices of the K largest scores, ties to the lower index.
+
+    Sort by (score descending, index ascending) and keep the first min(K, P);
+    the chosen indices are returned in ascending order. -0 and +0 compare
+    equal, so the index decides between them.
+    """
+    U = np.asarray(U, dtype=F64)
+    P = U.shape[0]
+    order = np.lexsort((np.arange(P), -U))
+    return np.sort(order[:min(k, P)])
+
+
+def select_topk(scores, page_indptr, page_indices, k, requests=None):
+    """Per (request, KV head): Top-K logical pages, their physical pages, count.
+
+    Returns sel_logical, sel_phys [batch, h_kv, k] (int32, -1 padded) and
+    sel_count [batch, h_kv] = min(k, P_r).
+    """
+    h_kv = scores.shape[0]
+    batch = len(page_indptr) - 1
+    sel_logical = np.full((batch, h_kv, k), -1, dtype=np.int32)
+    sel_phys = np.full((batch, h_kv, k), -1, dtype=np.int32)
+    sel_count = np.zeros((batch, h_kv), dtype=np.int32)
+    reqs = range(batch) if requests is None else requests
+    for r in reqs:
+        lo, hi = int(page_indptr[r]), int(page_indptr[r + 1])
+        for g in range(h_kv):
+            chosen = topk_pages(scores[g, lo:hi], k)
+            n = len(chosen)
+            sel_logical[r, g, :n] = chosen
+            sel_phys[r, g, :n] = np.asarray(page_indices, dtype=np.int64)[lo + chosen]
+            sel_count[r, g] = n
+    return sel_logical, sel_phys, sel_count
+
+
+# ---------------------------------------------------------------------------
+# a4/a5: attention over a candidate page set (Quest page Fig. 1, eq (6);
+#        PageWeaver notes §2 eq (1)-(2) for the exact token set and 1/sqrt(d))
+# ---------------------------------------------------------------------------
+
+def softmax_attention(q, keys, values, sm_scale):
+    """o = sum_t softmax(q.k_t * scale) v_t and lse over the given rows (fp64).
+
+    An empty key set gives o = 0 and lse = -inf (PageWeaver notes §2).
+    """
+    q = np.asarray(q, dtype=F64)
+    keys = np.asarray(keys, dtype=F64)
+    values = np.asarray(values, dtype=F64)
+    if keys.shape[0] == 0:
+        return np.zeros(values.shape[-1]), -np.inf
+    s = (keys @ q) * sm_scale
+    mx = s.max()
+    p = np.exp(s - mx)
+    z = p.sum()
+    return (p @ values) / z, mx + math.log(z)
+
+
+def candidate_tokens(k_pool, v_pool, page_indptr, page_indices, seq_lens, r, g,
+                     logical_pages):
+    """Keys/values of the valid tokens of the given logical pages of request r.
+
+    The list is a set: -1 entries are skipped and repeats add nothing
+    (PageWeaver notes §2). The tail page contributes only its valid tokens
+    (Quest page §1.2, last_page_len).
+    """
+    S = k_pool.shape[2]
+    L = int(seq_lens[r])
+    lo = int(page_indptr[r])
+    lps = sorted({int(x) for x in logical_pages if int(x) >= 0})
+    ks, vs = [], []
+    for lp in lps:
+        valid = min(S, L - lp * S)
+        if valid <= 0:
+            raise IndexError("selected page holds no valid token")
+        pp = int(page_indices[lo + lp])
+        ks.append(k_pool[pp, g, :valid, :])
+        vs.append(v_pool[pp, g, :valid, :])
+    d = k_pool.shape[3]
+    if not ks:
+        return np.zeros((0, d)), np.zeros((0, d))
+    return np.concatenate(ks).astype(F64), np.concatenate(vs).astype(F64)
+
+
+def sparse_attention(q, k_pool, v_pool, page_indptr, page_indices, seq_lens,
+                     sel_logical, group, sm_scale=None, requests=None):
+    """o [batch, h_q, d] and lse [batch, h_q] over each head's candidate set.
+
+    Query head h uses the set chosen for its KV head h // group; the softmax
+    denominator covers only the valid candidate tokens, so the result is the
+    renormalised approximation of eq (6) (Quest page Fig. 1, §1.1).
+    Rows of requests not listed are NaN.
+    """
+    batch, h_q, d = q.shape
+    h_kv = k_pool.shape[1]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    o = np.full((batch, h_q, d), np.nan)
+    lse = np.full((batch, h_q), np.nan)
+    reqs = range(batch) if requests is None else requests
+    for r in reqs:
+        for g in range(h_kv):
+            keys, vals = candidate_tokens(k_pool, v_pool, page_indptr,
+                                          page_indices, seq_lens, r, g,
+                                          sel_logical[r, g])
+            for h in range(g * group, (g + 1) * group):
+                o[r, h], lse[r, h] = softmax_attention(q[r, h], keys, vals,
+                                                       sm_scale)
+    return o, lse
+
+
+def dense_attention(q, keys, values, sm_scale=None):
+    """Plain attention of one query over contiguous, un-paged K/V (fp64)."""
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(np.asarray(q).shape[-1])
+    return softmax_attention(q, keys, values, sm_scale)
+
+
+def combine_partials(partials):
+    """Merge (o_c, lse_c) pieces of one row by log-sum-exp (Quest page §2.1).
+
+    Each piece is the attention over a disjoint token subset; the merge uses
+    the row's global maximum, never a per-piece softmax average.
+    """
+    live = [(o, l) for o, l in partials if l != -np.inf]
+    if not live:
+        d = len(partials[0][0]) if partials else 0
+        return np.zeros(d), -np.inf
+    mx = max(l for _, l in live)
+    w = np.array([math.exp(l - mx) for _, l in live])
+    o = sum(wi * np.asarray(oi, dtype=F64) for wi, (oi, _) in zip(w, live))
+    return o / w.sum(), mx + math.log(w.sum())
+
+
+# ---------------------------------------------------------------------------
+# Diagnostics (Quest page §1.1 eq (6)-(7), §3.1 page slack)
+# ---------------------------------------------------------------------------
+
+def excluded_mass(q, keys, mask, sm_scale):
+    """epsilon = dense softmax mass of the tokens outside the candidate set."""
+    s = (np.asarray(keys, dtype=F64) @ np.asarray(q, dtype=F64)) * sm_scale
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    return float(p[~np.asarray(mask, dtype=bool)].sum())
+
+
+def value_norm_max(values):
+    """V_max = max_t ||v_t||_2 (Quest page §1.1, eq (7))."""
+    return float(np.linalg.norm(np.asarray(values, dtype=F64), axis=-1).max())
+
+
+def page_slack(q, keys):
+    """g_p(q) = U_p(q) - max_r q.k_r >= 0 for one page (Quest page §3.1)."""
+    keys = np.asarray(keys)
+    m, M = page_summary(keys)
+    return float(page_bound(q, m, M) - (keys.astype(F64) @ np.asarray(q, F64)).max())
+
+
+# ---------------------------------------------------------------------------
+# Byte model (Quest page §2 eq (9)-(12))
+# ---------------------------------------------------------------------------
+
+def traffic_ratio(L, S, K):
+    """rho = (T_index + T_selected) / T_dense = 1/S + K S / L (eq (12))."""
+    return 1.0 / S + K * S / L
+
+
+def traffic_bytes(vec_bytes, L, S, K):
+    """(T_dense, T_index, T_selected) in bytes, eq (9)-(11); M = vec_bytes."""
+    P = L / S
+    return 2 * vec_bytes * L, 2 * vec_bytes * P, 2 * vec_bytes * K * S

@@ -1,0 +1,440 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Nothing here needs a GPU. Each test checks the oracle against a value the
+pages print, a closed form, a library routine or brute force, chosen so that
+a plausible slip (dropped term, wrong sign, transposed operand, wrong tie
+rule, padding leaking into a page) fails at least one of them.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import quest_oracle as qo
+
+
+def _np(x, dt=np.float64):
+    return np.asarray(x, dtype=dt)
+
+
+# --------------------------------------------------------------------------
+# Worked examples printed on the Quest page
+# --------------------------------------------------------------------------
+
+def test_worked_example_2d(golden):
+    ex = golden("worked_example_2d.json")
+    for dt in (np.float16, np.float32):
+        keys = _np(ex["page"]["keys"], dt)
+        m, M = qo.page_summary(keys)
+        assert m.tolist() == ex["page"]["m"]
+        assert M.tolist() == ex["page"]["M"]
+        q = _np(ex["q"])
+        assert qo.page_bound(q, m, M) == ex["U"]
+        assert (keys.astype(np.float64) @ q).tolist() == ex["dots"]
+        # eq (5): the bound equals the page's true maximum here
+        assert max(ex["dots"]) == ex["U"]
+
+
+def test_worked_example_swapped_keys(golden):
+    sw = golden("worked_example_2d.json")["swapped"]
+    keys = _np(sw["keys"], np.float32)
+    m, M = qo.page_summary(keys)
+    assert m.tolist() == sw["m"] and M.tolist() == sw["M"]
+    q = _np(golden("worked_example_2d.json")["q"])
+    assert qo.page_bound(q, m, M) == sw["U"]
+    assert (keys.astype(np.float64) @ q).tolist() == sw["dots"]
+    assert qo.page_slack(q, keys) == sw["slack"]
+
+
+def _fig2_state(ex, with_append):
+    S = ex["page_size"]
+    A = _np(ex["A_keys"], np.float32)
+    B = _np(ex["B_keys_before"], np.float32)
+    toks = np.concatenate([A, B])[:, None, :]             # [5, h_kv=1, d=2]
+    pool_shape = (2, 1, S, 2)
+    k_pool = np.full(pool_shape, np.nan, np.float32)
+    v_pool = np.full(pool_shape, np.nan, np.float32)
+    summ = np.full((2, 1, 2, 2), np.nan, np.float32)
+    # two requests' worth of pages is not needed: one request, pages A then B
+    indptr = np.array([0, 2], np.int32)
+    indices = np.array([0, 1], np.int32)
+    qo.append_kv(k_pool, v_pool, summ, indptr, indices, np.array([0]),
+                 np.array([0, 5]), toks, toks)
+    if with_append:
+        new = _np([ex["appended_key"]], np.float32)[:, None, :]
+        qo.append_kv(k_pool, v_pool, summ, indptr, indices, np.array([5]),
+                     np.array([0, 1]), new, new)
+    return k_pool, summ, indptr, indices
+
+
+def test_fig2_two_step(golden):
+    ex = golden("fig2_two_step.json")
+    pr = ex["printed"]
+    _, summ, indptr, indices = _fig2_state(ex, with_append=False)
+    q_t = _np(ex["q_t"], np.float32)[None, None, :]
+    sc = qo.score_pages(q_t, summ, indptr, indices, group=1)
+    assert sc[0].tolist() == [pr["U_A_qt"], pr["U_B_qt"]]
+    sel, _, cnt = qo.select_topk(sc, indptr, indices, k=1)
+    assert sel[0, 0, 0] == 0 and cnt[0, 0] == 1            # A
+    q_t1 = _np(ex["q_t1"], np.float32)[None, None, :]
+    assert qo.score_pages(q_t1, summ, indptr, indices, 1)[0, 1] == \
+        pr["U_B_qt1_without_append"]
+
+    _, summ, indptr, indices = _fig2_state(ex, with_append=True)
+    assert summ[1, 0, 0].tolist() == pr["m_B_after"]
+    assert summ[1, 0, 1].tolist() == pr["M_B_after"]
+    sc = qo.score_pages(q_t1, summ, indptr, indices, group=1)
+    assert sc[0].tolist() == [pr["U_A_qt1"], pr["U_B_qt1"]]
+    sel, _, _ = qo.select_topk(sc, indptr, indices, k=1)
+    assert sel[0, 0, 0] == 1                                # B
+
+
+def test_four_page_selection(golden):
+    ex = golden("four_page_selection.json")
+    names = ex["pages"]
+    for k, want in ex["selected"].items():
+        got = qo.topk_pages(ex["U"], int(k))
+        assert sorted(names[i] for i in got) == sorted(want)
+    # eq (4) holds on every page of the example
+    assert all(t <= u for t, u in zip(ex["true_max"], ex["U"]))
+
+
+def test_byte_model(golden):
+    ex = golden("byte_model.json")
+    assert ex["budget_tokens"] // ex["S"] == ex["K"]
+    assert qo.traffic_ratio(ex["L"], ex["S"], ex["K"]) == ex["rho"]
+    dense, index, sel = qo.traffic_bytes(ex["vec_bytes"], ex["L"], ex["S"], ex["K"])
+    mib = 1 << 20
+    assert dense == ex["dense_MiB_per_layer_head"] * mib
+    assert index == ex["index_MiB"] * mib
+    assert sel == ex["selected_MiB"] * mib
+    assert (index + sel) / dense == ex["rho"]
+
+
+# --------------------------------------------------------------------------
+# Summary: brute force, signed zero, tail lengths, slot reuse
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt", [np.float16, np.float32])
+def test_summary_brute_force(dt):
+    rng = np.random.default_rng(1)
+    for n in (1, 2, 7, 16, 32):
+        keys = rng.standard_normal((n, 64)).astype(dt)
+        keys[keys == 0] = 1                                 # no signed-zero ambiguity
+        m, M = qo.page_summary(keys)
+        assert np.array_equal(m, keys.min(axis=0))
+        assert np.array_equal(M, keys.max(axis=0))
+        assert m.dtype == dt and M.dtype == dt
+
+
+def test_summary_signed_zero_order():
+    keys = np.array([[0.0, -0.0, -0.0], [-0.0, 0.0, -0.0]], np.float16)
+    m, M = qo.page_summary(keys)
+    assert np.signbit(m).tolist() == [True, True, True]
+    assert np.signbit(M).tolist() == [False, False, True]
+
+
+def _prefill(L, S, d=16, h=2, dt=np.float32, seed=0, poison=True):
+    rng = np.random.default_rng(seed)
+    P = -(-L // S)
+    toks_k = rng.standard_normal((L, h, d)).astype(dt)
+    toks_v = rng.standard_normal((L, h, d)).astype(dt)
+    fill = np.nan if poison else 0
+    k_pool = np.full((P + 2, h, S, d), fill, dt)
+    v_pool = np.full((P + 2, h, S, d), fill, dt)
+    summ = np.full((P + 2, h, 2, d), fill, dt)
+    perm = rng.permutation(P + 2)[:P].astype(np.int32)
+    indptr = np.array([0, P], np.int32)
+    return toks_k, toks_v, k_pool, v_pool, summ, indptr, perm
+
+
+@pytest.mark.parametrize("L", [1, 15, 16, 17, 33])
+def test_append_tail_lengths(L):
+    S = 16
+    tk, tv, kp, vp, sm, indptr, perm = _prefill(L, S)
+    qo.append_kv(kp, vp, sm, indptr, perm, np.array([0]), np.array([0, L]), tk, tv)
+    P = -(-L // S)
+    for p in range(P):
+        valid = min(S, L - p * S)
+        rows = tk[p * S:p * S + valid]                      # [valid, h, d]
+        pp = perm[p]
+        assert np.array_equal(sm[pp, :, 0], rows.min(axis=0))
+        assert np.array_equal(sm[pp, :, 1], rows.max(axis=0))
+        assert np.all(np.isfinite(sm[pp]))                  # poison never read
+        assert np.array_equal(kp[pp, :, :valid], rows.transpose(1, 0, 2))
+    # one token at a time (decode) reaches the same state as one prefill call
+    tk2, tv2, kp2, vp2, sm2, _, _ = _prefill(L, S)
+    for t in range(L):
+        qo.append_kv(kp2, vp2, sm2, indptr, perm, np.array([t]), np.array([0, 1]),
+                     tk[t:t + 1], tv[t:t + 1])
+    for p in range(P):
+        assert np.array_equal(sm2[perm[p]], sm[perm[p]])
+    # build_summary over the pool is eq (1) over the same valid keys
+    sm3 = qo.build_summary(kp, indptr, perm, np.array([L]))
+    for p in range(P):
+        assert np.array_equal(sm3[perm[p]], sm[perm[p]])
+
+
+def test_slot_reuse_matches_fresh_page():
+    """Allocate, fill, free, reallocate one physical slot (Quest page §3)."""
+    S, d, h = 16, 8, 1
+    rng = np.random.default_rng(3)
+    old = (rng.standard_normal((S, h, d)) * 10).astype(np.float32)
+    new = rng.standard_normal((5, h, d)).astype(np.float32)
+    kp = np.zeros((1, h, S, d), np.float32)
+    vp = np.zeros_like(kp)
+    sm = np.zeros((1, h, 2, d), np.float32)
+    ind = np.array([0, 1], np.int32)
+    pages = np.array([0], np.int32)
+    qo.append_kv(kp, vp, sm, ind, pages, np.array([0]), np.array([0, S]), old, old)
+    qo.append_kv(kp, vp, sm, ind, pages, np.array([0]), np.array([0, 5]), new, new)
+    fresh_k = np.zeros_like(kp)
+    fresh_s = np.zeros_like(sm)
+    qo.append_kv(fresh_k, np.zeros_like(kp), fresh_s, ind, pages, np.array([0]),
+                 np.array([0, 5]), new, new)
+    assert np.array_equal(sm, fresh_s)
+
+
+# --------------------------------------------------------------------------
+# Score: eq (4) invariant, closed forms, GQA reduction
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt", [np.float16, np.float32])
+def test_bound_invariant_and_closed_forms(dt):
+    rng = np.random.default_rng(7)
+    for trial in range(200):
+        d = int(rng.choice([2, 8, 64, 128]))
+        n = int(rng.integers(1, 33))
+        keys = (rng.standard_normal((n, d)) * rng.uniform(0.1, 8)).astype(dt)
+        q = rng.standard_normal(d).astype(dt).astype(np.float64)
+        m, M = qo.page_summary(keys)
+        U = qo.page_bound(q, m, M)
+        dots = keys.astype(np.float64) @ q
+        tol = 1e-12 * (np.abs(q) @ np.maximum(np.abs(m), np.abs(M)).astype(np.float64))
+        assert dots.max() <= U + tol                         # eq (4)
+        # a one-key page is a point: the bound is that key's dot product
+        U1 = qo.page_bound(q, *qo.page_summary(keys[:1]))
+        assert abs(U1 - dots[0]) <= tol
+        # q >= 0 picks M, q <= 0 picks m (text after eq (2))
+        qp = np.abs(q)
+        assert abs(qo.page_bound(qp, m, M) - qp @ M.astype(np.float64)) <= tol
+        assert abs(qo.page_bound(-qp, m, M) - (-qp) @ m.astype(np.float64)) <= tol
+
+
+def test_score_pages_group_reduction():
+    rng = np.random.default_rng(11)
+    h_kv, G, d, S = 2, 4, 16, 4
+    summ = rng.standard_normal((6, h_kv, 2, d)).astype(np.float32)
+    summ[:, :, 0], summ[:, :, 1] = (np.minimum(summ[:, :, 0], summ[:, :, 1]),
+                                    np.maximum(summ[:, :, 0], summ[:, :, 1]))
+    indptr = np.array([0, 2, 5], np.int32)
+    indices = np.array([5, 0, 3, 1, 4], np.int32)
+    q = rng.standard_normal((2, h_kv * G, d)).astype(np.float32)
+    sc = qo.score_pages(q, summ, indptr, indices, group=G)
+    # group == 1 per query head, then the group max, equals the grouped call
+    per = [qo.score_pages(q[:, h:h + 1], summ[:, h // G:h // G + 1], indptr,
+                          indices, 1)[0] for h in range(h_kv * G)]
+    for g in range(h_kv):
+        assert np.array_equal(sc[g], np.max(per[g * G:(g + 1) * G], axis=0))
+    # direct eq (2)-(3) with explicit loops for one entry
+    r, i, g = 1, 3, 1
+    pp = indices[i]
+    want = -np.inf
+    for h in range(g * G, (g + 1) * G):
+        tot = 0.0
+        for j in range(d):
+            a = float(q[r, h, j]) * float(summ[pp, g, 0, j])
+            b = float(q[r, h, j]) * float(summ[pp, g, 1, j])
+            tot += max(a, b)
+        want = max(want, tot)
+    assert abs(sc[g, i] - want) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Selection: brute-force rank characterisation, ties, K >= P
+# --------------------------------------------------------------------------
+
+def _rank_select(U, k):
+    """Page i is chosen iff fewer than k pages beat it; a page beats i when its
+    score is larger, or equal with a smaller index."""
+    P = len(U)
+    out = []
+    for i in range(P):
+        beats = sum(1 for j in range(P) if U[j] > U[i] or (U[j] == U[i] and j < i))
+        if beats < k:
+            out.append(i)
+    return out
+
+
+def test_select_brute_force_with_ties():
+    rng = np.random.default_rng(5)
+    for trial in range(400):
+        P = int(rng.integers(1, 65))
+        k = int(rng.integers(1, 70))
+        if trial % 3 == 0:
+            U = rng.integers(-3, 4, P).astype(np.float64)   # many ties
+            U[U == 0] = rng.choice([0.0, -0.0], int((U == 0).sum()))
+        else:
+            U = rng.standard_normal(P)
+        got = qo.topk_pages(U, k).tolist()
+        assert got == _rank_select(U.tolist(), k)
+        assert len(got) == min(k, P) and len(set(got)) == len(got)
+
+
+def test_select_outputs_and_padding():
+    U = np.array([[3.0, 1.0, 2.0, 2.0, -1.0]])
+    indptr = np.array([0, 2, 5], np.int32)
+    indices = np.array([9, 4, 7, 1, 0], np.int32)
+    sl, sp, sc = qo.select_topk(U, indptr, indices, k=3)
+    assert sl[0, 0].tolist() == [0, 1, -1] and sc[0, 0] == 2
+    assert sp[0, 0].tolist() == [9, 4, -1]
+    assert sl[1, 0].tolist() == [0, 1, 2] and sc[1, 0] == 3
+    assert sp[1, 0].tolist() == [7, 1, 0]
+
+
+# --------------------------------------------------------------------------
+# Attention: library routine, K = P, eq (7), set semantics
+# --------------------------------------------------------------------------
+
+def test_dense_attention_matches_torch_sdpa():
+    rng = np.random.default_rng(2)
+    for L, d in ((1, 8), (37, 64), (300, 128)):
+        q = rng.standard_normal(d)
+        K = rng.standard_normal((L, d)) * 2
+        V = rng.standard_normal((L, d))
+        o, lse = qo.dense_attention(q, K, V)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.tensor(q)[None, None, None], torch.tensor(K)[None, None],
+            torch.tensor(V)[None, None])[0, 0, 0].numpy()
+        assert np.allclose(o, ref, rtol=1e-12, atol=1e-13)
+        s = K @ q / math.sqrt(d)
+        assert abs(lse - np.log(np.exp(s).sum())) < 1e-10
+
+
+def _paged_case(seed, lens, S=16, d=32, h_kv=2, G=1, dt=np.float16):
+    rng = np.random.default_rng(seed)
+    counts = [-(-L // S) for L in lens]
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    nnz = int(indptr[-1])
+    perm = rng.permutation(nnz + 3)[:nnz].astype(np.int32)
+    kp = np.full((nnz + 3, h_kv, S, d), np.nan, dt)
+    vp = np.full_like(kp, np.nan)
+    toks = []
+    for r, L in enumerate(lens):
+        k = rng.standard_normal((L, h_kv, d)).astype(dt)
+        v = rng.standard_normal((L, h_kv, d)).astype(dt)
+        for t in range(L):
+            pp = perm[indptr[r] + t // S]
+            kp[pp, :, t % S] = k[t]
+            vp[pp, :, t % S] = v[t]
+        toks.append((k, v))
+    q = rng.standard_normal((len(lens), h_kv * G, d)).astype(dt)
+    return kp, vp, indptr, perm, np.array(lens, np.int32), q, toks
+
+
+def test_all_pages_equals_dense():
+    lens = [1, 15, 16, 17, 100]
+    kp, vp, indptr, perm, sl, q, toks = _paged_case(4, lens, G=2)
+    G, h_kv = 2, 2
+    sel = np.full((len(lens), h_kv, 8), -1, np.int32)
+    for r, L in enumerate(lens):
+        P = -(-L // 16)
+        sel[r, :, :P] = np.arange(P)[::-1]                  # any order
+    o, lse = qo.sparse_attention(q, kp, vp, indptr, perm, sl, sel, G)
+    for r, (k, v) in enumerate(toks):
+        for h in range(h_kv * G):
+            od, ld = qo.dense_attention(q[r, h], k[:, h // G].astype(np.float64),
+                                        v[:, h // G].astype(np.float64))
+            assert np.allclose(o[r, h], od, rtol=1e-12, atol=1e-12)
+            assert abs(lse[r, h] - ld) < 1e-10
+
+
+def test_eq7_bound_and_set_semantics():
+    rng = np.random.default_rng(9)
+    lens = [200]
+    kp, vp, indptr, perm, sl, q, toks = _paged_case(6, lens, d=64, h_kv=1)
+    k, v = toks[0]
+    P = 13
+    for trial in range(30):
+        chosen = np.sort(rng.choice(P, size=int(rng.integers(1, P)), replace=False))
+        sel = np.full((1, 1, P), -1, np.int32)
+        sel[0, 0, :len(chosen)] = rng.permutation(chosen)
+        oc, _ = qo.sparse_attention(q, kp, vp, indptr, perm, sl, sel, 1)
+        od, _ = qo.dense_attention(q[0, 0], k[:, 0], v[:, 0])
+        mask = np.zeros(200, bool)
+        for p in chosen:
+            mask[p * 16:min(200, p * 16 + 16)] = True
+        eps = qo.excluded_mass(q[0, 0], k[:, 0], mask, 1 / 8)
+        vmax = qo.value_norm_max(v[:, 0])
+        assert np.linalg.norm(od - oc[0, 0]) <= 2 * eps * vmax + 1e-9   # eq (7)
+        # duplicates and -1 entries change nothing (set semantics)
+        dup = np.concatenate([sel[0, 0], chosen[:1], [-1]])[None, None]
+        od2, _ = qo.sparse_attention(q, kp, vp, indptr, perm, sl, dup, 1)
+        assert np.array_equal(od2, oc)
+
+
+def test_single_token_page_and_empty_set():
+    kp, vp, indptr, perm, sl, q, toks = _paged_case(8, [17], d=16, h_kv=1)
+    sel = np.array([[[1, -1]]], np.int32)                    # the 1-token tail page
+    o, lse = qo.sparse_attention(q, kp, vp, indptr, perm, sl, sel, 1)
+    assert np.array_equal(o[0, 0], toks[0][1][16, 0].astype(np.float64))
+    sel = np.array([[[-1, -1]]], np.int32)
+    o, lse = qo.sparse_attention(q, kp, vp, indptr, perm, sl, sel, 1)
+    assert np.all(o == 0) and lse[0, 0] == -np.inf
+
+
+def test_physical_shuffle_invariance():
+    lens = [77]
+    a = _paged_case(12, lens, d=16, h_kv=1)
+    kp, vp, indptr, perm, sl, q, toks = a
+    sel = np.array([[[0, 2, 4]]], np.int32)
+    o1, _ = qo.sparse_attention(q, kp, vp, indptr, perm, sl, sel, 1)
+    # move every page to a new physical slot
+    newperm = perm[::-1].copy()
+    kp2 = np.full_like(kp, np.nan)
+    vp2 = np.full_like(vp, np.nan)
+    kp2[newperm] = kp[perm]
+    vp2[newperm] = vp[perm]
+    o2, _ = qo.sparse_attention(q, kp2, vp2, indptr, newperm, sl, sel, 1)
+    assert np.array_equal(o1, o2)
+
+
+def test_combine_partials_is_global_softmax():
+    rng = np.random.default_rng(13)
+    q = rng.standard_normal(8)
+    K = rng.standard_normal((40, 8)) * 3
+    V = rng.standard_normal((40, 8))
+    o, l = qo.dense_attention(q, K, V)
+    cuts = [0, 5, 6, 23, 40]
+    parts = [qo.dense_attention(q, K[a:b], V[a:b]) for a, b in zip(cuts, cuts[1:])]
+    parts.append((np.zeros(8), -np.inf))                     # an empty piece
+    oc, lc = qo.combine_partials(parts)
+    assert np.allclose(oc, o, rtol=1e-12, atol=1e-13) and abs(lc - l) < 1e-12
+    # a per-piece softmax then plain average is a different (wrong) answer
+    avg = np.mean([p[0] for p in parts[:-1]], axis=0)
+    assert np.abs(avg - o).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
+# Planted mistakes: each plausible slip breaks at least one pin above
+# --------------------------------------------------------------------------
+
+def test_planted_mistakes_are_caught(golden, monkeypatch):
+    ex = golden("worked_example_2d.json")
+    keys = _np(ex["page"]["keys"], np.float32)
+    q = _np(ex["q"])
+    m, M = qo.page_summary(keys)
+    slips = {
+        "drop the max: q.M only": lambda q, m, M: float(np.dot(q, M)),
+        "wrong sign on m": lambda q, m, M: float(np.maximum(-q * m, q * M).sum()),
+        "min instead of max": lambda q, m, M: float(np.minimum(q * m, q * M).sum()),
+        "swapped m/M per dim": lambda q, m, M: float(np.maximum(q * M[::-1], q * m[::-1]).sum()),
+    }
+    for name, f in slips.items():
+        assert f(q, m, M) != ex["U"], name
+    # a tie rule that prefers the higher index breaks the brute-force pin
+    U = [1.0, 1.0, 0.5]
+    wrong = sorted(np.lexsort((-np.arange(3), -np.asarray(U)))[:1].tolist())
+    assert wrong != _rank_select(U, 1)
