@@ -1,0 +1,528 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the Quest hot path on one GB300.
+
+One step = one decode step of one attention layer for the Llama-2-7B-shaped
+workload (1 request, 32 heads, d_h 128, 32768-token context, page size 16,
+token budget 2048 -> K = 128 pages, fp16): append the new token's K/V (and
+its page summary), score all 2048 pages, select the top 128 per head, attend
+over the selected pages (split-K + combine). Steps run as CUDA-graph replays.
+
+Output: one JSON line (rank 0). `value` is the device-timed latency per layer
+(µs, lower is better) with inputs resident in HBM; `e2e` is the same step
+with the per-step inputs (q, new k/v) copied from pinned host memory and the
+output read back, host wall clock per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")          # the CPU oracle runs on one core
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "sparse decode-attn latency (µs/layer) & achieved HBM GB/s vs roofline"
+UNIT = "us/layer"
+MIB = 1 << 20
+
+
+# ---------------------------------------------------------------------------
+# Byte accounting (Quest page §2 eq (9)-(12)): algorithmic bytes of one step
+# ---------------------------------------------------------------------------
+
+def step_bytes(n_pages, h_kv, group, d, S, k_sel_pages, valid_tokens_selected, esize,
+               append_tokens=1):
+    """Algorithmic bytes of one decode step of one layer.
+
+    summary of every scored page (index term, eq (10)) + K/V of the valid
+    tokens of the selected pages (eq (11)) + q read + o written (fp32) + the
+    append (new k/v read, written to the pool, tail-page summary read+write).
+    Scores, ids and split-K partials are intermediates and not counted.
+    """
+    summary = n_pages * h_kv * 2 * d * esize
+    kv = valid_tokens_selected * h_kv * 2 * d * esize
+    q = h_kv * group * d * esize
+    o = h_kv * group * d * 4
+    append = append_tokens * h_kv * d * esize * 2 * 2 + h_kv * 2 * d * esize * 2
+    return dict(summary=summary, kv=kv, q=q, o=o, append=append,
+                total=summary + kv + q + o + append)
+
+
+def paper_traffic_ratio(L, S, budget_tokens):
+    """rho = 1/S + K/P (eq (12)) for a token budget B = K*S."""
+    K = budget_tokens // S
+    return 1.0 / S + K / (L / S)
+
+
+# ---------------------------------------------------------------------------
+# Helpers
+# ---------------------------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v
+                          and "Not" not in v})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].strip() not in ("", "[N/A]"))}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# Workload set-up on the device
+# ---------------------------------------------------------------------------
+
+class LayerSetup:
+    """The Llama-2-7B-shaped layer: pool built by the library's own append
+    (prefill of the first L-1 tokens), plus the decode token and query."""
+
+    def __init__(self, w: wl.Workload, nbuf: int, dev, sample_heads=4):
+        import query_aware_sparse_gb300 as qs
+        self.qs = qs
+        self.w = w
+        L = int(w.lengths()[0])
+        self.L = L
+        S, h, d = w.page_size, w.h_kv, w.head_dim
+        self.table_np = wl.make_page_table([L], S, seed=w.seed)
+        k_tok, v_tok = wl.request_tokens(w, 0, L, device=dev)
+        self.q = wl.queries(w, [L - 1], device=dev)
+        # host copies of a few heads of the generated inputs, for the oracle
+        self.sample = (k_tok[:, :sample_heads].cpu(), v_tok[:, :sample_heads].cpu(),
+                       self.q[:, :sample_heads * w.group].cpu())
+        i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32), device=dev)
+        t = self.table_np
+        self.table = qs.PageTable(i32(t.page_indptr), i32(t.page_indices), i32([L]))
+        kp, vp, sm = wl.empty_pool(t, h, d, w.dtype, device=dev, poison=False)
+        self.caches = [qs.PagedCache(kp, vp, sm)]
+        # prefill append of the first L-1 tokens through the library (timed once)
+        pre = qs.PageTable(self.table.page_indptr, self.table.page_indices, i32([L - 1]))
+        kpre, vpre = k_tok[:L - 1].contiguous(), v_tok[:L - 1].contiguous()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        qs.append_kv(self.caches[0], pre, kpre, vpre, i32([0, L - 1]), i32([0]))
+        e1.record()
+        torch.cuda.synchronize()
+        pre_ms = e0.elapsed_time(e1)
+        pre_bytes = (L - 1) * h * d * k_tok.element_size() * 4 + t.nnz * h * 2 * d * k_tok.element_size()
+        self.prefill = {"tokens": L - 1, "ms": pre_ms, "GBps": pre_bytes / pre_ms / 1e6}
+        assert qs.device_error() == 0
+        for _ in range(nbuf - 1):   # distinct copies: each step reads cold memory
+            c = self.caches[0]
+            self.caches.append(qs.PagedCache(c.k_pool.clone(), c.v_pool.clone(), c.summary.clone()))
+        self.k_dec = k_tok[L - 1:L].contiguous()
+        self.v_dec = v_tok[L - 1:L].contiguous()
+        del k_tok, v_tok, kpre, vpre
+        self.app_indptr = i32([0, 1])
+        self.before = i32([L - 1])
+        self.K = w.k
+        B, hq = 1, h * w.group
+        self.scores = torch.empty((h, t.nnz), dtype=torch.float32, device=dev)
+        self.sel = (torch.empty((B, h, self.K), dtype=torch.int32, device=dev),
+                    torch.empty((B, h, self.K), dtype=torch.int32, device=dev),
+                    torch.empty((B, h), dtype=torch.int32, device=dev))
+        self.out = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+        n = qs.attn_workspace_size(B, h, w.group, d, S, self.K)
+        self.ws = torch.empty(n, dtype=torch.uint8, device=dev)
+
+    # the four stages of one decode step on cache copy b
+    def append(self, b):
+        self.qs.append_kv(self.caches[b], self.table, self.k_dec, self.v_dec,
+                          self.app_indptr, self.before)
+
+    def score(self, b):
+        self.qs.score_pages(self.caches[b], self.table, self.q, self.w.group, self.scores)
+
+    def select(self, b):
+        self.qs.select_topk(self.table, self.w.h_kv, self.w.page_size, self.scores, self.K,
+                            out=self.sel)
+
+    def attend(self, b):
+        self.qs.sparse_decode_attn(self.caches[b], self.table, self.q, self.w.group,
+                                   self.sel[0], self.sel[1], self.K, self.out, self.lse,
+                                   workspace=self.ws)
+
+    def step(self, b):
+        self.append(b)
+        self.score(b)
+        self.select(b)
+        self.attend(b)
+
+    KERNELS_PER_STEP = 5   # append, score, select, attention split-K, combine
+
+    def bytes(self):
+        w = self.w
+        return step_bytes(self.table_np.nnz, w.h_kv, w.group, w.head_dim, w.page_size,
+                          self.K, self.K * w.page_size, self.k_dec.element_size())
+
+
+def time_events(fn, n, nbuf):
+    """Per-call device time (ms) of fn(b) with CUDA events on the current stream."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        ev[i][0].record()
+        fn(i % nbuf)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "query_aware_sparse_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, workload):
+    """dram bytes per launch recorded from an ncu capture, if the kernel's
+    source is unchanged since; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    e = rec.get(kernel_key)
+    if not e or e.get("workload") != workload:
+        return None
+    if e.get("source_hash") != source_hash(*e["sources"]):
+        return None
+    return e["dram_bytes_per_launch"]
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline key)
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """The oracle's decode step on a sample of the heads of the same layer,
+    built from the generated inputs (never from the device path's results)."""
+
+    def __init__(self, w: wl.Workload, k_tok, v_tok, q, heads: int):
+        from oracle import quest_oracle as qo
+        self.qo = qo
+        self.heads = heads
+        self.w = w
+        L = int(w.lengths()[0])
+        self.L = L
+        t = wl.make_page_table([L], w.page_size, seed=w.seed)
+        self.t = t
+        k_tok, v_tok = k_tok[:, :heads], v_tok[:, :heads]
+        kp, vp, _ = wl.empty_pool(t, heads, w.head_dim, w.dtype, poison=True)
+        ind = np.array([0, L - 1])
+        wl.place_tokens(kp, t, k_tok[:L - 1], ind)
+        wl.place_tokens(vp, t, v_tok[:L - 1], ind)
+        self.kp, self.vp = kp.numpy(), vp.numpy()
+        self.q = q[:, :heads * w.group].numpy()
+        self.kdec = k_tok[L - 1:L].numpy()
+        self.vdec = v_tok[L - 1:L].numpy()
+        self.sm = qo.build_summary(self.kp, t.page_indptr, t.page_indices,
+                                   np.array([L - 1], np.int32))
+
+    def step(self):
+        qo, t, w = self.qo, self.t, self.w
+        qo.append_kv(self.kp, self.vp, self.sm, t.page_indptr, t.page_indices,
+                     np.array([self.L - 1]), np.array([0, 1]), self.kdec, self.vdec)
+        sc = qo.score_pages(self.q, self.sm, t.page_indptr, t.page_indices, w.group)
+        sel, _, _ = qo.select_topk(sc, t.page_indptr, t.page_indices, w.k)
+        qo.sparse_attention(self.q, self.kp, self.vp, t.page_indptr, t.page_indices,
+                            np.array([self.L], np.int32), sel, w.group)
+
+    def time_steps(self, n):
+        ts = []
+        for _ in range(n):
+            t0 = time.perf_counter()
+            self.step()
+            ts.append(time.perf_counter() - t0)
+        scale = self.w.h_kv / self.heads          # µs per full layer
+        return [x * 1e6 * scale for x in ts]
+
+
+# ---------------------------------------------------------------------------
+# Main
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama_layer")
+    ap.add_argument("--nbuf", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-heads", type=int, default=4)
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = wl.WORKLOADS[args.workload]
+    cfg = {"workload": f"{w.name}: 1 request, {w.h_kv} heads (MHA), d_h {w.head_dim}, "
+                       f"context {int(w.lengths()[0])}, page {w.page_size}, "
+                       f"budget {w.k * w.page_size} tokens (K={w.k}), fp16, RoPE",
+           "n_pages": int(-(-int(w.lengths()[0]) // w.page_size)), "k": w.k,
+           "h_kv": w.h_kv, "group": w.group, "head_dim": w.head_dim,
+           "page_size": w.page_size, "seq_len": int(w.lengths()[0])}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, w, cfg, dev, ws)
+        return
+
+    import query_aware_sparse_gb300 as qs
+    qs.lib()
+    setup = LayerSetup(w, args.nbuf, dev, sample_heads=args.cpu_heads)
+    cfg["l2"] = (f"rotating {args.nbuf} distinct copies of the layer "
+                 f"({args.nbuf * (setup.caches[0].k_pool.nbytes * 2 + setup.caches[0].summary.nbytes) / 2**30:.1f} GiB)"
+                 " so every step reads memory not touched in the previous "
+                 f"{args.nbuf - 1} steps (> the 129 MB L2)")
+    nb = args.nbuf
+
+    # warm-up (also sets per-device kernel attributes before capture)
+    for i in range(max(args.warmup, nb)):
+        setup.step(i % nb)
+    torch.cuda.synchronize()
+    assert qs.device_error() == 0
+
+    # one CUDA graph per cache copy
+    s = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(s):
+        for b in range(nb):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                setup.step(b)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        graphs[i % nb].replay()
+    torch.cuda.synchronize()
+
+    # timed region: exactly K steps
+    K = args.steps
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    t_all = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_all[0].record()
+        for i in range(K):
+            per[i][0].record()
+            graphs[i % nb].replay()
+            per[i][1].record()
+        t_all[1].record()
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = t_all[0].elapsed_time(t_all[1])
+    steps_us = sorted(a.elapsed_time(b) * 1e3 for a, b in per)
+    ms_per_step = total_ms / K
+    if ws > 1:
+        tt = torch.tensor([ms_per_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(tt.item())
+    assert qs.device_error() == 0
+
+    # per-stage device time (each stage alone, rotating copies, events)
+    n_stage = 400
+    stage = {}
+    for name, fn in (("append", setup.append), ("score", setup.score),
+                     ("select", setup.select), ("attn", setup.attend)):
+        ts = time_events(fn, n_stage, nb)
+        stage[name] = statistics.median(ts) * 1e3
+    by = setup.bytes()
+
+    # e2e through the public API with host buffers
+    e2e = run_e2e(setup, graphs, nb, args.e2e_steps)
+
+    pk, pk_src = peaks()
+    value = ms_per_step * 1e3
+    path_gbs = by["total"] / (value * 1e-6) / 1e9
+    score_bytes = by["summary"] + by["q"]
+    score_gbs = score_bytes / (stage["score"] * 1e-6) / 1e9
+    attn_bytes = by["kv"] + by["q"] + by["o"]
+    attn_gbs = attn_bytes / (stage["attn"] * 1e-6) / 1e9
+    dominant = "score" if stage["score"] >= stage["attn"] else "attn"
+    dom_bytes, dom_gbs = (score_bytes, score_gbs) if dominant == "score" else (attn_bytes, attn_gbs)
+    kern = {"score": ("score_kernel", ["score.cu"]), "attn": ("attn_split_kernel", ["attn.cu"])}[dominant]
+    traffic = ncu_traffic(kern[0], w.name)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic (seeded N(0,1) K/V/q, 4 outlier channels x8, RoPE)",
+        "config": cfg,
+        "p50_us": round(steps_us[len(steps_us) // 2], 3),
+        "p95_us": round(steps_us[int(len(steps_us) * 0.95)], 3),
+        "stage_us": {k: round(v, 3) for k, v in stage.items()},
+        "path": {"bytes": by["total"], "GBps": round(path_gbs, 1),
+                 "frac": round(path_gbs / pk, 4), "frac_of_8TBps": round(path_gbs / 8000, 4)},
+        "roofline": {"bound": "hbm", "kernel": kern[0], "achieved": round(dom_gbs, 1),
+                     "peak": pk, "unit": "GB/s", "frac": round(dom_gbs / pk, 4),
+                     "peak_source": pk_src, "bytes_per_launch": dom_bytes,
+                     "traffic": traffic},
+        "append_prefill": {k: round(v, 3) for k, v in setup.prefill.items()},
+        "e2e": e2e,
+        "gpu_launches": K * LayerSetup.KERNELS_PER_STEP,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(setup, args.cpu_heads)
+        print(json.dumps(line))
+
+
+def run_e2e(setup, graphs, nb, n):
+    """Same step, per-step inputs from pinned host memory, result read back."""
+    h_q = setup.q.cpu().pin_memory()
+    h_k = setup.k_dec.cpu().pin_memory()
+    h_v = setup.v_dec.cpu().pin_memory()
+    h_o = torch.empty(setup.out.shape, dtype=setup.out.dtype).pin_memory()
+    h_l = torch.empty(setup.lse.shape, dtype=setup.lse.dtype).pin_memory()
+    ts = []
+    for i in range(n + 10):
+        t0 = time.perf_counter()
+        setup.q.copy_(h_q, non_blocking=True)
+        setup.k_dec.copy_(h_k, non_blocking=True)
+        setup.v_dec.copy_(h_v, non_blocking=True)
+        graphs[i % nb].replay()
+        h_o.copy_(setup.out, non_blocking=True)
+        h_l.copy_(setup.lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        if i >= 10:
+            ts.append(time.perf_counter() - t0)
+    ts.sort()
+    bi = h_q.nbytes + h_k.nbytes + h_v.nbytes
+    bo = h_o.nbytes + h_l.nbytes
+    return {"value": round(statistics.median(ts) * 1e6, 3), "unit": UNIT,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "p95": round(ts[int(len(ts) * 0.95)] * 1e6, 3)}
+
+
+def cpu_baseline(setup, heads):
+    o = OracleSample(setup.w, *setup.sample, heads)
+    o.time_steps(1)
+    t0 = time.perf_counter()
+    ts = []
+    while time.perf_counter() - t0 < 12.0 or len(ts) < 3:
+        ts += o.time_steps(1)
+    return {"value": round(statistics.median(ts), 1), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle decode step (append, score, select, attention) on "
+                      f"{heads} of {setup.w.h_kv} heads of the same layer, scaled x"
+                      f"{setup.w.h_kv // heads} to a full layer; {len(ts)} steps"}
+
+
+def run_reference(args, w, cfg, dev, ws):
+    """The oracle as the reference arm: same workload, metric and unit."""
+    L = int(w.lengths()[0])
+    k_tok, v_tok = wl.request_tokens(w, 0, L, device=dev)
+    q = wl.queries(w, [L - 1], device=dev)
+    h = args.cpu_heads
+    o = OracleSample(w, k_tok[:, :h].cpu(), v_tok[:, :h].cpu(), q[:, :h * w.group].cpu(), h)
+    del k_tok, v_tok
+    for _ in range(args.warmup):
+        o.time_steps(1)
+    # bounded: at most ~2 minutes of oracle work however many steps are asked
+    t0 = time.perf_counter()
+    ts = []
+    for _ in range(args.steps):
+        ts += o.time_steps(1)
+        if time.perf_counter() - t0 > 120:
+            break
+    v = statistics.median(ts)
+    line = {"metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": ws,
+            "steps": len(ts), "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": cfg, "impl": "reference",
+            "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{args.cpu_heads} of {w.h_kv} heads per step, scaled"},
+            "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * quest.h — C ABI of libquest: Quest-style query-aware page selection over a
+ * paged KV cache for long-context decode, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources. "Quest page" is the PaperTrace chapter
+ * "3.1.1 · Quest：用 min/max 上界筛选 KV 页"; "PageWeaver notes" is the
+ * reading-notes page "PageWeaver: KV-Guided Query Unions for Sparse
+ * Attention". Each entry point below names the passage that defines it.
+ *
+ * General contract
+ *  - Every pointer argument marked "device" must point to device memory of the
+ *    current CUDA device; the caller allocates and owns all of it (pools,
+ *    summaries, page tables, outputs, workspace). The library allocates no
+ *    memory. Its only state is a 4-byte device error word per device.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream). A QUEST_OK return means the work was enqueued.
+ *  - Host-side validation runs first; on any error nothing is enqueued and a
+ *    negative quest_status is returned. A failed launch returns QUEST_ERR_CUDA.
+ *  - Problems only visible on the device (a page index outside the pool, a
+ *    selected page with no valid token, an exhausted wait) never trap: the
+ *    offending item is skipped and a bit is OR-ed into the device error word,
+ *    which quest_get_device_error() returns and clears.
+ *  - Element types: QUEST_F32 or QUEST_F16 for K, V, summaries and q (all the
+ *    same type); outputs are fp32. head_dim in {64, 128}; page_size in
+ *    {16, 32}; GQA group in {1, 2, 4, 8}.
+ *  - Data pointers (pools, summary, q, k_new, v_new) must be 16-byte aligned.
+ */
+#ifndef QUEST_H
+#define QUEST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QUEST_API __attribute__((visibility("default")))
+#else
+#define QUEST_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QUEST_OK = 0,
+  QUEST_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misalignment        */
+  QUEST_ERR_UNSUPPORTED = -2,  /* dtype / head_dim / page_size / group not built */
+  QUEST_ERR_WORKSPACE = -3,    /* workspace missing or smaller than required   */
+  QUEST_ERR_CUDA = -4          /* a CUDA runtime call or launch failed         */
+} quest_status;
+
+typedef enum { QUEST_F32 = 0, QUEST_F16 = 1 } quest_dtype;
+
+/* Bits of the device error word. */
+#define QUEST_DEVERR_PAGE_RANGE   0x1u  /* physical page id outside [0, n_phys)      */
+#define QUEST_DEVERR_TABLE_RANGE  0x2u  /* append/selection beyond the page table    */
+#define QUEST_DEVERR_EMPTY_PAGE   0x4u  /* selected page holds no valid token        */
+#define QUEST_DEVERR_WAIT_TIMEOUT 0x8u  /* an in-kernel wait hit its iteration limit */
+
+/*
+ * One layer's paged cache (Quest page §1.2: the summary has logical shape
+ * [L, P, H_kv, 2, d_h] and is bound to the physical page; one struct = one L).
+ *   k_pool, v_pool : device, [n_phys, h_kv, page_size, head_dim], dtype
+ *   summary        : device, [n_phys, h_kv, 2, head_dim], dtype;
+ *                    [..., 0, :] = per-dimension min m, [..., 1, :] = max M
+ */
+typedef struct quest_cache {
+  void* k_pool;
+  void* v_pool;
+  void* summary;
+  int32_t n_phys;
+  int32_t h_kv;
+  int32_t page_size;
+  int32_t head_dim;
+  int32_t dtype; /* quest_dtype */
+} quest_cache;
+
+/*
+ * Ragged page table of a batch of requests (Quest page §2.1: requests are
+ * described by an indptr over pages; the page table maps logical pages to
+ * physical pages of the pool, Quest page Fig. 1).
+ *   page_indptr  : device int32 [batch + 1], page_indptr[0] = 0
+ *   page_indices : device int32 [nnz]; entry page_indptr[r] + p is the
+ *                  physical page holding logical page p of request r
+ *   seq_lens     : device int32 [batch], valid tokens of each request. Only
+ *                  the first ceil(seq_lens[r] / page_size) logical pages of a
+ *                  request hold tokens; later table entries are reserved pages.
+ *   nnz          : host copy of page_indptr[batch]
+ */
+typedef struct quest_pages {
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t nnz;
+} quest_pages;
+
+/*
+ * quest_append_kv — cache append with incremental summary update
+ * (Quest page §1.2 eq (8) and §3 eq (14); page recycling in §3).
+ *
+ * Token i of request r, append_indptr[r] <= i < append_indptr[r+1], is
+ * written at position pos = seq_lens_before[r] + (i - append_indptr[r]):
+ * logical page pos / page_size, slot pos % page_size. For each touched
+ * (page, KV head, dim): if slot 0 of the page is written by this call the
+ * summary restarts from the new keys (m = M = the first new key, then eq (8)),
+ * otherwise the new keys are folded into the stored m and M with eq (8).
+ * min/max order -0 below +0. Full pages that receive no token are not touched.
+ *   k_new, v_new      : device [n_new, h_kv, head_dim], dtype
+ *   n_new             : host, total new tokens (= append_indptr[batch])
+ *   append_indptr     : device int32 [batch + 1]
+ *   seq_lens_before   : device int32 [batch]
+ * pages->seq_lens is not read (the caller updates lengths itself). The page
+ * table must already map every page the new tokens land in; a token beyond it
+ * is skipped with QUEST_DEVERR_TABLE_RANGE. Calls that overlap on the GPU and
+ * touch the same page race.
+ */
+QUEST_API quest_status quest_append_kv(const quest_cache* cache, const quest_pages* pages,
+                             const void* k_new, const void* v_new, int32_t n_new,
+                             const int32_t* append_indptr,
+                             const int32_t* seq_lens_before, void* stream);
+
+/*
+ * quest_score_pages — page upper bounds (Quest page §1.1 eq (2)-(3)).
+ *
+ * scores[g * nnz + e] for table entry e of request r and KV head g is
+ *   U = sum_j max(q_{h,j} m_j, q_{h,j} M_j)
+ * for the query head h = g (group == 1); with group > 1 the G query heads
+ * g*G .. g*G+G-1 share one page set and U is their maximum (Quest page §2.1,
+ * group-max aggregation). Unscaled dot-product bounds, fp32 arithmetic.
+ * Reserved entries (logical page >= ceil(seq_lens[r] / page_size)) get -inf.
+ *   q      : device [batch, h_kv * group, head_dim], dtype
+ *   scores : device fp32 [h_kv, nnz]
+ */
+QUEST_API quest_status quest_score_pages(const quest_cache* cache, const quest_pages* pages,
+                               const void* q, int32_t group, float* scores,
+                               void* stream);
+
+/*
+ * quest_select_topk — fixed-budget Top-K pages (Quest page Fig. 1, §1.1 and
+ * §2: K pages, token budget K * page_size).
+ *
+ * For each (request r, KV head g) with P_r = ceil(seq_lens[r] / page_size)
+ * scored pages: the min(k, P_r) pages with the largest scores, ties broken
+ * by the lower logical page index (-0 equals +0). Emitted in ascending
+ * logical page order; unused slots hold -1.
+ *   page_size   : tokens per page (gives P_r from seq_lens); 16 or 32
+ *   scores      : device fp32 [h_kv, nnz] as written by quest_score_pages
+ *   sel_logical : device int32 [batch, h_kv, k] logical page ids
+ *   sel_phys    : device int32 [batch, h_kv, k] physical page ids (page table)
+ *   sel_count   : device int32 [batch, h_kv] = min(k, P_r)
+ */
+QUEST_API quest_status quest_select_topk(const quest_pages* pages, int32_t h_kv,
+                               int32_t page_size, const float* scores, int32_t k,
+                               int32_t* sel_logical, int32_t* sel_phys,
+                               int32_t* sel_count, void* stream);
+
+/*
+ * quest_sparse_decode_attn — attention over the selected pages only, read in
+ * place from the pool (Quest page Fig. 1 and §2.1; token set and 1/sqrt(d)
+ * scale as in PageWeaver notes §2 eq (1)-(2)).
+ *
+ * For query head h of request r with KV head g = h / group, the candidate
+ * tokens are the valid tokens of the pages listed in sel_logical[r, g, :]
+ * (physical ids in sel_phys; -1 entries skipped; the tail page contributes
+ * seq_lens[r] - p * page_size tokens). out = softmax(q k^T * sm_scale) V over
+ * those tokens only, lse = log of the softmax denominator (natural log, of the
+ * scaled logits). An empty set gives out = 0 and lse = -inf. Split-K: chunks
+ * of pages produce partial (o, max, sum) in `workspace`, merged by
+ * log-sum-exp in a second pass (Quest page §2.1). The ids of one (r, g) list
+ * must be distinct.
+ *   q          : device [batch, h_kv * group, head_dim], dtype
+ *   sel_*      : device int32 [batch, h_kv, k]
+ *   out        : device fp32 [batch, h_kv * group, head_dim]
+ *   lse        : device fp32 [batch, h_kv * group], or NULL
+ *   sm_scale   : <= 0 selects 1 / sqrt(head_dim)
+ *   workspace  : device, >= quest_attn_workspace_size(...) bytes, 16-B aligned
+ */
+QUEST_API quest_status quest_sparse_decode_attn(const quest_cache* cache,
+                                      const quest_pages* pages, const void* q,
+                                      int32_t group, const int32_t* sel_logical,
+                                      const int32_t* sel_phys, int32_t k,
+                                      float* out, float* lse, float sm_scale,
+                                      void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/* Workspace bytes quest_sparse_decode_attn needs for these sizes on the
+ * current device (the split-K chunking depends on its SM count). */
+QUEST_API size_t quest_attn_workspace_size(int32_t batch, int32_t h_kv, int32_t group,
+                                 int32_t head_dim, int32_t page_size,
+                                 int32_t k);
+
+/* Synchronises `stream`, returns the device error word of the current device
+ * (QUEST_DEVERR_* bits) and clears it. Returns -1 if a CUDA call fails. */
+QUEST_API int32_t quest_get_device_error(void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+QUEST_API const char* quest_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QUEST_H */

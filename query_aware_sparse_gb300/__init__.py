@@ -1,0 +1,199 @@
+"""query_aware_sparse_gb300 — Quest-style query-aware page selection on GB300.
+
+A thin Python binding over ``libquest.so`` (the C ABI in ``include/quest.h``).
+Every function here only marshals arguments (tensor data pointers, sizes and
+the current CUDA stream) and calls the library; all the computation runs in
+the library's CUDA kernels. There is no fallback: if the library is missing or
+a call fails, an exception is raised.
+
+Tensors are torch tensors on the current CUDA device (torch is used for device
+memory and streams only).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libquest.so")
+
+QUEST_F32, QUEST_F16 = 0, 1
+DEVERR = {1: "page id outside the pool", 2: "beyond the page table",
+          4: "selected page holds no valid token", 8: "in-kernel wait timed out"}
+
+
+class QuestCache(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("summary", ctypes.c_void_p), ("n_phys", ctypes.c_int32),
+                ("h_kv", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class QuestPages(ctypes.Structure):
+    _fields_ = [("page_indptr", ctypes.c_void_p), ("page_indices", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("batch", ctypes.c_int32),
+                ("nnz", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libquest.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m query_aware_sparse_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.quest_append_kv.argtypes = [P, P, P, P, I32, P, P, P]
+        L.quest_score_pages.argtypes = [P, P, P, I32, P, P]
+        L.quest_select_topk.argtypes = [P, I32, I32, P, I32, P, P, P, P]
+        L.quest_sparse_decode_attn.argtypes = [P, P, P, I32, P, P, I32, P, P,
+                                               ctypes.c_float, P, SZ, P]
+        L.quest_attn_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32]
+        L.quest_attn_workspace_size.restype = SZ
+        L.quest_get_device_error.argtypes = [P]
+        L.quest_get_device_error.restype = I32
+        L.quest_status_string.argtypes = [I32]
+        L.quest_status_string.restype = ctypes.c_char_p
+        for fn in ("quest_append_kv", "quest_score_pages", "quest_select_topk",
+                   "quest_sparse_decode_attn"):
+            getattr(L, fn).restype = I32
+        _lib = L
+    return _lib
+
+
+EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_select_topk",
+            "quest_sparse_decode_attn", "quest_attn_workspace_size",
+            "quest_get_device_error", "quest_status_string")
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise RuntimeError(lib().quest_status_string(status).decode())
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float16:
+        return QUEST_F16
+    if dt == torch.float32:
+        return QUEST_F32
+    raise ValueError(f"unsupported element type {dt}")
+
+
+class PagedCache:
+    """One layer's pool + summary (caller-owned torch tensors).
+
+    k_pool, v_pool: [n_phys, h_kv, page_size, head_dim]; summary:
+    [n_phys, h_kv, 2, head_dim] (index 0 = min, 1 = max).
+    """
+
+    def __init__(self, k_pool, v_pool, summary):
+        self.k_pool, self.v_pool, self.summary = k_pool, v_pool, summary
+        n_phys, h_kv, S, d = k_pool.shape
+        self.n_phys, self.h_kv, self.page_size, self.head_dim = n_phys, h_kv, S, d
+        self.dtype = k_pool.dtype
+        self.c = QuestCache(k_pool.data_ptr(), v_pool.data_ptr(), summary.data_ptr(),
+                            n_phys, h_kv, S, d, dtype_code(k_pool.dtype))
+
+    @classmethod
+    def empty(cls, n_phys, h_kv, page_size, head_dim, dtype, device="cuda"):
+        kp = torch.empty((n_phys, h_kv, page_size, head_dim), dtype=dtype, device=device)
+        vp = torch.empty_like(kp)
+        sm = torch.empty((n_phys, h_kv, 2, head_dim), dtype=dtype, device=device)
+        return cls(kp, vp, sm)
+
+
+class PageTable:
+    """Ragged page table on the device: page_indptr [B+1], page_indices [nnz],
+    seq_lens [B] (int32). ``nnz`` is kept on the host."""
+
+    def __init__(self, page_indptr, page_indices, seq_lens, nnz=None):
+        self.page_indptr, self.page_indices, self.seq_lens = page_indptr, page_indices, seq_lens
+        self.batch = int(seq_lens.shape[0])
+        self.nnz = int(page_indices.shape[0]) if nnz is None else int(nnz)
+        self.c = QuestPages(page_indptr.data_ptr(), page_indices.data_ptr(),
+                            seq_lens.data_ptr(), self.batch, self.nnz)
+
+
+def append_kv(cache: PagedCache, table: PageTable, k_new, v_new, append_indptr,
+              seq_lens_before, stream=None) -> None:
+    """quest_append_kv: write k_new/v_new [n_new, h_kv, d] into the pool and
+    update the page min/max summaries."""
+    _check(lib().quest_append_kv(ctypes.byref(cache.c), ctypes.byref(table.c),
+                                 _ptr(k_new), _ptr(v_new), int(k_new.shape[0]),
+                                 _ptr(append_indptr), _ptr(seq_lens_before),
+                                 _stream(stream)))
+
+
+def score_pages(cache: PagedCache, table: PageTable, q, group: int, scores=None,
+                stream=None):
+    """quest_score_pages: scores [h_kv, nnz] fp32 of every page-table entry."""
+    if scores is None:
+        scores = torch.empty((cache.h_kv, table.nnz), dtype=torch.float32, device=q.device)
+    _check(lib().quest_score_pages(ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(q),
+                                   int(group), _ptr(scores), _stream(stream)))
+    return scores
+
+
+def select_topk(table: PageTable, h_kv: int, page_size: int, scores, k: int,
+                out=None, stream=None):
+    """quest_select_topk: (sel_logical, sel_phys [B, h_kv, k], sel_count [B, h_kv])."""
+    if out is None:
+        dev = scores.device
+        out = (torch.empty((table.batch, h_kv, k), dtype=torch.int32, device=dev),
+               torch.empty((table.batch, h_kv, k), dtype=torch.int32, device=dev),
+               torch.empty((table.batch, h_kv), dtype=torch.int32, device=dev))
+    sl, sp, sc = out
+    _check(lib().quest_select_topk(ctypes.byref(table.c), int(h_kv), int(page_size),
+                                   _ptr(scores), int(k), _ptr(sl), _ptr(sp), _ptr(sc),
+                                   _stream(stream)))
+    return sl, sp, sc
+
+
+def attn_workspace_size(batch, h_kv, group, head_dim, page_size, k) -> int:
+    return int(lib().quest_attn_workspace_size(batch, h_kv, group, head_dim, page_size, k))
+
+
+def sparse_decode_attn(cache: PagedCache, table: PageTable, q, group: int, sel_logical,
+                       sel_phys, k: int, out=None, lse=None, sm_scale: float = 0.0,
+                       workspace=None, stream=None):
+    """quest_sparse_decode_attn: (out [B, h_q, d] fp32, lse [B, h_q] fp32)."""
+    B, h_q, d = q.shape
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, h_q, d), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, h_q), dtype=torch.float32, device=dev)
+    if workspace is None:
+        n = attn_workspace_size(B, cache.h_kv, group, d, cache.page_size, k)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    _check(lib().quest_sparse_decode_attn(
+        ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(q), int(group), _ptr(sel_logical),
+        _ptr(sel_phys), int(k), _ptr(out), _ptr(lse), float(sm_scale), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _stream(stream)))
+    return out, lse
+
+
+def device_error(stream=None) -> int:
+    """Synchronise and return (then clear) the device error word."""
+    v = int(lib().quest_get_device_error(_stream(stream)))
+    if v < 0:
+        raise RuntimeError("quest_get_device_error: CUDA call failed")
+    return v

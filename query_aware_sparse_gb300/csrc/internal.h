@@ -1,0 +1,66 @@
+// Host-side launch interfaces between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/quest.h"
+
+namespace quest {
+
+struct AppendArgs {
+  void* k_pool; void* v_pool; void* summary;
+  const void* k_new; const void* v_new;
+  const int32_t* page_indptr; const int32_t* page_indices;
+  const int32_t* append_indptr; const int32_t* seq_lens_before;
+  int32_t batch, n_new, n_phys, h_kv, page_size, head_dim, dtype;
+  unsigned* err;
+};
+
+struct ScoreArgs {
+  const void* summary; const void* q;
+  const int32_t* page_indptr; const int32_t* page_indices; const int32_t* seq_lens;
+  float* scores;
+  int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype;
+  unsigned* err;
+};
+
+struct SelectArgs {
+  const float* scores;
+  const int32_t* page_indptr; const int32_t* page_indices; const int32_t* seq_lens;
+  int32_t* sel_logical; int32_t* sel_phys; int32_t* sel_count;
+  int32_t batch, nnz, h_kv, k, page_size;
+  unsigned* err;
+};
+
+struct AttnArgs {
+  const void* q; const void* k_pool; const void* v_pool;
+  const int32_t* sel_logical; const int32_t* sel_phys; const int32_t* seq_lens;
+  float* out; float* lse;
+  float* part_o;     // [batch, h_q, n_chunks, head_dim]
+  float* part_ml;    // [batch, h_q, n_chunks, 2]  (running max in log2 units, sum)
+  int32_t batch, n_phys, h_kv, group, page_size, head_dim, dtype, k;
+  int32_t n_chunks, chunk_pages;
+  float scale_log2;  // sm_scale * log2(e)
+  unsigned* err;
+};
+
+// Split-K plan of the attention for a problem size on the current device.
+struct AttnPlan {
+  int32_t n_chunks;
+  int32_t chunk_pages;
+  size_t workspace_bytes;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_score(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+AttnPlan plan_attn(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
+                   int32_t page_size, int32_t dtype, int32_t k);
+
+bool attn_supported(int32_t dtype, int32_t head_dim, int32_t page_size, int32_t group);
+bool score_supported(int32_t dtype, int32_t head_dim, int32_t group);
+
+}  // namespace quest

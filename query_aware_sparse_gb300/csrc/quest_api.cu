@@ -1,0 +1,200 @@
+// C ABI of libquest: host-side validation, the device error word and the
+// dispatch to the kernel files. No torch types, no allocation.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+// The device error word: one per device that loads the library, living in
+// the module's global memory (no allocation). Kernels receive its address.
+__device__ unsigned int quest_device_error_word;
+
+namespace {
+
+using quest::AttnPlan;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+// Device address of the error word for the current device (set-up once per
+// device, with that device current).
+unsigned* err_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, quest_device_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+quest_status check_cache(const quest_cache* c) {
+  if (!c || !c->k_pool || !c->v_pool || !c->summary) return QUEST_ERR_INVALID_ARG;
+  if (c->n_phys <= 0 || c->h_kv <= 0) return QUEST_ERR_INVALID_ARG;
+  if (c->dtype != QUEST_F16 && c->dtype != QUEST_F32) return QUEST_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return QUEST_ERR_UNSUPPORTED;
+  if (c->page_size != 16 && c->page_size != 32) return QUEST_ERR_UNSUPPORTED;
+  if (!aligned16(c->k_pool) || !aligned16(c->v_pool) || !aligned16(c->summary))
+    return QUEST_ERR_INVALID_ARG;
+  return QUEST_OK;
+}
+
+quest_status check_pages(const quest_pages* p, bool need_seq_lens) {
+  if (!p || p->batch < 0 || p->nnz < 0) return QUEST_ERR_INVALID_ARG;
+  if (p->batch == 0) return QUEST_OK;
+  if (!p->page_indptr || (p->nnz > 0 && !p->page_indices)) return QUEST_ERR_INVALID_ARG;
+  if (need_seq_lens && !p->seq_lens) return QUEST_ERR_INVALID_ARG;
+  return QUEST_OK;
+}
+
+bool valid_group(int32_t g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+quest_status launched(cudaError_t e) { return e == cudaSuccess ? QUEST_OK : QUEST_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+quest_status quest_append_kv(const quest_cache* cache, const quest_pages* pages,
+                             const void* k_new, const void* v_new, int32_t n_new,
+                             const int32_t* append_indptr,
+                             const int32_t* seq_lens_before, void* stream) {
+  quest_status st = check_cache(cache);
+  if (st != QUEST_OK) return st;
+  if ((st = check_pages(pages, false)) != QUEST_OK) return st;
+  if (n_new < 0) return QUEST_ERR_INVALID_ARG;
+  if (pages->batch == 0 || n_new == 0) return QUEST_OK;
+  if (!k_new || !v_new || !append_indptr || !seq_lens_before) return QUEST_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return QUEST_ERR_INVALID_ARG;
+  quest::AppendArgs a{};
+  a.k_pool = cache->k_pool; a.v_pool = cache->v_pool; a.summary = cache->summary;
+  a.k_new = k_new; a.v_new = v_new;
+  a.page_indptr = pages->page_indptr; a.page_indices = pages->page_indices;
+  a.append_indptr = append_indptr; a.seq_lens_before = seq_lens_before;
+  a.batch = pages->batch; a.n_new = n_new; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
+  a.page_size = cache->page_size; a.head_dim = cache->head_dim; a.dtype = cache->dtype;
+  a.err = err_ptr();
+  if (!a.err) return QUEST_ERR_CUDA;
+  return launched(quest::launch_append(a, static_cast<cudaStream_t>(stream)));
+}
+
+quest_status quest_score_pages(const quest_cache* cache, const quest_pages* pages,
+                               const void* q, int32_t group, float* scores,
+                               void* stream) {
+  quest_status st = check_cache(cache);
+  if (st != QUEST_OK) return st;
+  if ((st = check_pages(pages, true)) != QUEST_OK) return st;
+  if (!valid_group(group)) return QUEST_ERR_UNSUPPORTED;
+  if (!quest::score_supported(cache->dtype, cache->head_dim, group)) return QUEST_ERR_UNSUPPORTED;
+  if (pages->batch == 0 || pages->nnz == 0) return QUEST_OK;
+  if (!q || !scores || !aligned16(q)) return QUEST_ERR_INVALID_ARG;
+  quest::ScoreArgs a{};
+  a.summary = cache->summary; a.q = q;
+  a.page_indptr = pages->page_indptr; a.page_indices = pages->page_indices;
+  a.seq_lens = pages->seq_lens; a.scores = scores;
+  a.batch = pages->batch; a.nnz = pages->nnz; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
+  a.group = group; a.page_size = cache->page_size; a.head_dim = cache->head_dim;
+  a.dtype = cache->dtype;
+  a.err = err_ptr();
+  if (!a.err) return QUEST_ERR_CUDA;
+  return launched(quest::launch_score(a, static_cast<cudaStream_t>(stream)));
+}
+
+quest_status quest_select_topk(const quest_pages* pages, int32_t h_kv,
+                               int32_t page_size, const float* scores, int32_t k,
+                               int32_t* sel_logical, int32_t* sel_phys,
+                               int32_t* sel_count, void* stream) {
+  quest_status st = check_pages(pages, true);
+  if (st != QUEST_OK) return st;
+  if (h_kv <= 0 || k < 1) return QUEST_ERR_INVALID_ARG;
+  if (page_size != 16 && page_size != 32) return QUEST_ERR_UNSUPPORTED;
+  if (pages->batch == 0) return QUEST_OK;
+  if ((!scores && pages->nnz > 0) || !sel_logical || !sel_phys || !sel_count)
+    return QUEST_ERR_INVALID_ARG;
+  quest::SelectArgs a{};
+  a.scores = scores;
+  a.page_indptr = pages->page_indptr; a.page_indices = pages->page_indices;
+  a.seq_lens = pages->seq_lens;
+  a.sel_logical = sel_logical; a.sel_phys = sel_phys; a.sel_count = sel_count;
+  a.batch = pages->batch; a.nnz = pages->nnz; a.h_kv = h_kv; a.k = k;
+  a.page_size = page_size;
+  a.err = err_ptr();
+  if (!a.err) return QUEST_ERR_CUDA;
+  return launched(quest::launch_select(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t quest_attn_workspace_size(int32_t batch, int32_t h_kv, int32_t group,
+                                 int32_t head_dim, int32_t page_size, int32_t k) {
+  if (batch <= 0 || h_kv <= 0 || k < 1 || !valid_group(group)) return 0;
+  // the plan does not depend on the element type beyond shared memory per
+  // CTA; take the larger (fp32) footprint so one size serves both types
+  AttnPlan p16 = quest::plan_attn(batch, h_kv, group, head_dim, page_size, QUEST_F16, k);
+  AttnPlan p32 = quest::plan_attn(batch, h_kv, group, head_dim, page_size, QUEST_F32, k);
+  return p16.workspace_bytes > p32.workspace_bytes ? p16.workspace_bytes : p32.workspace_bytes;
+}
+
+quest_status quest_sparse_decode_attn(const quest_cache* cache,
+                                      const quest_pages* pages, const void* q,
+                                      int32_t group, const int32_t* sel_logical,
+                                      const int32_t* sel_phys, int32_t k,
+                                      float* out, float* lse, float sm_scale,
+                                      void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  quest_status st = check_cache(cache);
+  if (st != QUEST_OK) return st;
+  if ((st = check_pages(pages, true)) != QUEST_OK) return st;
+  if (!valid_group(group) || k < 1) return QUEST_ERR_INVALID_ARG;
+  if (!quest::attn_supported(cache->dtype, cache->head_dim, cache->page_size, group))
+    return QUEST_ERR_UNSUPPORTED;
+  if (pages->batch == 0) return QUEST_OK;
+  if (!q || !sel_logical || !sel_phys || !out || !aligned16(q)) return QUEST_ERR_INVALID_ARG;
+  AttnPlan plan = quest::plan_attn(pages->batch, cache->h_kv, group, cache->head_dim,
+                                   cache->page_size, cache->dtype, k);
+  if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
+    return QUEST_ERR_WORKSPACE;
+  quest::AttnArgs a{};
+  a.q = q; a.k_pool = cache->k_pool; a.v_pool = cache->v_pool;
+  a.sel_logical = sel_logical; a.sel_phys = sel_phys; a.seq_lens = pages->seq_lens;
+  a.out = out; a.lse = lse;
+  const size_t rows = (size_t)pages->batch * cache->h_kv * group * plan.n_chunks;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_ml = a.part_o + rows * cache->head_dim;
+  a.batch = pages->batch; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv; a.group = group;
+  a.page_size = cache->page_size; a.head_dim = cache->head_dim; a.dtype = cache->dtype;
+  a.k = k; a.n_chunks = plan.n_chunks; a.chunk_pages = plan.chunk_pages;
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)cache->head_dim);
+  a.scale_log2 = scale * quest::LOG2E;
+  a.err = err_ptr();
+  if (!a.err) return QUEST_ERR_CUDA;
+  return launched(quest::launch_attn(a, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t quest_get_device_error(void* stream) {
+  unsigned* p = err_ptr();
+  if (!p) return -1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  const unsigned zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return -1;
+  return (int32_t)v;
+}
+
+const char* quest_status_string(int32_t status) {
+  switch (status) {
+    case QUEST_OK: return "QUEST_OK";
+    case QUEST_ERR_INVALID_ARG: return "QUEST_ERR_INVALID_ARG: null pointer, bad size or misaligned pointer";
+    case QUEST_ERR_UNSUPPORTED: return "QUEST_ERR_UNSUPPORTED: dtype, head_dim, page_size or group not supported";
+    case QUEST_ERR_WORKSPACE: return "QUEST_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case QUEST_ERR_CUDA: return "QUEST_ERR_CUDA: a CUDA call or kernel launch failed";
+  }
+  return "unknown quest_status";
+}
+
+}  // extern "C"

@@ -1,0 +1,154 @@
+// a2: page upper bounds U_p(q) = sum_j max(q_j m_j, q_j M_j)
+// (Quest page §1.1 eq (2)-(3)); GQA groups share one score, the maximum over
+// the group's query heads (Quest page §2.1).
+//
+// HBM-bound stream of the [n_phys, h_kv, 2, d] summary. A (page, KV head)
+// summary is 2*d contiguous elements; LPP lanes cover one page with 16-byte
+// loads (min half and max half of the same dims in the same lane), so one
+// warp instruction moves 32 x 16 B and the G query heads of the group reuse
+// the registers. Each lane keeps UNROLL pages of loads in flight.
+#include "common.cuh"
+#include "internal.h"
+
+namespace quest {
+namespace {
+
+constexpr int kScoreThreads = 256;
+constexpr int kScoreUnroll = 4;
+
+template <typename T, int D>
+struct ScoreShape {
+  static constexpr int VEC = Elem<T>::kVec;          // elements per lane-load
+  static constexpr int LPP = D / VEC;                // lanes per page
+  static constexpr int PPW = 32 / LPP;               // pages per warp step
+  static constexpr int WARPS = kScoreThreads / 32;
+  static constexpr int TILE = WARPS * PPW * kScoreUnroll;  // pages per CTA
+};
+
+__device__ __forceinline__ int find_request(const int32_t* indptr, int lo, int hi, int e) {
+  // largest r in [lo, hi] with indptr[r] <= e
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(indptr + mid) <= e) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <typename T, int D, int G>
+__device__ __forceinline__ void load_q(const ScoreArgs& a, int r, int g, int sub,
+                                       float (&q)[G][Elem<T>::kVec]) {
+  constexpr int VEC = Elem<T>::kVec;
+  const T* qp = static_cast<const T*>(a.q) +
+                ((size_t)r * a.h_kv * G + (size_t)g * G) * D + sub * VEC;
+#pragma unroll
+  for (int gi = 0; gi < G; ++gi) unpack16<T>(ld_nc_v4(qp + (size_t)gi * D), q[gi]);
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kScoreThreads)
+score_kernel(const ScoreArgs a) {
+  using Sh = ScoreShape<T, D>;
+  constexpr int VEC = Sh::VEC, LPP = Sh::LPP, PPW = Sh::PPW;
+  __shared__ int s_rfirst, s_rlast;
+
+  const int g = blockIdx.y;
+  const int e_begin = blockIdx.x * Sh::TILE;
+  const int e_end = min(a.nnz, e_begin + Sh::TILE);
+  if (threadIdx.x == 0) {
+    s_rfirst = find_request(a.page_indptr, 0, a.batch - 1, e_begin);
+    s_rlast = find_request(a.page_indptr, 0, a.batch - 1, e_end - 1);
+  }
+  __syncthreads();
+  const int rfirst = s_rfirst, rlast = s_rlast;
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int sub = lane % LPP;       // which 16-byte column of the page
+  const int pw = lane / LPP;        // which page of the warp step
+
+  float q[G][VEC];
+  int cur_r = rfirst;
+  load_q<T, D, G>(a, cur_r, g, sub, q);
+
+  // Page e handled by (warp, u, pw): consecutive warps take consecutive runs.
+  uint4 vm[kScoreUnroll], vM[kScoreUnroll];
+  int er[kScoreUnroll];
+  bool live[kScoreUnroll];
+#pragma unroll
+  for (int u = 0; u < kScoreUnroll; ++u) {
+    const int e = e_begin + (warp * kScoreUnroll + u) * PPW + pw;
+    int r = rfirst;
+    live[u] = false;
+    if (e < e_end) {
+      if (rfirst != rlast) r = find_request(a.page_indptr, rfirst, rlast, e);
+      const int lp = e - __ldg(a.page_indptr + r);
+      const int valid_pages = (__ldg(a.seq_lens + r) + a.page_size - 1) / a.page_size;
+      const int pp = __ldg(a.page_indices + e);
+      if (lp < valid_pages) {
+        if (pp >= 0 && pp < a.n_phys) {
+          const T* sp = static_cast<const T*>(a.summary) +
+                        ((size_t)pp * a.h_kv + g) * 2 * D + sub * VEC;
+          vm[u] = ld_stream_v4(sp);
+          vM[u] = ld_stream_v4(sp + D);
+          live[u] = true;
+        } else if (sub == 0) {
+          report(a.err, QUEST_DEVERR_PAGE_RANGE);
+        }
+      }
+    }
+    er[u] = r;
+  }
+
+#pragma unroll
+  for (int u = 0; u < kScoreUnroll; ++u) {
+    const int e = e_begin + (warp * kScoreUnroll + u) * PPW + pw;
+    if (er[u] != cur_r) {       // page of another request: its own query
+      cur_r = er[u];
+      load_q<T, D, G>(a, cur_r, g, sub, q);
+    }
+    float m[VEC], M[VEC];
+    unpack16<T>(vm[u], m);
+    unpack16<T>(vM[u], M);
+    float best = -INFINITY;
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      float s = 0.f;
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) s += fmaxf(q[gi][v] * m[v], q[gi][v] * M[v]);
+#pragma unroll
+      for (int o = 1; o < LPP; o <<= 1) s += __shfl_xor_sync(FULL, s, o);
+      best = fmaxf(best, s);
+    }
+    if (sub == 0 && e < e_end) a.scores[(size_t)g * a.nnz + e] = live[u] ? best : -INFINITY;
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_td(const ScoreArgs& a, cudaStream_t s) {
+  using Sh = ScoreShape<T, D>;
+  dim3 grid((a.nnz + Sh::TILE - 1) / Sh::TILE, a.h_kv);
+  switch (a.group) {
+    case 1: score_kernel<T, D, 1><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 2: score_kernel<T, D, 2><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 4: score_kernel<T, D, 4><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 8: score_kernel<T, D, 8><<<grid, kScoreThreads, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool score_supported(int32_t dtype, int32_t head_dim, int32_t group) {
+  return (dtype == QUEST_F16 || dtype == QUEST_F32) && (head_dim == 64 || head_dim == 128) &&
+         (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_score(const ScoreArgs& a, cudaStream_t s) {
+  if (a.nnz == 0 || a.batch == 0) return cudaSuccess;
+  if (a.dtype == QUEST_F16)
+    return a.head_dim == 128 ? launch_td<__half, 128>(a, s) : launch_td<__half, 64>(a, s);
+  return a.head_dim == 128 ? launch_td<float, 128>(a, s) : launch_td<float, 64>(a, s);
+}
+
+}  // namespace quest

@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every symbol include/quest.h
+declares; host-side validation rejects bad arguments before any CUDA call.
+No compute call is made here (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qlib():
+    from query_aware_sparse_gb300 import build
+    build.build()
+    import query_aware_sparse_gb300 as q
+    return q
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "quest.h")) as f:
+        src = f.read()
+    return set(re.findall(r"QUEST_API\s+[\w\s\*]+?\b(quest_\w+)\s*\(", src))
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = declared_symbols()
+    for n in ("quest_append_kv", "quest_score_pages", "quest_select_topk",
+              "quest_sparse_decode_attn"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(qlib):
+    L = qlib.lib()
+    names = declared_symbols()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(qlib.EXPORTED) == names
+
+
+def test_status_strings(qlib):
+    L = qlib.lib()
+    assert L.quest_status_string(0) == b"QUEST_OK"
+    for code in (-1, -2, -3, -4):
+        assert L.quest_status_string(code).startswith(b"QUEST_ERR_")
+    assert L.quest_status_string(99) == b"unknown quest_status"
+
+
+def test_host_validation_rejects_bad_arguments(qlib):
+    """These calls return before any CUDA call is made."""
+    L = qlib.lib()
+    C, Pg = qlib.QuestCache, qlib.QuestPages
+    fake = 0x10000                      # never dereferenced: validation fails first
+    good = C(fake, fake, fake, 8, 2, 16, 128, qlib.QUEST_F16)
+    pages = Pg(fake, fake, fake, 1, 8)
+    by = ctypes.byref
+    # null cache / pools
+    assert L.quest_append_kv(None, by(pages), fake, fake, 1, fake, fake, None) == -1
+    assert L.quest_score_pages(by(C(0, fake, fake, 8, 2, 16, 128, 1)), by(pages), fake, 1, fake, None) == -1
+    # unsupported head_dim / page_size / dtype / group
+    assert L.quest_score_pages(by(C(fake, fake, fake, 8, 2, 16, 96, 1)), by(pages), fake, 1, fake, None) == -2
+    assert L.quest_score_pages(by(C(fake, fake, fake, 8, 2, 24, 128, 1)), by(pages), fake, 1, fake, None) == -2
+    assert L.quest_score_pages(by(C(fake, fake, fake, 8, 2, 16, 128, 7)), by(pages), fake, 1, fake, None) == -2
+    assert L.quest_score_pages(by(good), by(pages), fake, 3, fake, None) == -2
+    # misaligned pointers
+    assert L.quest_score_pages(by(C(fake + 2, fake, fake, 8, 2, 16, 128, 1)), by(pages), fake, 1, fake, None) == -1
+    assert L.quest_score_pages(by(good), by(pages), fake + 4, 1, fake, None) == -1
+    # bad k / h_kv / page size for select
+    assert L.quest_select_topk(by(pages), 2, 16, fake, 0, fake, fake, fake, None) == -1
+    assert L.quest_select_topk(by(pages), 0, 16, fake, 4, fake, fake, fake, None) == -1
+    assert L.quest_select_topk(by(pages), 2, 12, fake, 4, fake, fake, fake, None) == -2
+    assert L.quest_select_topk(by(pages), 2, 16, fake, 4, None, fake, fake, None) == -1
+    # missing seq_lens where lengths are needed
+    assert L.quest_select_topk(by(Pg(fake, fake, None, 1, 8)), 2, 16, fake, 4, fake, fake, fake, None) == -1
+    # negative sizes
+    assert L.quest_append_kv(by(good), by(pages), fake, fake, -1, fake, fake, None) == -1
+    assert L.quest_append_kv(by(good), by(Pg(fake, fake, fake, -1, 8)), fake, fake, 1, fake, fake, None) == -1
+    # attention: missing workspace is reported before any launch
+    assert L.quest_sparse_decode_attn(by(good), by(pages), fake, 1, fake, fake, 4, fake, None,
+                                      ctypes.c_float(0.0), None, 0, None) in (-3, -4)
+    # empty batches are valid no-ops
+    empty = Pg(None, None, None, 0, 0)
+    assert L.quest_select_topk(by(empty), 2, 16, None, 4, None, None, None, None) == 0
+    assert L.quest_append_kv(by(good), by(empty), None, None, 0, None, None, None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import query_aware_sparse_gb300 as q
+    monkeypatch.setattr(q, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(q, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        q.lib()
