@@ -183,6 +183,7 @@ class LayerSetup:
         self.k_dec = k_tok[L - 1:L].contiguous()
         self.v_dec = v_tok[L - 1:L].contiguous()
         del k_tok, v_tok, kpre, vpre
+        torch.cuda.empty_cache()
         self.app_indptr = i32([0, 1])
         self.before = i32([L - 1])
         self.K = w.k
@@ -195,6 +196,8 @@ class LayerSetup:
         self.lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
         n = qs.attn_workspace_size(B, h, w.group, d, S, self.K)
         self.ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.fused = qs.DecodeStep(self.caches[0], self.table, w.group, self.K)
+        self.out, self.lse = self.fused.out, self.fused.lse
 
     # the four stages of one decode step on cache copy b
     def append(self, b):
@@ -213,31 +216,45 @@ class LayerSetup:
                                    self.sel[0], self.sel[1], self.K, self.out, self.lse,
                                    workspace=self.ws)
 
-    def step(self, b):
+    def unfused(self, b):
         self.append(b)
         self.score(b)
         self.select(b)
         self.attend(b)
 
-    KERNELS_PER_STEP = 5   # append, score, select, attention split-K, combine
+    def step(self, b):
+        """The fused decode step: append + score + select + attention in one launch."""
+        self.fused(self.caches[b], self.table, self.q, self.k_dec, self.v_dec)
 
-    def bytes(self):
+    KERNELS_PER_STEP = 1   # quest_decode_step is one cooperative kernel
+
+    def bytes(self):  # noqa: A003
         w = self.w
         return step_bytes(self.table_np.nnz, w.h_kv, w.group, w.head_dim, w.page_size,
                           self.K, self.K * w.page_size, self.k_dec.element_size())
 
 
-def time_events(fn, n, nbuf):
-    """Per-call device time (ms) of fn(b) with CUDA events on the current stream."""
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n)]
+def time_stage(fn, nbuf, reps):
+    """Average device time (ms) of one call of fn(b): a CUDA graph holds one
+    call per cache copy back to back; it is replayed `reps` times between two
+    events on the capturing stream, so host launch cost is not included."""
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for b in range(nbuf):
+                fn(b)
     torch.cuda.synchronize()
-    for i in range(n):
-        ev[i][0].record()
-        fn(i % nbuf)
-        ev[i][1].record()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in ev]
+    return e0.elapsed_time(e1) / (reps * nbuf)
 
 
 def source_hash(*names):
@@ -326,6 +343,9 @@ def main():
     ap.add_argument("--nbuf", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-heads", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="oracle timing budget for cpu_baseline (0 = skip)")
+    ap.add_argument("--stage-reps", type=int, default=100)
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -405,13 +425,13 @@ def main():
         ms_per_step = float(tt.item())
     assert qs.device_error() == 0
 
-    # per-stage device time (each stage alone, rotating copies, events)
-    n_stage = 400
+    # per-stage device time of the unfused four-call path (each stage alone,
+    # rotating copies, events); informational
     stage = {}
     for name, fn in (("append", setup.append), ("score", setup.score),
-                     ("select", setup.select), ("attn", setup.attend)):
-        ts = time_events(fn, n_stage, nb)
-        stage[name] = statistics.median(ts) * 1e3
+                     ("select", setup.select), ("attn", setup.attend),
+                     ("unfused_step", setup.unfused), ("fused_step", setup.step)):
+        stage[name] = time_stage(fn, nb, args.stage_reps) * 1e3
     by = setup.bytes()
 
     # e2e through the public API with host buffers
@@ -420,13 +440,10 @@ def main():
     pk, pk_src = peaks()
     value = ms_per_step * 1e3
     path_gbs = by["total"] / (value * 1e-6) / 1e9
-    score_bytes = by["summary"] + by["q"]
-    score_gbs = score_bytes / (stage["score"] * 1e-6) / 1e9
-    attn_bytes = by["kv"] + by["q"] + by["o"]
-    attn_gbs = attn_bytes / (stage["attn"] * 1e-6) / 1e9
-    dominant = "score" if stage["score"] >= stage["attn"] else "attn"
-    dom_bytes, dom_gbs = (score_bytes, score_gbs) if dominant == "score" else (attn_bytes, attn_gbs)
-    kern = {"score": ("score_kernel", ["score.cu"]), "attn": ("attn_split_kernel", ["attn.cu"])}[dominant]
+    # the dominant (only) kernel of the timed step is the fused step kernel
+    dom_bytes = by["total"]
+    dom_gbs = dom_bytes / (stage["fused_step"] * 1e-6) / 1e9
+    kern = ("step_kernel", ["step.cu", "attn_dev.cuh", "topk.cuh"])
     traffic = ncu_traffic(kern[0], w.name)
 
     line = {
@@ -450,7 +467,8 @@ def main():
         "clocks": clk.summary(),
     }
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(setup, args.cpu_heads)
+        if args.cpu_seconds > 0:
+            line["cpu_baseline"] = cpu_baseline(setup, args.cpu_heads, args.cpu_seconds)
         print(json.dumps(line))
 
 
@@ -481,12 +499,12 @@ def run_e2e(setup, graphs, nb, n):
             "p95": round(ts[int(len(ts) * 0.95)] * 1e6, 3)}
 
 
-def cpu_baseline(setup, heads):
+def cpu_baseline(setup, heads, seconds):
     o = OracleSample(setup.w, *setup.sample, heads)
     o.time_steps(1)
     t0 = time.perf_counter()
     ts = []
-    while time.perf_counter() - t0 < 12.0 or len(ts) < 3:
+    while time.perf_counter() - t0 < seconds or len(ts) < 3:
         ts += o.time_steps(1)
     return {"value": round(statistics.median(ts), 1), "unit": UNIT, "cores": 1,
             "kind": "oracle",

@@ -190,6 +190,46 @@ QUEST_API size_t quest_attn_workspace_size(int32_t batch, int32_t h_kv, int32_t 
                                  int32_t head_dim, int32_t page_size,
                                  int32_t k);
 
+/*
+ * quest_decode_step — one decode step of one layer in a single fused launch:
+ * the append of one new token per request (optional), page scoring, Top-K
+ * selection and sparse attention with its log-sum-exp merge (the four calls
+ * above, Quest page Fig. 1 and §1.2/§2.1, in one persistent cooperative
+ * kernel). Results equal those of quest_append_kv (one token per request at
+ * position seq_lens[r] - 1) followed by quest_score_pages, quest_select_topk
+ * and quest_sparse_decode_attn on the same arguments.
+ *   pages->seq_lens : lengths INCLUDING the new token
+ *   k_new, v_new    : device [batch, h_kv, head_dim] dtype, or both NULL
+ *                     (no append: the cache already holds every token)
+ *   q, group, k     : as quest_score_pages / quest_select_topk
+ *   scores          : device fp32 [h_kv, nnz] (written)
+ *   sel_logical, sel_phys, sel_count : as quest_select_topk (written)
+ *   out, lse        : as quest_sparse_decode_attn (lse may be NULL)
+ *   sm_scale        : <= 0 selects 1 / sqrt(head_dim)
+ *   workspace       : device, >= quest_decode_workspace_size(...) bytes,
+ *                     16-B aligned, ZERO-FILLED before its first use; a call
+ *                     that completes leaves its counters at zero again (after
+ *                     a QUEST_DEVERR_WAIT_TIMEOUT, zero it again). Calls that
+ *                     share a workspace must not overlap on the GPU.
+ * Needs a device that can keep one 256-thread CTA per SM resident (the launch
+ * is cooperative); returns QUEST_ERR_UNSUPPORTED for shapes whose shared
+ * memory does not fit.
+ */
+QUEST_API quest_status quest_decode_step(const quest_cache* cache, const quest_pages* pages,
+                                         const void* k_new, const void* v_new,
+                                         const void* q, int32_t group, int32_t k,
+                                         float* scores, int32_t* sel_logical,
+                                         int32_t* sel_phys, int32_t* sel_count,
+                                         float* out, float* lse, float sm_scale,
+                                         void* workspace, size_t workspace_bytes,
+                                         void* stream);
+
+/* Workspace bytes quest_decode_step needs on the current device (0 if the
+ * shape is unsupported). */
+QUEST_API size_t quest_decode_workspace_size(int32_t batch, int32_t h_kv, int32_t group,
+                                             int32_t head_dim, int32_t page_size,
+                                             int32_t dtype, int32_t k);
+
 /* Synchronises `stream`, returns the device error word of the current device
  * (QUEST_DEVERR_* bits) and clears it. Returns -1 if a CUDA call fails. */
 QUEST_API int32_t quest_get_device_error(void* stream);

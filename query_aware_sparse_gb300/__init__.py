@@ -58,6 +58,11 @@ def lib() -> ctypes.CDLL:
                                                ctypes.c_float, P, SZ, P]
         L.quest_attn_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32]
         L.quest_attn_workspace_size.restype = SZ
+        L.quest_decode_step.argtypes = [P, P, P, P, P, I32, I32, P, P, P, P, P, P,
+                                        ctypes.c_float, P, SZ, P]
+        L.quest_decode_step.restype = I32
+        L.quest_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I32]
+        L.quest_decode_workspace_size.restype = SZ
         L.quest_get_device_error.argtypes = [P]
         L.quest_get_device_error.restype = I32
         L.quest_status_string.argtypes = [I32]
@@ -71,6 +76,7 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_select_topk",
             "quest_sparse_decode_attn", "quest_attn_workspace_size",
+            "quest_decode_step", "quest_decode_workspace_size",
             "quest_get_device_error", "quest_status_string")
 
 
@@ -189,6 +195,41 @@ def sparse_decode_attn(cache: PagedCache, table: PageTable, q, group: int, sel_l
         _ptr(sel_phys), int(k), _ptr(out), _ptr(lse), float(sm_scale), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _stream(stream)))
     return out, lse
+
+
+def decode_workspace_size(batch, h_kv, group, head_dim, page_size, dtype, k) -> int:
+    return int(lib().quest_decode_workspace_size(batch, h_kv, group, head_dim, page_size,
+                                                 dtype_code(dtype), k))
+
+
+class DecodeStep:
+    """Buffers of quest_decode_step for a fixed problem shape: scores,
+    selections, outputs and a zero-filled workspace (reused across calls)."""
+
+    def __init__(self, cache: PagedCache, table: PageTable, group: int, k: int, device=None):
+        dev = device or cache.k_pool.device
+        B, h = table.batch, cache.h_kv
+        self.group, self.k = group, k
+        self.scores = torch.empty((h, max(table.nnz, 1)), dtype=torch.float32, device=dev)
+        self.sel = (torch.empty((B, h, k), dtype=torch.int32, device=dev),
+                    torch.empty((B, h, k), dtype=torch.int32, device=dev),
+                    torch.empty((B, h), dtype=torch.int32, device=dev))
+        self.out = torch.empty((B, h * group, cache.head_dim), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, h * group), dtype=torch.float32, device=dev)
+        n = decode_workspace_size(B, h, group, cache.head_dim, cache.page_size, cache.dtype, k)
+        if n == 0:
+            raise RuntimeError("quest_decode_step does not support this shape")
+        self.workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+
+    def __call__(self, cache: PagedCache, table: PageTable, q, k_new=None, v_new=None,
+                 sm_scale: float = 0.0, stream=None):
+        sl, sp, sc = self.sel
+        _check(lib().quest_decode_step(
+            ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(k_new), _ptr(v_new), _ptr(q),
+            int(self.group), int(self.k), _ptr(self.scores), _ptr(sl), _ptr(sp), _ptr(sc),
+            _ptr(self.out), _ptr(self.lse), float(sm_scale), _ptr(self.workspace),
+            int(self.workspace.numel()), _stream(stream)))
+        return self.out, self.lse
 
 
 def device_error(stream=None) -> int:

@@ -8,12 +8,11 @@
 // Each warp owns a ring of NST shared-memory slots; its lane 0 streams the
 // warp's pages in with 1-D bulk async copies (cp.async.bulk, completion on
 // an mbarrier): one (page, head) K block and V block are each S*d contiguous
-// elements of the pool. QK runs on FMA with lanes over d and a transposed
-// shuffle reduction over tokens; online softmax in fp32 (base-2 exponent);
-// AV accumulates in registers. The CTA merges its warps and writes one
-// partial (o, max, sum) per query head; the combine kernel merges chunks.
+// elements of the pool. The CTA merges its warps and writes one partial
+// (o, max, sum) per query head; the combine kernel merges the chunks.
 // Decode attention is a matrix-vector product per query head (G <= 8 rows
 // share a KV head), too thin for a tensor-core tile, so it stays on FMA.
+#include "attn_dev.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,86 +25,20 @@ constexpr int kMaxWarpPages = 32;
 
 template <typename T, int D, int S, int G>
 struct AttnShape {
-  static constexpr int VD = D / 32;                        // dims per lane
-  static constexpr int TT = (G * S <= 64) ? S : 64 / G;    // tokens per tile
-  static constexpr int NV = G * TT;                        // logits per tile
-  static constexpr int BLOCK_BYTES = S * D * (int)sizeof(T);  // one K (or V) page block
-  static constexpr int STAGE_BYTES = kNW * kNST * 2 * BLOCK_BYTES;
+  using W = WarpAttn<T, D, S, G>;
+  static constexpr int STAGE_BYTES = kNW * kNST * 2 * W::BLOCK_BYTES;
   static constexpr int BAR_OFF = STAGE_BYTES;
   static constexpr int LOGIT_OFF = BAR_OFF + kNW * kNST * 8;
-  static constexpr int DESC_OFF = LOGIT_OFF + kNW * NV * 4;
+  static constexpr int DESC_OFF = LOGIT_OFF + kNW * W::NV * 4;
   static constexpr int SMEM = DESC_OFF + kNW * kMaxWarpPages * 8;
   static_assert(kNW * G * (D + 2) * 4 <= STAGE_BYTES, "merge buffer must fit in the stage area");
 };
-
-// Load VD consecutive elements of T from shared memory as fp32.
-template <typename T, int VD>
-__device__ __forceinline__ void lds_row(const T* p, float (&out)[VD]);
-template <> __device__ __forceinline__ void lds_row<__half, 4>(const __half* p, float (&o)[4]) {
-  uint2 w = *reinterpret_cast<const uint2*>(p);
-  float2 a = __half22float2(*reinterpret_cast<__half2*>(&w.x));
-  float2 b = __half22float2(*reinterpret_cast<__half2*>(&w.y));
-  o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
-}
-template <> __device__ __forceinline__ void lds_row<__half, 2>(const __half* p, float (&o)[2]) {
-  float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
-  o[0] = a.x; o[1] = a.y;
-}
-template <> __device__ __forceinline__ void lds_row<float, 4>(const float* p, float (&o)[4]) {
-  float4 a = *reinterpret_cast<const float4*>(p);
-  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
-}
-template <> __device__ __forceinline__ void lds_row<float, 2>(const float* p, float (&o)[2]) {
-  float2 a = *reinterpret_cast<const float2*>(p);
-  o[0] = a.x; o[1] = a.y;
-}
-
-template <typename T, int VD>
-__device__ __forceinline__ void ldg_row(const T* p, float (&out)[VD]) {
-#pragma unroll
-  for (int v = 0; v < VD; ++v) out[v] = Elem<T>::to_f(p[v]);
-}
-
-// One halving step of the transposed butterfly: lanes with bit `o` set keep
-// the upper half of the N live values, the others the lower half; each adds
-// its partner's copy of the half it keeps.
-template <int N>
-__device__ __forceinline__ void tr_step(float* v, int lane, int o) {
-  constexpr int H = N / 2;
-  const bool up = (lane & o) != 0;
-#pragma unroll
-  for (int i = 0; i < H; ++i) {
-    const float send = up ? v[i] : v[i + H];
-    const float keep = up ? v[i + H] : v[i];
-    v[i] = keep + __shfl_xor_sync(FULL, send, o);
-  }
-}
-
-// Sum each of NV per-lane partial values over the 32 lanes. Afterwards, for
-// NV >= 32 lane l holds the sums of indices l*(NV/32) + i in v[i]; for
-// NV < 32 lane l holds the sum of index l >> (5 - log2(NV)) in v[0].
-template <int NV>
-__device__ __forceinline__ void transpose_reduce(float (&v)[NV], int lane) {
-  if constexpr (NV >= 2) tr_step<NV>(v, lane, 16);
-  if constexpr (NV >= 4) tr_step<NV / 2>(v, lane, 8);
-  if constexpr (NV >= 8) tr_step<NV / 4>(v, lane, 4);
-  if constexpr (NV >= 16) tr_step<NV / 8>(v, lane, 2);
-  if constexpr (NV >= 32) tr_step<NV / 16>(v, lane, 1);
-  if constexpr (NV < 32) {
-#pragma unroll
-    for (int o = 16 / NV; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(FULL, v[0], o);
-  }
-}
-
-template <int NV>
-struct Log2 { static constexpr int value = NV <= 1 ? 0 : 1 + Log2<NV / 2>::value; };
-template <> struct Log2<1> { static constexpr int value = 0; };
 
 template <typename T, int D, int S, int G>
 __global__ void __launch_bounds__(kNW * 32)
 attn_split_kernel(const AttnArgs a) {
   using Sh = AttnShape<T, D, S, G>;
-  constexpr int VD = Sh::VD, TT = Sh::TT, NV = Sh::NV;
+  using W = typename Sh::W;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::BAR_OFF);
   float* logits_all = reinterpret_cast<float*>(smem + Sh::LOGIT_OFF);
@@ -120,7 +53,7 @@ attn_split_kernel(const AttnArgs a) {
   const size_t sel_base = (size_t)unit * a.k;
 
   uint64_t* my_bars = bars + w * kNST;
-  float* lg = logits_all + w * NV;
+  float* lg = logits_all + w * W::NV;
   int2* desc = desc_all + w * kMaxWarpPages;
   T* my_stage = reinterpret_cast<T*>(smem) + (size_t)w * kNST * 2 * S * D;
 
@@ -159,97 +92,23 @@ attn_split_kernel(const AttnArgs a) {
     const int slot = n % kNST;
     const int pp = desc[n].x;
     T* dst = my_stage + (size_t)slot * 2 * head_block;
-    mbar_expect_tx(my_bars + slot, 2 * Sh::BLOCK_BYTES);
-    bulk_g2s(dst, kbase + (size_t)pp * page_stride, Sh::BLOCK_BYTES, my_bars + slot);
-    bulk_g2s(dst + head_block, vbase + (size_t)pp * page_stride, Sh::BLOCK_BYTES, my_bars + slot);
+    mbar_expect_tx(my_bars + slot, 2 * W::BLOCK_BYTES);
+    bulk_g2s(dst, kbase + (size_t)pp * page_stride, W::BLOCK_BYTES, my_bars + slot);
+    bulk_g2s(dst + head_block, vbase + (size_t)pp * page_stride, W::BLOCK_BYTES, my_bars + slot);
   };
   if (lane == 0)
     for (int n = 0; n < min(kNST, nv); ++n) issue(n);
 
-  // Queries of the group, pre-scaled so that exp2 gives e^(scale * q.k).
-  float q[G][VD];
-#pragma unroll
-  for (int gi = 0; gi < G; ++gi) {
-    ldg_row<T, VD>(static_cast<const T*>(a.q) + ((size_t)r * h_q + g * G + gi) * D + lane * VD, q[gi]);
-#pragma unroll
-    for (int v = 0; v < VD; ++v) q[gi][v] *= a.scale_log2;
-  }
-  float m_run[G], l_run[G], acc[G][VD];
-#pragma unroll
-  for (int gi = 0; gi < G; ++gi) {
-    m_run[gi] = -INFINITY;
-    l_run[gi] = 0.f;
-#pragma unroll
-    for (int v = 0; v < VD; ++v) acc[gi][v] = 0.f;
-  }
+  W st;
+  st.init(static_cast<const T*>(a.q) + ((size_t)r * h_q + g * G) * D, a.scale_log2, lane);
 
   for (int n = 0; n < nv; ++n) {
     const int slot = n % kNST;
-    const int valid = desc[n].y;
-    const bool ok = mbar_wait_bounded(my_bars + slot, (n / kNST) & 1);
-    if (!ok) {
+    if (!mbar_wait_bounded(my_bars + slot, (n / kNST) & 1)) {
       if (lane == 0) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
     } else {
       const T* Kb = my_stage + (size_t)slot * 2 * head_block;
-      const T* Vb = Kb + head_block;
-      for (int t0 = 0; t0 < valid; t0 += TT) {
-        float part[NV];
-#pragma unroll
-        for (int tt = 0; tt < TT; ++tt) {
-          float kr[VD];
-          lds_row<T, VD>(Kb + (size_t)(t0 + tt) * D + lane * VD, kr);
-#pragma unroll
-          for (int gi = 0; gi < G; ++gi) {
-            float s = 0.f;
-#pragma unroll
-            for (int v = 0; v < VD; ++v) s = fmaf(q[gi][v], kr[v], s);
-            part[gi * TT + tt] = s;
-          }
-        }
-        transpose_reduce<NV>(part, lane);
-        if constexpr (NV >= 32) {
-#pragma unroll
-          for (int i = 0; i < NV / 32; ++i) {
-            const int vi = lane * (NV / 32) + i;
-            lg[vi] = (t0 + vi % TT < valid) ? part[i] : -INFINITY;
-          }
-        } else {
-          constexpr int SH = 5 - Log2<NV>::value;
-          if ((lane & ((1 << SH) - 1)) == 0) {
-            const int vi = lane >> SH;
-            lg[vi] = (t0 + vi % TT < valid) ? part[0] : -INFINITY;
-          }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-          const float x = lg[gi * TT + (lane % TT)];
-          const float mt = warp_max(x);
-          const float m_new = fmaxf(m_run[gi], mt);
-          const float alpha = exp2f(m_run[gi] - m_new);
-          const float p = exp2f(x - m_new);
-          const float psum = warp_sum(lane < TT ? p : 0.f);
-          l_run[gi] = l_run[gi] * alpha + psum;
-          m_run[gi] = m_new;
-#pragma unroll
-          for (int v = 0; v < VD; ++v) acc[gi][v] *= alpha;
-          __syncwarp();
-          if (lane < TT) lg[gi * TT + lane] = p;
-        }
-        __syncwarp();
-        const int tv = min(TT, valid - t0);
-        for (int tt = 0; tt < tv; ++tt) {
-          float vr[VD];
-          lds_row<T, VD>(Vb + (size_t)(t0 + tt) * D + lane * VD, vr);
-#pragma unroll
-          for (int gi = 0; gi < G; ++gi) {
-            const float p = lg[gi * TT + tt];
-#pragma unroll
-            for (int v = 0; v < VD; ++v) acc[gi][v] = fmaf(p, vr[v], acc[gi][v]);
-          }
-        }
-        __syncwarp();
-      }
+      st.page(Kb, Kb + head_block, desc[n].y, lg, lane);
     }
     __syncwarp();
     if (lane == 0 && n + kNST < nv) {
@@ -262,40 +121,21 @@ attn_split_kernel(const AttnArgs a) {
   __syncthreads();
   float* mo = reinterpret_cast<float*>(smem);                 // [NW][G][D]
   float* ml = mo + kNW * G * D;                               // [NW][G][2]
-#pragma unroll
-  for (int gi = 0; gi < G; ++gi) {
-#pragma unroll
-    for (int v = 0; v < VD; ++v) mo[(w * G + gi) * D + lane * VD + v] = acc[gi][v];
-    if (lane == 0) {
-      ml[(w * G + gi) * 2 + 0] = m_run[gi];
-      ml[(w * G + gi) * 2 + 1] = l_run[gi];
-    }
-  }
+  st.stash(mo, ml, w, lane);
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += kNW * 32) {
-    const int gi = idx / D, col = idx % D;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kNW; ++ww) mx = fmaxf(mx, ml[(ww * G + gi) * 2]);
-    float o = 0.f, l = 0.f;
-    if (mx != -INFINITY) {
-#pragma unroll
-      for (int ww = 0; ww < kNW; ++ww) {
-        const float sc = exp2f(ml[(ww * G + gi) * 2] - mx);
-        o = fmaf(sc, mo[(ww * G + gi) * D + col], o);
-        l = fmaf(sc, ml[(ww * G + gi) * 2 + 1], l);
-      }
-    }
-    const size_t row = ((size_t)r * h_q + g * G + gi) * a.n_chunks + c;
-    a.part_o[row * D + col] = o;
-    if (col == 0) {
-      a.part_ml[row * 2 + 0] = mx;
-      a.part_ml[row * 2 + 1] = l;
-    }
-  }
+  const size_t row0 = ((size_t)r * h_q + g * G) * a.n_chunks + c;
+  merge_warps<D, G, kNW, kNW * 32>(
+      mo, ml,
+      [&](int gi, int col, float o) { a.part_o[(row0 + (size_t)gi * a.n_chunks) * D + col] = o; },
+      [&](int gi, float mx, float l) {
+        a.part_ml[(row0 + (size_t)gi * a.n_chunks) * 2 + 0] = mx;
+        a.part_ml[(row0 + (size_t)gi * a.n_chunks) * 2 + 1] = l;
+      });
 }
 
-// One warp per (request, query head): LSE merge of the chunk partials.
+// One warp per (request, query head): LSE merge of the chunk partials. The
+// chunk maxima are read lane-parallel; the weighted sum issues its loads
+// independently of each other.
 template <int D>
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const AttnArgs a) {
@@ -314,13 +154,23 @@ attn_combine_kernel(const AttnArgs a) {
   for (int v = 0; v < VD; ++v) o[v] = 0.f;
   float l = 0.f;
   if (mx != -INFINITY) {
-    for (int c = 0; c < a.n_chunks; ++c) {
-      const float mc = pml[c * 2];
-      if (mc == -INFINITY) continue;
-      const float sc = exp2f(mc - mx);
-      l = fmaf(sc, pml[c * 2 + 1], l);
+    for (int c0 = 0; c0 < a.n_chunks; c0 += 32) {
+      const int c = c0 + lane;
+      float wc = 0.f, lc = 0.f;
+      if (c < a.n_chunks) {
+        const float mc = pml[c * 2];
+        wc = mc == -INFINITY ? 0.f : exp2f(mc - mx);
+        lc = pml[c * 2 + 1];
+      }
+      l += warp_sum(wc * lc);
+      const int nc = min(32, a.n_chunks - c0);
+#pragma unroll 4
+      for (int i = 0; i < nc; ++i) {
+        const float wi = __shfl_sync(FULL, wc, i);
 #pragma unroll
-      for (int v = 0; v < VD; ++v) o[v] = fmaf(sc, po[(size_t)c * D + lane * VD + v], o[v]);
+        for (int v = 0; v < VD; ++v)
+          o[v] = fmaf(wi, po[(size_t)(c0 + i) * D + lane * VD + v], o[v]);
+      }
     }
   }
   const float inv = l > 0.f ? 1.f / l : 0.f;

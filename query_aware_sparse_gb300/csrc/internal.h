@@ -46,6 +46,34 @@ struct AttnArgs {
   unsigned* err;
 };
 
+// Fused decode step: append (optional, one token per request) + score +
+// select + attention + combine in one persistent launch.
+struct StepArgs {
+  void* k_pool; void* v_pool; void* summary;
+  const void* k_new; const void* v_new;      // [batch, h_kv, head_dim] or null
+  const void* q;
+  const int32_t* page_indptr; const int32_t* page_indices; const int32_t* seq_lens;
+  float* scores;                              // [h_kv, nnz]
+  int32_t* sel_logical; int32_t* sel_phys; int32_t* sel_count;
+  float* out; float* lse;
+  unsigned* counters;                         // [3 * units + 2], zero between calls
+  float* part_o; float* part_ml;              // [units, group, n_chunks, head_dim | 2]
+  int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype, k;
+  int32_t n_chunks, chunk_pages;
+  float scale_log2;
+  unsigned* err;
+};
+
+struct StepPlan {
+  bool ok;
+  int32_t grid, n_chunks, chunk_pages, smem;
+  size_t counters_bytes, workspace_bytes;
+};
+
+cudaError_t launch_step(const StepArgs& a, const StepPlan& p, cudaStream_t s);
+StepPlan plan_step(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
+                   int32_t page_size, int32_t dtype, int32_t k);
+
 // Split-K plan of the attention for a problem size on the current device.
 struct AttnPlan {
   int32_t n_chunks;

@@ -174,6 +174,59 @@ quest_status quest_sparse_decode_attn(const quest_cache* cache,
   return launched(quest::launch_attn(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t quest_decode_workspace_size(int32_t batch, int32_t h_kv, int32_t group,
+                                   int32_t head_dim, int32_t page_size, int32_t dtype,
+                                   int32_t k) {
+  if (batch <= 0 || h_kv <= 0 || k < 1 || !valid_group(group)) return 0;
+  if ((dtype != QUEST_F16 && dtype != QUEST_F32) || (head_dim != 64 && head_dim != 128) ||
+      (page_size != 16 && page_size != 32))
+    return 0;
+  quest::StepPlan p = quest::plan_step(batch, h_kv, group, head_dim, page_size, dtype, k);
+  return p.ok ? p.workspace_bytes : 0;
+}
+
+quest_status quest_decode_step(const quest_cache* cache, const quest_pages* pages,
+                               const void* k_new, const void* v_new, const void* q,
+                               int32_t group, int32_t k, float* scores,
+                               int32_t* sel_logical, int32_t* sel_phys, int32_t* sel_count,
+                               float* out, float* lse, float sm_scale, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  quest_status st = check_cache(cache);
+  if (st != QUEST_OK) return st;
+  if ((st = check_pages(pages, true)) != QUEST_OK) return st;
+  if (!valid_group(group)) return QUEST_ERR_UNSUPPORTED;
+  if (k < 1) return QUEST_ERR_INVALID_ARG;
+  if (pages->batch == 0) return QUEST_OK;
+  if (!q || !scores || !sel_logical || !sel_phys || !sel_count || !out || !aligned16(q))
+    return QUEST_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return QUEST_ERR_INVALID_ARG;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return QUEST_ERR_INVALID_ARG;
+  quest::StepPlan plan = quest::plan_step(pages->batch, cache->h_kv, group, cache->head_dim,
+                                          cache->page_size, cache->dtype, k);
+  if (!plan.ok) return QUEST_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
+    return QUEST_ERR_WORKSPACE;
+  quest::StepArgs a{};
+  a.k_pool = cache->k_pool; a.v_pool = cache->v_pool; a.summary = cache->summary;
+  a.k_new = k_new; a.v_new = v_new; a.q = q;
+  a.page_indptr = pages->page_indptr; a.page_indices = pages->page_indices;
+  a.seq_lens = pages->seq_lens;
+  a.scores = scores; a.sel_logical = sel_logical; a.sel_phys = sel_phys; a.sel_count = sel_count;
+  a.out = out; a.lse = lse;
+  a.counters = static_cast<unsigned*>(workspace);
+  const size_t rows = (size_t)pages->batch * cache->h_kv * group * plan.n_chunks;
+  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counters_bytes);
+  a.part_ml = a.part_o + rows * cache->head_dim;
+  a.batch = pages->batch; a.nnz = pages->nnz; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
+  a.group = group; a.page_size = cache->page_size; a.head_dim = cache->head_dim;
+  a.dtype = cache->dtype; a.k = k; a.n_chunks = plan.n_chunks; a.chunk_pages = plan.chunk_pages;
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)cache->head_dim);
+  a.scale_log2 = scale * quest::LOG2E;
+  a.err = err_ptr();
+  if (!a.err) return QUEST_ERR_CUDA;
+  return launched(quest::launch_step(a, plan, static_cast<cudaStream_t>(stream)));
+}
+
 int32_t quest_get_device_error(void* stream) {
   unsigned* p = err_ptr();
   if (!p) return -1;

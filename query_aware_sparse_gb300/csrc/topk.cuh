@@ -1,0 +1,195 @@
+// Block-wide fixed-budget Top-K over one (request, KV head) row of page
+// scores (Quest page Fig. 1, §1.1, §2): the K largest scores, ties to the
+// lower page index, emitted in ascending page order. Used by the standalone
+// select kernel and by the fused decode step.
+//
+// Scores map to order-preserving 32-bit keys (-0 folded onto +0). The block
+// first reduces min and max: bits above the highest bit where they differ
+// are common to every key, so the MSB-first radix select (8-bit digits,
+// shared-memory histogram) starts below them, and stops early once the
+// digit bucket holding the K-th key is taken whole. A block scan in page
+// order then emits the winners.
+#pragma once
+
+#include "common.cuh"
+
+namespace quest {
+
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t x = __float_as_uint(f == 0.f ? 0.f : f);   // -0 -> +0
+  return x ^ ((x & 0x80000000u) ? 0xffffffffu : 0x80000000u);
+}
+
+template <int NT>
+struct TopkSmem {
+  uint32_t hist[256];
+  uint32_t red[2][NT / 32];
+  unsigned long long scan[NT / 32];
+  uint32_t digit, krem, done;
+};
+
+// Exclusive block scan of a 64-bit value.
+template <int NT>
+__device__ __forceinline__ unsigned long long topk_excl_scan(unsigned long long v,
+                                                             TopkSmem<NT>& sm) {
+  constexpr int NWP = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    unsigned long long t = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sm.scan[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = lane < NWP ? sm.scan[lane] : 0ull;
+    unsigned long long wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      unsigned long long t = __shfl_up_sync(FULL, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < NWP) sm.scan[lane] = wi - w;
+  }
+  __syncthreads();
+  const unsigned long long r = sm.scan[warp] + incl - v;
+  __syncthreads();   // scan[] may be reused right after
+  return r;
+}
+
+// Top-K of P scores `sc` (global) for one row. `keys` is shared memory for up
+// to `cap` keys (P > cap re-reads the scores from global memory each pass).
+// Writes out_logical[0..K), out_phys[0..K) (-1 padded), *out_count.
+// `phys_of` maps a page index of the row to its physical page.
+// All NT threads of the block must call it (it synchronises the block).
+template <int NT, typename PhysOf>
+__device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t* keys, int cap,
+                           TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
+                           int32_t* out_count, PhysOf phys_of) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NWP = NT / 32;
+
+  if (P <= K) {                     // every scored page is selected
+    for (int i = tid; i < K; i += NT) {
+      out_logical[i] = i < P ? i : -1;
+      out_phys[i] = i < P ? phys_of(i) : -1;
+    }
+    if (tid == 0) *out_count = P;
+    return;
+  }
+  const bool cached = P <= cap;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int i = tid; i < P; i += NT) {
+    const uint32_t k = score_key(__ldcg(sc + i));
+    if (cached) keys[i] = k;
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(FULL, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(FULL, kmax, o));
+  }
+  if (lane == 0) { sm.red[0][warp] = kmin; sm.red[1][warp] = kmax; }
+  for (int i = tid; i < 256; i += NT) sm.hist[i] = 0;
+  __syncthreads();
+  kmin = sm.red[0][0];
+  kmax = sm.red[1][0];
+#pragma unroll
+  for (int w = 1; w < NWP; ++w) { kmin = min(kmin, sm.red[0][w]); kmax = max(kmax, sm.red[1][w]); }
+  auto key_at = [&](int i) -> uint32_t { return cached ? keys[i] : score_key(__ldcg(sc + i)); };
+
+  // Radix select below the common prefix of min and max.
+  uint32_t T, need;
+  bool ge_mode;            // select key >= T (bucket taken whole) vs the tie rule
+  if (kmin == kmax) {
+    T = kmin; need = K; ge_mode = false;
+  } else {
+    int hi = 31 - __clz(kmin ^ kmax);           // highest differing bit
+    uint32_t prefix = kmin & ~((hi == 31) ? 0xffffffffu : ((2u << hi) - 1u));
+    uint32_t krem = K;
+    ge_mode = false;
+    T = 0; need = 0;
+    while (true) {
+      const int shift = max(hi - 7, 0);
+      const int nbits = hi - shift + 1;
+      const uint32_t dmask = (1u << nbits) - 1u;
+      const uint32_t hi_mask = (hi == 31) ? 0u : ~((2u << hi) - 1u);
+      for (int base = 0; base < P; base += NT) {
+        const int i = base + tid;
+        if (i < P) {
+          const uint32_t k = key_at(i);
+          if ((k & hi_mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t h[8], tot = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { h[j] = sm.hist[lane * 8 + j]; tot += h[j]; }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          uint32_t t = __shfl_down_sync(FULL, incl, o);
+          if (lane + o < 32) incl += t;
+        }
+        uint32_t cum = incl - tot;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+          if (cum < krem && krem <= cum + h[j]) {
+            sm.digit = lane * 8 + j;
+            sm.krem = krem - cum;
+            sm.done = (h[j] == krem - cum) ? 1u : 0u;   // bucket taken whole
+          }
+          cum += h[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sm.hist[lane * 8 + j] = 0;   // ready for the next pass
+      }
+      __syncthreads();
+      prefix |= sm.digit << shift;
+      krem = sm.krem;
+      if (sm.done || shift == 0) {
+        T = prefix;
+        need = krem;
+        ge_mode = sm.done && shift > 0;
+        break;
+      }
+      hi = shift - 1;
+    }
+    __syncthreads();   // everyone has read sm.digit/krem/done
+  }
+
+  // Stable compaction in page order.
+  const int per = (P + NT - 1) / NT;
+  const int c0 = min(P, tid * per), c1 = min(P, c0 + per);
+  uint32_t gt = 0, eq = 0;
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t k = key_at(i);
+    if (ge_mode) gt += k >= T;
+    else { gt += k > T; eq += k == T; }
+  }
+  const unsigned long long ex = topk_excl_scan<NT>(((unsigned long long)gt << 32) | eq, sm);
+  uint32_t gt_b = (uint32_t)(ex >> 32), eq_b = (uint32_t)ex;
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t k = key_at(i);
+    int pos = -1;
+    if (ge_mode) {
+      if (k >= T) pos = gt_b++;
+    } else if (k > T) {
+      pos = gt_b + min(eq_b, need);
+      ++gt_b;
+    } else if (k == T) {
+      if (eq_b < need) pos = gt_b + eq_b;
+      ++eq_b;
+    }
+    if (pos >= 0 && pos < K) {
+      out_logical[pos] = i;
+      out_phys[pos] = phys_of(i);
+    }
+  }
+  if (tid == 0) *out_count = K;
+}
+
+}  // namespace quest

@@ -1,0 +1,145 @@
+"""Fused decode step (quest_decode_step): every output against the oracle's
+chain on the same inputs — summaries and pool bit-exact, scores within the
+score tolerance, selections under the near-tie rule, attention within 2e-3 —
+over several consecutive steps (the workspace counters must come back to
+zero), with and without the append, MHA and GQA, page sizes 16 and 32."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import quest_oracle as qo
+from tests._cases import (attn_close, check_selection, dev_i32, gpu_table, np_of,
+                          score_tol)
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefilled(w, lens, seed, spare=4):
+    """Pools holding every token but the last of each request (host+device),
+    and the tokens themselves."""
+    import query_aware_sparse_gb300 as qs
+    table = wl.make_page_table(lens, w.page_size, seed=seed, permute=True,
+                               spare_pages=spare, reserve_tokens=2 * w.page_size)
+    k_tok, v_tok, ind = wl.tokens_for_table(w, table)
+    return table, k_tok, v_tok, ind
+
+
+def _run(w, lens, steps, seed, append=True):
+    import query_aware_sparse_gb300 as qs
+    lens = np.asarray(lens)
+    full = lens + (steps if append else 0)
+    table, k_tok, v_tok, ind = _prefilled(w, full, seed)
+    h, d, S, B = w.h_kv, w.head_dim, w.page_size, len(lens)
+    start = lens.copy()
+    # both sides start from the first `lens` tokens of each request
+    kp, vp, sm = wl.empty_pool(table, h, d, w.dtype, device="cuda")
+    okp, ovp, osm = (np_of(x) for x in wl.empty_pool(table, h, d, w.dtype))
+    rows = np.concatenate([np.arange(ind[r], ind[r] + start[r]) for r in range(B)])
+    pre_ind = np.concatenate([[0], np.cumsum(start)]).astype(np.int32)
+    kn, vn = k_tok[rows].contiguous(), v_tok[rows].contiguous()
+    cache = qs.PagedCache(kp, vp, sm)
+    gt = gpu_table(table, seq_lens=start.astype(np.int32))
+    qs.append_kv(cache, gt, kn.cuda(), vn.cuda(), dev_i32(pre_ind), dev_i32(np.zeros(B)))
+    qo.append_kv(okp, ovp, osm, table.page_indptr, table.page_indices, np.zeros(B, np.int32),
+                 pre_ind, np_of(kn), np_of(vn))
+    step = None
+    cur = start.copy()
+    for s in range(steps):
+        if append:
+            cur = cur + 1
+            pos = ind[:-1] + cur - 1
+            k1, v1 = k_tok[pos].contiguous(), v_tok[pos].contiguous()
+        q = wl.queries(w, cur - 1, step=s)
+        tb = wl.PageTable(table.page_indptr, table.page_indices, cur.astype(np.int32),
+                          table.n_phys, S)
+        gtab = gpu_table(tb)
+        if step is None:
+            step = qs.DecodeStep(cache, gtab, w.group, w.k)
+        if append:
+            step(cache, gtab, q.cuda(), k1.cuda(), v1.cuda())
+            qo.append_kv(okp, ovp, osm, table.page_indptr, table.page_indices,
+                         (cur - 1).astype(np.int32), np.arange(B + 1), np_of(k1), np_of(v1))
+        else:
+            step(cache, gtab, q.cuda())
+        assert qs.device_error() == 0
+        # counters are back at zero after every call
+        assert int(step.workspace[:3 * B * h * 4 + 8].count_nonzero()) == 0
+        gsm = np_of(cache.summary)
+        for r in range(B):
+            P = -(-int(cur[r]) // S)
+            phys = table.page_indices[table.page_indptr[r]:table.page_indptr[r] + P]
+            assert np.array_equal(gsm[phys].view(np.uint8), osm[phys].view(np.uint8))
+            if append:
+                pp = table.page_indices[table.page_indptr[r] + (cur[r] - 1) // S]
+                slot = (cur[r] - 1) % S
+                assert np.array_equal(np_of(cache.k_pool[pp, :, slot]).view(np.uint8),
+                                      okp[pp, :, slot].view(np.uint8))
+        ref_scores = qo.score_pages(np_of(q), osm, table.page_indptr, table.page_indices, w.group)
+        tol = score_tol(np_of(q), osm, tb, w.group)
+        got = np_of(step.scores)
+        for r in range(B):
+            lo = table.page_indptr[r]
+            P = -(-int(cur[r]) // S)
+            assert np.all(np.abs(got[:, lo:lo + P] - ref_scores[:, lo:lo + P]) <= tol[:, lo:lo + P])
+            assert np.all(got[:, lo + P:table.page_indptr[r + 1]] == -np.inf)
+        sl, sp, cnt = (np_of(x) for x in step.sel)
+        check_selection(sl, cnt, ref_scores, tol, tb, w.k,
+                        [(r, g) for r in range(B) for g in range(h)])
+        ref_sel, _, _ = qo.select_topk(np.where(np.isfinite(ref_scores), ref_scores, -np.inf),
+                                       table.page_indptr, table.page_indices, w.k)
+        for r in range(B):
+            lo = table.page_indptr[r]
+            P = -(-int(cur[r]) // S)
+            for g in range(h):
+                ch = qo.topk_pages(ref_scores[g, lo:lo + P], w.k)
+                ref_sel[r, g] = -1
+                ref_sel[r, g, :len(ch)] = ch
+        assert np.array_equal(sp[sl >= 0], table.page_indices[(table.page_indptr[:-1, None, None] + sl)[sl >= 0]])
+        use = ref_sel if np.array_equal(sl, ref_sel) else sl
+        ro, rl = qo.sparse_attention(np_of(q), okp, ovp, table.page_indptr, table.page_indices,
+                                     cur.astype(np.int32), use, w.group)
+        o, lse = np_of(step.out), np_of(step.lse)
+        ok, rel = attn_close(o, ro)
+        assert ok.all(), rel.max()
+        fin = np.isfinite(rl)
+        assert np.allclose(lse[fin], rl[fin], rtol=1e-4, atol=1e-4)
+        assert np.all(lse[~fin] == -np.inf) and np.all(o[~fin] == 0)
+
+
+def _w(name, **kw):
+    base = dict(batch=1, h_kv=4, group=1, head_dim=128, page_size=16, k=16,
+                dtype=torch.float16, seed=500)
+    base.update(kw)
+    return wl.Workload(name, **base)
+
+
+def test_step_mha_crosses_page_boundaries():
+    # 30 -> 31, 32 (page full), 33 (fresh page: slot 0), 34
+    _run(_w("mha", batch=3, h_kv=4), [30, 1, 200], steps=4, seed=1)
+
+
+@pytest.mark.parametrize("group", [2, 4, 8])
+def test_step_gqa_ragged(group):
+    _run(_w("gqa", batch=5, h_kv=2, group=group, k=24), [1, 15, 16, 17, 900], steps=2,
+         seed=2 + group)
+
+
+def test_step_page32_fp16():
+    _run(_w("p32", batch=2, h_kv=3, page_size=32, k=8), [31, 500], steps=3, seed=7)
+
+
+def test_step_fp32_d64():
+    _run(_w("f32", batch=2, h_kv=2, head_dim=64, dtype=torch.float32, k=8), [1000, 63],
+         steps=2, seed=8)
+
+
+def test_step_without_append_and_k_above_pages():
+    _run(_w("noapp", batch=3, h_kv=2, k=40), [100, 700, 5], steps=2, seed=9, append=False)
+
+
+def test_step_many_units():
+    # more (request, head) units than select workers and CTAs per head
+    _run(_w("many", batch=24, h_kv=8, group=1, k=8, head_dim=64), list(range(10, 250, 10)),
+         steps=1, seed=10)
