@@ -224,9 +224,9 @@ QUEST_API quest_status quest_decode_step(const quest_cache* cache, const quest_p
                                          void* workspace, size_t workspace_bytes,
                                          void* stream);
 
-/* Workspace bytes quest_decode_step needs on the current device (0 if the
- * shape is unsupported). */
-QUEST_API size_t quest_decode_workspace_size(int32_t batch, int32_t h_kv, int32_t group,
+/* Workspace bytes quest_decode_step needs on the current device for a page
+ * table of nnz entries (0 if the shape is unsupported). */
+QUEST_API size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group,
                                              int32_t head_dim, int32_t page_size,
                                              int32_t dtype, int32_t k);
 

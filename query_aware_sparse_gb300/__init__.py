@@ -61,7 +61,7 @@ def lib() -> ctypes.CDLL:
         L.quest_decode_step.argtypes = [P, P, P, P, P, I32, I32, P, P, P, P, P, P,
                                         ctypes.c_float, P, SZ, P]
         L.quest_decode_step.restype = I32
-        L.quest_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I32]
+        L.quest_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32]
         L.quest_decode_workspace_size.restype = SZ
         L.quest_get_device_error.argtypes = [P]
         L.quest_get_device_error.restype = I32
@@ -197,8 +197,8 @@ def sparse_decode_attn(cache: PagedCache, table: PageTable, q, group: int, sel_l
     return out, lse
 
 
-def decode_workspace_size(batch, h_kv, group, head_dim, page_size, dtype, k) -> int:
-    return int(lib().quest_decode_workspace_size(batch, h_kv, group, head_dim, page_size,
+def decode_workspace_size(batch, nnz, h_kv, group, head_dim, page_size, dtype, k) -> int:
+    return int(lib().quest_decode_workspace_size(batch, nnz, h_kv, group, head_dim, page_size,
                                                  dtype_code(dtype), k))
 
 
@@ -216,7 +216,8 @@ class DecodeStep:
                     torch.empty((B, h), dtype=torch.int32, device=dev))
         self.out = torch.empty((B, h * group, cache.head_dim), dtype=torch.float32, device=dev)
         self.lse = torch.empty((B, h * group), dtype=torch.float32, device=dev)
-        n = decode_workspace_size(B, h, group, cache.head_dim, cache.page_size, cache.dtype, k)
+        n = decode_workspace_size(B, table.nnz, h, group, cache.head_dim, cache.page_size,
+                                  cache.dtype, k)
         if n == 0:
             raise RuntimeError("quest_decode_step does not support this shape")
         self.workspace = torch.zeros(n, dtype=torch.uint8, device=dev)

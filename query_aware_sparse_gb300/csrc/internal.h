@@ -56,7 +56,8 @@ struct StepArgs {
   float* scores;                              // [h_kv, nnz]
   int32_t* sel_logical; int32_t* sel_phys; int32_t* sel_count;
   float* out; float* lse;
-  unsigned* counters;                         // [3 * units + 2], zero between calls
+  unsigned* counters;                         // [4 + 2 * units], see step.cu
+  unsigned long long* tagged;                 // [h_kv, nnz] score bits | call tag << 32
   float* part_o; float* part_ml;              // [units, group, n_chunks, head_dim | 2]
   int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype, k;
   int32_t n_chunks, chunk_pages;
@@ -67,11 +68,11 @@ struct StepArgs {
 struct StepPlan {
   bool ok;
   int32_t grid, n_chunks, chunk_pages, smem;
-  size_t counters_bytes, workspace_bytes;
+  size_t counters_bytes, tagged_bytes, workspace_bytes;
 };
 
 cudaError_t launch_step(const StepArgs& a, const StepPlan& p, cudaStream_t s);
-StepPlan plan_step(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
+StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int32_t head_dim,
                    int32_t page_size, int32_t dtype, int32_t k);
 
 // Split-K plan of the attention for a problem size on the current device.

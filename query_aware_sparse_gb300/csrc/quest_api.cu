@@ -174,14 +174,14 @@ quest_status quest_sparse_decode_attn(const quest_cache* cache,
   return launched(quest::launch_attn(a, static_cast<cudaStream_t>(stream)));
 }
 
-size_t quest_decode_workspace_size(int32_t batch, int32_t h_kv, int32_t group,
+size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group,
                                    int32_t head_dim, int32_t page_size, int32_t dtype,
                                    int32_t k) {
-  if (batch <= 0 || h_kv <= 0 || k < 1 || !valid_group(group)) return 0;
+  if (batch <= 0 || nnz < 0 || h_kv <= 0 || k < 1 || !valid_group(group)) return 0;
   if ((dtype != QUEST_F16 && dtype != QUEST_F32) || (head_dim != 64 && head_dim != 128) ||
       (page_size != 16 && page_size != 32))
     return 0;
-  quest::StepPlan p = quest::plan_step(batch, h_kv, group, head_dim, page_size, dtype, k);
+  quest::StepPlan p = quest::plan_step(batch, nnz, h_kv, group, head_dim, page_size, dtype, k);
   return p.ok ? p.workspace_bytes : 0;
 }
 
@@ -201,8 +201,8 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
     return QUEST_ERR_INVALID_ARG;
   if ((k_new == nullptr) != (v_new == nullptr)) return QUEST_ERR_INVALID_ARG;
   if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return QUEST_ERR_INVALID_ARG;
-  quest::StepPlan plan = quest::plan_step(pages->batch, cache->h_kv, group, cache->head_dim,
-                                          cache->page_size, cache->dtype, k);
+  quest::StepPlan plan = quest::plan_step(pages->batch, pages->nnz, cache->h_kv, group,
+                                          cache->head_dim, cache->page_size, cache->dtype, k);
   if (!plan.ok) return QUEST_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
     return QUEST_ERR_WORKSPACE;
@@ -214,8 +214,11 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   a.scores = scores; a.sel_logical = sel_logical; a.sel_phys = sel_phys; a.sel_count = sel_count;
   a.out = out; a.lse = lse;
   a.counters = static_cast<unsigned*>(workspace);
+  a.tagged = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
+                                                   plan.counters_bytes);
   const size_t rows = (size_t)pages->batch * cache->h_kv * group * plan.n_chunks;
-  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counters_bytes);
+  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counters_bytes +
+                                      plan.tagged_bytes);
   a.part_ml = a.part_o + rows * cache->head_dim;
   a.batch = pages->batch; a.nnz = pages->nnz; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
   a.group = group; a.page_size = cache->page_size; a.head_dim = cache->head_dim;

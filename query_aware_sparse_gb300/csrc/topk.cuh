@@ -58,15 +58,14 @@ __device__ __forceinline__ unsigned long long topk_excl_scan(unsigned long long 
   return r;
 }
 
-// Top-K of P scores `sc` (global) for one row. `keys` is shared memory for up
-// to `cap` keys (P > cap re-reads the scores from global memory each pass).
-// Writes out_logical[0..K), out_phys[0..K) (-1 padded), *out_count.
-// `phys_of` maps a page index of the row to its physical page.
-// All NT threads of the block must call it (it synchronises the block).
-template <int NT, typename PhysOf>
-__device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t* keys, int cap,
-                           TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
-                           int32_t* out_count, PhysOf phys_of) {
+// Top-K of the P keys of one row, read through `key_at(i)` (shared memory or
+// global). Writes out_logical[0..K), out_phys[0..K) (-1 padded), *out_count.
+// `phys_of` maps a page index of the row to its physical page. All NT
+// threads of the block must call it (it synchronises the block).
+template <int NT, typename KeyAt, typename PhysOf>
+__device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm,
+                                int32_t* out_logical, int32_t* out_phys, int32_t* out_count,
+                                PhysOf phys_of) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWP = NT / 32;
 
@@ -78,11 +77,9 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
     if (tid == 0) *out_count = P;
     return;
   }
-  const bool cached = P <= cap;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
   for (int i = tid; i < P; i += NT) {
-    const uint32_t k = score_key(__ldcg(sc + i));
-    if (cached) keys[i] = k;
+    const uint32_t k = key_at(i);
     kmin = min(kmin, k);
     kmax = max(kmax, k);
   }
@@ -98,7 +95,6 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
   kmax = sm.red[1][0];
 #pragma unroll
   for (int w = 1; w < NWP; ++w) { kmin = min(kmin, sm.red[0][w]); kmax = max(kmax, sm.red[1][w]); }
-  auto key_at = [&](int i) -> uint32_t { return cached ? keys[i] : score_key(__ldcg(sc + i)); };
 
   // Radix select below the common prefix of min and max.
   uint32_t T, need;
@@ -190,6 +186,25 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
     }
   }
   if (tid == 0) *out_count = K;
+}
+
+// Top-K of P fp32 scores `sc` (global) for one row; `keys` caches up to `cap`
+// keys in shared memory (a longer row re-reads the scores from L2 per pass).
+template <int NT, typename PhysOf>
+__device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t* keys, int cap,
+                           TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
+                           int32_t* out_count, PhysOf phys_of) {
+  const bool cached = P <= cap && P > K;
+  if (cached) {
+    for (int i = threadIdx.x; i < P; i += NT) keys[i] = score_key(__ldcg(sc + i));
+    __syncthreads();
+  }
+  if (cached)
+    block_topk_keys<NT>(P, K, [keys](int i) { return keys[i]; }, sm, out_logical, out_phys,
+                        out_count, phys_of);
+  else
+    block_topk_keys<NT>(P, K, [sc](int i) { return score_key(__ldcg(sc + i)); }, sm,
+                        out_logical, out_phys, out_count, phys_of);
 }
 
 }  // namespace quest
