@@ -230,6 +230,18 @@ QUEST_API size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t
                                              int32_t head_dim, int32_t page_size,
                                              int32_t dtype, int32_t k);
 
+/* Phase trace of quest_decode_step (profiling aid, off by default): with a
+ * device buffer of at least 16 * max_ctas uint64 set, each later call whose
+ * grid has at most max_ctas CTAs writes, per CTA, 16 %globaltimer stamps (ns):
+ * [0] start, [1] scoring done, [2] selection done, [3..5] attention round 0
+ * start / pages done / merged, [6..8] the same for round 1, [9] exit,
+ * [10..15] completion of the CTA's 1st..6th select. NULL turns it off.
+ * Returns the grid size the current device uses for these shapes (0 if the
+ * shape is unsupported). */
+QUEST_API int32_t quest_set_trace(void* device_buffer, int32_t max_ctas, int32_t batch,
+                                  int32_t h_kv, int32_t group, int32_t head_dim,
+                                  int32_t page_size, int32_t dtype, int32_t k);
+
 /* Synchronises `stream`, returns the device error word of the current device
  * (QUEST_DEVERR_* bits) and clears it. Returns -1 if a CUDA call fails. */
 QUEST_API int32_t quest_get_device_error(void* stream);

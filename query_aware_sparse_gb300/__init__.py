@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.quest_decode_step.restype = I32
         L.quest_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32]
         L.quest_decode_workspace_size.restype = SZ
+        L.quest_set_trace.argtypes = [P, I32, I32, I32, I32, I32, I32, I32, I32]
+        L.quest_set_trace.restype = I32
         L.quest_get_device_error.argtypes = [P]
         L.quest_get_device_error.restype = I32
         L.quest_status_string.argtypes = [I32]
@@ -76,7 +78,7 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_select_topk",
             "quest_sparse_decode_attn", "quest_attn_workspace_size",
-            "quest_decode_step", "quest_decode_workspace_size",
+            "quest_decode_step", "quest_decode_workspace_size", "quest_set_trace",
             "quest_get_device_error", "quest_status_string")
 
 
@@ -231,6 +233,20 @@ class DecodeStep:
             _ptr(self.out), _ptr(self.lse), float(sm_scale), _ptr(self.workspace),
             int(self.workspace.numel()), _stream(stream)))
         return self.out, self.lse
+
+
+TRACE_NAMES = ("start", "scored", "selected", "r0_start", "r0_pages", "r0_merged",
+               "r1_start", "r1_pages", "r1_merged", "exit")
+
+
+def set_trace(buffer, max_ctas=0, batch=0, h_kv=0, group=1, head_dim=128, page_size=16,
+              dtype=torch.float16, k=1) -> int:
+    """quest_set_trace: per-CTA phase stamps of later decode steps into
+    `buffer` (uint64 device tensor of 16 * max_ctas entries); None disables.
+    Returns the grid size used for the given shape."""
+    return int(lib().quest_set_trace(_ptr(buffer), int(max_ctas), int(batch), int(h_kv),
+                                     int(group), int(head_dim), int(page_size),
+                                     dtype_code(dtype), int(k)))
 
 
 def device_error(stream=None) -> int:

@@ -111,6 +111,42 @@ template <> __device__ __forceinline__ void unpack16<__half>(uint4 v, float* out
   }
 }
 
+// Page upper-bound contribution of one 16-byte vector of dims (Quest page
+// §1.1 eq (2)): sum_j max(q_j m_j, q_j M_j). Since m_j <= M_j, the larger
+// product is q_j M_j when q_j >= 0 and q_j m_j otherwise, so each dim costs a
+// select and one FMA. For fp16 the select works on packed halves (sign mask)
+// and the products of two fp16 values are exact in fp32.
+template <typename T> __device__ __forceinline__ float bound16(uint4 q, uint4 m, uint4 M);
+template <> __device__ __forceinline__ float bound16<__half>(uint4 q, uint4 m, uint4 M) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+  const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
+  const uint32_t Mw[4] = {M.x, M.y, M.z, M.w};
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t mk = ((~qw[i] & 0x80008000u) >> 15) * 0xffffu;   // halves with q >= 0
+    const uint32_t xw = (Mw[i] & mk) | (mw[i] & ~mk);
+    const float2 qf = __half22float2(*reinterpret_cast<const __half2*>(&qw[i]));
+    const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xw));
+    s = fmaf(qf.x, xf.x, s);
+    s = fmaf(qf.y, xf.y, s);
+  }
+  return s;
+}
+template <> __device__ __forceinline__ float bound16<float>(uint4 q, uint4 m, uint4 M) {
+  const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+  const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
+  const uint32_t Mw[4] = {M.x, M.y, M.z, M.w};
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float qf = __uint_as_float(qw[i]);
+    const float xf = __uint_as_float((qw[i] & 0x80000000u) ? mw[i] : Mw[i]);
+    s = fmaf(qf, xf, s);
+  }
+  return s;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier + 1-D bulk async copy (global -> shared), CTA-local.
 // ---------------------------------------------------------------------------
@@ -139,11 +175,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
-// Bounded wait: returns false (and the caller reports) if the limit is hit.
+// try_wait that lets the thread sleep (up to `ns`) until the phase completes,
+// instead of spinning on the barrier.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(ns) : "memory");
+  return ok != 0;
+}
+// Bounded wait: returns false (and the caller reports) if the limit is hit
+// (2^21 tries of up to 1 us each).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < (1u << 21); ++i)
+    if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
   return false;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,
                                          uint64_t* bar) {

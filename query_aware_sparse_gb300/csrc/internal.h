@@ -62,6 +62,7 @@ struct StepArgs {
   int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype, k;
   int32_t n_chunks, chunk_pages;
   float scale_log2;
+  unsigned long long* trace;                  // [grid, 16] phase stamps, or null
   unsigned* err;
 };
 

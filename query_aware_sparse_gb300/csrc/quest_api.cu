@@ -54,6 +54,9 @@ quest_status check_pages(const quest_pages* p, bool need_seq_lens) {
 
 bool valid_group(int32_t g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
+unsigned long long* g_trace = nullptr;      // quest_set_trace buffer (device)
+int32_t g_trace_ctas = 0;
+
 quest_status launched(cudaError_t e) { return e == cudaSuccess ? QUEST_OK : QUEST_ERR_CUDA; }
 
 }  // namespace
@@ -225,9 +228,20 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   a.dtype = cache->dtype; a.k = k; a.n_chunks = plan.n_chunks; a.chunk_pages = plan.chunk_pages;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)cache->head_dim);
   a.scale_log2 = scale * quest::LOG2E;
+  a.trace = (g_trace && plan.grid <= g_trace_ctas) ? g_trace : nullptr;
   a.err = err_ptr();
   if (!a.err) return QUEST_ERR_CUDA;
   return launched(quest::launch_step(a, plan, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t quest_set_trace(void* device_buffer, int32_t max_ctas, int32_t batch, int32_t h_kv,
+                        int32_t group, int32_t head_dim, int32_t page_size, int32_t dtype,
+                        int32_t k) {
+  g_trace = static_cast<unsigned long long*>(device_buffer);
+  g_trace_ctas = device_buffer ? max_ctas : 0;
+  if (batch <= 0 || h_kv <= 0 || k < 1 || !valid_group(group)) return 0;
+  quest::StepPlan p = quest::plan_step(batch, 0, h_kv, group, head_dim, page_size, dtype, k);
+  return p.ok ? p.grid : 0;
 }
 
 int32_t quest_get_device_error(void* stream) {

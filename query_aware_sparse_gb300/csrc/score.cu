@@ -35,13 +35,12 @@ __device__ __forceinline__ int find_request(const int32_t* indptr, int lo, int h
 }
 
 template <typename T, int D, int G>
-__device__ __forceinline__ void load_q(const ScoreArgs& a, int r, int g, int sub,
-                                       float (&q)[G][Elem<T>::kVec]) {
+__device__ __forceinline__ void load_q(const ScoreArgs& a, int r, int g, int sub, uint4 (&q)[G]) {
   constexpr int VEC = Elem<T>::kVec;
   const T* qp = static_cast<const T*>(a.q) +
                 ((size_t)r * a.h_kv * G + (size_t)g * G) * D + sub * VEC;
 #pragma unroll
-  for (int gi = 0; gi < G; ++gi) unpack16<T>(ld_nc_v4(qp + (size_t)gi * D), q[gi]);
+  for (int gi = 0; gi < G; ++gi) q[gi] = ld_nc_v4(qp + (size_t)gi * D);
 }
 
 template <typename T, int D, int G>
@@ -66,7 +65,7 @@ score_kernel(const ScoreArgs a) {
   const int sub = lane % LPP;       // which 16-byte column of the page
   const int pw = lane / LPP;        // which page of the warp step
 
-  float q[G][VEC];
+  uint4 q[G];
   int cur_r = rfirst;
   load_q<T, D, G>(a, cur_r, g, sub, q);
 
@@ -106,15 +105,10 @@ score_kernel(const ScoreArgs a) {
       cur_r = er[u];
       load_q<T, D, G>(a, cur_r, g, sub, q);
     }
-    float m[VEC], M[VEC];
-    unpack16<T>(vm[u], m);
-    unpack16<T>(vM[u], M);
     float best = -INFINITY;
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) {
-      float s = 0.f;
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) s += fmaxf(q[gi][v] * m[v], q[gi][v] * M[v]);
+      float s = live[u] ? bound16<T>(q[gi], vm[u], vM[u]) : 0.f;
 #pragma unroll
       for (int o = 1; o < LPP; o <<= 1) s += __shfl_xor_sync(FULL, s, o);
       best = fmaxf(best, s);

@@ -44,13 +44,13 @@ namespace {
 
 constexpr int kNT = 256;              // threads per CTA
 constexpr int kNW = kNT / 32;
-constexpr int kNSS = 4;               // score ring stages (cp.async groups)
+constexpr int kPD = 3;                // scoring software-pipeline depth (items)
 constexpr int kKeysCap = 4096;        // selector keys cached in shared memory
-constexpr int kMaxSelectCtas = 16;    // select workers (no scoring)
 constexpr int kSliceCap = 1024;       // slice pages whose metadata is staged at once
 constexpr int kQBytes = 16384;        // queries of the slice's requests kept in smem
-constexpr int kRounds = 2;            // attention rounds
+constexpr int kRounds = 1;            // attention rounds
 constexpr int kMaxSeg = 4;            // unit segments per attention pass (G = 1)
+constexpr int kTraceSlots = 16;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem)), "l"(gmem)
@@ -89,13 +89,16 @@ template <typename T, int D, int S, int G>
 struct StepShape {
   using W = WarpAttn<T, D, S, G>;
   static constexpr int VEC = Elem<T>::kVec;
-  static constexpr int LPP = D / VEC;                 // lanes per page when scoring
-  static constexpr int PB = kNT / LPP;                // pages per score round
   static constexpr int NST = 1;                       // attention slots per warp
   static constexpr int MAXSEG = kMaxSeg / G > 0 ? kMaxSeg / G : 1;
+  // scoring: VPL 16-byte vectors of m (and of M) per lane, LPP lanes per
+  // (page, head) item, IPR items per round
+  static constexpr int VPL = G == 1 ? 2 : 1;
+  static constexpr int LPP = D * (int)sizeof(T) / (16 * VPL);
+  static constexpr int IPR = kNT / LPP;
+  static constexpr int WPL = 4 * VPL;                 // 32-bit words of m per lane
   // scoring-phase shared memory
-  static constexpr int RING = kNSS * kNT * 32;        // m and M, 16 B each
-  static constexpr int SMETA_OFF = RING;
+  static constexpr int SMETA_OFF = 0;
   static constexpr int QBUF_OFF = SMETA_OFF + kSliceCap * 8;
   static constexpr int SCORE_END = QBUF_OFF + kQBytes;
   // attention-phase shared memory (same region)
@@ -103,6 +106,7 @@ struct StepShape {
   static constexpr int STASH_O = STAGES;                                 // [MAXSEG][NW][G][D]
   static constexpr int STASH_ML = STASH_O + MAXSEG * kNW * G * D * 4;    // [MAXSEG][NW][G][2]
   static constexpr int ATT_END = STASH_ML + MAXSEG * kNW * G * 2 * 4;
+  static constexpr int MAX_PARTS = MAXSEG * kNW * D - 2;   // final-merge weights fit the stash
   static constexpr int KEYS_END = kKeysCap * 4;
   static constexpr int U1 = SCORE_END > ATT_END ? SCORE_END : ATT_END;
   static constexpr int UNION = U1 > KEYS_END ? U1 : KEYS_END;
@@ -137,7 +141,7 @@ step_kernel(const StepArgs a) {
   using Sh = StepShape<T, D, S, G>;
   using W = typename Sh::W;
   using KO = KeyOps<T>;
-  constexpr int VEC = Sh::VEC, LPP = Sh::LPP, PB = Sh::PB, NST = Sh::NST;
+  constexpr int VEC = Sh::VEC, NST = Sh::NST;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ TopkSmem<kNT> tsm;
   __shared__ int s_rf, s_rl, s_nlast, s_last[kMaxSeg];
@@ -154,22 +158,26 @@ step_kernel(const StepArgs a) {
   unsigned* att_done = ready + U;           // [U] attention slots finished
   unsigned tag = ld_relaxed_u32(epoch) + 1u;
   if (tag == 0u) tag = 1u;                  // 0 marks never-written entries
+  // optional phase trace: kTraceSlots globaltimer stamps per CTA
+  unsigned long long* trace = a.trace ? a.trace + (size_t)b * kTraceSlots : nullptr;
+  auto stamp = [&](int i) { if (trace && tid == 0) trace[i] = global_ns(); };
+  stamp(0);
 
   // =================== scoring (with the append folded in) ===================
-  const int nsel = min(U, kMaxSelectCtas);
-  const bool selector = b < nsel;
-  const int nscore = nblk - nsel;
-  const int per_cta = (a.nnz + nscore - 1) / nscore;
-  const int s0 = selector ? 0 : min(a.nnz, (b - nsel) * per_cta);
-  const int s1 = selector ? 0 : min(a.nnz, s0 + per_cta);
+  // CTA b scores table entries [s0, s1) for every KV head. Items (page i,
+  // head g) are taken page-major, IPR per round, so with IPR % h_kv == 0 a
+  // thread keeps one head (and its query registers) for the whole slice.
+  constexpr int LPP = Sh::LPP, VPL = Sh::VPL, WPL = Sh::WPL, IPR = Sh::IPR;
+  const int per_cta = (a.nnz + nblk - 1) / nblk;
+  const int s0 = min(a.nnz, b * per_cta);
+  const int s1 = min(a.nnz, s0 + per_cta);
   if (tid == 0) {
     s_rf = s1 > s0 ? find_req(a.page_indptr, 0, a.batch - 1, s0) : 0;
     s_rl = s1 > s0 ? find_req(a.page_indptr, 0, a.batch - 1, s1 - 1) : -1;
   }
   __syncthreads();
   const int rf = s_rf, rl = s_rl;
-  const int pw = tid / LPP, sub = tid % LPP;
-  uint4* ring = reinterpret_cast<uint4*>(smem);                          // [NSS][NT][2]
+  const int gp = tid / LPP, sub = tid % LPP;
   int2* smeta = reinterpret_cast<int2*>(smem + Sh::SMETA_OFF);           // [kSliceCap]
   T* qbuf = reinterpret_cast<T*>(smem + Sh::QBUF_OFF);
   const int nreq = rl - rf + 1;
@@ -181,6 +189,41 @@ step_kernel(const StepArgs a) {
     for (int i = tid; i < n16; i += kNT)
       reinterpret_cast<uint4*>(qbuf)[i] = ld_nc_v4(src + (size_t)i * VEC);
   }
+
+  // query of the current (request, head): per word a select mask (take M
+  // where q >= 0) and the query values as fp32
+  int q_r = -1, q_g = -1;
+  constexpr int QV = WPL * 4 / (int)sizeof(T);        // query values per lane
+  uint32_t qmask[G][WPL];
+  float qf[G][QV];
+  auto load_query = [&](int r, int g) {
+    q_r = r; q_g = g;
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      const size_t qo = ((size_t)(r - rf) * h_q + (size_t)g * G + gi) * D + sub * VPL * VEC;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const uint4 qv = q_in_smem ? reinterpret_cast<const uint4*>(qbuf + qo)[v]
+                                   : ld_nc_v4(static_cast<const T*>(a.q) + (size_t)rf * h_q * D + qo + v * VEC);
+        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if constexpr (sizeof(T) == 2) {
+            qmask[gi][v * 4 + j] = ((~w[j] & 0x80008000u) >> 15) * 0xffffu;
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+            qf[gi][(v * 4 + j) * 2 + 0] = f.x;
+            qf[gi][(v * 4 + j) * 2 + 1] = f.y;
+          } else {
+            qmask[gi][v * 4 + j] = (w[j] & 0x80000000u) ? 0u : 0xffffffffu;
+            qf[gi][v * 4 + j] = __uint_as_float(w[j]);
+          }
+        }
+      }
+    }
+  };
+
+  uint4 bm[kPD][VPL], bM[kPD][VPL];
+  int sl_x[kPD], sl_y[kPD], sl_i[kPD], sl_g[kPD];
 
 #pragma unroll 1
   for (int seg0 = s0; seg0 < s1; seg0 += kSliceCap) {
@@ -203,107 +246,123 @@ step_kernel(const StepArgs a) {
       smeta[e - seg0] = make_int2(phys, (r - rf) | (flags << 24));
     }
     __syncthreads();
-    const int R = (seg1 - seg0 + PB - 1) / PB;          // rounds per head
-    const int total = a.h_kv * R;
-
-    auto issue = [&](int t) {
-      if (t < total) {
-        const int g = t / R, rd = t % R;
-        const int i = rd * PB + pw;
-        if (seg0 + i < seg1) {
-          const int2 md = smeta[i];
-          if (md.y >> 24) {
-            const T* sp = static_cast<const T*>(a.summary) + ((size_t)md.x * a.h_kv + g) * 2 * D + sub * VEC;
-            cp_async16(&ring[((t % kNSS) * kNT + tid) * 2 + 0], sp);
-            cp_async16(&ring[((t % kNSS) * kNT + tid) * 2 + 1], sp + D);
+    const int n = seg1 - seg0;
+    const int rounds = (n * a.h_kv + IPR - 1) / IPR;
+    const int dg = IPR % a.h_kv, di = IPR / a.h_kv;
+    // walker over the thread's items (issued kPD ahead of their use)
+    int ig = gp % a.h_kv, ii = gp / a.h_kv;
+    auto issue = [&](int u) {
+      int x = -1, y = 0;
+      if (ii < n) {
+        const int2 md = smeta[ii];
+        x = md.x; y = md.y;
+        if (y >> 24) {
+          const T* sp = static_cast<const T*>(a.summary) + ((size_t)x * a.h_kv + ig) * 2 * D + sub * VPL * VEC;
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) {
+            bm[u][v] = ld_stream_v4(sp + v * VEC);
+            bM[u][v] = ld_stream_v4(sp + D + v * VEC);
           }
         }
       }
-      cp_async_commit();
+      sl_x[u] = x; sl_y[u] = y; sl_i[u] = ii; sl_g[u] = ig;
+      ig += dg; ii += di;
+      if (ig >= a.h_kv) { ig -= a.h_kv; ++ii; }
     };
-#pragma unroll 1
-    for (int t = 0; t < kNSS - 1; ++t) issue(t);
-#pragma unroll 1
-    for (int t = 0; t < total; ++t) {
-      issue(t + kNSS - 1);
-      cp_async_wait<kNSS - 1>();
-      const int g = t / R, rd = t % R;
-      const int i = rd * PB + pw;
-      const bool inside = seg0 + i < seg1;
-      const int2 md = inside ? smeta[i] : make_int2(-1, 0);
-      const int flags = md.y >> 24;
-      const int r = rf + (md.y & 0xffffff);
-      float sg[G];
 #pragma unroll
-      for (int gi = 0; gi < G; ++gi) sg[gi] = 0.f;
-      if (flags & 1) {
-        float q[G][VEC];
+    for (int u = 0; u < kPD; ++u) issue(u);
+#pragma unroll 1
+    for (int k0 = 0; k0 < rounds; k0 += kPD) {
 #pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-          const size_t qo = ((size_t)(r - rf) * h_q + (size_t)g * G + gi) * D + sub * VEC;
-          const uint4 qv = q_in_smem ? reinterpret_cast<const uint4*>(qbuf + qo)[0]
-                                     : ld_nc_v4(static_cast<const T*>(a.q) + (size_t)rf * h_q * D + qo);
-          unpack16<T>(qv, q[gi]);
-        }
-        uint4 vm = ring[((t % kNSS) * kNT + tid) * 2 + 0];
-        uint4 vM = ring[((t % kNSS) * kNT + tid) * 2 + 1];
-        if (flags & 2) {             // the new token lands in this (tail) page
-          const int pos = __ldg(a.seq_lens + r) - 1;
-          const int slot = pos % S;
-          const size_t src = ((size_t)r * a.h_kv + g) * D + sub * VEC;
-          const uint4 kn = ld_nc_v4(static_cast<const T*>(a.k_new) + src);
-          const uint4 vn = ld_nc_v4(static_cast<const T*>(a.v_new) + src);
-          const size_t dst = (((size_t)md.x * a.h_kv + g) * S + slot) * D + sub * VEC;
-          st_v4(static_cast<T*>(a.k_pool) + dst, kn);
-          st_v4(static_cast<T*>(a.v_pool) + dst, vn);
-          uint4 mn, mx;
-          if (slot == 0) {
-            mn = make_uint4(KO::to_key(kn.x), KO::to_key(kn.y), KO::to_key(kn.z), KO::to_key(kn.w));
-            mx = mn;
-          } else {
-            mn = make_uint4(KO::kmin(KO::to_key(vm.x), KO::to_key(kn.x)), KO::kmin(KO::to_key(vm.y), KO::to_key(kn.y)),
-                            KO::kmin(KO::to_key(vm.z), KO::to_key(kn.z)), KO::kmin(KO::to_key(vm.w), KO::to_key(kn.w)));
-            mx = make_uint4(KO::kmax(KO::to_key(vM.x), KO::to_key(kn.x)), KO::kmax(KO::to_key(vM.y), KO::to_key(kn.y)),
-                            KO::kmax(KO::to_key(vM.z), KO::to_key(kn.z)), KO::kmax(KO::to_key(vM.w), KO::to_key(kn.w)));
+      for (int u = 0; u < kPD; ++u) {
+        if (k0 + u < rounds) {               // CTA-uniform
+          // take everything of item k out of slot u before refilling it
+          const int flags = sl_y[u] >> 24;
+          const int r = rf + (sl_y[u] & 0xffffff);
+          const int g = sl_g[u], i = sl_i[u], pp = sl_x[u];
+          uint4 vm[VPL], vM[VPL];
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) { vm[v] = bm[u][v]; vM[v] = bM[u][v]; }
+          issue(u);                          // refill the slot kPD items ahead
+          float sg[G];
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) sg[gi] = 0.f;
+          if (flags & 1) {
+            if (r != q_r || g != q_g) load_query(r, g);
+            if (flags & 2) {                 // the new token lands in this (tail) page
+              const int pos = __ldg(a.seq_lens + r) - 1;
+              const int slot = pos % S;
+              const size_t src = ((size_t)r * a.h_kv + g) * D + sub * VPL * VEC;
+              const size_t dst = (((size_t)pp * a.h_kv + g) * S + slot) * D + sub * VPL * VEC;
+              T* sp = static_cast<T*>(a.summary) + ((size_t)pp * a.h_kv + g) * 2 * D + sub * VPL * VEC;
+#pragma unroll
+              for (int v = 0; v < VPL; ++v) {
+                const uint4 kn = ld_nc_v4(static_cast<const T*>(a.k_new) + src + v * VEC);
+                const uint4 vn = ld_nc_v4(static_cast<const T*>(a.v_new) + src + v * VEC);
+                st_v4(static_cast<T*>(a.k_pool) + dst + v * VEC, kn);
+                st_v4(static_cast<T*>(a.v_pool) + dst + v * VEC, vn);
+                uint4 mn, mx;
+                if (slot == 0) {
+                  mn = make_uint4(KO::to_key(kn.x), KO::to_key(kn.y), KO::to_key(kn.z), KO::to_key(kn.w));
+                  mx = mn;
+                } else {
+                  mn = make_uint4(KO::kmin(KO::to_key(vm[v].x), KO::to_key(kn.x)), KO::kmin(KO::to_key(vm[v].y), KO::to_key(kn.y)),
+                                  KO::kmin(KO::to_key(vm[v].z), KO::to_key(kn.z)), KO::kmin(KO::to_key(vm[v].w), KO::to_key(kn.w)));
+                  mx = make_uint4(KO::kmax(KO::to_key(vM[v].x), KO::to_key(kn.x)), KO::kmax(KO::to_key(vM[v].y), KO::to_key(kn.y)),
+                                  KO::kmax(KO::to_key(vM[v].z), KO::to_key(kn.z)), KO::kmax(KO::to_key(vM[v].w), KO::to_key(kn.w)));
+                }
+                vm[v] = make_uint4(KO::from_key(mn.x), KO::from_key(mn.y), KO::from_key(mn.z), KO::from_key(mn.w));
+                vM[v] = make_uint4(KO::from_key(mx.x), KO::from_key(mx.y), KO::from_key(mx.z), KO::from_key(mx.w));
+                st_v4(sp + v * VEC, vm[v]);
+                st_v4(sp + D + v * VEC, vM[v]);
+              }
+            }
+            // sum_j max(q_j m_j, q_j M_j) = sum_j q_j * (q_j >= 0 ? M_j : m_j)
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+              const uint32_t mw[4] = {vm[v].x, vm[v].y, vm[v].z, vm[v].w};
+              const uint32_t Mw[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi) {
+                  const uint32_t mk = qmask[gi][v * 4 + j];
+                  const uint32_t xw = (Mw[j] & mk) | (mw[j] & ~mk);
+                  if constexpr (sizeof(T) == 2) {
+                    const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xw));
+                    sg[gi] = fmaf(qf[gi][(v * 4 + j) * 2 + 0], xf.x, sg[gi]);
+                    sg[gi] = fmaf(qf[gi][(v * 4 + j) * 2 + 1], xf.y, sg[gi]);
+                  } else {
+                    sg[gi] = fmaf(qf[gi][v * 4 + j], __uint_as_float(xw), sg[gi]);
+                  }
+                }
+              }
+            }
           }
-          vm = make_uint4(KO::from_key(mn.x), KO::from_key(mn.y), KO::from_key(mn.z), KO::from_key(mn.w));
-          vM = make_uint4(KO::from_key(mx.x), KO::from_key(mx.y), KO::from_key(mx.z), KO::from_key(mx.w));
-          T* sp = static_cast<T*>(a.summary) + ((size_t)md.x * a.h_kv + g) * 2 * D + sub * VEC;
-          st_v4(sp, vm);
-          st_v4(sp + D, vM);
+          float best = -INFINITY;
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+#pragma unroll
+            for (int o = 1; o < LPP; o <<= 1) sg[gi] += __shfl_xor_sync(FULL, sg[gi], o);
+            best = fmaxf(best, sg[gi]);
+          }
+          if (i < n && sub == 0) {
+            const float sc = (flags & 1) ? best : -INFINITY;
+            const size_t at = (size_t)g * a.nnz + seg0 + i;
+            a.scores[at] = sc;
+            st_relaxed_u64(a.tagged + at, ((unsigned long long)tag << 32) | __float_as_uint(sc));
+          }
         }
-        float m[VEC], M[VEC];
-        unpack16<T>(vm, m);
-        unpack16<T>(vM, M);
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) sg[gi] += fmaxf(q[gi][v] * m[v], q[gi][v] * M[v]);
-        }
-      }
-      // per query head: sum over the page's LPP lanes; then the group maximum
-      float best = -INFINITY;
-#pragma unroll
-      for (int gi = 0; gi < G; ++gi) {
-#pragma unroll
-        for (int o = 1; o < LPP; o <<= 1) sg[gi] += __shfl_xor_sync(FULL, sg[gi], o);
-        best = fmaxf(best, sg[gi]);
-      }
-      if (inside && sub == 0) {
-        const float sc = (flags & 1) ? best : -INFINITY;
-        const size_t at = (size_t)g * a.nnz + seg0 + i;
-        a.scores[at] = sc;
-        st_relaxed_u64(a.tagged + at, ((unsigned long long)tag << 32) | __float_as_uint(sc));
       }
     }
-    cp_async_wait<0>();
   }
   __syncthreads();
+  stamp(1);
 
-  // =================== selection (select workers) ===================
-  if (selector) {
+  // =================== selection (CTA b takes units b, b + nblk, ... in head order) ===================
+  if (b < U) {
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-    for (int kk = b; kk < U; kk += nsel) {
+    for (int kk = b; kk < U; kk += nblk) {
       const int g = kk / a.batch, r = kk % a.batch;
       const int u = r * a.h_kv + g;
       const int lo = __ldg(a.page_indptr + r);
@@ -315,29 +374,21 @@ step_kernel(const StepArgs a) {
       }
       const unsigned long long* row = a.tagged + (size_t)g * a.nnz + lo;
       const bool cached = P <= kKeysCap;
-      for (uint32_t it = 0;; ++it) {         // until every score carries this call's tag
-        int cnt = 0;
-        for (int i = tid; i < P; i += kNT) {
-          const unsigned long long v = ld_relaxed_u64(row + i);
-          if ((unsigned)(v >> 32) == tag) {
-            ++cnt;
-            if (cached) keys[i] = score_key(__uint_as_float((unsigned)v));
-          }
+      // each thread waits for its own entries to carry this call's tag
+      bool late = false;
+      for (int i = tid; i < P; i += kNT) {
+        unsigned long long v = ld_relaxed_u64(row + i);
+        for (uint32_t it = 0; (unsigned)(v >> 32) != tag; ++it) {
+          if (it >= WAIT_LIMIT) { late = true; break; }
+          __nanosleep(32);
+          v = ld_relaxed_u64(row + i);
         }
-        cnt = __reduce_add_sync(FULL, cnt);
-        if (lane == 0) tsm.red[0][warp] = (uint32_t)cnt;
-        __syncthreads();
-        int totc = 0;
-#pragma unroll
-        for (int w2 = 0; w2 < kNW; ++w2) totc += (int)tsm.red[0][w2];
-        __syncthreads();
-        if (totc >= P) break;
-        if (it >= WAIT_LIMIT / 256) {
-          if (tid == 0) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
-          break;
-        }
-        __nanosleep(128);
+        if (cached) keys[i] = score_key(__uint_as_float((unsigned)v));
       }
+      if (late) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
+      __syncthreads();
+      const int nth = (kk - b) / nblk;       // this CTA's n-th select
+      if (nth < 3) stamp(10 + 2 * nth);
       const int32_t* idx = a.page_indices + lo;
       auto phys = [idx](int j) { return __ldg(idx + j); };
       int32_t* ol = a.sel_logical + (size_t)u * K;
@@ -354,9 +405,11 @@ step_kernel(const StepArgs a) {
         __threadfence();
         st_release(ready + u, tag);
       }
+      if (nth < 3) stamp(11 + 2 * nth);
     }
     __syncthreads();
   }
+  stamp(2);
 
   // =================== attention over the selected pages ===================
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::BAR_OFF) + warp * NST;
@@ -400,6 +453,7 @@ step_kernel(const StepArgs a) {
           if (it >= WAIT_LIMIT) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
         }
       }
+      if (pa == pb) stamp(3 + 3 * qr);
       // every warp starts each segment of the pass empty
       for (int s = 0; s < ns; ++s) {
 #pragma unroll
@@ -482,6 +536,7 @@ step_kernel(const StepArgs a) {
       if (cs >= 0)
         st.stash(stash_o + (size_t)cs * kNW * G * D, stash_ml + (size_t)cs * kNW * G * 2, warp, lane);
       __syncthreads();
+      stamp(4 + 3 * qr);
 
       // merge each segment's warps into this CTA's partial of the unit
       for (int s = 0; s < ns; ++s) {
@@ -519,39 +574,64 @@ step_kernel(const StepArgs a) {
         const int u = r * a.h_kv + g;
         const long long u0 = (long long)(ka + s) * K, u1 = u0 + K;
         const int b0 = rd.owner(u0);
+        const int nparts = rd.owner(u1 - 1) - b0 + 1;     // slots b0 .. owner(u1-1)
+        // the unit's partials: (max, sum) loaded lane-parallel, weights in smem
+        float* wbuf = stash_o;     // [G][NP] weights + [G][2] (max, sum); the stash is free here
+        for (int gi = 0; gi < G; ++gi) {
+          const size_t row0 = ((size_t)u * G + gi) * NP;
+          if (warp == 0) {
+            float mx = -INFINITY;
+            for (int j = lane; j < nparts; j += 32) {
+              const long long pj = max(u0, rd.start(b0 + j));
+              const bool has = pj < u1 && rd.owner(pj) == b0 + j;   // CTA b0+j owns positions of u
+              if (has) mx = fmaxf(mx, __ldcg(a.part_ml + (row0 + j) * 2));
+            }
+            mx = warp_max(mx);
+            float l = 0.f;
+            for (int j = lane; j < nparts; j += 32) {
+              const long long pj = max(u0, rd.start(b0 + j));
+              const bool has = pj < u1 && rd.owner(pj) == b0 + j;
+              float w = 0.f;
+              if (has && mx != -INFINITY) {
+                const float mc = __ldcg(a.part_ml + (row0 + j) * 2);
+                if (mc != -INFINITY) {
+                  w = exp2f(mc - mx);
+                  l = fmaf(w, __ldcg(a.part_ml + (row0 + j) * 2 + 1), l);
+                }
+              }
+              wbuf[gi * NP + j] = w;
+            }
+            l = warp_sum(l);
+            if (lane == 0) {
+              wbuf[G * NP + gi * 2 + 0] = mx;
+              wbuf[G * NP + gi * 2 + 1] = l;
+            }
+          }
+        }
+        __syncthreads();
         for (int idx = tid; idx < G * D; idx += kNT) {
           const int gi = idx / D, col = idx % D;
           const size_t row0 = ((size_t)u * G + gi) * NP;
-          float mx = -INFINITY;
-          for (long long p = u0; p < u1;) {
-            const int ob = rd.owner(p);
-            mx = fmaxf(mx, __ldcg(a.part_ml + (row0 + (ob - b0)) * 2));
-            p = rd.start(ob + 1);
-          }
-          float o = 0.f, l = 0.f;
-          if (mx != -INFINITY) {
-            for (long long p = u0; p < u1;) {
-              const int ob = rd.owner(p);
-              const size_t row = row0 + (ob - b0);
-              const float mc = __ldcg(a.part_ml + row * 2);
-              if (mc != -INFINITY) {
-                const float sc = exp2f(mc - mx);
-                l = fmaf(sc, __ldcg(a.part_ml + row * 2 + 1), l);
-                o = fmaf(sc, __ldcg(a.part_o + row * D + col), o);
-              }
-              p = rd.start(ob + 1);
-            }
+          const float mx = wbuf[G * NP + gi * 2 + 0], l = wbuf[G * NP + gi * 2 + 1];
+          float o = 0.f;
+#pragma unroll 8
+          for (int j = 0; j < nparts; ++j) {
+            const float w = wbuf[gi * NP + j];
+            if (w != 0.f) o = fmaf(w, __ldcg(a.part_o + (row0 + j) * D + col), o);
           }
           const size_t orow = (size_t)r * h_q + (size_t)g * G + gi;
           a.out[orow * D + col] = l > 0.f ? o / l : 0.f;
           if (col == 0 && a.lse) a.lse[orow] = l > 0.f ? (mx + log2f(l)) * LN2 : -INFINITY;
         }
         if (tid == 0) att_done[u] = 0;       // reset for the next call
+        __syncthreads();
       }
       __syncthreads();
       pa = pz;
+      if (pa >= pe) stamp(5 + 3 * qr);
     }
   }
+  stamp(9);
 
   if (tid == 0) {
     __threadfence();
@@ -659,7 +739,7 @@ StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int3
   const long long units = (long long)batch * h_kv;
   p.smem = smem;
   p.grid = sms * (per_sm > 2 ? 2 : per_sm);
-  p.ok = per_sm >= 1 && smem <= 227 * 1024 && p.grid > kMaxSelectCtas;
+  p.ok = per_sm >= 1 && smem <= 227 * 1024 && p.grid > 0;
   // partial slots per unit: CTAs whose round share can overlap one unit
   long long np = 1;
   const int rounds = units < kRounds ? (int)units : kRounds;

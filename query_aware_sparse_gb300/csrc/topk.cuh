@@ -5,10 +5,11 @@
 //
 // Scores map to order-preserving 32-bit keys (-0 folded onto +0). The block
 // first reduces min and max: bits above the highest bit where they differ
-// are common to every key, so the MSB-first radix select (8-bit digits,
-// shared-memory histogram) starts below them, and stops early once the
-// digit bucket holding the K-th key is taken whole. A block scan in page
-// order then emits the winners.
+// are common to every key, so the MSB-first radix select starts below them
+// with 11-bit digits (2048 shared-memory bins: a row of a few thousand
+// scores rarely puts many keys in one bin, so the bin atomics do not pile
+// up), and stops as soon as the digit bucket holding the K-th key is taken
+// whole. A block scan in page order then emits the winners.
 #pragma once
 
 #include "common.cuh"
@@ -20,9 +21,12 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return x ^ ((x & 0x80000000u) ? 0xffffffffu : 0x80000000u);
 }
 
+constexpr int kTopkBits = 11;                 // radix digit width
+constexpr int kTopkBins = 1 << kTopkBits;
+
 template <int NT>
 struct TopkSmem {
-  uint32_t hist[256];
+  uint32_t hist[kTopkBins];
   uint32_t red[2][NT / 32];
   unsigned long long scan[NT / 32];
   uint32_t digit, krem, done;
@@ -89,7 +93,7 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm,
     kmax = max(kmax, __shfl_xor_sync(FULL, kmax, o));
   }
   if (lane == 0) { sm.red[0][warp] = kmin; sm.red[1][warp] = kmax; }
-  for (int i = tid; i < 256; i += NT) sm.hist[i] = 0;
+  for (int i = tid; i < kTopkBins; i += NT) sm.hist[i] = 0;
   __syncthreads();
   kmin = sm.red[0][0];
   kmax = sm.red[1][0];
@@ -97,6 +101,8 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm,
   for (int w = 1; w < NWP; ++w) { kmin = min(kmin, sm.red[0][w]); kmax = max(kmax, sm.red[1][w]); }
 
   // Radix select below the common prefix of min and max.
+  constexpr int BPT = kTopkBins / NT;            // bins per thread in the digit search
+  static_assert(BPT * NT == kTopkBins, "bins must split evenly over the block");
   uint32_t T, need;
   bool ge_mode;            // select key >= T (bucket taken whole) vs the tie rule
   if (kmin == kmax) {
@@ -108,41 +114,41 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm,
     ge_mode = false;
     T = 0; need = 0;
     while (true) {
-      const int shift = max(hi - 7, 0);
+      const int shift = max(hi - (kTopkBits - 1), 0);
       const int nbits = hi - shift + 1;
       const uint32_t dmask = (1u << nbits) - 1u;
       const uint32_t hi_mask = (hi == 31) ? 0u : ~((2u << hi) - 1u);
-      for (int base = 0; base < P; base += NT) {
-        const int i = base + tid;
-        if (i < P) {
-          const uint32_t k = key_at(i);
-          if ((k & hi_mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
-        }
+      for (int i = tid; i < P; i += NT) {
+        const uint32_t k = key_at(i);
+        if ((k & hi_mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
       }
       __syncthreads();
-      if (warp == 0) {
-        uint32_t h[8], tot = 0;
+      // thread t owns bins [t*BPT, t*BPT + BPT); count of keys in higher bins
+      uint32_t h[BPT], tot = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) { h[j] = sm.hist[lane * 8 + j]; tot += h[j]; }
-        uint32_t incl = tot;
+      for (int j = 0; j < BPT; ++j) { h[j] = sm.hist[tid * BPT + j]; tot += h[j]; }
+      uint32_t incl = tot;                         // suffix sum within the warp
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          uint32_t t = __shfl_down_sync(FULL, incl, o);
-          if (lane + o < 32) incl += t;
-        }
-        uint32_t cum = incl - tot;
-#pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          if (cum < krem && krem <= cum + h[j]) {
-            sm.digit = lane * 8 + j;
-            sm.krem = krem - cum;
-            sm.done = (h[j] == krem - cum) ? 1u : 0u;   // bucket taken whole
-          }
-          cum += h[j];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) sm.hist[lane * 8 + j] = 0;   // ready for the next pass
+      for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_down_sync(FULL, incl, o);
+        if (lane + o < 32) incl += t;
       }
+      if (lane == 0) sm.red[0][warp] = incl;       // warp totals
+      __syncthreads();
+      uint32_t above = incl - tot;
+      for (int w = warp + 1; w < NWP; ++w) above += sm.red[0][w];
+      uint32_t cum = above;
+#pragma unroll
+      for (int j = BPT - 1; j >= 0; --j) {
+        if (cum < krem && krem <= cum + h[j]) {
+          sm.digit = tid * BPT + j;
+          sm.krem = krem - cum;
+          sm.done = (h[j] == krem - cum) ? 1u : 0u;   // bucket taken whole
+        }
+        cum += h[j];
+      }
+#pragma unroll
+      for (int j = 0; j < BPT; ++j) sm.hist[tid * BPT + j] = 0;   // ready for the next pass
       __syncthreads();
       prefix |= sm.digit << shift;
       krem = sm.krem;
