@@ -184,6 +184,32 @@ QUEST_API quest_status quest_sparse_decode_attn(const quest_cache* cache,
                                       void* workspace, size_t workspace_bytes,
                                       void* stream);
 
+/*
+ * quest_sparse_decode_attn_noalloc — the same attention as
+ * quest_sparse_decode_attn (same kernels, same arguments and results) without
+ * a workspace argument. The paper has no counterpart to this call; it exists
+ * for callers that cannot allocate device memory: a plug-in that only receives
+ * input and output pointers from its host program, or a serving loop that must
+ * not call cudaMalloc (which can synchronise the device) once it is running.
+ * The split-K partials go to a fixed 4 MiB buffer inside the library's own
+ * module memory (one per device that loads the library, kept until the
+ * process exits); the call allocates nothing. A problem whose partials need
+ * more than 4 MiB (quest_attn_workspace_size(...) > 4 MiB) is rejected with
+ * QUEST_ERR_WORKSPACE before anything is launched. The first call on a device
+ * looks up the buffer's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture. Every call shares
+ * the one buffer and leaves its contents behind; no part of it needs to start
+ * at zero, but calls that overlap on the GPU (other streams, other threads)
+ * race on it.
+ */
+QUEST_API quest_status quest_sparse_decode_attn_noalloc(const quest_cache* cache,
+                                                        const quest_pages* pages,
+                                                        const void* q, int32_t group,
+                                                        const int32_t* sel_logical,
+                                                        const int32_t* sel_phys, int32_t k,
+                                                        float* out, float* lse,
+                                                        float sm_scale, void* stream);
+
 /* Workspace bytes quest_sparse_decode_attn needs for these sizes on the
  * current device (the split-K chunking depends on its SM count). */
 QUEST_API size_t quest_attn_workspace_size(int32_t batch, int32_t h_kv, int32_t group,

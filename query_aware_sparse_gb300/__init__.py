@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
         L.quest_select_topk.argtypes = [P, I32, I32, P, I32, P, P, P, P]
         L.quest_sparse_decode_attn.argtypes = [P, P, P, I32, P, P, I32, P, P,
                                                ctypes.c_float, P, SZ, P]
+        L.quest_sparse_decode_attn_noalloc.argtypes = [P, P, P, I32, P, P, I32, P, P,
+                                                       ctypes.c_float, P]
+        L.quest_sparse_decode_attn_noalloc.restype = I32
         L.quest_attn_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32]
         L.quest_attn_workspace_size.restype = SZ
         L.quest_decode_step.argtypes = [P, P, P, P, P, I32, I32, P, P, P, P, P, P,
@@ -77,7 +80,8 @@ def lib() -> ctypes.CDLL:
 
 
 EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_select_topk",
-            "quest_sparse_decode_attn", "quest_attn_workspace_size",
+            "quest_sparse_decode_attn", "quest_sparse_decode_attn_noalloc",
+            "quest_attn_workspace_size",
             "quest_decode_step", "quest_decode_workspace_size", "quest_set_trace",
             "quest_get_device_error", "quest_status_string")
 
@@ -247,6 +251,23 @@ def set_trace(buffer, max_ctas=0, batch=0, h_kv=0, group=1, head_dim=128, page_s
     return int(lib().quest_set_trace(_ptr(buffer), int(max_ctas), int(batch), int(h_kv),
                                      int(group), int(head_dim), int(page_size),
                                      dtype_code(dtype), int(k)))
+
+
+def sparse_decode_attn_noalloc(cache: PagedCache, table: PageTable, q, group: int,
+                               sel_logical, sel_phys, k: int, out=None, lse=None,
+                               sm_scale: float = 0.0, stream=None):
+    """quest_sparse_decode_attn_noalloc: the same attention with the split-K
+    partials in the library's fixed 4 MiB buffer (for callers that cannot
+    allocate device memory); calls on overlapping streams race on it."""
+    B, h_q, d = q.shape
+    if out is None:
+        out = torch.empty((B, h_q, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, h_q), dtype=torch.float32, device=q.device)
+    _check(lib().quest_sparse_decode_attn_noalloc(
+        ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(q), int(group), _ptr(sel_logical),
+        _ptr(sel_phys), int(k), _ptr(out), _ptr(lse), float(sm_scale), _stream(stream)))
+    return out, lse
 
 
 def device_error(stream=None) -> int:

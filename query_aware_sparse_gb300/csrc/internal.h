@@ -91,6 +91,9 @@ AttnPlan plan_attn(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
                    int32_t page_size, int32_t dtype, int32_t k);
 
 bool attn_supported(int32_t dtype, int32_t head_dim, int32_t page_size, int32_t group);
+
+// Device address of the error word for the current device (null on failure).
+unsigned* error_word_ptr();
 bool score_supported(int32_t dtype, int32_t head_dim, int32_t group);
 
 }  // namespace quest

@@ -268,3 +268,7 @@ const char* quest_status_string(int32_t status) {
 }
 
 }  // extern "C"
+
+namespace quest {
+unsigned* error_word_ptr() { return err_ptr(); }
+}  // namespace quest
