@@ -239,8 +239,13 @@ class DecodeStep:
         return self.out, self.lse
 
 
-TRACE_NAMES = ("start", "scored", "selected", "r0_start", "r0_pages", "r0_merged",
-               "r1_start", "r1_pages", "r1_merged", "exit")
+TRACE_NAMES = ("start", "scored", "selected", "att_start", "att_pages", "att_merged",
+               "wave0_scored", "wave1_scored", "wave2_scored", "exit",
+               "sel0_polled | desc0", "sel0_done | page0", "sel1_polled | merged",
+               "sel1_done | fmerge0", "sel2_polled | fmerge1", "sel2_done")
+# slots 10-15 depend on the CTA's role: select stamps on selectors (the CTAs
+# whose "scored" stamp precedes any scoring), attention and final-merge stamps
+# on the others
 
 
 def set_trace(buffer, max_ctas=0, batch=0, h_kv=0, group=1, head_dim=128, page_size=16,

@@ -5,28 +5,33 @@
 //   a4 attention over the selected pages (Quest page Fig. 1, §2.1), and
 //   a5 the log-sum-exp merge of its split-K partials (Quest page §2.1).
 //
-// Scoring. The first NSEL CTAs are select workers; every other CTA scores a
-// fixed slice of the page table for each KV head in turn (head-major), so
-// head g is complete after about (g+1)/h_kv of the scoring time. The slice's
-// page metadata and queries are staged in shared memory once; summaries
-// stream through a per-thread cp.async ring, so the loop never waits on a
-// dependent load, a barrier or another CTA. Each score is also stored with
-// the call's tag in the upper half of a 64-bit word: a reader tells a score
-// of this call from a stale one without any fence on the writer's side.
+// Roles. The first NSEL CTAs (about one in eight, at most one per unit) only
+// select; the others ("workers") score and then attend.
 //
-// Selection. Select workers take the (request, KV head) units in head order,
-// poll a unit's tagged row until it is complete, run the block-wide Top-K and
-// publish the unit's ready flag (set to the tag): the selects of early heads
-// overlap the scoring of later ones.
+// Scoring. Each worker scores an equal share of the (page, head) items of
+// the page table, page-major with a fixed head per thread, so the query
+// stays in registers. Start-up is two dependent loads deep (page table ->
+// summary): the first items take their physical pages from the table while
+// the slice's metadata is staged in shared memory. Summaries stream through
+// a register pipeline kPD items deep, so the loop never waits on a dependent
+// load, a barrier or another CTA. Each score is also stored with the call's
+// tag in the upper half of a 64-bit word: a reader tells a score of this
+// call from a stale one without any fence on the writer's side. Each worker
+// then bumps a relaxed "scored" counter, a hint that lets the selectors read
+// their rows once instead of polling them while the workers stream.
+//
+// Selection. Selectors take the (request, KV head) units in head order, read
+// a unit's tagged row (batches of independent loads, re-polling only stale
+// entries; key min and max reduced on the way), run the block-wide Top-K and
+// publish the unit's ready flag (set to the tag) with a release store.
 //
 // Attention. The selected-page slots of all units, in head order, form one
-// list split into rounds; each CTA takes an equal contiguous share of every
-// round (early heads first, so later heads have been selected by the time a
-// CTA reaches them). Its warps stream their pages with bulk async copies
-// (cp.async.bulk + mbarrier), fold them with the online softmax and stash one
-// state per (unit segment, warp); the CTA merges each segment into one
-// partial. Per unit, a counter of processed slots tells the CTA that
-// completes the unit to merge all the unit's partials into the output.
+// list; each worker takes an equal contiguous share. Its warps stream their
+// pages with bulk async copies (cp.async.bulk + mbarrier), fold them with the
+// online softmax and stash one state per (unit segment, warp); the CTA merges
+// each segment into one partial. Per unit, a counter of processed slots
+// (acquire-release fetch-and-add) tells the worker that completes the unit
+// to merge all the unit's partials into the output, in one round trip to L2.
 //
 // The launch is cooperative, so every CTA is resident and every wait (select
 // workers on scoring, attention on select workers) ends; each wait is also
@@ -44,10 +49,9 @@ namespace {
 
 constexpr int kNT = 256;              // threads per CTA
 constexpr int kNW = kNT / 32;
-constexpr int kPD = 3;                // scoring software-pipeline depth (items)
+constexpr int kPD = 2;                // scoring software-pipeline depth (items)
 constexpr int kKeysCap = 4096;        // selector keys cached in shared memory
 constexpr int kSliceCap = 1024;       // slice pages whose metadata is staged at once
-constexpr int kQBytes = 16384;        // queries of the slice's requests kept in smem
 constexpr int kRounds = 1;            // attention rounds
 constexpr int kMaxSeg = 4;            // unit segments per attention pass (G = 1)
 constexpr int kTraceSlots = 16;
@@ -76,6 +80,9 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -84,6 +91,21 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
 __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async;" ::: "memory");
 }
+// fetch-and-add that releases this CTA's prior writes (ordered before it by a
+// barrier) and acquires those released by earlier adds to the same word
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// CTAs that only select (the rest score and attend): about one per eight,
+// at most one per unit.
+__host__ __device__ __forceinline__ int select_ctas(int units, int nblk) {
+  const int n = nblk / 8 > 1 ? nblk / 8 : 1;
+  return units < n ? units : n;
+}
+
 
 template <typename T, int D, int S, int G>
 struct StepShape {
@@ -99,15 +121,14 @@ struct StepShape {
   static constexpr int WPL = 4 * VPL;                 // 32-bit words of m per lane
   // scoring-phase shared memory
   static constexpr int SMETA_OFF = 0;
-  static constexpr int QBUF_OFF = SMETA_OFF + kSliceCap * 8;
-  static constexpr int SCORE_END = QBUF_OFF + kQBytes;
+  static constexpr int SCORE_END = SMETA_OFF + kSliceCap * 8;
   // attention-phase shared memory (same region)
   static constexpr int STAGES = kNW * NST * 2 * W::BLOCK_BYTES;
   static constexpr int STASH_O = STAGES;                                 // [MAXSEG][NW][G][D]
   static constexpr int STASH_ML = STASH_O + MAXSEG * kNW * G * D * 4;    // [MAXSEG][NW][G][2]
   static constexpr int ATT_END = STASH_ML + MAXSEG * kNW * G * 2 * 4;
   static constexpr int MAX_PARTS = MAXSEG * kNW * D - 2;   // final-merge weights fit the stash
-  static constexpr int KEYS_END = kKeysCap * 4;
+  static constexpr int KEYS_END = kKeysCap * 8;              // keys + physical pages
   static constexpr int U1 = SCORE_END > ATT_END ? SCORE_END : ATT_END;
   static constexpr int UNION = U1 > KEYS_END ? U1 : KEYS_END;
   static constexpr int BAR_OFF = (UNION + 15) / 16 * 16;
@@ -156,6 +177,7 @@ step_kernel(const StepArgs a) {
   unsigned* exit_cnt = a.counters + 2;      // CTAs finished
   unsigned* ready = a.counters + 4;         // [U] tag of the published selection
   unsigned* att_done = ready + U;           // [U] attention slots finished
+  unsigned* scored_cnt = att_done + U;      // workers done scoring (a hint for the selectors)
   unsigned tag = ld_relaxed_u32(epoch) + 1u;
   if (tag == 0u) tag = 1u;                  // 0 marks never-written entries
   // optional phase trace: kTraceSlots globaltimer stamps per CTA
@@ -163,14 +185,24 @@ step_kernel(const StepArgs a) {
   auto stamp = [&](int i) { if (trace && tid == 0) trace[i] = global_ns(); };
   stamp(0);
 
+  const int NSEL = select_ctas(U, nblk);    // CTAs [0, NSEL) select; the rest score and attend
+  const bool selector = b < NSEL;
+  const int nbw = nblk - NSEL, bw = b - NSEL;
+
   // =================== scoring (with the append folded in) ===================
-  // CTA b scores table entries [s0, s1) for every KV head. Items (page i,
-  // head g) are taken page-major, IPR per round, so with IPR % h_kv == 0 a
-  // thread keeps one head (and its query registers) for the whole slice.
+  // Worker bw scores an equal share [t0, t1) of the (page, head) items in
+  // page-major order (entries [s0, s1) of the table). Items are taken IPR
+  // per round, so with IPR % h_kv == 0 a thread keeps one head (and its
+  // query registers) for the whole slice. Start-up is two dependent loads
+  // deep: the first kPD items take their physical pages straight from the
+  // page table, and the query and the slice's metadata load while those
+  // summaries are in flight.
   constexpr int LPP = Sh::LPP, VPL = Sh::VPL, WPL = Sh::WPL, IPR = Sh::IPR;
-  const int per_cta = (a.nnz + nblk - 1) / nblk;
-  const int s0 = min(a.nnz, b * per_cta);
-  const int s1 = min(a.nnz, s0 + per_cta);
+  const long long n_items = (long long)a.nnz * a.h_kv;
+  const long long t0 = selector ? 0 : bw * n_items / nbw;
+  const long long t1 = selector ? 0 : (bw + 1) * n_items / nbw;
+  const int s0 = (int)(t0 / a.h_kv);
+  const int s1 = t1 > t0 ? (int)((t1 - 1) / a.h_kv) + 1 : s0;
   if (tid == 0) {
     s_rf = s1 > s0 ? find_req(a.page_indptr, 0, a.batch - 1, s0) : 0;
     s_rl = s1 > s0 ? find_req(a.page_indptr, 0, a.batch - 1, s1 - 1) : -1;
@@ -179,16 +211,6 @@ step_kernel(const StepArgs a) {
   const int rf = s_rf, rl = s_rl;
   const int gp = tid / LPP, sub = tid % LPP;
   int2* smeta = reinterpret_cast<int2*>(smem + Sh::SMETA_OFF);           // [kSliceCap]
-  T* qbuf = reinterpret_cast<T*>(smem + Sh::QBUF_OFF);
-  const int nreq = rl - rf + 1;
-  const bool q_in_smem = (size_t)nreq * h_q * D * sizeof(T) <= (size_t)kQBytes;
-
-  if (s1 > s0 && q_in_smem) {               // queries of the slice's requests
-    const int n16 = nreq * h_q * D / VEC;
-    const T* src = static_cast<const T*>(a.q) + (size_t)rf * h_q * D;
-    for (int i = tid; i < n16; i += kNT)
-      reinterpret_cast<uint4*>(qbuf)[i] = ld_nc_v4(src + (size_t)i * VEC);
-  }
 
   // query of the current (request, head): per word a select mask (take M
   // where q >= 0) and the query values as fp32
@@ -196,15 +218,22 @@ step_kernel(const StepArgs a) {
   constexpr int QV = WPL * 4 / (int)sizeof(T);        // query values per lane
   uint32_t qmask[G][WPL];
   float qf[G][QV];
-  auto load_query = [&](int r, int g) {
+  auto query_raw = [&](int r, int g, uint4 (&qr)[G][VPL]) {
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      const T* qp = static_cast<const T*>(a.q) + ((size_t)r * h_q + (size_t)g * G + gi) * D +
+                    sub * VPL * VEC;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) qr[gi][v] = ld_nc_v4(qp + v * VEC);
+    }
+  };
+  auto set_query = [&](int r, int g, const uint4 (&qr)[G][VPL]) {
     q_r = r; q_g = g;
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) {
-      const size_t qo = ((size_t)(r - rf) * h_q + (size_t)g * G + gi) * D + sub * VPL * VEC;
 #pragma unroll
       for (int v = 0; v < VPL; ++v) {
-        const uint4 qv = q_in_smem ? reinterpret_cast<const uint4*>(qbuf + qo)[v]
-                                   : ld_nc_v4(static_cast<const T*>(a.q) + (size_t)rf * h_q * D + qo + v * VEC);
+        const uint4 qv = qr[gi][v];
         const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -221,14 +250,54 @@ step_kernel(const StepArgs a) {
       }
     }
   };
+  auto load_query = [&](int r, int g) {
+    uint4 qr[G][VPL];
+    query_raw(r, g, qr);
+    set_query(r, g, qr);
+  };
 
   uint4 bm[kPD][VPL], bM[kPD][VPL];
-  int sl_x[kPD], sl_y[kPD], sl_i[kPD], sl_g[kPD];
+  int sl_i[kPD], sl_g[kPD];                  // page (n = none) and head of each slot
 
 #pragma unroll 1
   for (int seg0 = s0; seg0 < s1; seg0 += kSliceCap) {
     const int seg1 = min(s1, seg0 + kSliceCap);
+    const int n = seg1 - seg0;
+    const long long ta = max(t0, (long long)seg0 * a.h_kv);   // the segment's items [ta, tb)
+    const int nit = (int)(min(t1, (long long)seg1 * a.h_kv) - ta);
+    const int rounds = (nit + IPR - 1) / IPR;
+    const int dg = IPR % a.h_kv, di = IPR / a.h_kv;
     __syncthreads();                        // previous segment's metadata consumed
+    // walker over the thread's items ta + ti (issued kPD ahead of their use):
+    // page seg0 + ii, head ig; the physical page comes from smem, or from
+    // the table before it is staged
+    const int rel0 = (int)(ta - (long long)seg0 * a.h_kv) + gp;
+    int ti = gp, ig = rel0 % a.h_kv, ii = rel0 / a.h_kv;
+    auto issue = [&](int u, bool staged) {
+      int ip = n;
+      if (ti < nit) {
+        ip = ii;
+        const int x = staged ? smeta[ii].x : __ldg(a.page_indices + seg0 + ii);
+        if (x >= 0 && x < a.n_phys) {        // reserved entries load harmlessly
+          const T* sp = static_cast<const T*>(a.summary) + ((size_t)x * a.h_kv + ig) * 2 * D + sub * VPL * VEC;
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) {
+            bm[u][v] = ld_stream_v4(sp + v * VEC);
+            bM[u][v] = ld_stream_v4(sp + D + v * VEC);
+          }
+        }
+      }
+      sl_i[u] = ip; sl_g[u] = ig;
+      ti += IPR; ig += dg; ii += di;
+      if (ig >= a.h_kv) { ig -= a.h_kv; ++ii; }
+    };
+#pragma unroll
+    for (int u = 0; u < kPD; ++u) issue(u, false);
+    // the first item's query (its request is usually the slice's first):
+    // loaded now, converted once the metadata is staged
+    const bool pre_q = seg0 == s0 && sl_i[0] < n;
+    uint4 qr0[G][VPL];
+    if (pre_q) query_raw(rf, sl_g[0], qr0);
     for (int e = seg0 + tid; e < seg1; e += kNT) {
       const int r = rf == rl ? rf : find_req(a.page_indptr, rf, rl, e);
       const int lp = e - __ldg(a.page_indptr + r);
@@ -243,47 +312,24 @@ step_kernel(const StepArgs a) {
           report(a.err, QUEST_DEVERR_PAGE_RANGE);
         }
       }
-      smeta[e - seg0] = make_int2(phys, (r - rf) | (flags << 24));
+      smeta[e - seg0] = make_int2(phys, r | (flags << 24));
     }
+    if (pre_q) set_query(rf, sl_g[0], qr0);
     __syncthreads();
-    const int n = seg1 - seg0;
-    const int rounds = (n * a.h_kv + IPR - 1) / IPR;
-    const int dg = IPR % a.h_kv, di = IPR / a.h_kv;
-    // walker over the thread's items (issued kPD ahead of their use)
-    int ig = gp % a.h_kv, ii = gp / a.h_kv;
-    auto issue = [&](int u) {
-      int x = -1, y = 0;
-      if (ii < n) {
-        const int2 md = smeta[ii];
-        x = md.x; y = md.y;
-        if (y >> 24) {
-          const T* sp = static_cast<const T*>(a.summary) + ((size_t)x * a.h_kv + ig) * 2 * D + sub * VPL * VEC;
-#pragma unroll
-          for (int v = 0; v < VPL; ++v) {
-            bm[u][v] = ld_stream_v4(sp + v * VEC);
-            bM[u][v] = ld_stream_v4(sp + D + v * VEC);
-          }
-        }
-      }
-      sl_x[u] = x; sl_y[u] = y; sl_i[u] = ii; sl_g[u] = ig;
-      ig += dg; ii += di;
-      if (ig >= a.h_kv) { ig -= a.h_kv; ++ii; }
-    };
-#pragma unroll
-    for (int u = 0; u < kPD; ++u) issue(u);
 #pragma unroll 1
     for (int k0 = 0; k0 < rounds; k0 += kPD) {
 #pragma unroll
       for (int u = 0; u < kPD; ++u) {
         if (k0 + u < rounds) {               // CTA-uniform
           // take everything of item k out of slot u before refilling it
-          const int flags = sl_y[u] >> 24;
-          const int r = rf + (sl_y[u] & 0xffffff);
-          const int g = sl_g[u], i = sl_i[u], pp = sl_x[u];
+          const int g = sl_g[u], i = sl_i[u];
           uint4 vm[VPL], vM[VPL];
 #pragma unroll
           for (int v = 0; v < VPL; ++v) { vm[v] = bm[u][v]; vM[v] = bM[u][v]; }
-          issue(u);                          // refill the slot kPD items ahead
+          issue(u, true);                    // refill the slot kPD items ahead
+          const int2 md = i < n ? smeta[i] : make_int2(-1, 0);
+          const int flags = md.y >> 24;
+          const int r = md.y & 0xffffff, pp = md.x;
           float sg[G];
 #pragma unroll
           for (int gi = 0; gi < G; ++gi) sg[gi] = 0.f;
@@ -357,12 +403,15 @@ step_kernel(const StepArgs a) {
     }
   }
   __syncthreads();
+  if (!selector && tid == 0) red_relaxed_add(scored_cnt, 1u);   // hint for the selectors
   stamp(1);
 
-  // =================== selection (CTA b takes units b, b + nblk, ... in head order) ===================
-  if (b < U) {
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-    for (int kk = b; kk < U; kk += nblk) {
+  // =================== selection (selector b takes units b, b + NSEL, ... in head order) ===================
+  if (selector) {
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                      // [kKeysCap]
+    int32_t* physs = reinterpret_cast<int32_t*>(smem + kKeysCap * 4);        // [kKeysCap]
+    for (int i = tid; i < kTopkBins; i += kNT) tsm.hist[i] = 0;   // block_topk_smem keeps it zero
+    for (int kk = b; kk < U; kk += NSEL) {
       const int g = kk / a.batch, r = kk % a.batch;
       const int u = r * a.h_kv + g;
       const int lo = __ldg(a.page_indptr + r);
@@ -373,38 +422,68 @@ step_kernel(const StepArgs a) {
         P = tp;
       }
       const unsigned long long* row = a.tagged + (size_t)g * a.nnz + lo;
+      const int32_t* idx = a.page_indices + lo;
       const bool cached = P <= kKeysCap;
-      // each thread waits for its own entries to carry this call's tag
+      // gate: one thread waits (bounded) until every worker has finished
+      // scoring, so the block reads the row once instead of polling it while
+      // the workers stream; the row's tags still decide below
+      if (tid == 0)
+        for (uint32_t it = 0; ld_relaxed_u32(scored_cnt) < (unsigned)nbw && it < (1u << 20); ++it)
+          __nanosleep(128);
+      __syncthreads();
+      // each thread waits for its own entries to carry this call's tag: a
+      // batch of PB independent loads (with the entries' physical pages),
+      // then a re-poll of only those still stale; the keys' min and max are
+      // reduced on the way
+      constexpr int PB = 8;
       bool late = false;
-      for (int i = tid; i < P; i += kNT) {
-        unsigned long long v = ld_relaxed_u64(row + i);
-        for (uint32_t it = 0; (unsigned)(v >> 32) != tag; ++it) {
-          if (it >= WAIT_LIMIT) { late = true; break; }
-          __nanosleep(32);
-          v = ld_relaxed_u64(row + i);
+      uint32_t kmin = 0xffffffffu, kmax = 0u;
+      for (int i0 = tid; i0 < P; i0 += kNT * PB) {
+        unsigned long long v[PB];
+        int32_t ph[PB];
+#pragma unroll
+        for (int j = 0; j < PB; ++j) {
+          const int i = i0 + j * kNT;
+          v[j] = i < P ? ld_relaxed_u64(row + i) : (unsigned long long)tag << 32;
+          ph[j] = (cached && i < P) ? __ldg(idx + i) : 0;
         }
-        if (cached) keys[i] = score_key(__uint_as_float((unsigned)v));
+#pragma unroll
+        for (int j = 0; j < PB; ++j) {
+          const int i = i0 + j * kNT;
+          for (uint32_t it = 0; (unsigned)(v[j] >> 32) != tag; ++it) {
+            if (it >= WAIT_LIMIT) { late = true; break; }
+            __nanosleep(32);
+            v[j] = ld_relaxed_u64(row + i);
+          }
+          if (cached && i < P) {
+            const uint32_t key = score_key(__uint_as_float((unsigned)v[j]));
+            keys[i] = key;
+            physs[i] = ph[j];
+            kmin = min(kmin, key);
+            kmax = max(kmax, key);
+          }
+        }
       }
       if (late) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
+      kmin = warp_min_u32(kmin);
+      kmax = warp_max_u32(kmax);
+      if (lane == 0) { tsm.red[0][warp] = kmin; tsm.red[1][warp] = kmax; }
       __syncthreads();
-      const int nth = (kk - b) / nblk;       // this CTA's n-th select
+#pragma unroll
+      for (int w = 0; w < kNW; ++w) { kmin = min(kmin, tsm.red[0][w]); kmax = max(kmax, tsm.red[1][w]); }
+      const int nth = (kk - b) / NSEL;       // this CTA's n-th select
       if (nth < 3) stamp(10 + 2 * nth);
-      const int32_t* idx = a.page_indices + lo;
-      auto phys = [idx](int j) { return __ldg(idx + j); };
+      auto phys = [idx, physs, cached](int j) { return cached ? physs[j] : __ldg(idx + j); };
       int32_t* ol = a.sel_logical + (size_t)u * K;
       int32_t* op = a.sel_phys + (size_t)u * K;
       if (cached)
-        block_topk_keys<kNT>(P, K, [keys](int i) { return keys[i]; }, tsm, ol, op,
-                             a.sel_count + u, phys);
+        block_topk_smem<kNT>(P, K, keys, kmin, kmax, tsm, ol, op, a.sel_count + u, phys);
       else
         block_topk_keys<kNT>(P, K, [row](int i) {
                                return score_key(__uint_as_float((unsigned)ld_relaxed_u64(row + i)));
                              }, tsm, ol, op, a.sel_count + u, phys);
       __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        st_release(ready + u, tag);
-      }
+      if (tid == 0) st_release(ready + u, tag);   // releases the block's selection writes
       if (nth < 3) stamp(11 + 2 * nth);
     }
     __syncthreads();
@@ -426,7 +505,7 @@ step_kernel(const StepArgs a) {
   unsigned phase = 0;                       // parity bit per slot
   const size_t head_block = (size_t)S * D;
   const size_t page_stride = (size_t)a.h_kv * head_block;
-  const int nrounds = min(kRounds, U);
+  const int nrounds = selector ? 0 : min(kRounds, U);
 
 #pragma unroll 1
   for (int qr = 0; qr < nrounds; ++qr) {
@@ -434,8 +513,8 @@ step_kernel(const StepArgs a) {
     rd.k0 = (int)((long long)qr * U / nrounds);
     rd.k1 = (int)((long long)(qr + 1) * U / nrounds);
     rd.len = (long long)(rd.k1 - rd.k0) * K;
-    rd.nblk = nblk;
-    const long long pb = rd.start(b), pe = rd.start(b + 1);   // relative to unit k0
+    rd.nblk = nbw;
+    const long long pb = rd.start(bw), pe = rd.start(bw + 1);   // relative to unit k0
 #pragma unroll 1
     for (long long pa = pb; pa < pe;) {
       // one pass: the positions [pa, pz) of at most MAXSEG consecutive units
@@ -453,7 +532,7 @@ step_kernel(const StepArgs a) {
           if (it >= WAIT_LIMIT) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
         }
       }
-      if (pa == pb) stamp(3 + 3 * qr);
+      if (pa == pb && qr == 0) stamp(3);
       // every warp starts each segment of the pass empty
       for (int s = 0; s < ns; ++s) {
 #pragma unroll
@@ -493,6 +572,7 @@ step_kernel(const StepArgs a) {
         const int nv = __popc(vmask);
         if (my_val > 0) desc[__popc(vmask & ((1u << lane) - 1))] = make_int2(my_pp, my_val);
         __syncwarp();
+        if (pa == pb && base == 0) stamp(10);
         auto issue = [&](int n) {
           const int slot = n % NST;
           const int kk = rd.k0 + ka + (desc[n].y >> 8);
@@ -524,6 +604,7 @@ step_kernel(const StepArgs a) {
             const T* Kb = stage_base + (size_t)slot * 2 * head_block;
             st.page(Kb, Kb + head_block, desc[n].y & 0xff, lg, lane);
           }
+          if (pa == pb && base == 0 && n == 0) stamp(11);
           phase ^= 1u << slot;
           __syncwarp();
           if (lane == 0 && n + NST < nv) {
@@ -536,13 +617,13 @@ step_kernel(const StepArgs a) {
       if (cs >= 0)
         st.stash(stash_o + (size_t)cs * kNW * G * D, stash_ml + (size_t)cs * kNW * G * 2, warp, lane);
       __syncthreads();
-      stamp(4 + 3 * qr);
+      if (qr == 0) stamp(4);
 
       // merge each segment's warps into this CTA's partial of the unit
       for (int s = 0; s < ns; ++s) {
         const int kk = rd.k0 + ka + s;
         const int u = (kk % a.batch) * a.h_kv + kk / a.batch;
-        const int pslot = b - rd.owner((long long)(ka + s) * K);
+        const int pslot = bw - rd.owner((long long)(ka + s) * K);
         const size_t prow = (size_t)u * G * NP + pslot;          // (u, gi = 0, pslot)
         merge_warps<D, G, kNW, kNT>(
             stash_o + (size_t)s * kNW * G * D, stash_ml + (size_t)s * kNW * G * 2,
@@ -554,19 +635,19 @@ step_kernel(const StepArgs a) {
       }
       __syncthreads();
       if (tid == 0) {
-        __threadfence();
         int nl = 0;
         for (int s = 0; s < ns; ++s) {
           const int kk = rd.k0 + ka + s;
           const int u = (kk % a.batch) * a.h_kv + kk / a.batch;
           const long long u0 = (long long)(ka + s) * K, u1 = u0 + K;
           const unsigned n = (unsigned)(min(pz, u1) - max(pa, u0));
-          if (atomicAdd(att_done + u, n) + n == (unsigned)K) s_last[nl++] = s;
+          if (atom_add_acq_rel(att_done + u, n) + n == (unsigned)K) s_last[nl++] = s;
         }
         s_nlast = nl;
-        if (nl) __threadfence();
       }
       __syncthreads();
+      stamp(12);
+      if (s_nlast > 0) stamp(13);
       for (int x = 0; x < s_nlast; ++x) {    // this CTA completed the unit: final merge
         const int s = s_last[x];
         const int kk = rd.k0 + ka + s;
@@ -575,49 +656,92 @@ step_kernel(const StepArgs a) {
         const long long u0 = (long long)(ka + s) * K, u1 = u0 + K;
         const int b0 = rd.owner(u0);
         const int nparts = rd.owner(u1 - 1) - b0 + 1;     // slots b0 .. owner(u1-1)
-        // the unit's partials: (max, sum) loaded lane-parallel, weights in smem
+        // one round trip to L2: every thread loads its columns' first kFC
+        // partial outputs while warp gi loads group gi's (max, sum) pairs
+        // lane-parallel and turns them into weights; after one barrier the
+        // columns combine from registers (later partials, if any, from L2)
         float* wbuf = stash_o;     // [G][NP] weights + [G][2] (max, sum); the stash is free here
-        for (int gi = 0; gi < G; ++gi) {
+        constexpr int kCPT = (G * D + kNT - 1) / kNT;       // columns per thread
+        constexpr int kFC = kCPT >= 4 ? 4 : 16 / kCPT;      // partials prefetched per column
+        float ov[kCPT][kFC];
+#pragma unroll
+        for (int c = 0; c < kCPT; ++c) {
+          const int idx = tid + c * kNT;
+          if (idx < G * D) {
+            const size_t row0 = ((size_t)u * G + idx / D) * NP;
+#pragma unroll
+            for (int j = 0; j < kFC; ++j)
+              ov[c][j] = j < nparts ? __ldcg(a.part_o + (row0 + j) * D + idx % D) : 0.f;
+          }
+        }
+        if (warp < G) {
+          const int gi = warp;
           const size_t row0 = ((size_t)u * G + gi) * NP;
-          if (warp == 0) {
-            float mx = -INFINITY;
-            for (int j = lane; j < nparts; j += 32) {
-              const long long pj = max(u0, rd.start(b0 + j));
-              const bool has = pj < u1 && rd.owner(pj) == b0 + j;   // CTA b0+j owns positions of u
-              if (has) mx = fmaxf(mx, __ldcg(a.part_ml + (row0 + j) * 2));
+          constexpr int kML = 2;             // (max, sum) pairs per lane held in registers
+          float2 ml[kML];
+          bool has[kML];
+#pragma unroll
+          for (int t = 0; t < kML; ++t) {
+            const int j = lane + 32 * t;
+            const long long pj = max(u0, rd.start(b0 + j));
+            has[t] = j < nparts && pj < u1 && rd.owner(pj) == b0 + j;   // CTA b0+j owns positions of u
+            ml[t] = has[t] ? __ldcg(reinterpret_cast<const float2*>(a.part_ml) + row0 + j)
+                           : make_float2(-INFINITY, 0.f);
+          }
+          float mx = -INFINITY;
+#pragma unroll
+          for (int t = 0; t < kML; ++t) mx = fmaxf(mx, ml[t].x);
+          for (int j = lane + 32 * kML; j < nparts; j += 32) {      // more than 64 partials
+            const long long pj = max(u0, rd.start(b0 + j));
+            if (pj < u1 && rd.owner(pj) == b0 + j) mx = fmaxf(mx, __ldcg(a.part_ml + (row0 + j) * 2));
+          }
+          mx = warp_max(mx);
+          float l = 0.f;
+#pragma unroll
+          for (int t = 0; t < kML; ++t) {
+            const int j = lane + 32 * t;
+            float w = 0.f;
+            if (has[t] && mx != -INFINITY && ml[t].x != -INFINITY) {
+              w = exp2f(ml[t].x - mx);
+              l = fmaf(w, ml[t].y, l);
             }
-            mx = warp_max(mx);
-            float l = 0.f;
-            for (int j = lane; j < nparts; j += 32) {
-              const long long pj = max(u0, rd.start(b0 + j));
-              const bool has = pj < u1 && rd.owner(pj) == b0 + j;
-              float w = 0.f;
-              if (has && mx != -INFINITY) {
-                const float mc = __ldcg(a.part_ml + (row0 + j) * 2);
-                if (mc != -INFINITY) {
-                  w = exp2f(mc - mx);
-                  l = fmaf(w, __ldcg(a.part_ml + (row0 + j) * 2 + 1), l);
-                }
+            if (j < nparts) wbuf[gi * NP + j] = w;
+          }
+          for (int j = lane + 32 * kML; j < nparts; j += 32) {
+            const long long pj = max(u0, rd.start(b0 + j));
+            float w = 0.f;
+            if (pj < u1 && rd.owner(pj) == b0 + j && mx != -INFINITY) {
+              const float2 mlj = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + row0 + j);
+              if (mlj.x != -INFINITY) {
+                w = exp2f(mlj.x - mx);
+                l = fmaf(w, mlj.y, l);
               }
-              wbuf[gi * NP + j] = w;
             }
-            l = warp_sum(l);
-            if (lane == 0) {
-              wbuf[G * NP + gi * 2 + 0] = mx;
-              wbuf[G * NP + gi * 2 + 1] = l;
-            }
+            wbuf[gi * NP + j] = w;
+          }
+          l = warp_sum(l);
+          if (lane == 0) {
+            wbuf[G * NP + gi * 2 + 0] = mx;
+            wbuf[G * NP + gi * 2 + 1] = l;
           }
         }
         __syncthreads();
-        for (int idx = tid; idx < G * D; idx += kNT) {
+#pragma unroll
+        for (int c = 0; c < kCPT; ++c) {
+          const int idx = tid + c * kNT;
+          if (idx >= G * D) break;
           const int gi = idx / D, col = idx % D;
           const size_t row0 = ((size_t)u * G + gi) * NP;
           const float mx = wbuf[G * NP + gi * 2 + 0], l = wbuf[G * NP + gi * 2 + 1];
           float o = 0.f;
-#pragma unroll 8
-          for (int j = 0; j < nparts; ++j) {
+#pragma unroll
+          for (int j = 0; j < kFC; ++j)          // absent partials hold anything: weight 0 skips them
+            if (j < nparts) { const float w = wbuf[gi * NP + j]; o = fmaf(w, w != 0.f ? ov[c][j] : 0.f, o); }
+#pragma unroll 4
+          for (int j = kFC; j < nparts; ++j) {
             const float w = wbuf[gi * NP + j];
-            if (w != 0.f) o = fmaf(w, __ldcg(a.part_o + (row0 + j) * D + col), o);
+            const float v = __ldcg(a.part_o + (row0 + j) * D + col);
+            o = fmaf(w, w != 0.f ? v : 0.f, o);
           }
           const size_t orow = (size_t)r * h_q + (size_t)g * G + gi;
           a.out[orow * D + col] = l > 0.f ? o / l : 0.f;
@@ -626,9 +750,10 @@ step_kernel(const StepArgs a) {
         if (tid == 0) att_done[u] = 0;       // reset for the next call
         __syncthreads();
       }
+      if (s_nlast > 0) stamp(14);
       __syncthreads();
       pa = pz;
-      if (pa >= pe) stamp(5 + 3 * qr);
+      if (pa >= pe && qr == 0) stamp(5);
     }
   }
   stamp(9);
@@ -637,6 +762,7 @@ step_kernel(const StepArgs a) {
     __threadfence();
     if (atomicAdd(exit_cnt, 1u) == (unsigned)(nblk - 1)) {   // last CTA out
       *exit_cnt = 0;
+      *scored_cnt = 0;
       *epoch = tag;
     }
   }
@@ -740,20 +866,21 @@ StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int3
   p.smem = smem;
   p.grid = sms * (per_sm > 2 ? 2 : per_sm);
   p.ok = per_sm >= 1 && smem <= 227 * 1024 && p.grid > 0;
-  // partial slots per unit: CTAs whose round share can overlap one unit
+  // partial slots per unit: worker CTAs whose round share can overlap one unit
   long long np = 1;
   const int rounds = units < kRounds ? (int)units : kRounds;
-  for (int q = 0; q < rounds && p.grid > 0; ++q) {
+  const int workers = p.grid > 0 ? p.grid - select_ctas((int)units, p.grid) : 0;
+  for (int q = 0; q < rounds && workers > 0; ++q) {
     const long long k0 = q * units / rounds, k1 = (q + 1) * units / rounds;
     const long long len = (k1 - k0) * k;
-    const long long minlen = len / p.grid;
-    const long long n = minlen == 0 ? p.grid : (k + minlen - 1) / minlen + 1;
+    const long long minlen = len / workers;
+    const long long n = minlen == 0 ? workers : (k + minlen - 1) / minlen + 1;
     np = n > np ? n : np;
   }
-  if (np > p.grid) np = p.grid;
+  if (np > workers) np = workers > 0 ? workers : 1;
   p.chunk_pages = 0;
   p.n_chunks = (int32_t)np;
-  p.counters_bytes = ((size_t)(4 + 2 * units) * sizeof(unsigned) + 255) & ~(size_t)255;
+  p.counters_bytes = ((size_t)(4 + 2 * units + 1) * sizeof(unsigned) + 255) & ~(size_t)255;
   p.tagged_bytes = ((size_t)h_kv * nnz * sizeof(unsigned long long) + 255) & ~(size_t)255;
   const size_t rows = (size_t)units * group * p.n_chunks;
   p.workspace_bytes = p.counters_bytes + p.tagged_bytes + rows * head_dim * sizeof(float) +

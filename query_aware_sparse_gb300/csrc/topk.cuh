@@ -9,7 +9,10 @@
 // with 11-bit digits (2048 shared-memory bins: a row of a few thousand
 // scores rarely puts many keys in one bin, so the bin atomics do not pile
 // up), and stops as soon as the digit bucket holding the K-th key is taken
-// whole. A block scan in page order then emits the winners.
+// whole. A block scan in page order then emits the winners. Rows whose keys
+// sit in shared memory (up to 16 per thread) take block_topk_smem: once the
+// first digit has isolated a boundary bucket of at most kTopkGather keys,
+// that bucket is ranked directly instead of taking further digits.
 #pragma once
 
 #include "common.cuh"
@@ -24,12 +27,16 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 constexpr int kTopkBits = 11;                 // radix digit width
 constexpr int kTopkBins = 1 << kTopkBits;
 
+constexpr int kTopkGather = 256;              // largest boundary bucket ranked directly
+
 template <int NT>
 struct TopkSmem {
-  uint32_t hist[kTopkBins];
+  alignas(16) uint32_t hist[kTopkBins];
   uint32_t red[2][NT / 32];
   unsigned long long scan[NT / 32];
-  uint32_t digit, krem, done;
+  uint32_t gkey[kTopkGather];
+  int32_t gidx[kTopkGather];
+  uint32_t digit, krem, done, bcnt, gcount;
 };
 
 // Exclusive block scan of a 64-bit value.
@@ -199,18 +206,198 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm,
 template <int NT, typename PhysOf>
 __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t* keys, int cap,
                            TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
+                           int32_t* out_count, PhysOf phys_of);
+
+// Top-K of P <= 16 * NT keys held in shared memory (`keys`, overwritten),
+// whose block-wide min and max the caller has already reduced. Same result
+// as block_topk_keys. `sm.hist` must be all zero on entry and is all zero
+// on return. After the first radix digit, a boundary bucket of at most
+// kTopkGather keys is ranked directly (key, then lower index) instead of
+// taking more digits: its winners are marked with the top key and its
+// losers with 0, so one threshold then selects exactly K keys.
+template <int NT, typename PhysOf>
+__device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
+                                TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
+                                int32_t* out_count, PhysOf phys_of) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NWP = NT / 32;
+  constexpr int BPT = kTopkBins / NT;            // bins per thread in the digit search
+  static_assert(BPT % 4 == 0, "bins are read as 16-byte vectors");
+  constexpr int KPT = 16;                        // keys per thread in the compaction (max)
+
+  if (P <= K) {                     // every scored page is selected
+    for (int i = tid; i < K; i += NT) {
+      out_logical[i] = i < P ? i : -1;
+      out_phys[i] = i < P ? phys_of(i) : -1;
+    }
+    if (tid == 0) *out_count = P;
+    return;
+  }
+  uint32_t T, need;
+  bool ge_mode;            // select key >= T vs (key > T, then `need` of key == T)
+  if (kmin == kmax) {
+    T = kmin; need = K; ge_mode = false;
+  } else {
+    int hi = 31 - __clz(kmin ^ kmax);           // highest differing bit
+    uint32_t prefix = kmin & ~((hi == 31) ? 0xffffffffu : ((2u << hi) - 1u));
+    uint32_t krem = K;
+    while (true) {
+      const int shift = max(hi - (kTopkBits - 1), 0);
+      const int nbits = hi - shift + 1;
+      const uint32_t dmask = (1u << nbits) - 1u;
+      const uint32_t hi_mask = (hi == 31) ? 0u : ~((2u << hi) - 1u);
+      for (int i = tid; i < P; i += NT) {
+        const uint32_t k = keys[i];
+        if ((k & hi_mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
+      }
+      if (tid == 0) sm.gcount = 0;
+      __syncthreads();
+      // thread t owns bins [t*BPT, t*BPT + BPT); count of keys in higher bins
+      uint32_t h[BPT], tot = 0;
+#pragma unroll
+      for (int j = 0; j < BPT; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(&sm.hist[tid * BPT + j]);
+        h[j] = v.x; h[j + 1] = v.y; h[j + 2] = v.z; h[j + 3] = v.w;
+        tot += v.x + v.y + v.z + v.w;
+      }
+#pragma unroll
+      for (int j = 0; j < BPT; j += 4)
+        *reinterpret_cast<uint4*>(&sm.hist[tid * BPT + j]) = make_uint4(0u, 0u, 0u, 0u);
+      uint32_t incl = tot;                         // suffix sum within the warp
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_down_sync(FULL, incl, o);
+        if (lane + o < 32) incl += t;
+      }
+      if (lane == 0) sm.red[0][warp] = incl;       // warp totals
+      __syncthreads();
+      uint32_t above = incl - tot;
+#pragma unroll
+      for (int w = 0; w < NWP; ++w)
+        if (w > warp) above += sm.red[0][w];
+      uint32_t cum = above;
+#pragma unroll
+      for (int j = BPT - 1; j >= 0; --j) {
+        if (cum < krem && krem <= cum + h[j]) {
+          sm.digit = tid * BPT + j;
+          sm.krem = krem - cum;
+          sm.bcnt = h[j];
+          sm.done = (h[j] == krem - cum) ? 1u : 0u;   // bucket taken whole
+        }
+        cum += h[j];
+      }
+      __syncthreads();
+      prefix |= sm.digit << shift;
+      krem = sm.krem;
+      const uint32_t bcnt = sm.bcnt;
+      if (sm.done || shift == 0) {
+        T = prefix;
+        need = krem;
+        ge_mode = sm.done && shift > 0;
+        break;
+      }
+      if (bcnt <= (uint32_t)kTopkGather) {
+        // rank the bucket [prefix, prefix + 2^shift) directly
+        const uint32_t span = (1u << shift) - 1u;
+        for (int i = tid; i < P; i += NT) {
+          const uint32_t k = keys[i];
+          if ((k & ~span) == prefix) {
+            const uint32_t at = atomicAdd(&sm.gcount, 1u);
+            sm.gkey[at] = k;
+            sm.gidx[at] = i;
+          }
+        }
+        __syncthreads();
+        if (tid < (int)bcnt) {
+          const uint32_t mk = sm.gkey[tid];
+          const int mi = sm.gidx[tid];
+          uint32_t rank = 0;
+          for (int j = 0; j < (int)bcnt; ++j) {
+            const uint32_t kj = sm.gkey[j];
+            rank += (kj > mk) || (kj == mk && sm.gidx[j] < mi);
+          }
+          keys[mi] = rank < krem ? 0xffffffffu : 0u;
+        }
+        const unsigned long long top = (unsigned long long)prefix + (1ull << shift);
+        T = top > 0xffffffffull ? 0xffffffffu : (uint32_t)top;
+        need = 0;
+        ge_mode = true;
+        break;
+      }
+      hi = shift - 1;
+    }
+    __syncthreads();   // marks written; sm.digit/krem/done read by all
+  }
+
+  // Stable compaction in page order: thread t takes keys [c0, c1) into registers.
+  const int per = (P + NT - 1) / NT;
+  const int c0 = min(P, tid * per), c1 = min(P, c0 + per);
+  uint32_t kr[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) kr[j] = (j < c1 - c0) ? keys[c0 + j] : 0u;
+  uint32_t gt = 0, eq = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    if (j < c1 - c0) {
+      if (ge_mode) gt += kr[j] >= T;
+      else { gt += kr[j] > T; eq += kr[j] == T; }
+    }
+  }
+  const unsigned long long ex = topk_excl_scan<NT>(((unsigned long long)gt << 32) | eq, sm);
+  uint32_t gt_b = (uint32_t)(ex >> 32), eq_b = (uint32_t)ex;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    if (j < c1 - c0) {
+      const uint32_t k = kr[j];
+      int pos = -1;
+      if (ge_mode) {
+        if (k >= T) pos = gt_b++;
+      } else if (k > T) {
+        pos = gt_b + min(eq_b, need);
+        ++gt_b;
+      } else if (k == T) {
+        if (eq_b < need) pos = gt_b + eq_b;
+        ++eq_b;
+      }
+      if (pos >= 0 && pos < K) {
+        out_logical[pos] = c0 + j;
+        out_phys[pos] = phys_of(c0 + j);
+      }
+    }
+  }
+  if (tid == 0) *out_count = K;
+}
+
+template <int NT, typename PhysOf>
+__device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t* keys, int cap,
+                           TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
                            int32_t* out_count, PhysOf phys_of) {
   const bool cached = P <= cap && P > K;
-  if (cached) {
-    for (int i = threadIdx.x; i < P; i += NT) keys[i] = score_key(__ldcg(sc + i));
-    __syncthreads();
-  }
-  if (cached)
-    block_topk_keys<NT>(P, K, [keys](int i) { return keys[i]; }, sm, out_logical, out_phys,
-                        out_count, phys_of);
-  else
+  if (!cached) {
     block_topk_keys<NT>(P, K, [sc](int i) { return score_key(__ldcg(sc + i)); }, sm,
                         out_logical, out_phys, out_count, phys_of);
+    return;
+  }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int i = tid; i < P; i += NT) {
+    const uint32_t k = score_key(__ldcg(sc + i));
+    keys[i] = k;
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+  kmin = warp_min_u32(kmin);
+  kmax = warp_max_u32(kmax);
+  if (lane == 0) { sm.red[0][warp] = kmin; sm.red[1][warp] = kmax; }
+  for (int i = tid; i < kTopkBins; i += NT) sm.hist[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) { kmin = min(kmin, sm.red[0][w]); kmax = max(kmax, sm.red[1][w]); }
+  if (P <= 16 * NT)
+    block_topk_smem<NT>(P, K, keys, kmin, kmax, sm, out_logical, out_phys, out_count, phys_of);
+  else            // longer cached rows: the general routine over the shared-memory keys
+    block_topk_keys<NT>(P, K, [keys](int i) { return keys[i]; }, sm, out_logical, out_phys,
+                        out_count, phys_of);
 }
 
 }  // namespace quest

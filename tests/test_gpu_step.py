@@ -64,10 +64,10 @@ def _run(w, lens, steps, seed, append=True):
         else:
             step(cache, gtab, q.cuda())
         assert qs.device_error() == 0
-        # after every call: queue and exit counters and the per-unit chunk
-        # counters are back at zero; the call tag and the ready flags hold
-        # the number of calls made so far
-        cnt = step.workspace[:(4 + 2 * B * h) * 4].view(torch.int32).cpu().numpy()
+        # after every call: the exit counter, the per-unit slot counters and
+        # the scored-workers counter are back at zero; the call tag and the
+        # ready flags hold the number of calls made so far
+        cnt = step.workspace[:(4 + 2 * B * h + 1) * 4].view(torch.int32).cpu().numpy()
         assert cnt[0] == s + 1 and cnt[1] == 0 and cnt[2] == 0
         assert np.all(cnt[4:4 + B * h] == s + 1) and np.all(cnt[4 + B * h:] == 0)
         gsm = np_of(cache.summary)
