@@ -43,6 +43,7 @@ attn_split_kernel(const AttnArgs a) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::BAR_OFF);
   float* logits_all = reinterpret_cast<float*>(smem + Sh::LOGIT_OFF);
   int2* desc_all = reinterpret_cast<int2*>(smem + Sh::DESC_OFF);
+  const uint64_t pol = evict_first_policy();   // K/V pages are read once
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = blockIdx.x % a.n_chunks;
@@ -93,8 +94,8 @@ attn_split_kernel(const AttnArgs a) {
     const int pp = desc[n].x;
     T* dst = my_stage + (size_t)slot * 2 * head_block;
     mbar_expect_tx(my_bars + slot, 2 * W::BLOCK_BYTES);
-    bulk_g2s(dst, kbase + (size_t)pp * page_stride, W::BLOCK_BYTES, my_bars + slot);
-    bulk_g2s(dst + head_block, vbase + (size_t)pp * page_stride, W::BLOCK_BYTES, my_bars + slot);
+    bulk_g2s_hint(dst, kbase + (size_t)pp * page_stride, W::BLOCK_BYTES, my_bars + slot, pol);
+    bulk_g2s_hint(dst + head_block, vbase + (size_t)pp * page_stride, W::BLOCK_BYTES, my_bars + slot, pol);
   };
   if (lane == 0)
     for (int n = 0; n < min(kNST, nv); ++n) issue(n);

@@ -51,6 +51,7 @@ score_kernel(const ScoreArgs a) {
   __shared__ int s_rfirst, s_rlast;
 
   const int g = blockIdx.y;
+  const uint64_t pol = evict_first_policy();   // summaries are read once
   const int e_begin = blockIdx.x * Sh::TILE;
   const int e_end = min(a.nnz, e_begin + Sh::TILE);
   if (threadIdx.x == 0) {
@@ -87,8 +88,8 @@ score_kernel(const ScoreArgs a) {
         if (pp >= 0 && pp < a.n_phys) {
           const T* sp = static_cast<const T*>(a.summary) +
                         ((size_t)pp * a.h_kv + g) * 2 * D + sub * VEC;
-          vm[u] = ld_stream_v4(sp);
-          vM[u] = ld_stream_v4(sp + D);
+          vm[u] = ld_stream_v4_hint(sp, pol);
+          vM[u] = ld_stream_v4_hint(sp + D, pol);
           live[u] = true;
         } else if (sub == 0) {
           report(a.err, QUEST_DEVERR_PAGE_RANGE);

@@ -17,8 +17,9 @@
 // load, a barrier or another CTA. Each score is also stored with the call's
 // tag in the upper half of a 64-bit word: a reader tells a score of this
 // call from a stale one without any fence on the writer's side. Each worker
-// then bumps a relaxed "scored" counter, a hint that lets the selectors read
-// their rows once instead of polling them while the workers stream.
+// then bumps a "scored" counter with a release; a selector acquires it before
+// reading its row once (instead of polling it while the workers stream), so
+// the appended K/V rows are ordered before the attention's copies of them.
 //
 // Selection. Selectors take the (request, KV head) units in head order, read
 // a unit's tagged row (batches of independent loads, re-polling only stale
@@ -80,8 +81,8 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   unsigned v;
@@ -177,13 +178,14 @@ step_kernel(const StepArgs a) {
   unsigned* exit_cnt = a.counters + 2;      // CTAs finished
   unsigned* ready = a.counters + 4;         // [U] tag of the published selection
   unsigned* att_done = ready + U;           // [U] attention slots finished
-  unsigned* scored_cnt = att_done + U;      // workers done scoring (a hint for the selectors)
+  unsigned* scored_cnt = att_done + U;      // workers done scoring (released by each)
   unsigned tag = ld_relaxed_u32(epoch) + 1u;
   if (tag == 0u) tag = 1u;                  // 0 marks never-written entries
   // optional phase trace: kTraceSlots globaltimer stamps per CTA
   unsigned long long* trace = a.trace ? a.trace + (size_t)b * kTraceSlots : nullptr;
   auto stamp = [&](int i) { if (trace && tid == 0) trace[i] = global_ns(); };
   stamp(0);
+  const uint64_t pol_stream = evict_first_policy();   // summaries and K/V pages: read once
 
   const int NSEL = select_ctas(U, nblk);    // CTAs [0, NSEL) select; the rest score and attend
   const bool selector = b < NSEL;
@@ -282,8 +284,8 @@ step_kernel(const StepArgs a) {
           const T* sp = static_cast<const T*>(a.summary) + ((size_t)x * a.h_kv + ig) * 2 * D + sub * VPL * VEC;
 #pragma unroll
           for (int v = 0; v < VPL; ++v) {
-            bm[u][v] = ld_stream_v4(sp + v * VEC);
-            bM[u][v] = ld_stream_v4(sp + D + v * VEC);
+            bm[u][v] = ld_stream_v4_hint(sp + v * VEC, pol_stream);
+            bM[u][v] = ld_stream_v4_hint(sp + D + v * VEC, pol_stream);
           }
         }
       }
@@ -403,7 +405,10 @@ step_kernel(const StepArgs a) {
     }
   }
   __syncthreads();
-  if (!selector && tid == 0) red_relaxed_add(scored_cnt, 1u);   // hint for the selectors
+  // release: the appends and tagged scores of this worker happen before a
+  // selector's acquire of the count (and so before the attention that
+  // follows the selection)
+  if (!selector && tid == 0) red_release_add(scored_cnt, 1u);
   stamp(1);
 
   // =================== selection (selector b takes units b, b + NSEL, ... in head order) ===================
@@ -428,7 +433,7 @@ step_kernel(const StepArgs a) {
       // scoring, so the block reads the row once instead of polling it while
       // the workers stream; the row's tags still decide below
       if (tid == 0)
-        for (uint32_t it = 0; ld_relaxed_u32(scored_cnt) < (unsigned)nbw && it < (1u << 20); ++it)
+        for (uint32_t it = 0; ld_acquire(scored_cnt) < (unsigned)nbw && it < (1u << 20); ++it)
           __nanosleep(128);
       __syncthreads();
       // each thread waits for its own entries to carry this call's tag: a
@@ -580,8 +585,8 @@ step_kernel(const StepArgs a) {
           T* dst = stage_base + (size_t)slot * 2 * head_block;
           const size_t off = (size_t)desc[n].x * page_stride + (size_t)g * head_block;
           mbar_expect_tx(bars + slot, 2 * W::BLOCK_BYTES);
-          bulk_g2s(dst, static_cast<const T*>(a.k_pool) + off, W::BLOCK_BYTES, bars + slot);
-          bulk_g2s(dst + head_block, static_cast<const T*>(a.v_pool) + off, W::BLOCK_BYTES, bars + slot);
+          bulk_g2s_hint(dst, static_cast<const T*>(a.k_pool) + off, W::BLOCK_BYTES, bars + slot, pol_stream);
+          bulk_g2s_hint(dst + head_block, static_cast<const T*>(a.v_pool) + off, W::BLOCK_BYTES, bars + slot, pol_stream);
         };
         if (lane == 0 && nv > 0) {
           fence_proxy_async_all();           // acquired pool writes and reused stages
@@ -648,8 +653,15 @@ step_kernel(const StepArgs a) {
       __syncthreads();
       stamp(12);
       if (s_nlast > 0) stamp(13);
-      for (int x = 0; x < s_nlast; ++x) {    // this CTA completed the unit: final merge
-        const int s = s_last[x];
+      // this CTA completed these units: final merges, kUP units at a time
+      // (each on its own part of the block when a unit needs at most half)
+      constexpr int kUP = (G * D * 2 <= kNT) ? 2 : 1;
+      constexpr int kTPU = kNT / kUP, kWPU = kNW / kUP;
+      for (int x0 = 0; x0 < s_nlast; x0 += kUP) {
+        const int hx = tid / kTPU, ltid = tid % kTPU, lwarp = warp % kWPU;
+        const int x = x0 + hx;
+        const bool act = x < s_nlast;
+        const int s = act ? s_last[x] : 0;
         const int kk = rd.k0 + ka + s;
         const int r = kk % a.batch, g = kk / a.batch;
         const int u = r * a.h_kv + g;
@@ -660,22 +672,22 @@ step_kernel(const StepArgs a) {
         // partial outputs while warp gi loads group gi's (max, sum) pairs
         // lane-parallel and turns them into weights; after one barrier the
         // columns combine from registers (later partials, if any, from L2)
-        float* wbuf = stash_o;     // [G][NP] weights + [G][2] (max, sum); the stash is free here
-        constexpr int kCPT = (G * D + kNT - 1) / kNT;       // columns per thread
+        float* wbuf = stash_o + hx * (G * NP + 2 * G);   // [G][NP] weights + [G][2] (max, sum)
+        constexpr int kCPT = (G * D + kTPU - 1) / kTPU;      // columns per thread
         constexpr int kFC = kCPT >= 4 ? 4 : 16 / kCPT;      // partials prefetched per column
         float ov[kCPT][kFC];
 #pragma unroll
         for (int c = 0; c < kCPT; ++c) {
-          const int idx = tid + c * kNT;
-          if (idx < G * D) {
+          const int idx = ltid + c * kTPU;
+          if (act && idx < G * D) {
             const size_t row0 = ((size_t)u * G + idx / D) * NP;
 #pragma unroll
             for (int j = 0; j < kFC; ++j)
               ov[c][j] = j < nparts ? __ldcg(a.part_o + (row0 + j) * D + idx % D) : 0.f;
           }
         }
-        if (warp < G) {
-          const int gi = warp;
+        if (act && lwarp < G) {
+          const int gi = lwarp;
           const size_t row0 = ((size_t)u * G + gi) * NP;
           constexpr int kML = 2;             // (max, sum) pairs per lane held in registers
           float2 ml[kML];
@@ -728,8 +740,8 @@ step_kernel(const StepArgs a) {
         __syncthreads();
 #pragma unroll
         for (int c = 0; c < kCPT; ++c) {
-          const int idx = tid + c * kNT;
-          if (idx >= G * D) break;
+          const int idx = ltid + c * kTPU;
+          if (!act || idx >= G * D) break;
           const int gi = idx / D, col = idx % D;
           const size_t row0 = ((size_t)u * G + gi) * NP;
           const float mx = wbuf[G * NP + gi * 2 + 0], l = wbuf[G * NP + gi * 2 + 1];
@@ -747,7 +759,7 @@ step_kernel(const StepArgs a) {
           a.out[orow * D + col] = l > 0.f ? o / l : 0.f;
           if (col == 0 && a.lse) a.lse[orow] = l > 0.f ? (mx + log2f(l)) * LN2 : -INFINITY;
         }
-        if (tid == 0) att_done[u] = 0;       // reset for the next call
+        if (act && ltid == 0) att_done[u] = 0;   // reset for the next call
         __syncthreads();
       }
       if (s_nlast > 0) stamp(14);
