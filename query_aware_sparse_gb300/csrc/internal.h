@@ -58,7 +58,7 @@ struct StepArgs {
   float* out; float* lse;
   unsigned* counters;                         // [4 + 2 * units], see step.cu
   unsigned long long* tagged;                 // [h_kv, nnz] score bits | call tag << 32
-  float* part_o; float* part_ml;              // [units, group, n_chunks, head_dim | 2]
+  float* part_o; float* part_ml;              // [units, group, n_chunks, head_dim | 4 (max, sum, tag, 0)]
   int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype, k;
   int32_t n_chunks, chunk_pages;
   float scale_log2;

@@ -146,14 +146,30 @@ __device__ __forceinline__ int find_req(const int32_t* indptr, int lo, int hi, i
   return lo;
 }
 
-// Attention round: units [k0, k1) in head order, `len` slot positions split
-// over `nblk` CTAs; CTA b owns positions [start(b), start(b+1)).
+// Attention round: units [k0, k1) in head order, `len` = units * K slot
+// positions over `nblk` worker CTAs; worker b owns positions [start(b),
+// start(b+1)). With no more units than workers, unit u gets its own group of
+// workers [u*nblk/units, (u+1)*nblk/units) and its K positions are split
+// evenly inside the group, so no worker spans two units; otherwise the
+// positions are split evenly over all workers.
 struct Round {
   long long len;
-  int k0, k1, nblk;
-  __device__ long long start(int b) const { return (long long)b * len / nblk; }
+  int k0, k1, nblk, K;
+  __device__ bool aligned() const { return k1 - k0 <= nblk; }
+  __device__ int group0(int u) const { return (int)((long long)u * nblk / (k1 - k0)); }
+  __device__ long long start(int b) const {
+    if (!aligned()) return (long long)b * len / nblk;
+    const int nu = k1 - k0;
+    const int u = (int)(((long long)(b + 1) * nu - 1) / nblk);   // largest u with group0(u) <= b
+    if (u >= nu) return len;
+    const int j = b - group0(u), n = group0(u + 1) - group0(u);
+    return (long long)u * K + (long long)j * K / n;
+  }
   __device__ int owner(long long p) const {      // largest b with start(b) <= p
-    return (int)(((p + 1) * nblk - 1) / len);
+    if (!aligned()) return (int)(((p + 1) * nblk - 1) / len);
+    const int u = (int)(p / K), o = (int)(p % K);
+    const int n = group0(u + 1) - group0(u);
+    return group0(u) + (int)(((long long)(o + 1) * n - 1) / K);
   }
 };
 
@@ -519,6 +535,7 @@ step_kernel(const StepArgs a) {
     rd.k1 = (int)((long long)(qr + 1) * U / nrounds);
     rd.len = (long long)(rd.k1 - rd.k0) * K;
     rd.nblk = nbw;
+    rd.K = K;
     const long long pb = rd.start(bw), pe = rd.start(bw + 1);   // relative to unit k0
 #pragma unroll 1
     for (long long pa = pb; pa < pe;) {
@@ -633,9 +650,9 @@ step_kernel(const StepArgs a) {
         merge_warps<D, G, kNW, kNT>(
             stash_o + (size_t)s * kNW * G * D, stash_ml + (size_t)s * kNW * G * 2,
             [&](int gi, int col, float o) { a.part_o[(prow + (size_t)gi * NP) * D + col] = o; },
-            [&](int gi, float mx, float l) {
-              a.part_ml[(prow + (size_t)gi * NP) * 2 + 0] = mx;
-              a.part_ml[(prow + (size_t)gi * NP) * 2 + 1] = l;
+            [&](int gi, float mx, float l) {   // (max, sum, call tag, 0): the tag marks it current
+              reinterpret_cast<float4*>(a.part_ml)[prow + (size_t)gi * NP] =
+                  make_float4(mx, l, __uint_as_float(tag), 0.f);
             });
       }
       __syncthreads();
@@ -665,9 +682,7 @@ step_kernel(const StepArgs a) {
         const int kk = rd.k0 + ka + s;
         const int r = kk % a.batch, g = kk / a.batch;
         const int u = r * a.h_kv + g;
-        const long long u0 = (long long)(ka + s) * K, u1 = u0 + K;
-        const int b0 = rd.owner(u0);
-        const int nparts = rd.owner(u1 - 1) - b0 + 1;     // slots b0 .. owner(u1-1)
+        const int nparts = NP;               // every slot; those not written this call weigh 0
         // one round trip to L2: every thread loads its columns' first kFC
         // partial outputs while warp gi loads group gi's (max, sum) pairs
         // lane-parallel and turns them into weights; after one barrier the
@@ -689,23 +704,24 @@ step_kernel(const StepArgs a) {
         if (act && lwarp < G) {
           const int gi = lwarp;
           const size_t row0 = ((size_t)u * G + gi) * NP;
+          const float4* mlr = reinterpret_cast<const float4*>(a.part_ml) + row0;
+          // a slot holds a partial of this call iff it carries the call's tag
+          // (workers with no position of the unit leave theirs stale)
           constexpr int kML = 2;             // (max, sum) pairs per lane held in registers
           float2 ml[kML];
-          bool has[kML];
 #pragma unroll
           for (int t = 0; t < kML; ++t) {
             const int j = lane + 32 * t;
-            const long long pj = max(u0, rd.start(b0 + j));
-            has[t] = j < nparts && pj < u1 && rd.owner(pj) == b0 + j;   // CTA b0+j owns positions of u
-            ml[t] = has[t] ? __ldcg(reinterpret_cast<const float2*>(a.part_ml) + row0 + j)
-                           : make_float2(-INFINITY, 0.f);
+            float4 v = j < nparts ? __ldcg(mlr + j) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+            if (__float_as_uint(v.z) != tag) v.x = -INFINITY;
+            ml[t] = make_float2(v.x, v.y);
           }
           float mx = -INFINITY;
 #pragma unroll
           for (int t = 0; t < kML; ++t) mx = fmaxf(mx, ml[t].x);
           for (int j = lane + 32 * kML; j < nparts; j += 32) {      // more than 64 partials
-            const long long pj = max(u0, rd.start(b0 + j));
-            if (pj < u1 && rd.owner(pj) == b0 + j) mx = fmaxf(mx, __ldcg(a.part_ml + (row0 + j) * 2));
+            const float4 v = __ldcg(mlr + j);
+            if (__float_as_uint(v.z) == tag) mx = fmaxf(mx, v.x);
           }
           mx = warp_max(mx);
           float l = 0.f;
@@ -713,21 +729,18 @@ step_kernel(const StepArgs a) {
           for (int t = 0; t < kML; ++t) {
             const int j = lane + 32 * t;
             float w = 0.f;
-            if (has[t] && mx != -INFINITY && ml[t].x != -INFINITY) {
+            if (mx != -INFINITY && ml[t].x != -INFINITY) {
               w = exp2f(ml[t].x - mx);
               l = fmaf(w, ml[t].y, l);
             }
             if (j < nparts) wbuf[gi * NP + j] = w;
           }
           for (int j = lane + 32 * kML; j < nparts; j += 32) {
-            const long long pj = max(u0, rd.start(b0 + j));
+            const float4 v = __ldcg(mlr + j);
             float w = 0.f;
-            if (pj < u1 && rd.owner(pj) == b0 + j && mx != -INFINITY) {
-              const float2 mlj = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + row0 + j);
-              if (mlj.x != -INFINITY) {
-                w = exp2f(mlj.x - mx);
-                l = fmaf(w, mlj.y, l);
-              }
+            if (__float_as_uint(v.z) == tag && mx != -INFINITY && v.x != -INFINITY) {
+              w = exp2f(v.x - mx);
+              l = fmaf(w, v.y, l);
             }
             wbuf[gi * NP + j] = w;
           }
@@ -885,8 +898,13 @@ StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int3
   for (int q = 0; q < rounds && workers > 0; ++q) {
     const long long k0 = q * units / rounds, k1 = (q + 1) * units / rounds;
     const long long len = (k1 - k0) * k;
-    const long long minlen = len / workers;
-    const long long n = minlen == 0 ? workers : (k + minlen - 1) / minlen + 1;
+    long long n;
+    if (k1 - k0 <= workers) {                  // a group of workers per unit
+      n = (workers + (k1 - k0) - 1) / (k1 - k0);
+    } else {
+      const long long minlen = len / workers;
+      n = minlen == 0 ? workers : (k + minlen - 1) / minlen + 1;
+    }
     np = n > np ? n : np;
   }
   if (np > workers) np = workers > 0 ? workers : 1;
@@ -896,7 +914,7 @@ StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int3
   p.tagged_bytes = ((size_t)h_kv * nnz * sizeof(unsigned long long) + 255) & ~(size_t)255;
   const size_t rows = (size_t)units * group * p.n_chunks;
   p.workspace_bytes = p.counters_bytes + p.tagged_bytes + rows * head_dim * sizeof(float) +
-                      rows * 2 * sizeof(float);
+                      rows * 4 * sizeof(float);
   p.workspace_bytes = (p.workspace_bytes + 255) & ~(size_t)255;
   return p;
 }
