@@ -214,7 +214,9 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
 // on return. After the first radix digit, a boundary bucket of at most
 // kTopkGather keys is ranked directly (key, then lower index) instead of
 // taking more digits: its winners are marked with the top key and its
-// losers with 0, so one threshold then selects exactly K keys.
+// losers with 0, so one threshold then selects exactly K keys. Loops stay
+// rolled (this runs once per row: its code is fetched cold) and the page-
+// order scan packs (greater, equal) counts into 32 bits with one barrier.
 template <int NT, typename PhysOf>
 __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
                                 TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
@@ -223,7 +225,6 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
   constexpr int NWP = NT / 32;
   constexpr int BPT = kTopkBins / NT;            // bins per thread in the digit search
   static_assert(BPT % 4 == 0, "bins are read as 16-byte vectors");
-  constexpr int KPT = 16;                        // keys per thread in the compaction (max)
 
   if (P <= K) {                     // every scored page is selected
     for (int i = tid; i < K; i += NT) {
@@ -246,6 +247,7 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
       const int nbits = hi - shift + 1;
       const uint32_t dmask = (1u << nbits) - 1u;
       const uint32_t hi_mask = (hi == 31) ? 0u : ~((2u << hi) - 1u);
+#pragma unroll 1
       for (int i = tid; i < P; i += NT) {
         const uint32_t k = keys[i];
         if ((k & hi_mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
@@ -259,10 +261,8 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
         const uint4 v = *reinterpret_cast<const uint4*>(&sm.hist[tid * BPT + j]);
         h[j] = v.x; h[j + 1] = v.y; h[j + 2] = v.z; h[j + 3] = v.w;
         tot += v.x + v.y + v.z + v.w;
-      }
-#pragma unroll
-      for (int j = 0; j < BPT; j += 4)
         *reinterpret_cast<uint4*>(&sm.hist[tid * BPT + j]) = make_uint4(0u, 0u, 0u, 0u);
+      }
       uint32_t incl = tot;                         // suffix sum within the warp
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -271,11 +271,10 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
       }
       if (lane == 0) sm.red[0][warp] = incl;       // warp totals
       __syncthreads();
-      uint32_t above = incl - tot;
+      uint32_t cum = incl - tot;
 #pragma unroll
       for (int w = 0; w < NWP; ++w)
-        if (w > warp) above += sm.red[0][w];
-      uint32_t cum = above;
+        if (w > warp) cum += sm.red[0][w];
 #pragma unroll
       for (int j = BPT - 1; j >= 0; --j) {
         if (cum < krem && krem <= cum + h[j]) {
@@ -299,6 +298,7 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
       if (bcnt <= (uint32_t)kTopkGather) {
         // rank the bucket [prefix, prefix + 2^shift) directly
         const uint32_t span = (1u << shift) - 1u;
+#pragma unroll 1
         for (int i = tid; i < P; i += NT) {
           const uint32_t k = keys[i];
           if ((k & ~span) == prefix) {
@@ -312,6 +312,7 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
           const uint32_t mk = sm.gkey[tid];
           const int mi = sm.gidx[tid];
           uint32_t rank = 0;
+#pragma unroll 1
           for (int j = 0; j < (int)bcnt; ++j) {
             const uint32_t kj = sm.gkey[j];
             rank += (kj > mk) || (kj == mk && sm.gidx[j] < mi);
@@ -329,40 +330,46 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
     __syncthreads();   // marks written; sm.digit/krem/done read by all
   }
 
-  // Stable compaction in page order: thread t takes keys [c0, c1) into registers.
+  // Stable compaction in page order: thread t takes keys [c0, c1); its
+  // (greater, equal) counts are packed 16:16 (P <= 4096 fits).
   const int per = (P + NT - 1) / NT;
   const int c0 = min(P, tid * per), c1 = min(P, c0 + per);
-  uint32_t kr[KPT];
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) kr[j] = (j < c1 - c0) ? keys[c0 + j] : 0u;
-  uint32_t gt = 0, eq = 0;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    if (j < c1 - c0) {
-      if (ge_mode) gt += kr[j] >= T;
-      else { gt += kr[j] > T; eq += kr[j] == T; }
-    }
+  uint32_t cnt = 0;
+#pragma unroll 1
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t k = keys[i];
+    if (ge_mode) cnt += (k >= T) << 16;
+    else cnt += ((k > T) << 16) | (k == T);
   }
-  const unsigned long long ex = topk_excl_scan<NT>(((unsigned long long)gt << 32) | eq, sm);
-  uint32_t gt_b = (uint32_t)(ex >> 32), eq_b = (uint32_t)ex;
+  uint32_t incl = cnt;
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    if (j < c1 - c0) {
-      const uint32_t k = kr[j];
-      int pos = -1;
-      if (ge_mode) {
-        if (k >= T) pos = gt_b++;
-      } else if (k > T) {
-        pos = gt_b + min(eq_b, need);
-        ++gt_b;
-      } else if (k == T) {
-        if (eq_b < need) pos = gt_b + eq_b;
-        ++eq_b;
-      }
-      if (pos >= 0 && pos < K) {
-        out_logical[pos] = c0 + j;
-        out_phys[pos] = phys_of(c0 + j);
-      }
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sm.red[1][warp] = incl;
+  __syncthreads();
+  uint32_t ex = incl - cnt;
+#pragma unroll
+  for (int w = 0; w < NWP; ++w)
+    if (w < warp) ex += sm.red[1][w];
+  uint32_t gt_b = ex >> 16, eq_b = ex & 0xffffu;
+#pragma unroll 1
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t k = keys[i];
+    int pos = -1;
+    if (ge_mode) {
+      if (k >= T) pos = gt_b++;
+    } else if (k > T) {
+      pos = gt_b + min(eq_b, need);
+      ++gt_b;
+    } else if (k == T) {
+      if (eq_b < need) pos = gt_b + eq_b;
+      ++eq_b;
+    }
+    if (pos >= 0 && pos < K) {
+      out_logical[pos] = i;
+      out_phys[pos] = phys_of(i);
     }
   }
   if (tid == 0) *out_count = K;
