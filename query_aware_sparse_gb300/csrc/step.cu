@@ -494,15 +494,18 @@ step_kernel(const StepArgs a) {
       for (int w = 0; w < kNW; ++w) { kmin = min(kmin, tsm.red[0][w]); kmax = max(kmax, tsm.red[1][w]); }
       const int nth = (kk - b) / NSEL;       // this CTA's n-th select
       if (nth < 3) stamp(10 + 2 * nth);
-      auto phys = [idx, physs, cached](int j) { return cached ? physs[j] : __ldg(idx + j); };
       int32_t* ol = a.sel_logical + (size_t)u * K;
       int32_t* op = a.sel_phys + (size_t)u * K;
+      const int nsel = min(P, K);
+      for (int q = nsel + tid; q < K; q += kNT) { ol[q] = -1; op[q] = -1; }
+      if (tid == 0) a.sel_count[u] = nsel;
+      auto emit = [&](int pos, int i) { ol[pos] = i; op[pos] = cached ? physs[i] : __ldg(idx + i); };
       if (cached)
-        block_topk_smem<kNT>(P, K, keys, kmin, kmax, tsm, ol, op, a.sel_count + u, phys);
+        block_topk_smem<kNT>(P, K, keys, kmin, kmax, tsm, emit);
       else
         block_topk_keys<kNT>(P, K, [row](int i) {
                                return score_key(__uint_as_float((unsigned)ld_relaxed_u64(row + i)));
-                             }, tsm, ol, op, a.sel_count + u, phys);
+                             }, tsm, emit);
       __syncthreads();
       if (tid == 0) st_release(ready + u, tag);   // releases the block's selection writes
       if (nth < 3) stamp(11 + 2 * nth);

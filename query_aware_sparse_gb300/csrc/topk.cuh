@@ -70,22 +70,16 @@ __device__ __forceinline__ unsigned long long topk_excl_scan(unsigned long long 
 }
 
 // Top-K of the P keys of one row, read through `key_at(i)` (shared memory or
-// global). Writes out_logical[0..K), out_phys[0..K) (-1 padded), *out_count.
-// `phys_of` maps a page index of the row to its physical page. All NT
-// threads of the block must call it (it synchronises the block).
-template <int NT, typename KeyAt, typename PhysOf>
-__device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm,
-                                int32_t* out_logical, int32_t* out_phys, int32_t* out_count,
-                                PhysOf phys_of) {
+// global): emit(pos, i) is called once for each of the min(P, K) selected
+// pages i, pos being its place in ascending page order. All NT threads of
+// the block must call it (it synchronises the block).
+template <int NT, typename KeyAt, typename Emit>
+__device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Emit emit) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWP = NT / 32;
 
   if (P <= K) {                     // every scored page is selected
-    for (int i = tid; i < K; i += NT) {
-      out_logical[i] = i < P ? i : -1;
-      out_phys[i] = i < P ? phys_of(i) : -1;
-    }
-    if (tid == 0) *out_count = P;
+    for (int i = tid; i < P; i += NT) emit(i, i);
     return;
   }
   uint32_t kmin = 0xffffffffu, kmax = 0u;
@@ -193,12 +187,8 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm,
       if (eq_b < need) pos = gt_b + eq_b;
       ++eq_b;
     }
-    if (pos >= 0 && pos < K) {
-      out_logical[pos] = i;
-      out_phys[pos] = phys_of(i);
-    }
+    if (pos >= 0 && pos < K) emit(pos, i);
   }
-  if (tid == 0) *out_count = K;
 }
 
 // Top-K of P fp32 scores `sc` (global) for one row; `keys` caches up to `cap`
@@ -217,21 +207,16 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
 // losers with 0, so one threshold then selects exactly K keys. Loops stay
 // rolled (this runs once per row: its code is fetched cold) and the page-
 // order scan packs (greater, equal) counts into 32 bits with one barrier.
-template <int NT, typename PhysOf>
+template <int NT, typename Emit>
 __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
-                                TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
-                                int32_t* out_count, PhysOf phys_of) {
+                                TopkSmem<NT>& sm, Emit emit) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWP = NT / 32;
   constexpr int BPT = kTopkBins / NT;            // bins per thread in the digit search
   static_assert(BPT % 4 == 0, "bins are read as 16-byte vectors");
 
   if (P <= K) {                     // every scored page is selected
-    for (int i = tid; i < K; i += NT) {
-      out_logical[i] = i < P ? i : -1;
-      out_phys[i] = i < P ? phys_of(i) : -1;
-    }
-    if (tid == 0) *out_count = P;
+    for (int i = tid; i < P; i += NT) emit(i, i);
     return;
   }
   uint32_t T, need;
@@ -367,22 +352,22 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
       if (eq_b < need) pos = gt_b + eq_b;
       ++eq_b;
     }
-    if (pos >= 0 && pos < K) {
-      out_logical[pos] = i;
-      out_phys[pos] = phys_of(i);
-    }
+    if (pos >= 0 && pos < K) emit(pos, i);
   }
-  if (tid == 0) *out_count = K;
 }
 
 template <int NT, typename PhysOf>
 __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t* keys, int cap,
                            TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
                            int32_t* out_count, PhysOf phys_of) {
+  // outputs: out_logical / out_phys [K] in ascending page order, -1 padded
+  auto emit = [&](int pos, int i) { out_logical[pos] = i; out_phys[pos] = phys_of(i); };
+  const int n = P < K ? P : K;
+  for (int i = n + threadIdx.x; i < K; i += NT) { out_logical[i] = -1; out_phys[i] = -1; }
+  if (threadIdx.x == 0) *out_count = n;
   const bool cached = P <= cap && P > K;
   if (!cached) {
-    block_topk_keys<NT>(P, K, [sc](int i) { return score_key(__ldcg(sc + i)); }, sm,
-                        out_logical, out_phys, out_count, phys_of);
+    block_topk_keys<NT>(P, K, [sc](int i) { return score_key(__ldcg(sc + i)); }, sm, emit);
     return;
   }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -401,10 +386,9 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
 #pragma unroll
   for (int w = 0; w < NT / 32; ++w) { kmin = min(kmin, sm.red[0][w]); kmax = max(kmax, sm.red[1][w]); }
   if (P <= 16 * NT)
-    block_topk_smem<NT>(P, K, keys, kmin, kmax, sm, out_logical, out_phys, out_count, phys_of);
+    block_topk_smem<NT>(P, K, keys, kmin, kmax, sm, emit);
   else            // longer cached rows: the general routine over the shared-memory keys
-    block_topk_keys<NT>(P, K, [keys](int i) { return keys[i]; }, sm, out_logical, out_phys,
-                        out_count, phys_of);
+    block_topk_keys<NT>(P, K, [keys](int i) { return keys[i]; }, sm, emit);
 }
 
 }  // namespace quest
