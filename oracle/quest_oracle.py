@@ -234,6 +234,65 @@ def select_topk(scores, page_indptr, page_indices, k, requests=None):
     return sel_logical, sel_phys, sel_count
 
 
+def forced_pages(P, n_sink, n_local):
+    """Pages kept whatever their score: the first n_sink (sink) and the last
+    n_local (local window, tail page included) of the P valid pages, as one
+    set (Quest page §3.2: C_local and C_sink may overlap; pages are counted
+    after the union)."""
+    return sorted(set(range(min(n_sink, P))) | set(range(max(0, P - n_local), P)))
+
+
+def hybrid_pages(U, P, k, n_sink, n_local):
+    """C = C_local ∪ C_sink ∪ C_quest (Quest page §3.2; budget split of §2.2).
+
+    The forced pages are always chosen; the remaining budget k - |forced|
+    goes to Quest: the other valid pages (index < P) ranked by (score
+    descending, index ascending). The chosen indices are returned in
+    ascending order; there are min(k, P) of them. Requires
+    n_sink + n_local <= k.
+    """
+    U = np.asarray(U, dtype=F64)
+    forced = forced_pages(P, n_sink, n_local)
+    assert len(forced) <= k
+    rest = np.array([i for i in range(P) if i not in set(forced)], dtype=np.int64)
+    order = rest[np.lexsort((rest, -U[rest]))] if len(rest) else rest
+    quest = order[:max(0, min(k, P) - len(forced))]
+    return np.sort(np.concatenate([np.asarray(forced, dtype=np.int64), quest]))
+
+
+def select_hybrid(scores, page_indptr, page_indices, seq_lens, page_size, k, n_sink, n_local,
+                  requests=None):
+    """select_topk with the local window + sink pages forced (hybrid_pages);
+    only the P_r = ceil(L_r / S) valid pages of each request compete.
+    n_sink = n_local = 0 is plain Quest Top-K over the valid pages."""
+    h_kv = scores.shape[0]
+    batch = len(page_indptr) - 1
+    sel_logical = np.full((batch, h_kv, k), -1, dtype=np.int32)
+    sel_phys = np.full((batch, h_kv, k), -1, dtype=np.int32)
+    sel_count = np.zeros((batch, h_kv), dtype=np.int32)
+    reqs = range(batch) if requests is None else requests
+    for r in reqs:
+        lo = int(page_indptr[r])
+        P = min(-(-int(seq_lens[r]) // page_size), int(page_indptr[r + 1]) - lo)
+        for g in range(h_kv):
+            chosen = hybrid_pages(scores[g, lo:lo + P], P, k, n_sink, n_local)
+            n = len(chosen)
+            sel_logical[r, g, :n] = chosen
+            sel_phys[r, g, :n] = np.asarray(page_indices, dtype=np.int64)[lo + chosen]
+            sel_count[r, g] = n
+    return sel_logical, sel_phys, sel_count
+
+
+def hybrid_budget_pages(budget_tokens, local_tokens, sink_tokens, page_size):
+    """Page counts of the budget split in Quest page §2.2: local window and
+    sinks in whole pages (ceil), the rest of the token budget as whole pages
+    for Quest (floor). Returns (k, n_local, n_sink, quest_pages)."""
+    n_local = -(-local_tokens // page_size)
+    n_sink = -(-sink_tokens // page_size)
+    quest = (budget_tokens - local_tokens - sink_tokens) // page_size
+    return n_local + n_sink + quest, n_local, n_sink, quest
+
+
 # ---------------------------------------------------------------------------
 # a4/a5: attention over a candidate page set (Quest page Fig. 1, eq (6);
 #        PageWeaver notes §2 eq (1)-(2) for the exact token set and 1/sqrt(d))

@@ -295,6 +295,66 @@ def test_select_outputs_and_padding():
 
 
 # --------------------------------------------------------------------------
+# Local window + sink + Quest hybrid budget (Quest page §2.2, §3.2)
+# --------------------------------------------------------------------------
+
+def test_hybrid_budget_split_of_the_page():
+    # Quest page §2.2: a 2048-token budget keeps 512 recent tokens and 4
+    # sinks, and spends the remaining 1532 tokens as whole pages on Quest.
+    # At S = 16: 32 local pages, 1 sink page, floor(1532 / 16) = 95 pages.
+    assert qo.hybrid_budget_pages(2048, 512, 4, 16) == (128, 32, 1, 95)
+    assert 32 + 1 + 95 == 2048 // 16
+
+
+def test_hybrid_brute_force():
+    """Forced pages (first n_sink, last n_local of the P valid pages) are
+    always chosen; every other chosen page beats every other unchosen page
+    under (score desc, index asc); min(k, P) pages in ascending order."""
+    rng = np.random.default_rng(11)
+    for trial in range(600):
+        P = int(rng.integers(1, 40))
+        k = int(rng.integers(1, 45))
+        n_sink = int(rng.integers(0, k + 1))
+        n_local = int(rng.integers(0, k - n_sink + 1))
+        U = (rng.integers(-3, 4, P).astype(np.float64) if trial % 3 == 0
+             else rng.standard_normal(P))
+        got = qo.hybrid_pages(U, P, k, n_sink, n_local).tolist()
+        forced = {i for i in range(P) if i < n_sink or i >= P - n_local}
+        assert got == sorted(set(got)) and len(got) == min(k, P)
+        assert forced <= set(got)
+        quest, out = set(got) - forced, set(range(P)) - set(got) - forced
+        for c in quest:
+            for x in out:
+                assert (U[c], -c) > (U[x], -x)
+
+
+def test_hybrid_reductions():
+    rng = np.random.default_rng(12)
+    for _ in range(100):
+        P = int(rng.integers(1, 50))
+        k = int(rng.integers(1, 60))
+        U = rng.standard_normal(P)
+        # nothing forced: plain Top-K (pinned by the rank characterisation)
+        assert qo.hybrid_pages(U, P, k, 0, 0).tolist() == _rank_select(U.tolist(), k)
+    # a short request: sink and window overlap and cover every page
+    assert qo.hybrid_pages([0.1, 0.2, 0.3], 3, 8, 2, 2).tolist() == [0, 1, 2]
+    # the window alone fills the budget: Quest gets nothing
+    assert qo.hybrid_pages([9.0, 8.0, 7.0, 1.0, 0.5], 5, 2, 0, 2).tolist() == [3, 4]
+    # one sink, one local, one Quest page (ties to the lower index)
+    assert qo.hybrid_pages([1.0, 5.0, 5.0, 2.0], 4, 3, 1, 1).tolist() == [0, 1, 3]
+
+
+def test_select_hybrid_outputs():
+    U = np.array([[3.0, 1.0, 2.0, 2.0, -1.0, 0.5, 0.25]])
+    indptr = np.array([0, 7], np.int32)
+    indices = np.array([9, 4, 7, 1, 0, 3, 2], np.int32)
+    # 6 valid pages (L = 90, S = 16): entry 6 is a reserved one and never competes
+    sl, sp, sc = qo.select_hybrid(U, indptr, indices, np.array([90]), 16, k=4, n_sink=1, n_local=1)
+    assert sl[0, 0].tolist() == [0, 2, 3, 5] and sc[0, 0] == 4
+    assert sp[0, 0].tolist() == [9, 7, 1, 3]
+
+
+# --------------------------------------------------------------------------
 # Attention: library routine, K = P, eq (7), set semantics
 # --------------------------------------------------------------------------
 
