@@ -146,7 +146,7 @@ class LayerSetup:
     """The Llama-2-7B-shaped layer: pool built by the library's own append
     (prefill of the first L-1 tokens), plus the decode token and query."""
 
-    def __init__(self, w: wl.Workload, nbuf: int, dev, sample_heads=4):
+    def __init__(self, w: wl.Workload, nbuf: int, dev, sample_heads=4, n_sink=0, n_local=0):
         import query_aware_sparse_gb300 as qs
         self.qs = qs
         self.w = w
@@ -196,7 +196,9 @@ class LayerSetup:
         self.lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
         n = qs.attn_workspace_size(B, h, w.group, d, S, self.K)
         self.ws = torch.empty(n, dtype=torch.uint8, device=dev)
-        self.fused = qs.DecodeStep(self.caches[0], self.table, w.group, self.K)
+        self.n_sink, self.n_local = n_sink, n_local
+        self.fused = qs.DecodeStep(self.caches[0], self.table, w.group, self.K,
+                                   n_sink=n_sink, n_local=n_local)
         self.out, self.lse = self.fused.out, self.fused.lse
 
     # the four stages of one decode step on cache copy b
@@ -209,7 +211,7 @@ class LayerSetup:
 
     def select(self, b):
         self.qs.select_topk(self.table, self.w.h_kv, self.w.page_size, self.scores, self.K,
-                            out=self.sel)
+                            out=self.sel, n_sink=self.n_sink, n_local=self.n_local)
 
     def attend(self, b):
         self.qs.sparse_decode_attn(self.caches[b], self.table, self.q, self.w.group,
@@ -289,9 +291,10 @@ class OracleSample:
     """The oracle's decode step on a sample of the heads of the same layer,
     built from the generated inputs (never from the device path's results)."""
 
-    def __init__(self, w: wl.Workload, k_tok, v_tok, q, heads: int):
+    def __init__(self, w: wl.Workload, k_tok, v_tok, q, heads: int, n_sink=0, n_local=0):
         from oracle import quest_oracle as qo
         self.qo = qo
+        self.n_sink, self.n_local = n_sink, n_local
         self.heads = heads
         self.w = w
         L = int(w.lengths()[0])
@@ -315,7 +318,8 @@ class OracleSample:
         qo.append_kv(self.kp, self.vp, self.sm, t.page_indptr, t.page_indices,
                      np.array([self.L - 1]), np.array([0, 1]), self.kdec, self.vdec)
         sc = qo.score_pages(self.q, self.sm, t.page_indptr, t.page_indices, w.group)
-        sel, _, _ = qo.select_topk(sc, t.page_indptr, t.page_indices, w.k)
+        sel, _, _ = qo.select_hybrid(sc, t.page_indptr, t.page_indices, np.array([self.L]),
+                                     w.page_size, w.k, self.n_sink, self.n_local)
         qo.sparse_attention(self.q, self.kp, self.vp, t.page_indptr, t.page_indices,
                             np.array([self.L], np.int32), sel, w.group)
 
@@ -346,6 +350,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="oracle timing budget for cpu_baseline (0 = skip)")
     ap.add_argument("--stage-reps", type=int, default=100)
+    ap.add_argument("--sink-tokens", type=int, default=0,
+                    help="hybrid budget: sink tokens kept (whole pages, ceil)")
+    ap.add_argument("--local-tokens", type=int, default=0,
+                    help="hybrid budget: recent-window tokens kept (whole pages, ceil)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -363,6 +371,16 @@ def main():
            "h_kv": w.h_kv, "group": w.group, "head_dim": w.head_dim,
            "page_size": w.page_size, "seq_len": int(w.lengths()[0])}
 
+    n_sink = -(-args.sink_tokens // w.page_size)
+    n_local = -(-args.local_tokens // w.page_size)
+    if n_sink or n_local:
+        # Quest page 2.2: the budget keeps its page count; sinks and the window
+        # take whole pages out of it and Quest gets the rest
+        cfg["hybrid"] = {"sink_tokens": args.sink_tokens, "local_tokens": args.local_tokens,
+                         "sink_pages": n_sink, "local_pages": n_local,
+                         "quest_pages": w.k - n_sink - n_local}
+    args.n_sink, args.n_local = n_sink, n_local
+
     if args.impl == "reference":
         if rank != 0:
             return
@@ -371,7 +389,8 @@ def main():
 
     import query_aware_sparse_gb300 as qs
     qs.lib()
-    setup = LayerSetup(w, args.nbuf, dev, sample_heads=args.cpu_heads)
+    setup = LayerSetup(w, args.nbuf, dev, sample_heads=args.cpu_heads,
+                       n_sink=n_sink, n_local=n_local)
     cfg["l2"] = (f"rotating {args.nbuf} distinct copies of the layer "
                  f"({args.nbuf * (setup.caches[0].k_pool.nbytes * 2 + setup.caches[0].summary.nbytes) / 2**30:.1f} GiB)"
                  " so every step reads memory not touched in the previous "
@@ -516,7 +535,7 @@ def run_e2e(setup, graphs, nb, n):
 
 
 def cpu_baseline(setup, heads, seconds):
-    o = OracleSample(setup.w, *setup.sample, heads)
+    o = OracleSample(setup.w, *setup.sample, heads, setup.n_sink, setup.n_local)
     o.time_steps(1)
     t0 = time.perf_counter()
     ts = []
@@ -535,7 +554,8 @@ def run_reference(args, w, cfg, dev, ws):
     k_tok, v_tok = wl.request_tokens(w, 0, L, device=dev)
     q = wl.queries(w, [L - 1], device=dev)
     h = args.cpu_heads
-    o = OracleSample(w, k_tok[:, :h].cpu(), v_tok[:, :h].cpu(), q[:, :h * w.group].cpu(), h)
+    o = OracleSample(w, k_tok[:, :h].cpu(), v_tok[:, :h].cpu(), q[:, :h * w.group].cpu(), h,
+                     args.n_sink, args.n_local)
     del k_tok, v_tok
     for _ in range(args.warmup):
         o.time_steps(1)

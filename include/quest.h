@@ -144,14 +144,22 @@ QUEST_API quest_status quest_score_pages(const quest_cache* cache, const quest_p
  * scored pages: the min(k, P_r) pages with the largest scores, ties broken
  * by the lower logical page index (-0 equals +0). Emitted in ascending
  * logical page order; unused slots hold -1.
+ * Hybrid budget (local window + sink + Quest; Quest page §2.2 and §3.2,
+ * C = C_local u C_sink u C_quest): the first n_sink and the last n_local of
+ * the P_r valid pages are always kept (their union, the tail page being the
+ * last local page), and the rest of the k pages are the Top-K of the other
+ * pages by the rule above. n_sink = n_local = 0 is plain Quest.
  *   page_size   : tokens per page (gives P_r from seq_lens); 16 or 32
  *   scores      : device fp32 [h_kv, nnz] as written by quest_score_pages
+ *   n_sink, n_local : forced pages, >= 0 each, n_sink + n_local <= k
+ *                 (else QUEST_ERR_INVALID_ARG)
  *   sel_logical : device int32 [batch, h_kv, k] logical page ids
  *   sel_phys    : device int32 [batch, h_kv, k] physical page ids (page table)
  *   sel_count   : device int32 [batch, h_kv] = min(k, P_r)
  */
 QUEST_API quest_status quest_select_topk(const quest_pages* pages, int32_t h_kv,
                                int32_t page_size, const float* scores, int32_t k,
+                               int32_t n_sink, int32_t n_local,
                                int32_t* sel_logical, int32_t* sel_phys,
                                int32_t* sel_count, void* stream);
 
@@ -227,7 +235,7 @@ QUEST_API size_t quest_attn_workspace_size(int32_t batch, int32_t h_kv, int32_t 
  *   pages->seq_lens : lengths INCLUDING the new token
  *   k_new, v_new    : device [batch, h_kv, head_dim] dtype, or both NULL
  *                     (no append: the cache already holds every token)
- *   q, group, k     : as quest_score_pages / quest_select_topk
+ *   q, group, k, n_sink, n_local : as quest_score_pages / quest_select_topk
  *   scores          : device fp32 [h_kv, nnz] (written)
  *   sel_logical, sel_phys, sel_count : as quest_select_topk (written)
  *   out, lse        : as quest_sparse_decode_attn (lse may be NULL)
@@ -244,6 +252,7 @@ QUEST_API size_t quest_attn_workspace_size(int32_t batch, int32_t h_kv, int32_t 
 QUEST_API quest_status quest_decode_step(const quest_cache* cache, const quest_pages* pages,
                                          const void* k_new, const void* v_new,
                                          const void* q, int32_t group, int32_t k,
+                                         int32_t n_sink, int32_t n_local,
                                          float* scores, int32_t* sel_logical,
                                          int32_t* sel_phys, int32_t* sel_count,
                                          float* out, float* lse, float sm_scale,

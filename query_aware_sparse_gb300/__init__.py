@@ -53,7 +53,7 @@ def lib() -> ctypes.CDLL:
         P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
         L.quest_append_kv.argtypes = [P, P, P, P, I32, P, P, P]
         L.quest_score_pages.argtypes = [P, P, P, I32, P, P]
-        L.quest_select_topk.argtypes = [P, I32, I32, P, I32, P, P, P, P]
+        L.quest_select_topk.argtypes = [P, I32, I32, P, I32, I32, I32, P, P, P, P]
         L.quest_sparse_decode_attn.argtypes = [P, P, P, I32, P, P, I32, P, P,
                                                ctypes.c_float, P, SZ, P]
         L.quest_sparse_decode_attn_noalloc.argtypes = [P, P, P, I32, P, P, I32, P, P,
@@ -61,7 +61,7 @@ def lib() -> ctypes.CDLL:
         L.quest_sparse_decode_attn_noalloc.restype = I32
         L.quest_attn_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32]
         L.quest_attn_workspace_size.restype = SZ
-        L.quest_decode_step.argtypes = [P, P, P, P, P, I32, I32, P, P, P, P, P, P,
+        L.quest_decode_step.argtypes = [P, P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P,
                                         ctypes.c_float, P, SZ, P]
         L.quest_decode_step.restype = I32
         L.quest_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32]
@@ -165,8 +165,9 @@ def score_pages(cache: PagedCache, table: PageTable, q, group: int, scores=None,
 
 
 def select_topk(table: PageTable, h_kv: int, page_size: int, scores, k: int,
-                out=None, stream=None):
-    """quest_select_topk: (sel_logical, sel_phys [B, h_kv, k], sel_count [B, h_kv])."""
+                out=None, stream=None, n_sink: int = 0, n_local: int = 0):
+    """quest_select_topk: (sel_logical, sel_phys [B, h_kv, k], sel_count [B, h_kv]).
+    n_sink / n_local: first / last valid pages always kept (hybrid budget)."""
     if out is None:
         dev = scores.device
         out = (torch.empty((table.batch, h_kv, k), dtype=torch.int32, device=dev),
@@ -174,8 +175,8 @@ def select_topk(table: PageTable, h_kv: int, page_size: int, scores, k: int,
                torch.empty((table.batch, h_kv), dtype=torch.int32, device=dev))
     sl, sp, sc = out
     _check(lib().quest_select_topk(ctypes.byref(table.c), int(h_kv), int(page_size),
-                                   _ptr(scores), int(k), _ptr(sl), _ptr(sp), _ptr(sc),
-                                   _stream(stream)))
+                                   _ptr(scores), int(k), int(n_sink), int(n_local),
+                                   _ptr(sl), _ptr(sp), _ptr(sc), _stream(stream)))
     return sl, sp, sc
 
 
@@ -210,12 +211,15 @@ def decode_workspace_size(batch, nnz, h_kv, group, head_dim, page_size, dtype, k
 
 class DecodeStep:
     """Buffers of quest_decode_step for a fixed problem shape: scores,
-    selections, outputs and a zero-filled workspace (reused across calls)."""
+    selections, outputs and a zero-filled workspace (reused across calls).
+    n_sink / n_local: first / last valid pages always kept (hybrid budget)."""
 
-    def __init__(self, cache: PagedCache, table: PageTable, group: int, k: int, device=None):
+    def __init__(self, cache: PagedCache, table: PageTable, group: int, k: int, device=None,
+                 n_sink: int = 0, n_local: int = 0):
         dev = device or cache.k_pool.device
         B, h = table.batch, cache.h_kv
         self.group, self.k = group, k
+        self.n_sink, self.n_local = n_sink, n_local
         self.scores = torch.empty((h, max(table.nnz, 1)), dtype=torch.float32, device=dev)
         self.sel = (torch.empty((B, h, k), dtype=torch.int32, device=dev),
                     torch.empty((B, h, k), dtype=torch.int32, device=dev),
@@ -233,14 +237,15 @@ class DecodeStep:
         sl, sp, sc = self.sel
         _check(lib().quest_decode_step(
             ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(k_new), _ptr(v_new), _ptr(q),
-            int(self.group), int(self.k), _ptr(self.scores), _ptr(sl), _ptr(sp), _ptr(sc),
+            int(self.group), int(self.k), int(self.n_sink), int(self.n_local),
+            _ptr(self.scores), _ptr(sl), _ptr(sp), _ptr(sc),
             _ptr(self.out), _ptr(self.lse), float(sm_scale), _ptr(self.workspace),
             int(self.workspace.numel()), _stream(stream)))
         return self.out, self.lse
 
 
 TRACE_NAMES = ("start", "scored", "selected", "att_start", "att_pages", "att_merged",
-               "wave0_scored", "wave1_scored", "wave2_scored", "exit",
+               "", "", "", "exit",
                "sel0_polled | desc0", "sel0_done | page0", "sel1_polled | merged",
                "sel1_done | fmerge0", "sel2_polled | fmerge1", "sel2_done")
 # slots 10-15 depend on the CTA's role: select stamps on selectors (the CTAs

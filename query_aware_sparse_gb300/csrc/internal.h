@@ -31,6 +31,7 @@ struct SelectArgs {
   const int32_t* page_indptr; const int32_t* page_indices; const int32_t* seq_lens;
   int32_t* sel_logical; int32_t* sel_phys; int32_t* sel_count;
   int32_t batch, nnz, h_kv, k, page_size;
+  int32_t n_sink, n_local;                    // pages always kept (hybrid budget)
   unsigned* err;
 };
 
@@ -60,6 +61,7 @@ struct StepArgs {
   unsigned long long* tagged;                 // [h_kv, nnz] score bits | call tag << 32
   float* part_o; float* part_ml;              // [units, group, n_chunks, head_dim | 4 (max, sum, tag, 0)]
   int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype, k;
+  int32_t n_sink, n_local;                    // pages always kept (hybrid budget)
   int32_t n_chunks, chunk_pages;
   float scale_log2;
   unsigned long long* trace;                  // [grid, 16] phase stamps, or null

@@ -110,11 +110,13 @@ quest_status quest_score_pages(const quest_cache* cache, const quest_pages* page
 
 quest_status quest_select_topk(const quest_pages* pages, int32_t h_kv,
                                int32_t page_size, const float* scores, int32_t k,
+                               int32_t n_sink, int32_t n_local,
                                int32_t* sel_logical, int32_t* sel_phys,
                                int32_t* sel_count, void* stream) {
   quest_status st = check_pages(pages, true);
   if (st != QUEST_OK) return st;
   if (h_kv <= 0 || k < 1) return QUEST_ERR_INVALID_ARG;
+  if (n_sink < 0 || n_local < 0 || (int64_t)n_sink + n_local > k) return QUEST_ERR_INVALID_ARG;
   if (page_size != 16 && page_size != 32) return QUEST_ERR_UNSUPPORTED;
   if (pages->batch == 0) return QUEST_OK;
   if ((!scores && pages->nnz > 0) || !sel_logical || !sel_phys || !sel_count)
@@ -126,6 +128,7 @@ quest_status quest_select_topk(const quest_pages* pages, int32_t h_kv,
   a.sel_logical = sel_logical; a.sel_phys = sel_phys; a.sel_count = sel_count;
   a.batch = pages->batch; a.nnz = pages->nnz; a.h_kv = h_kv; a.k = k;
   a.page_size = page_size;
+  a.n_sink = n_sink; a.n_local = n_local;
   a.err = err_ptr();
   if (!a.err) return QUEST_ERR_CUDA;
   return launched(quest::launch_select(a, static_cast<cudaStream_t>(stream)));
@@ -190,7 +193,8 @@ size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t h_kv, int
 
 quest_status quest_decode_step(const quest_cache* cache, const quest_pages* pages,
                                const void* k_new, const void* v_new, const void* q,
-                               int32_t group, int32_t k, float* scores,
+                               int32_t group, int32_t k, int32_t n_sink, int32_t n_local,
+                               float* scores,
                                int32_t* sel_logical, int32_t* sel_phys, int32_t* sel_count,
                                float* out, float* lse, float sm_scale, void* workspace,
                                size_t workspace_bytes, void* stream) {
@@ -199,6 +203,7 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   if ((st = check_pages(pages, true)) != QUEST_OK) return st;
   if (!valid_group(group)) return QUEST_ERR_UNSUPPORTED;
   if (k < 1) return QUEST_ERR_INVALID_ARG;
+  if (n_sink < 0 || n_local < 0 || (int64_t)n_sink + n_local > k) return QUEST_ERR_INVALID_ARG;
   if (pages->batch == 0) return QUEST_OK;
   if (!q || !scores || !sel_logical || !sel_phys || !sel_count || !out || !aligned16(q))
     return QUEST_ERR_INVALID_ARG;
@@ -226,6 +231,7 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   a.batch = pages->batch; a.nnz = pages->nnz; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
   a.group = group; a.page_size = cache->page_size; a.head_dim = cache->head_dim;
   a.dtype = cache->dtype; a.k = k; a.n_chunks = plan.n_chunks; a.chunk_pages = plan.chunk_pages;
+  a.n_sink = n_sink; a.n_local = n_local;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)cache->head_dim);
   a.scale_log2 = scale * quest::LOG2E;
   a.trace = (g_trace && plan.grid <= g_trace_ctas) ? g_trace : nullptr;

@@ -1,6 +1,8 @@
 // a3: fixed-budget Top-K pages per (request, KV head) (Quest page Fig. 1,
 // §1.1 and §2: K pages for a token budget of K * S tokens). Ties go to the
 // lower logical page index; winners are emitted in ascending page order.
+// Hybrid budget (Quest page §2.2, §3.2): the first n_sink and last n_local
+// valid pages are always kept and Quest fills the rest of the K pages.
 // One CTA per (request, KV head) runs the block-wide select of topk.cuh.
 #include "common.cuh"
 #include "internal.h"
@@ -27,10 +29,14 @@ select_kernel(const SelectArgs a) {
   }
   const size_t out = ((size_t)r * a.h_kv + g) * a.k;
   const int32_t* idx = a.page_indices + lo;
+  // forced pages: [0, f_lo) and [f_hi, P)
+  const int f_lo = min(a.n_sink, P), f_hi = max(f_lo, P - a.n_local);
   block_topk<kSelThreads>(a.scores + (size_t)g * a.nnz + lo, P, a.k, s_keys, kSelSmemKeys, sm,
                           a.sel_logical + out, a.sel_phys + out,
                           a.sel_count + (size_t)r * a.h_kv + g,
-                          [idx](int i) { return idx[i]; });
+                          [idx](int i) { return idx[i]; },
+                          [f_lo, f_hi](int i) { return i < f_lo || i >= f_hi; },
+                          f_lo + (P - f_hi));
 }
 
 }  // namespace

@@ -445,6 +445,10 @@ step_kernel(const StepArgs a) {
       const unsigned long long* row = a.tagged + (size_t)g * a.nnz + lo;
       const int32_t* idx = a.page_indices + lo;
       const bool cached = P <= kKeysCap;
+      // local window + sink pages (hybrid budget) are kept outright:
+      // forced = [0, f_lo) and [f_hi, P)
+      const int f_lo = min(a.n_sink, P), f_hi = max(f_lo, P - a.n_local);
+      auto forced = [f_lo, f_hi](int i) { return i < f_lo || i >= f_hi; };
       // gate: one thread waits (bounded) until every worker has finished
       // scoring, so the block reads the row once instead of polling it while
       // the workers stream; the row's tags still decide below
@@ -480,8 +484,10 @@ step_kernel(const StepArgs a) {
             const uint32_t key = score_key(__uint_as_float((unsigned)v[j]));
             keys[i] = key;
             physs[i] = ph[j];
-            kmin = min(kmin, key);
-            kmax = max(kmax, key);
+            if (i >= f_lo && i < f_hi) {     // min/max over the pages that compete
+              kmin = min(kmin, key);
+              kmax = max(kmax, key);
+            }
           }
         }
       }
@@ -501,10 +507,11 @@ step_kernel(const StepArgs a) {
       if (tid == 0) a.sel_count[u] = nsel;
       auto emit = [&](int pos, int i) { ol[pos] = i; op[pos] = cached ? physs[i] : __ldg(idx + i); };
       if (cached)
-        block_topk_smem<kNT>(P, K, keys, kmin, kmax, tsm, emit);
+        block_topk_smem<kNT>(P, K, keys, kmin, kmax, tsm, emit, forced, f_lo + (P - f_hi));
       else
-        block_topk_keys<kNT>(P, K, [row](int i) {
-                               return score_key(__uint_as_float((unsigned)ld_relaxed_u64(row + i)));
+        block_topk_keys<kNT>(P, K, [row, forced](int i) {
+                               return forced(i) ? 0xffffffffu
+                                                : score_key(__uint_as_float((unsigned)ld_relaxed_u64(row + i)));
                              }, tsm, emit);
       __syncthreads();
       if (tid == 0) st_release(ready + u, tag);   // releases the block's selection writes

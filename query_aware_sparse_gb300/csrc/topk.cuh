@@ -193,23 +193,27 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Em
 
 // Top-K of P fp32 scores `sc` (global) for one row; `keys` caches up to `cap`
 // keys in shared memory (a longer row re-reads the scores from L2 per pass).
-template <int NT, typename PhysOf>
+// Pages with forced(i) (nforced of [0, P), at most K: the local window +
+// sink pages of the hybrid budget) are always kept.
+template <int NT, typename PhysOf, typename Forced>
 __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t* keys, int cap,
                            TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
-                           int32_t* out_count, PhysOf phys_of);
+                           int32_t* out_count, PhysOf phys_of, Forced forced, int nforced);
 
 // Top-K of P <= 16 * NT keys held in shared memory (`keys`, overwritten),
 // whose block-wide min and max the caller has already reduced. Same result
-// as block_topk_keys. `sm.hist` must be all zero on entry and is all zero
-// on return. After the first radix digit, a boundary bucket of at most
+// as block_topk_keys. Pages with forced(i) (nforced of them, at most K) are
+// kept outright and the other pages compete for the remaining K - nforced;
+// kmin / kmax are over the other pages' keys only. `sm.hist` must be all
+// zero on entry and is all zero on return. After the first radix digit, a boundary bucket of at most
 // kTopkGather keys is ranked directly (key, then lower index) instead of
 // taking more digits: its winners are marked with the top key and its
 // losers with 0, so one threshold then selects exactly K keys. Loops stay
 // rolled (this runs once per row: its code is fetched cold) and the page-
 // order scan packs (greater, equal) counts into 32 bits with one barrier.
-template <int NT, typename Emit>
+template <int NT, typename Emit, typename Forced>
 __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
-                                TopkSmem<NT>& sm, Emit emit) {
+                                TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWP = NT / 32;
   constexpr int BPT = kTopkBins / NT;            // bins per thread in the digit search
@@ -219,14 +223,18 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
     for (int i = tid; i < P; i += NT) emit(i, i);
     return;
   }
-  uint32_t T, need;
-  bool ge_mode;            // select key >= T vs (key > T, then `need` of key == T)
-  if (kmin == kmax) {
-    T = kmin; need = K; ge_mode = false;
+  // forced pages are kept outright; the others compete for the rest
+  const int Kq = K - nforced;
+  uint32_t T = 0xffffffffu, need = 0;
+  bool ge_mode = false;    // select key >= T vs (key > T, then `need` of key == T)
+  if (Kq <= 0) {
+    need = 0;              // no key passes: (> 0xffffffff) is false, need 0
+  } else if (kmin == kmax) {
+    T = kmin; need = Kq; ge_mode = false;
   } else {
     int hi = 31 - __clz(kmin ^ kmax);           // highest differing bit
     uint32_t prefix = kmin & ~((hi == 31) ? 0xffffffffu : ((2u << hi) - 1u));
-    uint32_t krem = K;
+    uint32_t krem = Kq;
     while (true) {
       const int shift = max(hi - (kTopkBits - 1), 0);
       const int nbits = hi - shift + 1;
@@ -235,7 +243,7 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
 #pragma unroll 1
       for (int i = tid; i < P; i += NT) {
         const uint32_t k = keys[i];
-        if ((k & hi_mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
+        if ((k & hi_mask) == prefix && !forced(i)) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
       }
       if (tid == 0) sm.gcount = 0;
       __syncthreads();
@@ -286,7 +294,7 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
 #pragma unroll 1
         for (int i = tid; i < P; i += NT) {
           const uint32_t k = keys[i];
-          if ((k & ~span) == prefix) {
+          if ((k & ~span) == prefix && !forced(i)) {
             const uint32_t at = atomicAdd(&sm.gcount, 1u);
             sm.gkey[at] = k;
             sm.gidx[at] = i;
@@ -323,8 +331,9 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
 #pragma unroll 1
   for (int i = c0; i < c1; ++i) {
     const uint32_t k = keys[i];
-    if (ge_mode) cnt += (k >= T) << 16;
-    else cnt += ((k > T) << 16) | (k == T);
+    const bool f = forced(i);
+    if (ge_mode) cnt += (uint32_t)(f || k >= T) << 16;
+    else cnt += ((uint32_t)(f || k > T) << 16) | (uint32_t)(!f && k == T);
   }
   uint32_t incl = cnt;
 #pragma unroll
@@ -342,10 +351,11 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
 #pragma unroll 1
   for (int i = c0; i < c1; ++i) {
     const uint32_t k = keys[i];
+    const bool f = forced(i);
     int pos = -1;
     if (ge_mode) {
-      if (k >= T) pos = gt_b++;
-    } else if (k > T) {
+      if (f || k >= T) pos = gt_b++;
+    } else if (f || k > T) {
       pos = gt_b + min(eq_b, need);
       ++gt_b;
     } else if (k == T) {
@@ -356,10 +366,10 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
   }
 }
 
-template <int NT, typename PhysOf>
+template <int NT, typename PhysOf, typename Forced>
 __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t* keys, int cap,
                            TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
-                           int32_t* out_count, PhysOf phys_of) {
+                           int32_t* out_count, PhysOf phys_of, Forced forced, int nforced) {
   // outputs: out_logical / out_phys [K] in ascending page order, -1 padded
   auto emit = [&](int pos, int i) { out_logical[pos] = i; out_phys[pos] = phys_of(i); };
   const int n = P < K ? P : K;
@@ -367,7 +377,9 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
   if (threadIdx.x == 0) *out_count = n;
   const bool cached = P <= cap && P > K;
   if (!cached) {
-    block_topk_keys<NT>(P, K, [sc](int i) { return score_key(__ldcg(sc + i)); }, sm, emit);
+    block_topk_keys<NT>(P, K, [sc, forced](int i) {
+                          return forced(i) ? 0xffffffffu : score_key(__ldcg(sc + i));
+                        }, sm, emit);
     return;
   }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -375,8 +387,10 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
   for (int i = tid; i < P; i += NT) {
     const uint32_t k = score_key(__ldcg(sc + i));
     keys[i] = k;
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
+    if (!forced(i)) {
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
   }
   kmin = warp_min_u32(kmin);
   kmax = warp_max_u32(kmax);
@@ -385,10 +399,12 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
   __syncthreads();
 #pragma unroll
   for (int w = 0; w < NT / 32; ++w) { kmin = min(kmin, sm.red[0][w]); kmax = max(kmax, sm.red[1][w]); }
-  if (P <= 16 * NT)
-    block_topk_smem<NT>(P, K, keys, kmin, kmax, sm, emit);
-  else            // longer cached rows: the general routine over the shared-memory keys
-    block_topk_keys<NT>(P, K, [keys](int i) { return keys[i]; }, sm, emit);
+  if (P <= 16 * NT) {
+    block_topk_smem<NT>(P, K, keys, kmin, kmax, sm, emit, forced, nforced);
+  } else {        // longer cached rows: the general routine over the shared-memory keys
+    block_topk_keys<NT>(P, K, [keys, forced](int i) { return forced(i) ? 0xffffffffu : keys[i]; },
+                        sm, emit);
+  }
 }
 
 }  // namespace quest

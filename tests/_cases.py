@@ -87,24 +87,33 @@ def attn_close(o_gpu, o_ref, rel=2e-3):
     return err <= rel * den, err / den
 
 
-def check_selection(sel_gpu, cnt_gpu, scores_ref, tol, table, k, rows):
+def check_selection(sel_gpu, cnt_gpu, scores_ref, tol, table, k, rows, n_sink=0, n_local=0):
     """GPU sets equal the oracle's except pages whose oracle score lies within
-    the score tolerance of the oracle's K-th score; no duplicates; counts."""
+    the score tolerance of the oracle's last Quest score; forced pages (hybrid
+    budget: first n_sink, last n_local) always present; no duplicates; counts."""
     from oracle import quest_oracle as qo
     for (r, g) in rows:
         lo = int(table.page_indptr[r])
         P = -(-int(table.seq_lens[r]) // table.page_size)
         U = scores_ref[g, lo:lo + P]
-        want = set(qo.topk_pages(U, k).tolist())
+        forced = set(qo.forced_pages(P, n_sink, n_local))
+        want = set(qo.hybrid_pages(U, P, k, n_sink, n_local).tolist())
         got_list = [int(x) for x in sel_gpu[r, g] if x >= 0]
         got = set(got_list)
         assert len(got) == len(got_list), "duplicate page ids"
         assert int(cnt_gpu[r, g]) == min(k, P) == len(got)
+        assert forced <= got, (r, g, sorted(forced - got))
         if P <= k:
             assert got == set(range(P))
             continue
-        kth = np.sort(U)[::-1][k - 1]
+        kq = k - len(forced)                 # Quest's share of the budget
+        if kq == 0:
+            assert got == forced
+            continue
+        rest = np.array([U[i] for i in range(P) if i not in forced])
+        kth = np.sort(rest)[::-1][kq - 1]
         for p in got ^ want:
+            assert p not in forced
             assert abs(U[p] - kth) <= tol[g, lo + p] + 1e-12, (r, g, p, U[p], kth)
 
 

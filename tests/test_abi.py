@@ -69,12 +69,15 @@ def test_host_validation_rejects_bad_arguments(qlib):
     assert L.quest_score_pages(by(C(fake + 2, fake, fake, 8, 2, 16, 128, 1)), by(pages), fake, 1, fake, None) == -1
     assert L.quest_score_pages(by(good), by(pages), fake + 4, 1, fake, None) == -1
     # bad k / h_kv / page size for select
-    assert L.quest_select_topk(by(pages), 2, 16, fake, 0, fake, fake, fake, None) == -1
-    assert L.quest_select_topk(by(pages), 0, 16, fake, 4, fake, fake, fake, None) == -1
-    assert L.quest_select_topk(by(pages), 2, 12, fake, 4, fake, fake, fake, None) == -2
-    assert L.quest_select_topk(by(pages), 2, 16, fake, 4, None, fake, fake, None) == -1
+    assert L.quest_select_topk(by(pages), 2, 16, fake, 0, 0, 0, fake, fake, fake, None) == -1
+    assert L.quest_select_topk(by(pages), 0, 16, fake, 4, 0, 0, fake, fake, fake, None) == -1
+    assert L.quest_select_topk(by(pages), 2, 12, fake, 4, 0, 0, fake, fake, fake, None) == -2
+    assert L.quest_select_topk(by(pages), 2, 16, fake, 4, 0, 0, None, fake, fake, None) == -1
+    # hybrid budget: forced pages must be >= 0 and fit the budget
+    assert L.quest_select_topk(by(pages), 2, 16, fake, 4, -1, 0, fake, fake, fake, None) == -1
+    assert L.quest_select_topk(by(pages), 2, 16, fake, 4, 3, 2, fake, fake, fake, None) == -1
     # missing seq_lens where lengths are needed
-    assert L.quest_select_topk(by(Pg(fake, fake, None, 1, 8)), 2, 16, fake, 4, fake, fake, fake, None) == -1
+    assert L.quest_select_topk(by(Pg(fake, fake, None, 1, 8)), 2, 16, fake, 4, 0, 0, fake, fake, fake, None) == -1
     # negative sizes
     assert L.quest_append_kv(by(good), by(pages), fake, fake, -1, fake, fake, None) == -1
     assert L.quest_append_kv(by(good), by(Pg(fake, fake, fake, -1, 8)), fake, fake, 1, fake, fake, None) == -1
@@ -83,7 +86,7 @@ def test_host_validation_rejects_bad_arguments(qlib):
                                       ctypes.c_float(0.0), None, 0, None) in (-3, -4)
     # empty batches are valid no-ops
     empty = Pg(None, None, None, 0, 0)
-    assert L.quest_select_topk(by(empty), 2, 16, None, 4, None, None, None, None) == 0
+    assert L.quest_select_topk(by(empty), 2, 16, None, 4, 0, 0, None, None, None, None) == 0
     assert L.quest_append_kv(by(good), by(empty), None, None, 0, None, None, None) == 0
 
 

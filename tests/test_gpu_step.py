@@ -26,7 +26,7 @@ def _prefilled(w, lens, seed, spare=4):
     return table, k_tok, v_tok, ind
 
 
-def _run(w, lens, steps, seed, append=True):
+def _run(w, lens, steps, seed, append=True, n_sink=0, n_local=0):
     import query_aware_sparse_gb300 as qs
     lens = np.asarray(lens)
     full = lens + (steps if append else 0)
@@ -56,7 +56,7 @@ def _run(w, lens, steps, seed, append=True):
                           table.n_phys, S)
         gtab = gpu_table(tb)
         if step is None:
-            step = qs.DecodeStep(cache, gtab, w.group, w.k)
+            step = qs.DecodeStep(cache, gtab, w.group, w.k, n_sink=n_sink, n_local=n_local)
         if append:
             step(cache, gtab, q.cuda(), k1.cuda(), v1.cuda())
             qo.append_kv(okp, ovp, osm, table.page_indptr, table.page_indices,
@@ -90,16 +90,10 @@ def _run(w, lens, steps, seed, append=True):
             assert np.all(got[:, lo + P:table.page_indptr[r + 1]] == -np.inf)
         sl, sp, cnt = (np_of(x) for x in step.sel)
         check_selection(sl, cnt, ref_scores, tol, tb, w.k,
-                        [(r, g) for r in range(B) for g in range(h)])
-        ref_sel, _, _ = qo.select_topk(np.where(np.isfinite(ref_scores), ref_scores, -np.inf),
-                                       table.page_indptr, table.page_indices, w.k)
-        for r in range(B):
-            lo = table.page_indptr[r]
-            P = -(-int(cur[r]) // S)
-            for g in range(h):
-                ch = qo.topk_pages(ref_scores[g, lo:lo + P], w.k)
-                ref_sel[r, g] = -1
-                ref_sel[r, g, :len(ch)] = ch
+                        [(r, g) for r in range(B) for g in range(h)], n_sink, n_local)
+        ref_sel, _, _ = qo.select_hybrid(np.where(np.isfinite(ref_scores), ref_scores, -np.inf),
+                                         table.page_indptr, table.page_indices, cur, S, w.k,
+                                         n_sink, n_local)
         assert np.array_equal(sp[sl >= 0], table.page_indices[(table.page_indptr[:-1, None, None] + sl)[sl >= 0]])
         use = ref_sel if np.array_equal(sl, ref_sel) else sl
         ro, rl = qo.sparse_attention(np_of(q), okp, ovp, table.page_indptr, table.page_indices,
@@ -147,3 +141,11 @@ def test_step_many_units():
     # more (request, head) units than select workers and CTAs per head
     _run(_w("many", batch=24, h_kv=8, group=1, k=8, head_dim=64), list(range(10, 250, 10)),
          steps=1, seed=10)
+
+
+@pytest.mark.parametrize("n_sink,n_local", [(1, 4), (2, 0), (0, 16)])
+def test_step_hybrid_budget(n_sink, n_local):
+    """Local window + sink pages forced (Quest page §2.2, §3.2), through the
+    fused step, with short requests whose window and sinks overlap."""
+    _run(_w("hyb", batch=4, h_kv=3, k=16), [40, 1, 300, 700], steps=3, seed=20 + n_local,
+         n_sink=n_sink, n_local=n_local)
