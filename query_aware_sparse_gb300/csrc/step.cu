@@ -39,7 +39,8 @@
 // bounded and reports QUEST_DEVERR_WAIT_TIMEOUT instead of hanging.
 // Publication is release/acquire; a proxy fence orders it before the bulk
 // copies read the pool. The call tag lives in the workspace and is advanced
-// by the last CTA to leave; the per-unit counters are reset by their last user.
+// by the selectors once every CTA has read it; the per-unit counters are reset
+// by their last user and the scored counters are double-buffered by tag parity.
 #include "attn_dev.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -190,13 +191,19 @@ step_kernel(const StepArgs a) {
   const int h_q = a.h_kv * G;
   const int K = a.k;
   const int NP = a.n_chunks;                // partial slots per unit
-  unsigned* epoch = a.counters;             // tag of the previous call
-  unsigned* exit_cnt = a.counters + 2;      // CTAs finished
+  unsigned* epoch = a.counters;             // tag of the last call
   unsigned* ready = a.counters + 4;         // [U] tag of the published selection
   unsigned* att_done = ready + U;           // [U] attention slots finished
-  unsigned* scored_cnt = att_done + U;      // workers done scoring (released by each)
+  // tags 1, 2, ..., 0xffffffff, 2, ...: 0 marks never-written entries and the
+  // parity alternates from call to call
   unsigned tag = ld_relaxed_u32(epoch) + 1u;
-  if (tag == 0u) tag = 1u;                  // 0 marks never-written entries
+  if (tag == 0u) tag = 2u;
+  // CTAs counted in (a worker after scoring, a selector at once; released by
+  // each), in one of two banks by tag parity: the bank of the next call was
+  // last used by the previous call, which has finished, so this call clears
+  // it (no exit protocol at the end)
+  unsigned* scored_cnt = a.counters + 2 + (tag & 1u);
+  if (b == 0 && tid == 0) a.counters[2 + ((tag + 1u) & 1u)] = 0u;
   // optional phase trace: kTraceSlots globaltimer stamps per CTA
   unsigned long long* trace = a.trace ? a.trace + (size_t)b * kTraceSlots : nullptr;
   auto stamp = [&](int i) { if (trace && tid == 0) trace[i] = global_ns(); };
@@ -205,6 +212,9 @@ step_kernel(const StepArgs a) {
 
   const int NSEL = select_ctas(U, nblk);    // CTAs [0, NSEL) select; the rest score and attend
   const bool selector = b < NSEL;
+  // a selector has read the tag: count it in at once (a worker counts in
+  // after scoring), so the complete count means every CTA has read the tag
+  if (selector && tid == 0) red_release_add(scored_cnt, 1u);
   const int nbw = nblk - NSEL, bw = b - NSEL;
 
   // =================== scoring (with the append folded in) ===================
@@ -452,9 +462,12 @@ step_kernel(const StepArgs a) {
       // gate: one thread waits (bounded) until every worker has finished
       // scoring, so the block reads the row once instead of polling it while
       // the workers stream; the row's tags still decide below
-      if (tid == 0)
-        for (uint32_t it = 0; ld_acquire(scored_cnt) < (unsigned)nbw && it < (1u << 20); ++it)
+      if (tid == 0) {
+        for (uint32_t it = 0; ld_acquire(scored_cnt) < (unsigned)nblk && it < (1u << 20); ++it)
           __nanosleep(128);
+        // every CTA read the epoch before its release of this count: advance it
+        *epoch = tag;
+      }
       __syncthreads();
       // each thread waits for its own entries to carry this call's tag: a
       // batch of PB independent loads (with the entries' physical pages),
@@ -792,15 +805,6 @@ step_kernel(const StepArgs a) {
     }
   }
   stamp(9);
-
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(exit_cnt, 1u) == (unsigned)(nblk - 1)) {   // last CTA out
-      *exit_cnt = 0;
-      *scored_cnt = 0;
-      *epoch = tag;
-    }
-  }
 }
 
 template <typename T, int D, int S, int G>
@@ -920,7 +924,7 @@ StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int3
   if (np > workers) np = workers > 0 ? workers : 1;
   p.chunk_pages = 0;
   p.n_chunks = (int32_t)np;
-  p.counters_bytes = ((size_t)(4 + 2 * units + 1) * sizeof(unsigned) + 255) & ~(size_t)255;
+  p.counters_bytes = ((size_t)(4 + 2 * units) * sizeof(unsigned) + 255) & ~(size_t)255;
   p.tagged_bytes = ((size_t)h_kv * nnz * sizeof(unsigned long long) + 255) & ~(size_t)255;
   const size_t rows = (size_t)units * group * p.n_chunks;
   p.workspace_bytes = p.counters_bytes + p.tagged_bytes + rows * head_dim * sizeof(float) +

@@ -64,11 +64,13 @@ def _run(w, lens, steps, seed, append=True, n_sink=0, n_local=0):
         else:
             step(cache, gtab, q.cuda())
         assert qs.device_error() == 0
-        # after every call: the exit counter, the per-unit slot counters and
-        # the scored-workers counter are back at zero; the call tag and the
-        # ready flags hold the number of calls made so far
-        cnt = step.workspace[:(4 + 2 * B * h + 1) * 4].view(torch.int32).cpu().numpy()
-        assert cnt[0] == s + 1 and cnt[1] == 0 and cnt[2] == 0
+        # after every call: the call tag and the ready flags hold the number
+        # of calls made so far, the per-unit slot counters are back at zero,
+        # this call's counted-in bank (tag parity) holds every CTA and the
+        # next call's bank is clear
+        cnt = step.workspace[:(4 + 2 * B * h) * 4].view(torch.int32).cpu().numpy()
+        assert cnt[0] == s + 1 and cnt[1] == 0
+        assert cnt[2 + ((s + 1) & 1)] > 0 and cnt[2 + ((s + 2) & 1)] == 0
         assert np.all(cnt[4:4 + B * h] == s + 1) and np.all(cnt[4 + B * h:] == 0)
         gsm = np_of(cache.summary)
         for r in range(B):
