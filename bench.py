@@ -49,19 +49,22 @@ MIB = 1 << 20
 # ---------------------------------------------------------------------------
 
 def step_bytes(n_pages, h_kv, group, d, S, k_sel_pages, valid_tokens_selected, esize,
-               append_tokens=1):
+               append_tokens=1, batch=1, kv_tokens_total=None):
     """Algorithmic bytes of one decode step of one layer.
 
     summary of every scored page (index term, eq (10)) + K/V of the valid
     tokens of the selected pages (eq (11)) + q read + o written (fp32) + the
     append (new k/v read, written to the pool, tail-page summary read+write).
     Scores, ids and split-K partials are intermediates and not counted.
+    n_pages: scored pages of all requests; valid_tokens_selected: per (request,
+    KV head) when all are alike, else kv_tokens_total sums them over both.
     """
     summary = n_pages * h_kv * 2 * d * esize
-    kv = valid_tokens_selected * h_kv * 2 * d * esize
-    q = h_kv * group * d * esize
-    o = h_kv * group * d * 4
-    append = append_tokens * h_kv * d * esize * 2 * 2 + h_kv * 2 * d * esize * 2
+    kv_tok = valid_tokens_selected * h_kv if kv_tokens_total is None else kv_tokens_total
+    kv = kv_tok * 2 * d * esize
+    q = batch * h_kv * group * d * esize
+    o = batch * h_kv * group * d * 4
+    append = batch * (append_tokens * h_kv * d * esize * 2 * 2 + h_kv * 2 * d * esize * 2)
     return dict(summary=summary, kv=kv, q=q, o=o, append=append,
                 total=summary + kv + q + o + append)
 
@@ -131,6 +134,26 @@ class ClockSampler:
                 "power_w_max": max(float(r[3]) for r in rows if r[3].strip() not in ("", "[N/A]"))}
 
 
+def workload_config(w: wl.Workload):
+    """The bench line's `config`: the workload by what it is, with its sizes."""
+    lens = w.lengths().astype(np.int64)
+    B = len(lens)
+    heads = (f"{w.h_kv} heads (MHA)" if w.group == 1
+             else f"{w.h_kv} KV heads x {w.group} query heads (GQA, group max)")
+    ctx = (f"context {int(lens[0])}" if B == 1 else
+           f"contexts {int(lens.min())}-{int(lens.max())} (total {int(lens.sum())})")
+    dt = "fp16" if w.dtype == torch.float16 else "fp32"
+    desc = (f"{w.name}: {B} request{'s' if B > 1 else ''}, {heads}, d_h {w.head_dim}, {ctx}, "
+            f"page {w.page_size}, budget {w.k * w.page_size} tokens (K={w.k}), {dt}"
+            + (", RoPE" if w.rope else "") + (", physical pages permuted" if w.permute_pages else ""))
+    cfg = {"workload": desc, "n_pages": int((-(-lens // w.page_size)).sum()), "k": w.k,
+           "h_kv": w.h_kv, "group": w.group, "head_dim": w.head_dim,
+           "page_size": w.page_size, "seq_len": int(lens[0]) if B == 1 else int(lens.sum())}
+    if B > 1:
+        cfg["batch"] = B
+    return cfg
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -143,51 +166,61 @@ def dist_env():
 # ---------------------------------------------------------------------------
 
 class LayerSetup:
-    """The Llama-2-7B-shaped layer: pool built by the library's own append
-    (prefill of the first L-1 tokens), plus the decode token and query."""
+    """One attention layer of the workload: pools built by the library's own
+    append (prefill of all but the last token of each request), plus each
+    request's decode token and query."""
 
     def __init__(self, w: wl.Workload, nbuf: int, dev, sample_heads=4, n_sink=0, n_local=0):
         import query_aware_sparse_gb300 as qs
         self.qs = qs
         self.w = w
-        L = int(w.lengths()[0])
-        self.L = L
+        lens = w.lengths().astype(np.int64)
+        B = len(lens)
+        self.lens, self.L = lens, int(lens[0])
         S, h, d = w.page_size, w.h_kv, w.head_dim
-        self.table_np = wl.make_page_table([L], S, seed=w.seed)
-        k_tok, v_tok = wl.request_tokens(w, 0, L, device=dev)
-        self.q = wl.queries(w, [L - 1], device=dev)
-        # host copies of a few heads of the generated inputs, for the oracle
-        self.sample = (k_tok[:, :sample_heads].cpu(), v_tok[:, :sample_heads].cpu(),
-                       self.q[:, :sample_heads * w.group].cpu())
+        t = wl.make_page_table(lens, S, seed=w.seed, permute=w.permute_pages,
+                               spare_pages=64 if w.permute_pages else 0)
+        self.table_np = t
+        k_tok, v_tok, ind = wl.tokens_for_table(w, t, device=dev)
+        self.q = wl.queries(w, lens - 1, device=dev)
+        # host copies of a few heads of request 0's inputs, for the oracle
+        L0 = int(lens[0])
+        self.sample = (k_tok[:L0, :sample_heads].cpu(), v_tok[:L0, :sample_heads].cpu(),
+                       self.q[:1, :sample_heads * w.group].cpu())
         i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32), device=dev)
-        t = self.table_np
-        self.table = qs.PageTable(i32(t.page_indptr), i32(t.page_indices), i32([L]))
+        self.table = qs.PageTable(i32(t.page_indptr), i32(t.page_indices), i32(lens))
         kp, vp, sm = wl.empty_pool(t, h, d, w.dtype, device=dev, poison=False)
         self.caches = [qs.PagedCache(kp, vp, sm)]
-        # prefill append of the first L-1 tokens through the library (timed once)
-        pre = qs.PageTable(self.table.page_indptr, self.table.page_indices, i32([L - 1]))
-        kpre, vpre = k_tok[:L - 1].contiguous(), v_tok[:L - 1].contiguous()
+        # prefill append of all but the last token of each request through
+        # the library (timed once)
+        pre = qs.PageTable(self.table.page_indptr, self.table.page_indices, i32(lens - 1))
+        rows = torch.cat([torch.arange(int(ind[r]), int(ind[r]) + int(lens[r]) - 1, device=dev)
+                          for r in range(B)])
+        kpre, vpre = k_tok[rows].contiguous(), v_tok[rows].contiguous()
+        pre_ind = np.concatenate([[0], np.cumsum(lens - 1)])
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        qs.append_kv(self.caches[0], pre, kpre, vpre, i32([0, L - 1]), i32([0]))
+        qs.append_kv(self.caches[0], pre, kpre, vpre, i32(pre_ind), i32(np.zeros(B)))
         e1.record()
         torch.cuda.synchronize()
         pre_ms = e0.elapsed_time(e1)
-        pre_bytes = (L - 1) * h * d * k_tok.element_size() * 4 + t.nnz * h * 2 * d * k_tok.element_size()
-        self.prefill = {"tokens": L - 1, "ms": pre_ms, "GBps": pre_bytes / pre_ms / 1e6}
+        n_pre = int(pre_ind[-1])
+        pre_bytes = n_pre * h * d * k_tok.element_size() * 4 + t.nnz * h * 2 * d * k_tok.element_size()
+        self.prefill = {"tokens": n_pre, "ms": pre_ms, "GBps": pre_bytes / pre_ms / 1e6}
         assert qs.device_error() == 0
         for _ in range(nbuf - 1):   # distinct copies: each step reads cold memory
             c = self.caches[0]
             self.caches.append(qs.PagedCache(c.k_pool.clone(), c.v_pool.clone(), c.summary.clone()))
-        self.k_dec = k_tok[L - 1:L].contiguous()
-        self.v_dec = v_tok[L - 1:L].contiguous()
+        last = torch.as_tensor(ind[:-1] + lens - 1, device=dev)
+        self.k_dec = k_tok[last].contiguous()
+        self.v_dec = v_tok[last].contiguous()
         del k_tok, v_tok, kpre, vpre
         torch.cuda.empty_cache()
-        self.app_indptr = i32([0, 1])
-        self.before = i32([L - 1])
+        self.app_indptr = i32(np.arange(B + 1))
+        self.before = i32(lens - 1)
         self.K = w.k
-        B, hq = 1, h * w.group
+        hq = h * w.group
         self.scores = torch.empty((h, t.nnz), dtype=torch.float32, device=dev)
         self.sel = (torch.empty((B, h, self.K), dtype=torch.int32, device=dev),
                     torch.empty((B, h, self.K), dtype=torch.int32, device=dev),
@@ -231,9 +264,16 @@ class LayerSetup:
     KERNELS_PER_STEP = 1   # quest_decode_step is one cooperative kernel
 
     def bytes(self):  # noqa: A003
-        w = self.w
-        return step_bytes(self.table_np.nnz, w.h_kv, w.group, w.head_dim, w.page_size,
-                          self.K, self.K * w.page_size, self.k_dec.element_size())
+        """Algorithmic bytes of one step: the summaries of every valid page and
+        the K/V of the valid tokens of the pages the last fused step chose."""
+        w, S = self.w, self.w.page_size
+        P = -(-self.lens // S)
+        sl = self.fused.sel[0].cpu().numpy()                 # [B, h_kv, K] logical ids
+        lens = self.lens[:, None, None]
+        valid = np.where(sl >= 0, np.clip(lens - sl.astype(np.int64) * S, 0, S), 0)
+        return step_bytes(int(P.sum()), w.h_kv, w.group, w.head_dim, S, self.K, 0,
+                          self.k_dec.element_size(), batch=len(self.lens),
+                          kv_tokens_total=int(valid.sum()))
 
 
 def time_stage(fn, nbuf, reps):
@@ -329,7 +369,10 @@ class OracleSample:
             t0 = time.perf_counter()
             self.step()
             ts.append(time.perf_counter() - t0)
-        scale = self.w.h_kv / self.heads          # µs per full layer
+        # µs per full layer: all KV heads, all requests (by their pages)
+        lens = self.w.lengths().astype(np.int64)
+        pages = -(-lens // self.w.page_size)
+        scale = self.w.h_kv / self.heads * float(pages.sum()) / float(pages[0])
         return [x * 1e6 * scale for x in ts]
 
 
@@ -364,12 +407,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = wl.WORKLOADS[args.workload]
-    cfg = {"workload": f"{w.name}: 1 request, {w.h_kv} heads (MHA), d_h {w.head_dim}, "
-                       f"context {int(w.lengths()[0])}, page {w.page_size}, "
-                       f"budget {w.k * w.page_size} tokens (K={w.k}), fp16, RoPE",
-           "n_pages": int(-(-int(w.lengths()[0]) // w.page_size)), "k": w.k,
-           "h_kv": w.h_kv, "group": w.group, "head_dim": w.head_dim,
-           "page_size": w.page_size, "seq_len": int(w.lengths()[0])}
+    cfg = workload_config(w)
 
     n_sink = -(-args.sink_tokens // w.page_size)
     n_local = -(-args.local_tokens // w.page_size)
@@ -544,8 +582,8 @@ def cpu_baseline(setup, heads, seconds):
     return {"value": round(statistics.median(ts), 1), "unit": UNIT, "cores": 1,
             "kind": "oracle",
             "sample": f"fp64 numpy oracle decode step (append, score, select, attention) on "
-                      f"{heads} of {setup.w.h_kv} heads of the same layer, scaled x"
-                      f"{setup.w.h_kv // heads} to a full layer; {len(ts)} steps"}
+                      f"{heads} of {setup.w.h_kv} heads of request 0 of the same layer, scaled "
+                      f"to every head and request by pages; {len(ts)} steps"}
 
 
 def run_reference(args, w, cfg, dev, ws):
