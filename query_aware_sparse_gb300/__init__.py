@@ -245,12 +245,13 @@ class DecodeStep:
 
 
 TRACE_NAMES = ("start", "scored", "selected", "att_start", "att_pages", "att_merged",
-               "", "", "", "exit",
+               "sel_begin", "sel_end", "", "exit",
                "sel0_polled | desc0", "sel0_done | page0", "sel1_polled | merged",
                "sel1_done | fmerge0", "sel2_polled | fmerge1", "sel2_done")
-# slots 10-15 depend on the CTA's role: select stamps on selectors (the CTAs
-# whose "scored" stamp precedes any scoring), attention and final-merge stamps
-# on the others
+# slots 6-7: the first select's start (after the scored gate) and the last
+# select's end, on every CTA that selects; slots 10-15 depend on the CTA's
+# role: select stamps on dedicated selectors (the CTAs whose "scored" stamp
+# precedes any scoring), attention and final-merge stamps on the others
 
 
 def set_trace(buffer, max_ctas=0, batch=0, h_kv=0, group=1, head_dim=128, page_size=16,

@@ -5,26 +5,29 @@
 //   a4 attention over the selected pages (Quest page Fig. 1, §2.1), and
 //   a5 the log-sum-exp merge of its split-K partials (Quest page §2.1).
 //
-// Roles. The first NSEL CTAs (about one in eight, at most one per unit) only
-// select; the others ("workers") score and then attend.
+// Roles. While there are at most one unit (request, KV head) per eight
+// CTAs, the first NSEL = units CTAs only select and the others ("workers")
+// score and then attend. With more units every CTA is a worker and also
+// selects units after scoring.
 //
 // Scoring. Each worker scores an equal share of the (page, head) items of
 // the page table, page-major with a fixed head per thread, so the query
 // stays in registers. Start-up is two dependent loads deep (page table ->
 // summary): the first items take their physical pages from the table while
 // the slice's metadata is staged in shared memory. Summaries stream through
-// a register pipeline kPD items deep, so the loop never waits on a dependent
+// a register pipeline PD items deep, so the loop never waits on a dependent
 // load, a barrier or another CTA. Each score is also stored with the call's
 // tag in the upper half of a 64-bit word: a reader tells a score of this
 // call from a stale one without any fence on the writer's side. Each worker
-// then bumps a "scored" counter with a release; a selector acquires it before
-// reading its row once (instead of polling it while the workers stream), so
+// then bumps a "scored" counter with a release; a selecting CTA acquires it
+// before reading its rows once (instead of polling it while the workers stream), so
 // the appended K/V rows are ordered before the attention's copies of them.
 //
-// Selection. Selectors take the (request, KV head) units in head order, read
-// a unit's tagged row (batches of independent loads, re-polling only stale
-// entries; key min and max reduced on the way), run the block-wide Top-K and
-// publish the unit's ready flag (set to the tag) with a release store.
+// Selection. CTA b takes units b, b + grid, ... in head order: it waits for
+// the complete scored count once, reads each unit's tagged row (batches of
+// independent loads, re-polling only stale entries; key min and max reduced
+// on the way), runs the block-wide Top-K and publishes the unit's ready flag
+// (set to the tag) with a release store.
 //
 // Attention. The selected-page slots of all units, in head order, form one
 // list; each worker takes an equal contiguous share. Its warps stream their
@@ -39,8 +42,10 @@
 // bounded and reports QUEST_DEVERR_WAIT_TIMEOUT instead of hanging.
 // Publication is release/acquire; a proxy fence orders it before the bulk
 // copies read the pool. The call tag lives in the workspace and is advanced
-// by the selectors once every CTA has read it; the per-unit counters are reset
+// by the selecting CTAs once every CTA has read it; the per-unit counters are reset
 // by their last user and the scored counters are double-buffered by tag parity.
+#include <cstdlib>
+
 #include "attn_dev.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -51,8 +56,7 @@ namespace {
 
 constexpr int kNT = 256;              // threads per CTA
 constexpr int kNW = kNT / 32;
-constexpr int kPD = 2;                // scoring software-pipeline depth (items)
-constexpr int kKeysCap = 4096;        // selector keys cached in shared memory
+constexpr int kKeysCap = 8192;        // selector keys cached in shared memory
 constexpr int kSliceCap = 1024;       // slice pages whose metadata is staged at once
 constexpr int kRounds = 1;            // attention rounds
 constexpr int kMaxSeg = 4;            // unit segments per attention pass (G = 1)
@@ -101,11 +105,12 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
   return old;
 }
 
-// CTAs that only select (the rest score and attend): about one per eight,
-// at most one per unit.
+// CTAs that only select (the rest score and attend): one per unit while
+// the units are at most one CTA in eight; with more units every CTA scores
+// and the selects are spread over all of them after scoring.
 __host__ __device__ __forceinline__ int select_ctas(int units, int nblk) {
   const int n = nblk / 8 > 1 ? nblk / 8 : 1;
-  return units < n ? units : n;
+  return units <= n ? units : 0;
 }
 
 
@@ -113,11 +118,17 @@ template <typename T, int D, int S, int G>
 struct StepShape {
   using W = WarpAttn<T, D, S, G>;
   static constexpr int VEC = Elem<T>::kVec;
-  static constexpr int NST = 1;                       // attention slots per warp
+  // one CTA per SM (larger groups need the registers; stages of 8 KiB pages
+  // do not fit twice): each thread then keeps more bytes in flight, with a
+  // deeper scoring pipeline and, where they fit, two attention stages per warp
+  static constexpr bool ONE = G >= 4 || S * D * (int)sizeof(T) > 4096;
+  static constexpr int MINB = ONE ? 1 : 2;            // resident CTAs per SM
+  static constexpr int NST = (ONE && 4 * kNW * W::BLOCK_BYTES <= 128 * 1024) ? 2 : 1;
   static constexpr int MAXSEG = kMaxSeg / G > 0 ? kMaxSeg / G : 1;
   // scoring: VPL 16-byte vectors of m (and of M) per lane, LPP lanes per
-  // (page, head) item, IPR items per round
+  // (page, head) item, IPR items per round, PD items in flight per thread
   static constexpr int VPL = G == 1 ? 2 : 1;
+  static constexpr int PD = !ONE ? 2 : VPL == 2 ? 4 : G <= 4 ? 8 : 4;
   static constexpr int LPP = D * (int)sizeof(T) / (16 * VPL);
   static constexpr int IPR = kNT / LPP;
   static constexpr int WPL = 4 * VPL;                 // 32-bit words of m per lane
@@ -175,7 +186,7 @@ struct Round {
 };
 
 template <typename T, int D, int S, int G>
-__global__ void __launch_bounds__(kNT, G >= 4 ? 1 : 2)   // larger groups need the registers
+__global__ void __launch_bounds__(kNT, StepShape<T, D, S, G>::MINB)
 step_kernel(const StepArgs a) {
   using Sh = StepShape<T, D, S, G>;
   using W = typename Sh::W;
@@ -191,6 +202,12 @@ step_kernel(const StepArgs a) {
   const int h_q = a.h_kv * G;
   const int K = a.k;
   const int NP = a.n_chunks;                // partial slots per unit
+  // programmatic dependent launch: the next kernel on the stream may be
+  // scheduled now (its CTAs take SMs as this grid's CTAs exit), and this
+  // grid waits here until the previous kernel has completed and its writes
+  // (pool, summaries, workspace counters) are visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   unsigned* epoch = a.counters;             // tag of the last call
   unsigned* ready = a.counters + 4;         // [U] tag of the published selection
   unsigned* att_done = ready + U;           // [U] attention slots finished
@@ -225,7 +242,7 @@ step_kernel(const StepArgs a) {
   // deep: the first kPD items take their physical pages straight from the
   // page table, and the query and the slice's metadata load while those
   // summaries are in flight.
-  constexpr int LPP = Sh::LPP, VPL = Sh::VPL, WPL = Sh::WPL, IPR = Sh::IPR;
+  constexpr int LPP = Sh::LPP, VPL = Sh::VPL, WPL = Sh::WPL, IPR = Sh::IPR, kPD = Sh::PD;
   const long long n_items = (long long)a.nnz * a.h_kv;
   const long long t0 = selector ? 0 : bw * n_items / nbw;
   const long long t1 = selector ? 0 : (bw + 1) * n_items / nbw;
@@ -437,12 +454,13 @@ step_kernel(const StepArgs a) {
   if (!selector && tid == 0) red_release_add(scored_cnt, 1u);
   stamp(1);
 
-  // =================== selection (selector b takes units b, b + NSEL, ... in head order) ===================
-  if (selector) {
+  // ============ selection (CTA b takes units b, b + nblk, ... in head order) ============
+  // with dedicated selectors these are exactly the selectors' units
+  if (b < U) {
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                      // [kKeysCap]
     int32_t* physs = reinterpret_cast<int32_t*>(smem + kKeysCap * 4);        // [kKeysCap]
     for (int i = tid; i < kTopkBins; i += kNT) tsm.hist[i] = 0;   // block_topk_smem keeps it zero
-    for (int kk = b; kk < U; kk += NSEL) {
+    for (int kk = b; kk < U; kk += nblk) {
       const int g = kk / a.batch, r = kk % a.batch;
       const int u = r * a.h_kv + g;
       const int lo = __ldg(a.page_indptr + r);
@@ -462,7 +480,7 @@ step_kernel(const StepArgs a) {
       // gate: one thread waits (bounded) until every worker has finished
       // scoring, so the block reads the row once instead of polling it while
       // the workers stream; the row's tags still decide below
-      if (tid == 0) {
+      if (tid == 0 && kk == b) {
         for (uint32_t it = 0; ld_acquire(scored_cnt) < (unsigned)nblk && it < (1u << 20); ++it)
           __nanosleep(128);
         // every CTA read the epoch before its release of this count: advance it
@@ -511,8 +529,9 @@ step_kernel(const StepArgs a) {
       __syncthreads();
 #pragma unroll
       for (int w = 0; w < kNW; ++w) { kmin = min(kmin, tsm.red[0][w]); kmax = max(kmax, tsm.red[1][w]); }
-      const int nth = (kk - b) / NSEL;       // this CTA's n-th select
-      if (nth < 3) stamp(10 + 2 * nth);
+      const int nth = (kk - b) / nblk;       // this CTA's n-th select
+      if (nth == 0) stamp(6);
+      if (selector && nth < 3) stamp(10 + 2 * nth);
       int32_t* ol = a.sel_logical + (size_t)u * K;
       int32_t* op = a.sel_phys + (size_t)u * K;
       const int nsel = min(P, K);
@@ -528,7 +547,8 @@ step_kernel(const StepArgs a) {
                              }, tsm, emit);
       __syncthreads();
       if (tid == 0) st_release(ready + u, tag);   // releases the block's selection writes
-      if (nth < 3) stamp(11 + 2 * nth);
+      if (selector && nth < 3) stamp(11 + 2 * nth);
+      stamp(7);
     }
     __syncthreads();
   }
@@ -838,12 +858,26 @@ cudaError_t launch_t(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
   cfg.blockDim = dim3(kNT);
   cfg.dynamicSmemBytes = Sh::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: the waits end
   attr[0].val.cooperative = 1;
+  // the launch may overlap the previous kernel's tail (the kernel waits for
+  // it with griddepcontrol.wait before touching memory)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // -1 untried, 0 refused (or QUEST_NO_PDL set in the environment), 1 accepted
+  static int pdl_ok = getenv("QUEST_NO_PDL") ? 0 : -1;
+  cfg.numAttrs = pdl_ok == 0 ? 1 : 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, step_kernel<T, D, S, G>, a);
+  if (e != cudaSuccess && cfg.numAttrs == 2 && pdl_ok == -1) {   // not with this launch: plain
+    cudaGetLastError();
+    pdl_ok = 0;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, step_kernel<T, D, S, G>, a);
+  } else if (e == cudaSuccess) {
+    pdl_ok = cfg.numAttrs == 2 ? 1 : pdl_ok;
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

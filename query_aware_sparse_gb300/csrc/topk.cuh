@@ -10,9 +10,10 @@
 // scores rarely puts many keys in one bin, so the bin atomics do not pile
 // up), and stops as soon as the digit bucket holding the K-th key is taken
 // whole. A block scan in page order then emits the winners. Rows whose keys
-// sit in shared memory (up to 16 per thread) take block_topk_smem: once the
-// first digit has isolated a boundary bucket of at most kTopkGather keys,
-// that bucket is ranked directly instead of taking further digits.
+// sit in shared memory (up to 32 per thread) take block_topk_smem, which
+// holds each thread's keys in registers: once the first digit has isolated a
+// boundary bucket of at most kTopkGather keys, that bucket is ranked directly
+// instead of taking further digits.
 #pragma once
 
 #include "common.cuh"
@@ -34,8 +35,8 @@ struct TopkSmem {
   alignas(16) uint32_t hist[kTopkBins];
   uint32_t red[2][NT / 32];
   unsigned long long scan[NT / 32];
-  uint32_t gkey[kTopkGather];
-  int32_t gidx[kTopkGather];
+  alignas(16) uint32_t gkey[kTopkGather];
+  alignas(16) int32_t gidx[kTopkGather];
   uint32_t digit, krem, done, bcnt, gcount;
 };
 
@@ -200,37 +201,55 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
                            TopkSmem<NT>& sm, int32_t* out_logical, int32_t* out_phys,
                            int32_t* out_count, PhysOf phys_of, Forced forced, int nforced);
 
-// Top-K of P <= 16 * NT keys held in shared memory (`keys`, overwritten),
-// whose block-wide min and max the caller has already reduced. Same result
-// as block_topk_keys. Pages with forced(i) (nforced of them, at most K) are
-// kept outright and the other pages compete for the remaining K - nforced;
+// Top-K of P <= 32 * NT keys held in shared memory (`keys`, P rounded up to
+// a multiple of 4 * NT readable, 16-byte aligned; overwritten), whose
+// block-wide min and max the caller has already reduced. Same result as
+// block_topk_keys. Pages with forced(i) (nforced of them, at most K) are kept
+// outright and the other pages compete for the remaining K - nforced;
 // kmin / kmax are over the other pages' keys only. `sm.hist` must be all
-// zero on entry and is all zero on return. After the first radix digit, a boundary bucket of at most
+// zero on entry and is all zero on return.
+//
+// Thread t holds the keys [t*per, t*per + per) in registers (per a multiple
+// of 4, at most KPT), read once with 16-byte loads; every pass then works on
+// registers. After the first radix digit, a boundary bucket of at most
 // kTopkGather keys is ranked directly (key, then lower index) instead of
 // taking more digits: its winners are marked with the top key and its
-// losers with 0, so one threshold then selects exactly K keys. Loops stay
-// rolled (this runs once per row: its code is fetched cold) and the page-
-// order scan packs (greater, equal) counts into 32 bits with one barrier.
-template <int NT, typename Emit, typename Forced>
-__device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
-                                TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced) {
+// losers with 0, so one threshold then selects exactly K keys. The page-
+// order compaction packs (greater, equal) counts into 32 bits (P < 65536).
+template <int NT, int KPT, typename Emit, typename Forced>
+__device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
+                          TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced) {
+  static_assert(KPT % 4 == 0 && KPT <= 32, "keys per thread: a multiple of 4, at most 32");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NWP = NT / 32;
   constexpr int BPT = kTopkBins / NT;            // bins per thread in the digit search
   static_assert(BPT % 4 == 0, "bins are read as 16-byte vectors");
 
-  if (P <= K) {                     // every scored page is selected
-    for (int i = tid; i < P; i += NT) emit(i, i);
-    return;
+  const int per = (P + 4 * NT - 1) / (4 * NT) * 4;
+  const int c0 = tid * per;
+  uint32_t kr[KPT];
+  uint32_t inr = 0, comp = 0;                    // bit j: key c0 + j exists / competes
+#pragma unroll
+  for (int v = 0; v < KPT / 4; ++v) {
+    const uint4 x = 4 * v < per ? *reinterpret_cast<const uint4*>(keys + c0 + 4 * v)
+                                : make_uint4(0u, 0u, 0u, 0u);
+    kr[4 * v] = x.x; kr[4 * v + 1] = x.y; kr[4 * v + 2] = x.z; kr[4 * v + 3] = x.w;
+#pragma unroll
+    for (int j = 4 * v; j < 4 * v + 4; ++j) {
+      const int i = c0 + j;
+      if (j < per && i < P) {
+        inr |= 1u << j;
+        if (!forced(i)) comp |= 1u << j;
+      }
+    }
   }
-  // forced pages are kept outright; the others compete for the rest
-  const int Kq = K - nforced;
+  const int Kq = K - nforced;                    // the competing pages' share
   uint32_t T = 0xffffffffu, need = 0;
   bool ge_mode = false;    // select key >= T vs (key > T, then `need` of key == T)
   if (Kq <= 0) {
-    need = 0;              // no key passes: (> 0xffffffff) is false, need 0
+    need = 0;              // no competing key passes: (> 0xffffffff) is false, need 0
   } else if (kmin == kmax) {
-    T = kmin; need = Kq; ge_mode = false;
+    T = kmin; need = Kq;
   } else {
     int hi = 31 - __clz(kmin ^ kmax);           // highest differing bit
     uint32_t prefix = kmin & ~((hi == 31) ? 0xffffffffu : ((2u << hi) - 1u));
@@ -240,11 +259,10 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
       const int nbits = hi - shift + 1;
       const uint32_t dmask = (1u << nbits) - 1u;
       const uint32_t hi_mask = (hi == 31) ? 0u : ~((2u << hi) - 1u);
-#pragma unroll 1
-      for (int i = tid; i < P; i += NT) {
-        const uint32_t k = keys[i];
-        if ((k & hi_mask) == prefix && !forced(i)) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
-      }
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+        if (((comp >> j) & 1u) && (kr[j] & hi_mask) == prefix)
+          atomicAdd(&sm.hist[(kr[j] >> shift) & dmask], 1u);
       if (tid == 0) sm.gcount = 0;
       __syncthreads();
       // thread t owns bins [t*BPT, t*BPT + BPT); count of keys in higher bins
@@ -291,27 +309,41 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
       if (bcnt <= (uint32_t)kTopkGather) {
         // rank the bucket [prefix, prefix + 2^shift) directly
         const uint32_t span = (1u << shift) - 1u;
-#pragma unroll 1
-        for (int i = tid; i < P; i += NT) {
-          const uint32_t k = keys[i];
-          if ((k & ~span) == prefix && !forced(i)) {
+        uint32_t inb = 0;                          // bit j: key c0 + j is in the bucket
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+          if (((comp >> j) & 1u) && (kr[j] & ~span) == prefix) {
+            inb |= 1u << j;
             const uint32_t at = atomicAdd(&sm.gcount, 1u);
-            sm.gkey[at] = k;
-            sm.gidx[at] = i;
+            sm.gkey[at] = kr[j];
+            sm.gidx[at] = c0 + j;
           }
         }
         __syncthreads();
         if (tid < (int)bcnt) {
           const uint32_t mk = sm.gkey[tid];
           const int mi = sm.gidx[tid];
-          uint32_t rank = 0;
+          uint32_t r4[4] = {0u, 0u, 0u, 0u};
+          const int n4 = (int)bcnt & ~3;
 #pragma unroll 1
-          for (int j = 0; j < (int)bcnt; ++j) {
-            const uint32_t kj = sm.gkey[j];
-            rank += (kj > mk) || (kj == mk && sm.gidx[j] < mi);
+          for (int j = 0; j < n4; j += 4) {          // four independent counts per step
+            const uint4 kj = *reinterpret_cast<const uint4*>(&sm.gkey[j]);
+            const int4 ij = *reinterpret_cast<const int4*>(&sm.gidx[j]);
+            r4[0] += (kj.x > mk) || (kj.x == mk && ij.x < mi);
+            r4[1] += (kj.y > mk) || (kj.y == mk && ij.y < mi);
+            r4[2] += (kj.z > mk) || (kj.z == mk && ij.z < mi);
+            r4[3] += (kj.w > mk) || (kj.w == mk && ij.w < mi);
           }
-          keys[mi] = rank < krem ? 0xffffffffu : 0u;
+          for (int j = n4; j < (int)bcnt; ++j) {
+            const uint32_t kj = sm.gkey[j];
+            r4[0] += (kj > mk) || (kj == mk && sm.gidx[j] < mi);
+          }
+          keys[mi] = (r4[0] + r4[1] + r4[2] + r4[3]) < krem ? 0xffffffffu : 0u;
         }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < KPT; ++j)               // take the marks back
+          if ((inb >> j) & 1u) kr[j] = keys[c0 + j];
         const unsigned long long top = (unsigned long long)prefix + (1ull << shift);
         T = top > 0xffffffffull ? 0xffffffffu : (uint32_t)top;
         need = 0;
@@ -320,21 +352,24 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
       }
       hi = shift - 1;
     }
-    __syncthreads();   // marks written; sm.digit/krem/done read by all
+    __syncthreads();   // sm.digit/krem/done/bcnt read by all before any reuse
   }
 
-  // Stable compaction in page order: thread t takes keys [c0, c1); its
-  // (greater, equal) counts are packed 16:16 (P <= 4096 fits).
-  const int per = (P + NT - 1) / NT;
-  const int c0 = min(P, tid * per), c1 = min(P, c0 + per);
-  uint32_t cnt = 0;
-#pragma unroll 1
-  for (int i = c0; i < c1; ++i) {
-    const uint32_t k = keys[i];
-    const bool f = forced(i);
-    if (ge_mode) cnt += (uint32_t)(f || k >= T) << 16;
-    else cnt += ((uint32_t)(f || k > T) << 16) | (uint32_t)(!f && k == T);
+  // Stable compaction in page order over the register keys (branch-free:
+  // `win` = selected outright, `tie` = a key equal to T competing for `need`).
+  // In ge_mode, keys >= T win: the same as keys > T - 1 with no ties (T > 0
+  // there, as a digit bucket above the lowest one was taken whole).
+  const uint32_t Tg = ge_mode ? T - 1u : T;
+  uint32_t wins = 0, ties = 0;                   // bit j: key c0 + j wins / ties
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t f = (inr & ~comp) >> j & 1u;
+    const uint32_t w = f | (uint32_t)(kr[j] > Tg);
+    const uint32_t t = (uint32_t)(!ge_mode) & (comp >> j & 1u) & (uint32_t)(kr[j] == T);
+    wins |= (w & (inr >> j)) << j;
+    ties |= t << j;
   }
+  const uint32_t cnt = ((uint32_t)__popc(wins) << 16) | (uint32_t)__popc(ties);
   uint32_t incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -347,23 +382,33 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
 #pragma unroll
   for (int w = 0; w < NWP; ++w)
     if (w < warp) ex += sm.red[1][w];
-  uint32_t gt_b = ex >> 16, eq_b = ex & 0xffffu;
-#pragma unroll 1
-  for (int i = c0; i < c1; ++i) {
-    const uint32_t k = keys[i];
-    const bool f = forced(i);
-    int pos = -1;
-    if (ge_mode) {
-      if (f || k >= T) pos = gt_b++;
-    } else if (f || k > T) {
-      pos = gt_b + min(eq_b, need);
-      ++gt_b;
-    } else if (k == T) {
-      if (eq_b < need) pos = gt_b + eq_b;
-      ++eq_b;
-    }
-    if (pos >= 0 && pos < K) emit(pos, i);
+  // a winner's place: winners before it (all of them precede it in page
+  // order) + ties before it that were taken (at most `need`); a tie's place
+  // likewise, if it is among the first `need` ties
+  const uint32_t gt_b = ex >> 16, eq_b = ex & 0xffffu;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t below = (1u << j) - 1u;
+    const uint32_t gt = gt_b + (uint32_t)__popc(wins & below);
+    const uint32_t eq = eq_b + (uint32_t)__popc(ties & below);
+    const bool w = (wins >> j) & 1u, t = ((ties >> j) & 1u) && eq < need;
+    const int pos = (int)(gt + min(eq, need));
+    if ((w || t) && pos < K) emit(pos, c0 + j);
   }
+}
+
+// Top-K of P <= 32 * NT keys in shared memory (see topk_regs): picks the
+// register footprint for the row length.
+template <int NT, typename Emit, typename Forced>
+__device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
+                                TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced) {
+  if (P <= K) {                     // every scored page is selected
+    for (int i = threadIdx.x; i < P; i += NT) emit(i, i);
+    return;
+  }
+  if (P <= 8 * NT) topk_regs<NT, 8>(P, K, keys, kmin, kmax, sm, emit, forced, nforced);
+  else if (P <= 16 * NT) topk_regs<NT, 16>(P, K, keys, kmin, kmax, sm, emit, forced, nforced);
+  else topk_regs<NT, 32>(P, K, keys, kmin, kmax, sm, emit, forced, nforced);
 }
 
 template <int NT, typename PhysOf, typename Forced>
@@ -399,7 +444,7 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
   __syncthreads();
 #pragma unroll
   for (int w = 0; w < NT / 32; ++w) { kmin = min(kmin, sm.red[0][w]); kmax = max(kmax, sm.red[1][w]); }
-  if (P <= 16 * NT) {
+  if (P <= 32 * NT && P <= cap) {
     block_topk_smem<NT>(P, K, keys, kmin, kmax, sm, emit, forced, nforced);
   } else {        // longer cached rows: the general routine over the shared-memory keys
     block_topk_keys<NT>(P, K, [keys, forced](int i) { return forced(i) ? 0xffffffffu : keys[i]; },

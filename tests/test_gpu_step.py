@@ -145,6 +145,26 @@ def test_step_many_units():
          steps=1, seed=10)
 
 
+def test_step_units_above_grid():
+    # more units than CTAs (one per SM at G = 4): CTAs select several units
+    # each after scoring
+    _run(_w("above", batch=20, h_kv=8, group=4, k=4, head_dim=64),
+         [17 + 13 * i for i in range(20)], steps=2, seed=11)
+
+
+@pytest.mark.parametrize("group,lens", [(1, [70000, 900]), (4, [140000, 3000])])
+def test_step_long_rows(group, lens):
+    # rows above the 4096 and 8192 keys the selecting CTA caches in shared
+    # memory (the second reads its keys from L2)
+    _run(_w("long", batch=2, h_kv=2, group=group, k=64, head_dim=64), lens, steps=2,
+         seed=12 + group)
+
+
+def test_step_fp32_d128_gqa():
+    _run(_w("f32g", batch=3, h_kv=2, group=2, head_dim=128, dtype=torch.float32, k=8),
+         [300, 17, 1000], steps=2, seed=13)
+
+
 @pytest.mark.parametrize("n_sink,n_local", [(1, 4), (2, 0), (0, 16)])
 def test_step_hybrid_budget(n_sink, n_local):
     """Local window + sink pages forced (Quest page §2.2, §3.2), through the
