@@ -154,6 +154,16 @@ def workload_config(w: wl.Workload):
     return cfg
 
 
+def data_desc(w: wl.Workload):
+    """The bench line's `data`: how the synthetic inputs are made."""
+    extra = ""
+    if w.outlier_channels:
+        extra += f", {w.outlier_channels} outlier channels x{w.outlier_scale:g}"
+    if w.rope:
+        extra += ", RoPE"
+    return f"synthetic (seeded N(0,1) K/V/q{extra})"
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -516,14 +526,13 @@ def main():
     # stream: its average launch duration is the region's time per step
     dom_bytes = by["total"]
     dom_gbs = dom_bytes / (value * 1e-6) / 1e9
-    kern = ("step_kernel", ["step.cu", "attn_dev.cuh", "topk.cuh"])
-    traffic = ncu_traffic(kern[0], w.name)
+    traffic = ncu_traffic("step_kernel", w.name)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16", "data": "synthetic (seeded N(0,1) K/V/q, 4 outlier channels x8, RoPE)",
+        "dtype": "f16", "data": data_desc(w),
         "config": cfg,
         "p50_us": round(steps_us[len(steps_us) // 2], 3),
         "p95_us": round(steps_us[int(len(steps_us) * 0.95)], 3),

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libquest.so")
 SOURCES = ["quest_api.cu", "append.cu", "score.cu", "select.cu", "attn.cu", "step.cu", "noalloc.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.h", "topk.cuh", "attn_dev.cuh")] + [
+HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.h", "topk.cuh", "attn_dev.cuh",
+                                           "attn_mma.cuh")] + [
            os.path.join(ROOT, "include", "quest.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

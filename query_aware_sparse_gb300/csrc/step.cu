@@ -45,8 +45,10 @@
 // by the selecting CTAs once every CTA has read it; the per-unit counters are reset
 // by their last user and the scored counters are double-buffered by tag parity.
 #include <cstdlib>
+#include <type_traits>
 
 #include "attn_dev.cuh"
+#include "attn_mma.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "topk.cuh"
@@ -611,7 +613,11 @@ step_kernel(const StepArgs a) {
         }
       }
       __syncthreads();
-      W st;
+      // fp16 groups of 4 or 8 query heads: QK and AV on the warp MMA, each
+      // page loaded straight into registers (a second page in flight spills)
+      constexpr bool kMma = sizeof(T) == 2 && G >= 4 && S == 16;
+      using WA = std::conditional_t<kMma, WarpAttnMma<D, G>, W>;
+      WA st;
       int cs = -1;                           // segment of the running state
 #pragma unroll 1
       for (int base = 0; base * kNW < npass; base += 32) {
@@ -638,6 +644,34 @@ step_kernel(const StepArgs a) {
         if (my_val > 0) desc[__popc(vmask & ((1u << lane) - 1))] = make_int2(my_pp, my_val);
         __syncwarp();
         if (pa == pb && base == 0) stamp(10);
+        auto set_seg = [&](int n) {
+          const int seg = desc[n].y >> 8;
+          if (seg != cs) {                   // unit changes: stash the running state
+            if (cs >= 0)
+              st.stash(stash_o + (size_t)cs * kNW * G * D, stash_ml + (size_t)cs * kNW * G * 2, warp, lane);
+            const int kk = rd.k0 + ka + seg;
+            const int r = kk % a.batch, g = kk / a.batch;
+            st.init(static_cast<const T*>(a.q) + ((size_t)r * h_q + (size_t)g * G) * D, a.scale_log2, lane);
+            cs = seg;
+          }
+        };
+        if constexpr (kMma) {
+          typename WA::Page pA;
+          auto load = [&](int n, typename WA::Page& pg) {
+            const int kk = rd.k0 + ka + (desc[n].y >> 8);
+            const size_t off = (size_t)desc[n].x * page_stride + (size_t)(kk / a.batch) * head_block;
+            WA::load(static_cast<const T*>(a.k_pool) + off, static_cast<const T*>(a.v_pool) + off, lane,
+                     pol_stream, pg);
+          };
+          for (int n = 0; n < nv; ++n) {
+            load(n, pA);
+            set_seg(n);
+            st.page(pA, desc[n].y & 0xff, lg, lane);
+            if (pa == pb && base == 0 && n == 0) stamp(11);
+          }
+          __syncwarp();
+          continue;
+        } else {
         auto issue = [&](int n) {
           const int slot = n % NST;
           const int kk = rd.k0 + ka + (desc[n].y >> 8);
@@ -654,15 +688,7 @@ step_kernel(const StepArgs a) {
         }
         for (int n = 0; n < nv; ++n) {
           const int slot = n % NST;
-          const int seg = desc[n].y >> 8;
-          if (seg != cs) {                   // unit changes: stash the running state
-            if (cs >= 0)
-              st.stash(stash_o + (size_t)cs * kNW * G * D, stash_ml + (size_t)cs * kNW * G * 2, warp, lane);
-            const int kk = rd.k0 + ka + seg;
-            const int r = kk % a.batch, g = kk / a.batch;
-            st.init(static_cast<const T*>(a.q) + ((size_t)r * h_q + (size_t)g * G) * D, a.scale_log2, lane);
-            cs = seg;
-          }
+          set_seg(n);
           if (!mbar_wait_bounded(bars + slot, (phase >> slot) & 1u)) {
             if (lane == 0) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
           } else {
@@ -678,6 +704,7 @@ step_kernel(const StepArgs a) {
           }
         }
         __syncwarp();
+        }
       }
       if (cs >= 0)
         st.stash(stash_o + (size_t)cs * kNW * G * D, stash_ml + (size_t)cs * kNW * G * 2, warp, lane);
