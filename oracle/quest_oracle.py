@@ -415,6 +415,65 @@ def page_slack(q, keys):
     return float(page_bound(q, m, M) - (keys.astype(F64) @ np.asarray(q, F64)).max())
 
 
+def topr_tokens(logits, R):
+    """Indices of the min(R, n) largest logits, ties to the lower index (the
+    select's order rule, applied to tokens)."""
+    s = np.asarray(logits, dtype=F64)
+    order = np.lexsort((np.arange(len(s)), -s))
+    return order[:min(R, len(s))]
+
+
+def topr_page_recall(logits, token_page, selected_pages, R):
+    """Top-R token recall (Quest page §1.1, recall paragraph): the share of the
+    R tokens with the highest dense logits whose page is a selected page."""
+    top = topr_tokens(logits, R)
+    sel = {int(p) for p in selected_pages if int(p) >= 0}
+    return sum(int(token_page[i]) in sel for i in top) / len(top)
+
+
+def recall_diagnostics(q, k_pool, v_pool, page_indptr, page_indices, seq_lens,
+                       sel_logical, group, R, sm_scale=None):
+    """Per-query-head diagnostics of a selection against dense attention over
+    each request's valid tokens (Quest page §1.1 eq (6)-(7) and its recall
+    paragraph; §3.1 page slack). Query head h uses the pages chosen for its
+    KV head h // group.
+
+    slack [h_q, nnz]    g_p(q_h) = U_p(q_h) - max over the page's valid keys
+                        of q_h.k (unscaled); NaN past a request's pages
+    eps   [batch, h_q]  dense softmax mass outside the candidate pages
+    topr  [batch, h_q]  top-R token recall of the candidate pages
+    vmax  [batch, h_kv] max_t ||v_t||_2
+    """
+    batch, h_q, d = q.shape
+    h_kv, S = k_pool.shape[1], k_pool.shape[2]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    slack = np.full((h_q, len(page_indices)), np.nan)
+    eps = np.full((batch, h_q), np.nan)
+    topr = np.full((batch, h_q), np.nan)
+    vmax = np.full((batch, h_kv), np.nan)
+    for r in range(batch):
+        L = int(seq_lens[r])
+        P = -(-L // S)
+        lo = int(page_indptr[r])
+        token_page = np.arange(L) // S
+        for g in range(h_kv):
+            keys, vals = candidate_tokens(k_pool, v_pool, page_indptr, page_indices,
+                                          seq_lens, r, g, range(P))
+            sel = [int(p) for p in sel_logical[r, g] if int(p) >= 0]
+            mask = np.isin(token_page, sel)
+            vmax[r, g] = value_norm_max(vals)
+            for h in range(g * group, (g + 1) * group):
+                qh = q[r, h]
+                eps[r, h] = excluded_mass(qh, keys, mask, sm_scale)
+                topr[r, h] = topr_page_recall(keys @ np.asarray(qh, dtype=F64),
+                                              token_page, sel, R)
+                for lp in range(P):
+                    pp = int(page_indices[lo + lp])
+                    slack[h, lo + lp] = page_slack(qh, k_pool[pp, g, :min(S, L - lp * S)])
+    return dict(slack=slack, eps=eps, topr=topr, vmax=vmax)
+
+
 # ---------------------------------------------------------------------------
 # Byte model (Quest page §2 eq (9)-(12))
 # ---------------------------------------------------------------------------

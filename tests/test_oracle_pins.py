@@ -498,3 +498,68 @@ def test_planted_mistakes_are_caught(golden, monkeypatch):
     U = [1.0, 1.0, 0.5]
     wrong = sorted(np.lexsort((-np.arange(3), -np.asarray(U)))[:1].tolist())
     assert wrong != _rank_select(U, 1)
+
+
+# ---------------------------------------------------------------------------
+# Recall diagnostics (Quest page §1.1 recall paragraph and its four-page
+# example; eq (6)-(7); §3.1 page slack)
+# ---------------------------------------------------------------------------
+
+def test_topr_tokens_brute_force():
+    rng = np.random.default_rng(31)
+    for trial in range(50):
+        n = int(rng.integers(1, 40))
+        s = rng.integers(-3, 4, size=n).astype(np.float64)          # many ties
+        R = int(rng.integers(1, 50))
+        want = sorted(range(n), key=lambda i: (-s[i], i))[:min(R, n)]
+        assert list(qo.topr_tokens(s, R)) == want
+
+
+def test_recall_four_page_example():
+    """Pages A-D with true maxima 10, 3, 2, 1 and bounds 10, 14, 12, 4: K = 2
+    takes B and C and misses the page of the highest logit; K = 3 recalls it."""
+    logits = np.array([10., 0., 3., -1., 2., 0., 1., 0.])        # two tokens per page
+    token_page = np.arange(8) // 2
+    U = np.array([10., 14., 12., 4.])
+    sel2 = qo.topk_pages(U, 2)
+    assert sorted(sel2.tolist()) == [1, 2]
+    assert qo.topr_page_recall(logits, token_page, sel2, 1) == 0.0
+    assert qo.topr_page_recall(logits, token_page, sel2, 2) == 0.5   # 10 (A) and 3 (B)
+    sel3 = qo.topk_pages(U, 3)
+    assert sorted(sel3.tolist()) == [0, 1, 2]
+    assert qo.topr_page_recall(logits, token_page, sel3, 1) == 1.0
+
+
+def test_recall_diagnostics_special_cases():
+    lens = [1, 16, 33, 70]
+    kp, vp, indptr, perm, sl, q, toks = _paged_case(12, lens, G=2)
+    G, h_kv, S = 2, 2, 16
+    P = [-(-L // S) for L in lens]
+    # every page selected: nothing excluded, every top token recalled
+    full = np.full((len(lens), h_kv, 8), -1, np.int32)
+    for r in range(len(lens)):
+        full[r, :, :P[r]] = np.arange(P[r])
+    d = qo.recall_diagnostics(q, kp, vp, indptr, perm, sl, full, G, R=5)
+    assert np.all(d["eps"] == 0) and np.all(d["topr"] == 1)
+    # a one-token page has an exact bound (m = M = k): slack 0 (request 0, and
+    # the tail page of request 2); every slack is >= 0 (eq (4)); none past P
+    assert np.all(d["slack"][:, indptr[0]] == 0)
+    assert np.all(d["slack"][:, indptr[2] + 2] == 0)
+    assert np.all(d["slack"] >= -1e-12)
+    # V_max is the largest row norm of the request's values
+    for r, (k, v) in enumerate(toks):
+        for g in range(h_kv):
+            assert d["vmax"][r, g] == np.linalg.norm(v[:, g].astype(np.float64), axis=-1).max()
+    # nothing selected: all mass excluded, no top token recalled
+    none = np.full((len(lens), h_kv, 8), -1, np.int32)
+    d0 = qo.recall_diagnostics(q, kp, vp, indptr, perm, sl, none, G, R=3)
+    assert np.allclose(d0["eps"], 1.0) and np.all(d0["topr"] == 0)
+    # eq (7) on a partial selection: ||o - o_C|| <= 2 eps V_max
+    part = full.copy()
+    part[:, :, 1:] = -1                                              # first page only
+    dp = qo.recall_diagnostics(q, kp, vp, indptr, perm, sl, part, G, R=3)
+    oc, _ = qo.sparse_attention(q, kp, vp, indptr, perm, sl, part, G)
+    for r, (k, v) in enumerate(toks):
+        for h in range(h_kv * G):
+            od, _ = qo.dense_attention(q[r, h], k[:, h // G], v[:, h // G])
+            assert np.linalg.norm(od - oc[r, h]) <= 2 * dp["eps"][r, h] * dp["vmax"][r, h // G] + 1e-9
