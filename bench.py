@@ -407,6 +407,8 @@ def main():
                     help="hybrid budget: sink tokens kept (whole pages, ceil)")
     ap.add_argument("--local-tokens", type=int, default=0,
                     help="hybrid budget: recent-window tokens kept (whole pages, ceil)")
+    ap.add_argument("--diagnostics", type=int, default=0, metavar="R",
+                    help="also time quest_recall_diagnostics with top-R = R (0 = off)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -539,7 +541,7 @@ def main():
         "stage_us": {k: round(v, 3) for k, v in stage.items()},
         "path": {"bytes": by["total"], "GBps": round(path_gbs, 1),
                  "frac": round(path_gbs / pk, 4), "frac_of_8TBps": round(path_gbs / 8000, 4)},
-        "roofline": {"bound": "hbm", "kernel": kern[0], "achieved": round(dom_gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": "step_kernel", "achieved": round(dom_gbs, 1),
                      "peak": pk, "unit": "GB/s", "frac": round(dom_gbs / pk, 4),
                      "peak_source": pk_src, "bytes_per_launch": dom_bytes,
                      "traffic": traffic},
@@ -548,10 +550,43 @@ def main():
         "gpu_launches": K * LayerSetup.KERNELS_PER_STEP,
         "clocks": clk.summary(),
     }
+    if args.diagnostics > 0:
+        line["diagnostics"] = time_diagnostics(setup, args.diagnostics, args.stage_reps, pk)
     if rank == 0:
         if args.cpu_seconds > 0:
             line["cpu_baseline"] = cpu_baseline(setup, args.cpu_heads, args.cpu_seconds)
         print(json.dumps(line))
+
+
+def time_diagnostics(setup, R, reps, peak_gbs):
+    """quest_recall_diagnostics (dense pass + reduction) on the workload with
+    the fused step's latest selection: device time per call (one call per
+    cache copy, so every call reads memory not touched by the previous one),
+    its algorithmic bytes (every valid key and value, every page summary) and
+    the diagnostics themselves, summarised over heads."""
+    qs, w = setup.qs, setup.w
+    sel = setup.fused.sel[0]
+    nbuf = len(setup.caches)
+    ws = torch.empty(max(qs.diag_workspace_size(w.h_kv, w.group, setup.table.nnz, w.page_size), 16),
+                     dtype=torch.uint8, device=setup.q.device)
+    fn = lambda b: qs.recall_diagnostics(setup.caches[b], setup.table, setup.q, w.group, sel,
+                                         setup.K, R, workspace=ws)
+    ms = time_stage(fn, nbuf, reps)
+    d = fn(0)
+    assert qs.device_error() == 0
+    esz = setup.k_dec.element_size()
+    P = -(-setup.lens // w.page_size)
+    nbytes = int(2 * setup.lens.sum() * w.h_kv * w.head_dim * esz
+                 + P.sum() * w.h_kv * 2 * w.head_dim * esz)
+    slack = d["slack"].flatten()
+    slack = slack[~torch.isnan(slack)]
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernels": "diag_pages_kernel + diag_reduce_kernel", "top_r": R,
+            "us": round(ms * 1e3, 2), "bytes": nbytes, "GBps": round(gbs, 1),
+            "frac": round(gbs / peak_gbs, 4),
+            "eps_mean": float(d["eps"].mean()), "eps_max": float(d["eps"].max()),
+            "topr_recall_mean": float(d["topr"].mean()), "topr_recall_min": float(d["topr"].min()),
+            "slack_median": float(slack.median()), "vmax_max": float(d["vmax"].max())}
 
 
 def run_e2e(setup, graphs, nb, n):

@@ -265,14 +265,52 @@ QUEST_API size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t
                                              int32_t head_dim, int32_t page_size,
                                              int32_t dtype, int32_t k);
 
+/*
+ * quest_recall_diagnostics — how well a selection covers dense attention, per
+ * query head (Quest page §1.1: the recall paragraph and eq (6)-(7); §3.1 page
+ * slack), computed on the GPU from the cache itself. Query head h is judged
+ * by the pages chosen for its KV head h / group; every quantity runs over the
+ * request's valid tokens (pages->seq_lens).
+ *   q           : device [batch, h_kv * group, head_dim], dtype
+ *   sel_logical : device int32 [batch, h_kv, k] logical page ids, -1 = empty
+ *                 slot (as quest_select_topk writes them)
+ *   top_r       : >= 1; the row's min(top_r, seq_len) largest dense logits
+ *                 (ties to the lower position) are the top-R tokens
+ *   sm_scale    : <= 0 selects 1 / sqrt(head_dim) (used by eps only)
+ *   slack       : device fp32 [h_kv * group, nnz]: g_p(q_h) = U_p(q_h) - the
+ *                 largest q_h.k over the page's valid keys (unscaled; U_p from
+ *                 the stored summary, per query head, no group max); NaN for
+ *                 table entries past a request's ceil(seq_len / page_size)
+ *   eps         : device fp32 [batch, h_kv * group]: dense softmax mass of the
+ *                 tokens outside the selected pages
+ *   topr        : device fp32 [batch, h_kv * group]: the share of the top-R
+ *                 tokens that lie on selected pages
+ *   vmax        : device fp32 [batch, h_kv]: max_t ||v_t||_2 (eq (7))
+ *   workspace   : device, >= quest_diag_workspace_size(...) bytes, 16-B aligned
+ * Rows of more than 65536 pages are cut to their first 65536 pages. A dense
+ * pass over every valid key and value: a diagnostic, off the decode path.
+ */
+QUEST_API quest_status quest_recall_diagnostics(const quest_cache* cache, const quest_pages* pages,
+                                                const void* q, int32_t group,
+                                                const int32_t* sel_logical, int32_t k,
+                                                int32_t top_r, float sm_scale, float* slack,
+                                                float* eps, float* topr, float* vmax,
+                                                void* workspace, size_t workspace_bytes,
+                                                void* stream);
+
+/* Workspace bytes quest_recall_diagnostics needs (0 for unsupported sizes). */
+QUEST_API size_t quest_diag_workspace_size(int32_t h_kv, int32_t group, int32_t nnz,
+                                           int32_t page_size);
+
 /* Phase trace of quest_decode_step (profiling aid, off by default): with a
  * device buffer of at least 16 * max_ctas uint64 set, each later call whose
  * grid has at most max_ctas CTAs writes, per CTA, 16 %globaltimer stamps (ns):
- * [0] start, [1] scoring done, [2] selection done, [3..5] attention round 0
- * start / pages done / merged, [6..8] the same for round 1, [9] exit,
- * [10..15] completion of the CTA's 1st..6th select. NULL turns it off.
- * Returns the grid size the current device uses for these shapes (0 if the
- * shape is unsupported). */
+ * [0] start, [1] scoring done, [2] selection done, [3..5] attention start /
+ * pages done / merged, [6..7] first select started / last select done (CTAs
+ * that select), [9] exit; [10..15] on CTAs that only select: polled / done of
+ * their 1st..3rd select; on the others: descriptors loaded, first page done,
+ * partials merged, final merges. NULL turns it off. Returns the grid size the
+ * current device uses for these shapes (0 if the shape is unsupported). */
 QUEST_API int32_t quest_set_trace(void* device_buffer, int32_t max_ctas, int32_t batch,
                                   int32_t h_kv, int32_t group, int32_t head_dim,
                                   int32_t page_size, int32_t dtype, int32_t k);

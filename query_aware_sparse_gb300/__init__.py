@@ -66,6 +66,11 @@ def lib() -> ctypes.CDLL:
         L.quest_decode_step.restype = I32
         L.quest_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32]
         L.quest_decode_workspace_size.restype = SZ
+        L.quest_recall_diagnostics.argtypes = [P, P, P, I32, P, I32, I32, ctypes.c_float, P, P,
+                                               P, P, P, SZ, P]
+        L.quest_recall_diagnostics.restype = I32
+        L.quest_diag_workspace_size.argtypes = [I32, I32, I32, I32]
+        L.quest_diag_workspace_size.restype = SZ
         L.quest_set_trace.argtypes = [P, I32, I32, I32, I32, I32, I32, I32, I32]
         L.quest_set_trace.restype = I32
         L.quest_get_device_error.argtypes = [P]
@@ -82,7 +87,8 @@ def lib() -> ctypes.CDLL:
 EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_select_topk",
             "quest_sparse_decode_attn", "quest_sparse_decode_attn_noalloc",
             "quest_attn_workspace_size",
-            "quest_decode_step", "quest_decode_workspace_size", "quest_set_trace",
+            "quest_decode_step", "quest_decode_workspace_size",
+            "quest_recall_diagnostics", "quest_diag_workspace_size", "quest_set_trace",
             "quest_get_device_error", "quest_status_string")
 
 
@@ -202,6 +208,30 @@ def sparse_decode_attn(cache: PagedCache, table: PageTable, q, group: int, sel_l
         _ptr(sel_phys), int(k), _ptr(out), _ptr(lse), float(sm_scale), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _stream(stream)))
     return out, lse
+
+
+def diag_workspace_size(h_kv, group, nnz, page_size) -> int:
+    return int(lib().quest_diag_workspace_size(h_kv, group, nnz, page_size))
+
+
+def recall_diagnostics(cache: PagedCache, table: PageTable, q, group: int, sel_logical,
+                       k: int, top_r: int, sm_scale: float = 0.0, workspace=None, stream=None):
+    """quest_recall_diagnostics: dict of slack [h_q, nnz], eps [B, h_q],
+    topr [B, h_q] and vmax [B, h_kv] (fp32)."""
+    B, h_q, d = q.shape
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(slack=torch.empty((h_q, table.nnz), **f32), eps=torch.empty((B, h_q), **f32),
+               topr=torch.empty((B, h_q), **f32), vmax=torch.empty((B, cache.h_kv), **f32))
+    if workspace is None:
+        n = diag_workspace_size(cache.h_kv, group, table.nnz, cache.page_size)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    _check(lib().quest_recall_diagnostics(
+        ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(q), int(group), _ptr(sel_logical),
+        int(k), int(top_r), float(sm_scale), _ptr(out["slack"]), _ptr(out["eps"]),
+        _ptr(out["topr"]), _ptr(out["vmax"]), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _stream(stream)))
+    return out
 
 
 def decode_workspace_size(batch, nnz, h_kv, group, head_dim, page_size, dtype, k) -> int:

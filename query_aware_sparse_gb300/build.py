@@ -18,7 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libquest.so")
-SOURCES = ["quest_api.cu", "append.cu", "score.cu", "select.cu", "attn.cu", "step.cu", "noalloc.cu"]
+SOURCES = ["quest_api.cu", "append.cu", "score.cu", "select.cu", "attn.cu", "step.cu", "noalloc.cu",
+           "diag.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.h", "topk.cuh", "attn_dev.cuh",
                                            "attn_mma.cuh")] + [
            os.path.join(ROOT, "include", "quest.h")]

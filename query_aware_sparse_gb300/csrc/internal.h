@@ -68,6 +68,27 @@ struct StepArgs {
   unsigned* err;
 };
 
+// Recall diagnostics (quest_recall_diagnostics): per query head, against
+// dense attention over each request's valid tokens.
+struct DiagArgs {
+  const void* k_pool; const void* v_pool; const void* summary; const void* q;
+  const int32_t* page_indptr; const int32_t* page_indices; const int32_t* seq_lens;
+  const int32_t* sel_logical;                 // [batch, h_kv, k]
+  float* slack;                               // [h_q, nnz]
+  float* eps; float* topr;                    // [batch, h_q]
+  float* vmax;                                // [batch, h_kv]
+  float* logits;                              // workspace [h_q, nnz * page_size]
+  float2* stats;                              // workspace [h_q, nnz] (base-2 max, sum)
+  float* vnorm;                               // workspace [h_kv, nnz]
+  int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype, k, top_r;
+  float scale_log2;
+  unsigned* err;
+};
+
+cudaError_t launch_diag(const DiagArgs& a, cudaStream_t s);
+size_t diag_workspace_bytes(int32_t h_kv, int32_t group, int32_t nnz, int32_t page_size);
+void diag_carve(DiagArgs& a, void* workspace);
+
 struct StepPlan {
   bool ok;
   int32_t grid, n_chunks, chunk_pages, smem;

@@ -240,6 +240,42 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   return launched(quest::launch_step(a, plan, static_cast<cudaStream_t>(stream)));
 }
 
+size_t quest_diag_workspace_size(int32_t h_kv, int32_t group, int32_t nnz, int32_t page_size) {
+  if (h_kv <= 0 || nnz < 0 || !valid_group(group) || (page_size != 16 && page_size != 32)) return 0;
+  return quest::diag_workspace_bytes(h_kv, group, nnz, page_size);
+}
+
+quest_status quest_recall_diagnostics(const quest_cache* cache, const quest_pages* pages,
+                                      const void* q, int32_t group, const int32_t* sel_logical,
+                                      int32_t k, int32_t top_r, float sm_scale, float* slack,
+                                      float* eps, float* topr, float* vmax, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  quest_status st = check_cache(cache);
+  if (st != QUEST_OK) return st;
+  if ((st = check_pages(pages, true)) != QUEST_OK) return st;
+  if (!valid_group(group)) return QUEST_ERR_UNSUPPORTED;
+  if (k < 1 || top_r < 1) return QUEST_ERR_INVALID_ARG;
+  if (pages->batch == 0) return QUEST_OK;
+  if (!q || !sel_logical || !slack || !eps || !topr || !vmax || !aligned16(q))
+    return QUEST_ERR_INVALID_ARG;
+  const size_t need = quest::diag_workspace_bytes(cache->h_kv, group, pages->nnz, cache->page_size);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return QUEST_ERR_WORKSPACE;
+  quest::DiagArgs a{};
+  a.k_pool = cache->k_pool; a.v_pool = cache->v_pool; a.summary = cache->summary; a.q = q;
+  a.page_indptr = pages->page_indptr; a.page_indices = pages->page_indices;
+  a.seq_lens = pages->seq_lens; a.sel_logical = sel_logical;
+  a.slack = slack; a.eps = eps; a.topr = topr; a.vmax = vmax;
+  a.batch = pages->batch; a.nnz = pages->nnz; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
+  a.group = group; a.page_size = cache->page_size; a.head_dim = cache->head_dim;
+  a.dtype = cache->dtype; a.k = k; a.top_r = top_r;
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)cache->head_dim);
+  a.scale_log2 = scale * quest::LOG2E;
+  quest::diag_carve(a, workspace);
+  a.err = err_ptr();
+  if (!a.err) return QUEST_ERR_CUDA;
+  return launched(quest::launch_diag(a, static_cast<cudaStream_t>(stream)));
+}
+
 int32_t quest_set_trace(void* device_buffer, int32_t max_ctas, int32_t batch, int32_t h_kv,
                         int32_t group, int32_t head_dim, int32_t page_size, int32_t dtype,
                         int32_t k) {
