@@ -475,6 +475,90 @@ def recall_diagnostics(q, k_pool, v_pool, page_indptr, page_indices, seq_lens,
 
 
 # ---------------------------------------------------------------------------
+# FP8 (E4M3) page summaries with directed rounding (Quest page §3, the
+# paragraph on the summary dtype: min rounded toward -inf, max toward +inf,
+# so the stored box still contains the page's keys and eq (4) stays a bound)
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_values():
+    """The real value of each of the 256 E4M3 codes (NaN for the NaN codes).
+
+    Format (OCP 8-bit floating point, E4M3 variant without infinities): bit 7
+    sign, bits 6..3 exponent field e (bias 7), bits 2..0 mantissa m. e = 0 is
+    subnormal, (m / 8) * 2^-6; otherwise (1 + m / 8) * 2^(e - 7); e = 15 with
+    m = 7 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.
+    """
+    out = np.empty(256, dtype=F64)
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 0x7
+        if e == 15 and m == 7:
+            out[c] = np.nan
+        elif e == 0:
+            out[c] = sign * (m / 8.0) * 2.0 ** -6
+        else:
+            out[c] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return out
+
+
+def _e4m3_ladder():
+    """Finite E4M3 values in increasing order with their codes; zero appears
+    once, as code 0x00 (reading: a rounded zero is stored as +0)."""
+    vals = e4m3_values()
+    codes = [c for c in range(256) if not np.isnan(vals[c]) and c != 0x80]
+    codes.sort(key=lambda c: vals[c])
+    return vals[codes], np.array(codes, dtype=np.uint8)
+
+
+def e4m3_round(x, toward):
+    """Directed rounding of finite reals into E4M3 codes.
+
+    toward = -1: the largest E4M3 value <= x; toward = +1: the smallest
+    E4M3 value >= x. Exactly representable x keep their value. Returns
+    (codes uint8, overflow bool): where no E4M3 value lies on the required
+    side (x < -448 rounding down, x > 448 rounding up) the code saturates at
+    -448 / +448 and overflow is set, since the result then no longer bounds x.
+    """
+    x = np.asarray(x, dtype=F64)
+    ladder, codes = _e4m3_ladder()
+    if toward < 0:
+        i = np.searchsorted(ladder, x, side="right") - 1
+        ovf = i < 0
+    else:
+        i = np.searchsorted(ladder, x, side="left")
+        ovf = i >= len(ladder)
+    i = np.clip(i, 0, len(ladder) - 1)
+    return codes[i], ovf
+
+
+def e4m3_decode(codes):
+    """fp64 value of E4M3 codes."""
+    return e4m3_values()[np.asarray(codes, dtype=np.int64)]
+
+
+def summary_to_e4m3(summary):
+    """FP8 summary of an exact one: [..., 0, :] (min) rounded toward -inf,
+    [..., 1, :] (max) toward +inf. Returns (codes uint8 of the same shape,
+    overflow bool of the same shape)."""
+    summary = np.asarray(summary)
+    codes = np.empty(summary.shape, dtype=np.uint8)
+    ovf = np.zeros(summary.shape, dtype=bool)
+    codes[..., 0, :], ovf[..., 0, :] = e4m3_round(summary[..., 0, :], -1)
+    codes[..., 1, :], ovf[..., 1, :] = e4m3_round(summary[..., 1, :], +1)
+    return codes, ovf
+
+
+def score_pages_e4m3(q, summary_codes, page_indptr, page_indices, group, requests=None,
+                     heads=None):
+    """score_pages over the decoded FP8 summary: U of the rounded-out box."""
+    return score_pages(q, e4m3_decode(summary_codes), page_indptr, page_indices, group,
+                       requests=requests, heads=heads)
+
+
+# ---------------------------------------------------------------------------
 # Byte model (Quest page §2 eq (9)-(12))
 # ---------------------------------------------------------------------------
 

@@ -563,3 +563,146 @@ def test_recall_diagnostics_special_cases():
         for h in range(h_kv * G):
             od, _ = qo.dense_attention(q[r, h], k[:, h // G], v[:, h // G])
             assert np.linalg.norm(od - oc[r, h]) <= 2 * dp["eps"][r, h] * dp["vmax"][r, h // G] + 1e-9
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) summaries with directed rounding (Quest page §3, the paragraph on
+# the summary dtype; §1.2 on keeping min/max in the quantized domain)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_table_matches_torch_float8():
+    """The oracle's decoding of all 256 codes equals torch's float8_e4m3fn
+    (a library routine written independently of the oracle)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = qo.e4m3_values()
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+    assert np.array_equal(np.signbit(ref[ok]), np.signbit(got[ok]))
+
+
+def test_e4m3_closed_forms():
+    v = qo.e4m3_values()
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0 and qo.E4M3_MAX == 448.0
+    assert v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9 and v[0x08] == 2.0 ** -6
+    assert v[0x38] == 1.0 and v[0x39] == 1.125 and v[0x30] == 0.5 and v[0xB8] == -1.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    assert int((~np.isnan(v)).sum()) == 254
+
+
+def _e4m3_test_values(seed):
+    rng = np.random.default_rng(seed)
+    ladder = np.unique(qo.e4m3_values()[~np.isnan(qo.e4m3_values())])
+    x = np.concatenate([
+        rng.standard_normal(4000) * 4.0,                   # the bulk
+        rng.standard_normal(500) * 100.0,                  # large
+        rng.standard_normal(500) * 2.0 ** -8,              # subnormal range
+        ladder,                                            # every representable value
+        (ladder[:-1] + ladder[1:]) / 2,                    # midpoints (RNE ties)
+        [0.0, -0.0, 448.0, -448.0, 2.0 ** -10, -2.0 ** -10],
+    ])
+    x = np.clip(x, -448.0, 448.0).astype(np.float16).astype(np.float64)
+    return x, ladder
+
+
+def test_e4m3_directed_rounding_brackets_and_rne():
+    x, ladder = _e4m3_test_values(7)
+    d, od = qo.e4m3_round(x, -1)
+    u, ou = qo.e4m3_round(x, +1)
+    assert not od.any() and not ou.any()
+    vd, vu = qo.e4m3_decode(d), qo.e4m3_decode(u)
+    assert (vd <= x).all() and (vu >= x).all()
+    # adjacent ladder values (or equal when x is representable)
+    i = np.searchsorted(ladder, vd)
+    exact = vd == vu
+    assert np.array_equal(exact, np.isin(x, ladder))
+    assert (ladder[np.minimum(i + 1, len(ladder) - 1)][~exact] == vu[~exact]).all()
+    # torch's round-to-nearest-even lands on the nearer of the two
+    rn = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert ((rn == vd) | (rn == vu)).all()
+    lo, hi = x - vd, vu - x
+    assert (rn[lo < hi] == vd[lo < hi]).all() and (rn[lo > hi] == vu[lo > hi]).all()
+    # zero is stored as +0 whichever way it is rounded
+    z = qo.e4m3_round(np.array([0.0, -0.0, 1e-6]), -1)[0]
+    assert list(z) == [0, 0, 0]
+    assert list(qo.e4m3_round(np.array([-0.0, -1e-6]), +1)[0]) == [0, 0]
+
+
+def test_e4m3_overflow_flags_only_the_unbounded_side():
+    c, o = qo.e4m3_round(np.array([449.0, 1e4, -449.0, -1e4]), -1)
+    assert list(o) == [False, False, True, True]
+    assert list(qo.e4m3_decode(c)) == [448.0, 448.0, -448.0, -448.0]
+    c, o = qo.e4m3_round(np.array([449.0, -449.0]), +1)
+    assert list(o) == [True, False]
+    assert list(qo.e4m3_decode(c)) == [448.0, -448.0]
+
+
+def test_e4m3_summary_keeps_the_bound():
+    """The rounded-out box contains the page's keys, so U over it bounds the
+    exact U and every q.k of the page (eq (4)), loosened by at most one
+    E4M3 step per dimension (< |x| / 8 for |x| >= 2^-6, < 2^-9 below)."""
+    rng = np.random.default_rng(11)
+    d, S = 64, 16
+    for trial in range(200):
+        keys = rng.standard_normal((S, d)) * rng.choice([0.01, 1.0, 8.0])
+        keys[:, :4] *= 8.0
+        keys = keys.astype(np.float16)
+        m, M = qo.page_summary(keys)
+        summ = np.stack([m, M])
+        codes, ovf = qo.summary_to_e4m3(summ)
+        assert not ovf.any()
+        m8, M8 = qo.e4m3_decode(codes[0]), qo.e4m3_decode(codes[1])
+        assert (m8 <= m.astype(np.float64)).all() and (M8 >= M.astype(np.float64)).all()
+        q = rng.standard_normal(d).astype(np.float16)
+        U = qo.page_bound(q, m, M)
+        U8 = qo.page_bound(q, m8, M8)
+        true_max = (keys.astype(np.float64) @ q.astype(np.float64)).max()
+        assert U8 >= U >= true_max - 1e-9
+        mag = np.maximum(np.abs(m), np.abs(M)).astype(np.float64)
+        step = np.where(mag >= 2.0 ** -6, mag / 8.0, 2.0 ** -9)
+        assert U8 - U <= (np.abs(q.astype(np.float64)) * step).sum() + 1e-12
+
+
+def test_e4m3_worked_example_is_on_the_grid(golden):
+    """The 2-D example's box (-1,-2)..(3,4) is representable: U stays 8."""
+    ex = golden("worked_example_2d.json")
+    keys = _np(ex["page"]["keys"], np.float16)
+    m, M = qo.page_summary(keys)
+    codes, _ = qo.summary_to_e4m3(np.stack([m, M]))
+    assert list(qo.e4m3_decode(codes[0])) == [-1.0, -2.0]
+    assert list(qo.e4m3_decode(codes[1])) == [3.0, 4.0]
+    q = _np(ex["q"])
+    assert qo.page_bound(q, qo.e4m3_decode(codes[0]), qo.e4m3_decode(codes[1])) == 8.0
+
+
+def test_e4m3_fold_in_code_domain_equals_rounded_exact_summary():
+    """Keeping the FP8 summary up to date token by token in the code domain,
+    m8 <- down(min(m8, k)) and M8 <- up(max(M8, k)), ends at the rounding of
+    the exact summary: directed rounding is monotone, so it commutes with
+    min/max. This is why an append may fold new keys straight into the codes."""
+    rng = np.random.default_rng(5)
+    d = 32
+    for trial in range(50):
+        n = int(rng.integers(1, 33))
+        keys = (rng.standard_normal((n, d)) * 3).astype(np.float16)
+        m8 = qo.e4m3_round(keys[0].astype(np.float64), -1)[0]
+        M8 = qo.e4m3_round(keys[0].astype(np.float64), +1)[0]
+        for t in range(1, n):
+            k = keys[t].astype(np.float64)
+            m8 = qo.e4m3_round(np.minimum(qo.e4m3_decode(m8), k), -1)[0]
+            M8 = qo.e4m3_round(np.maximum(qo.e4m3_decode(M8), k), +1)[0]
+        m, M = qo.page_summary(keys)
+        codes, _ = qo.summary_to_e4m3(np.stack([m, M]))
+        assert np.array_equal(m8, codes[0]) and np.array_equal(M8, codes[1])
+
+
+def test_score_pages_e4m3_is_score_pages_of_the_decoded_box():
+    kp, vp, indptr, perm, sl, q, toks = _paged_case(3, [40, 17], S=16, d=32, h_kv=2, G=2)
+    summ = qo.build_summary(kp, indptr, perm, sl)
+    codes, _ = qo.summary_to_e4m3(summ)
+    a = qo.score_pages_e4m3(q, codes, indptr, perm, 2)
+    b = qo.score_pages(q, summ, indptr, perm, 2)
+    assert (a >= b - 1e-12).all()
+    c = qo.score_pages(q, qo.e4m3_decode(codes), indptr, perm, 2)
+    assert np.array_equal(a, c)
