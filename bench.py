@@ -49,7 +49,7 @@ MIB = 1 << 20
 # ---------------------------------------------------------------------------
 
 def step_bytes(n_pages, h_kv, group, d, S, k_sel_pages, valid_tokens_selected, esize,
-               append_tokens=1, batch=1, kv_tokens_total=None):
+               append_tokens=1, batch=1, kv_tokens_total=None, summary_esize=None):
     """Algorithmic bytes of one decode step of one layer.
 
     summary of every scored page (index term, eq (10)) + K/V of the valid
@@ -58,13 +58,15 @@ def step_bytes(n_pages, h_kv, group, d, S, k_sel_pages, valid_tokens_selected, e
     Scores, ids and split-K partials are intermediates and not counted.
     n_pages: scored pages of all requests; valid_tokens_selected: per (request,
     KV head) when all are alike, else kv_tokens_total sums them over both.
+    summary_esize: bytes per summary element (1 for E4M3 codes; default esize).
     """
-    summary = n_pages * h_kv * 2 * d * esize
+    sz = esize if summary_esize is None else summary_esize
+    summary = n_pages * h_kv * 2 * d * sz
     kv_tok = valid_tokens_selected * h_kv if kv_tokens_total is None else kv_tokens_total
     kv = kv_tok * 2 * d * esize
     q = batch * h_kv * group * d * esize
     o = batch * h_kv * group * d * 4
-    append = batch * (append_tokens * h_kv * d * esize * 2 * 2 + h_kv * 2 * d * esize * 2)
+    append = batch * (append_tokens * h_kv * d * esize * 2 * 2 + h_kv * 2 * d * sz * 2)
     return dict(summary=summary, kv=kv, q=q, o=o, append=append,
                 total=summary + kv + q + o + append)
 
@@ -180,10 +182,12 @@ class LayerSetup:
     append (prefill of all but the last token of each request), plus each
     request's decode token and query."""
 
-    def __init__(self, w: wl.Workload, nbuf: int, dev, sample_heads=4, n_sink=0, n_local=0):
+    def __init__(self, w: wl.Workload, nbuf: int, dev, sample_heads=4, n_sink=0, n_local=0,
+                 summary_fp8=False):
         import query_aware_sparse_gb300 as qs
         self.qs = qs
         self.w = w
+        self.summary_fp8 = summary_fp8
         lens = w.lengths().astype(np.int64)
         B = len(lens)
         self.lens, self.L = lens, int(lens[0])
@@ -200,6 +204,8 @@ class LayerSetup:
         i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32), device=dev)
         self.table = qs.PageTable(i32(t.page_indptr), i32(t.page_indices), i32(lens))
         kp, vp, sm = wl.empty_pool(t, h, d, w.dtype, device=dev, poison=False)
+        if summary_fp8:            # E4M3 codes with directed rounding instead
+            sm = torch.zeros(sm.shape, dtype=torch.uint8, device=dev)
         self.caches = [qs.PagedCache(kp, vp, sm)]
         # prefill append of all but the last token of each request through
         # the library (timed once)
@@ -216,7 +222,7 @@ class LayerSetup:
         torch.cuda.synchronize()
         pre_ms = e0.elapsed_time(e1)
         n_pre = int(pre_ind[-1])
-        pre_bytes = n_pre * h * d * k_tok.element_size() * 4 + t.nnz * h * 2 * d * k_tok.element_size()
+        pre_bytes = n_pre * h * d * k_tok.element_size() * 4 + t.nnz * h * 2 * d * sm.element_size()
         self.prefill = {"tokens": n_pre, "ms": pre_ms, "GBps": pre_bytes / pre_ms / 1e6}
         assert qs.device_error() == 0
         for _ in range(nbuf - 1):   # distinct copies: each step reads cold memory
@@ -283,7 +289,8 @@ class LayerSetup:
         valid = np.where(sl >= 0, np.clip(lens - sl.astype(np.int64) * S, 0, S), 0)
         return step_bytes(int(P.sum()), w.h_kv, w.group, w.head_dim, S, self.K, 0,
                           self.k_dec.element_size(), batch=len(self.lens),
-                          kv_tokens_total=int(valid.sum()))
+                          kv_tokens_total=int(valid.sum()),
+                          summary_esize=self.caches[0].summary.element_size())
 
 
 def time_stage(fn, nbuf, reps):
@@ -341,9 +348,11 @@ class OracleSample:
     """The oracle's decode step on a sample of the heads of the same layer,
     built from the generated inputs (never from the device path's results)."""
 
-    def __init__(self, w: wl.Workload, k_tok, v_tok, q, heads: int, n_sink=0, n_local=0):
+    def __init__(self, w: wl.Workload, k_tok, v_tok, q, heads: int, n_sink=0, n_local=0,
+                 summary_fp8=False):
         from oracle import quest_oracle as qo
         self.qo = qo
+        self.summary_fp8 = summary_fp8
         self.n_sink, self.n_local = n_sink, n_local
         self.heads = heads
         self.w = w
@@ -367,7 +376,11 @@ class OracleSample:
         qo, t, w = self.qo, self.t, self.w
         qo.append_kv(self.kp, self.vp, self.sm, t.page_indptr, t.page_indices,
                      np.array([self.L - 1]), np.array([0, 1]), self.kdec, self.vdec)
-        sc = qo.score_pages(self.q, self.sm, t.page_indptr, t.page_indices, w.group)
+        if self.summary_fp8:      # the oracle rounds its exact summary out to E4M3
+            codes, _ = qo.summary_to_e4m3(self.sm)
+            sc = qo.score_pages_e4m3(self.q, codes, t.page_indptr, t.page_indices, w.group)
+        else:
+            sc = qo.score_pages(self.q, self.sm, t.page_indptr, t.page_indices, w.group)
         sel, _, _ = qo.select_hybrid(sc, t.page_indptr, t.page_indices, np.array([self.L]),
                                      w.page_size, w.k, self.n_sink, self.n_local)
         qo.sparse_attention(self.q, self.kp, self.vp, t.page_indptr, t.page_indices,
@@ -409,6 +422,8 @@ def main():
                     help="hybrid budget: recent-window tokens kept (whole pages, ceil)")
     ap.add_argument("--diagnostics", type=int, default=0, metavar="R",
                     help="also time quest_recall_diagnostics with top-R = R (0 = off)")
+    ap.add_argument("--summary", choices=["kv", "e4m3"], default="kv",
+                    help="page summaries in the K/V dtype or as E4M3 codes (directed rounding)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -430,6 +445,9 @@ def main():
                          "sink_pages": n_sink, "local_pages": n_local,
                          "quest_pages": w.k - n_sink - n_local}
     args.n_sink, args.n_local = n_sink, n_local
+    args.summary_fp8 = args.summary == "e4m3"
+    if args.summary_fp8:
+        cfg["summary_dtype"] = "e4m3 (min toward -inf, max toward +inf)"
 
     if args.impl == "reference":
         if rank != 0:
@@ -440,7 +458,7 @@ def main():
     import query_aware_sparse_gb300 as qs
     qs.lib()
     setup = LayerSetup(w, args.nbuf, dev, sample_heads=args.cpu_heads,
-                       n_sink=n_sink, n_local=n_local)
+                       n_sink=n_sink, n_local=n_local, summary_fp8=args.summary_fp8)
     cfg["l2"] = (f"rotating {args.nbuf} distinct copies of the layer "
                  f"({args.nbuf * (setup.caches[0].k_pool.nbytes * 2 + setup.caches[0].summary.nbytes) / 2**30:.1f} GiB)"
                  " so every step reads memory not touched in the previous "
@@ -550,7 +568,7 @@ def main():
         "gpu_launches": K * LayerSetup.KERNELS_PER_STEP,
         "clocks": clk.summary(),
     }
-    if args.diagnostics > 0:
+    if args.diagnostics > 0 and not args.summary_fp8:   # the diagnostics read kv-dtype summaries
         line["diagnostics"] = time_diagnostics(setup, args.diagnostics, args.stage_reps, pk)
     if rank == 0:
         if args.cpu_seconds > 0:
@@ -617,7 +635,8 @@ def run_e2e(setup, graphs, nb, n):
 
 
 def cpu_baseline(setup, heads, seconds):
-    o = OracleSample(setup.w, *setup.sample, heads, setup.n_sink, setup.n_local)
+    o = OracleSample(setup.w, *setup.sample, heads, setup.n_sink, setup.n_local,
+                     summary_fp8=setup.summary_fp8)
     o.time_steps(1)
     t0 = time.perf_counter()
     ts = []
@@ -637,7 +656,7 @@ def run_reference(args, w, cfg, dev, ws):
     q = wl.queries(w, [L - 1], device=dev)
     h = args.cpu_heads
     o = OracleSample(w, k_tok[:, :h].cpu(), v_tok[:, :h].cpu(), q[:, :h * w.group].cpu(), h,
-                     args.n_sink, args.n_local)
+                     args.n_sink, args.n_local, summary_fp8=args.summary_fp8)
     del k_tok, v_tok
     for _ in range(args.warmup):
         o.time_steps(1)

@@ -56,6 +56,7 @@ typedef enum { QUEST_F32 = 0, QUEST_F16 = 1 } quest_dtype;
 #define QUEST_DEVERR_TABLE_RANGE  0x2u  /* append/selection beyond the page table    */
 #define QUEST_DEVERR_EMPTY_PAGE   0x4u  /* selected page holds no valid token        */
 #define QUEST_DEVERR_WAIT_TIMEOUT 0x8u  /* an in-kernel wait hit its iteration limit */
+#define QUEST_DEVERR_FP8_RANGE    0x10u /* a key beyond +-448 under an E4M3 summary  */
 
 /*
  * One layer's paged cache (Quest page §1.2: the summary has logical shape
@@ -63,6 +64,20 @@ typedef enum { QUEST_F32 = 0, QUEST_F16 = 1 } quest_dtype;
  *   k_pool, v_pool : device, [n_phys, h_kv, page_size, head_dim], dtype
  *   summary        : device, [n_phys, h_kv, 2, head_dim], dtype;
  *                    [..., 0, :] = per-dimension min m, [..., 1, :] = max M
+ *   summary_fp8    : 0 = the summary above. 1 = the summary is uint8 E4M3
+ *                    codes of the same shape instead (Quest page §3, the
+ *                    paragraph on the summary dtype): the OCP 8-bit float
+ *                    without infinities (bias 7, 3 mantissa bits, largest
+ *                    finite 448), m rounded toward -inf and M toward +inf, so
+ *                    the box still contains every key of the page and U_p
+ *                    stays an upper bound; a rounded zero is stored as +0.
+ *                    Appends fold new keys straight into the codes (rounding
+ *                    commutes with min/max, so the result equals rounding the
+ *                    exact summary); scoring reads the codes. Half the
+ *                    summary bytes of fp16. Needs dtype QUEST_F16. A key
+ *                    beyond +-448 cannot be bounded: its code saturates and
+ *                    QUEST_DEVERR_FP8_RANGE is set. quest_recall_diagnostics
+ *                    does not take E4M3 summaries (QUEST_ERR_UNSUPPORTED).
  */
 typedef struct quest_cache {
   void* k_pool;
@@ -72,7 +87,8 @@ typedef struct quest_cache {
   int32_t h_kv;
   int32_t page_size;
   int32_t head_dim;
-  int32_t dtype; /* quest_dtype */
+  int32_t dtype;       /* quest_dtype */
+  int32_t summary_fp8; /* 0: summary in dtype; 1: E4M3 codes, directed rounding */
 } quest_cache;
 
 /*

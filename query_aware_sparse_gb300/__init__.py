@@ -22,14 +22,16 @@ LIB_PATH = os.path.join(_PKG, "libquest.so")
 
 QUEST_F32, QUEST_F16 = 0, 1
 DEVERR = {1: "page id outside the pool", 2: "beyond the page table",
-          4: "selected page holds no valid token", 8: "in-kernel wait timed out"}
+          4: "selected page holds no valid token", 8: "in-kernel wait timed out",
+          16: "key beyond +-448 under an E4M3 summary"}
 
 
 class QuestCache(ctypes.Structure):
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
                 ("summary", ctypes.c_void_p), ("n_phys", ctypes.c_int32),
                 ("h_kv", ctypes.c_int32), ("page_size", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("summary_fp8", ctypes.c_int32)]
 
 
 class QuestPages(ctypes.Structure):
@@ -119,7 +121,9 @@ class PagedCache:
     """One layer's pool + summary (caller-owned torch tensors).
 
     k_pool, v_pool: [n_phys, h_kv, page_size, head_dim]; summary:
-    [n_phys, h_kv, 2, head_dim] (index 0 = min, 1 = max).
+    [n_phys, h_kv, 2, head_dim] (index 0 = min, 1 = max), either in the K/V
+    dtype or, as a torch.uint8 tensor, E4M3 codes with directed rounding
+    (fp16 K/V only; see summary_fp8 in quest.h).
     """
 
     def __init__(self, k_pool, v_pool, summary):
@@ -127,14 +131,18 @@ class PagedCache:
         n_phys, h_kv, S, d = k_pool.shape
         self.n_phys, self.h_kv, self.page_size, self.head_dim = n_phys, h_kv, S, d
         self.dtype = k_pool.dtype
+        self.summary_fp8 = summary.dtype == torch.uint8
+        if not self.summary_fp8 and summary.dtype != k_pool.dtype:
+            raise ValueError("summary must have the K/V dtype or be uint8 E4M3 codes")
         self.c = QuestCache(k_pool.data_ptr(), v_pool.data_ptr(), summary.data_ptr(),
-                            n_phys, h_kv, S, d, dtype_code(k_pool.dtype))
+                            n_phys, h_kv, S, d, dtype_code(k_pool.dtype), int(self.summary_fp8))
 
     @classmethod
-    def empty(cls, n_phys, h_kv, page_size, head_dim, dtype, device="cuda"):
+    def empty(cls, n_phys, h_kv, page_size, head_dim, dtype, device="cuda", summary_fp8=False):
         kp = torch.empty((n_phys, h_kv, page_size, head_dim), dtype=dtype, device=device)
         vp = torch.empty_like(kp)
-        sm = torch.empty((n_phys, h_kv, 2, head_dim), dtype=dtype, device=device)
+        sm = torch.empty((n_phys, h_kv, 2, head_dim), dtype=torch.uint8 if summary_fp8 else dtype,
+                         device=device)
         return cls(kp, vp, sm)
 
 

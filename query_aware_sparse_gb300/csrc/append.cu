@@ -6,6 +6,11 @@
 // the pool and folds them into that page's summary for every KV head without
 // any cross-CTA reduction. A page whose slot 0 is written by this call
 // restarts its summary from the new keys (fresh page / recycled slot).
+// With E4M3 summaries (fp16 keys only) the old codes decode exactly into
+// fp16, the fold runs as usual, and the result is rounded out again (min
+// toward -inf, max toward +inf): rounding is monotone, so this equals the
+// rounding of the exact summary (Quest page §1.2: min/max kept in the
+// quantized domain; §3: directed rounding keeps the box conservative).
 #include "common.cuh"
 #include "internal.h"
 
@@ -55,9 +60,10 @@ __device__ bool find_segment(const AppendArgs& a, int seg, int* r_out, int* j_ou
   return s_r >= 0;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(kAppendThreads)
 append_kernel(const AppendArgs a) {
+  static_assert(!F8 || sizeof(T) == 2, "E4M3 summaries take fp16 keys");
   using K = KeyOps<T>;
   constexpr int VEC = Elem<T>::kVec;   // elements per 16 B
   constexpr int CH = D / VEC;          // 16-byte chunks per row
@@ -92,6 +98,8 @@ append_kernel(const AppendArgs a) {
   T* kp = static_cast<T*>(a.k_pool) + (size_t)pp * a.h_kv * S * D;
   T* vp = static_cast<T*>(a.v_pool) + (size_t)pp * a.h_kv * S * D;
   T* sm = static_cast<T*>(a.summary) + (size_t)pp * a.h_kv * 2 * D;
+  uint8_t* sm8 = static_cast<uint8_t*>(a.summary) + (size_t)pp * a.h_kv * 2 * D;
+  bool ovf = false;
 
   for (int item = threadIdx.x; item < a.h_kv * CH; item += blockDim.x) {
     const int g = item / CH;
@@ -101,8 +109,16 @@ append_kernel(const AppendArgs a) {
       mn = make_uint4(K::kMinInit, K::kMinInit, K::kMinInit, K::kMinInit);
       mx = make_uint4(K::kMaxInit, K::kMaxInit, K::kMaxInit, K::kMaxInit);
     } else {
-      uint4 om = ld_v4(sm + ((size_t)g * 2 + 0) * D + c * VEC);
-      uint4 oM = ld_v4(sm + ((size_t)g * 2 + 1) * D + c * VEC);
+      uint4 om, oM;
+      if constexpr (F8) {        // VEC codes -> VEC exact fp16 values
+        const uint2 cm = *reinterpret_cast<const uint2*>(sm8 + ((size_t)g * 2 + 0) * D + c * VEC);
+        const uint2 cM = *reinterpret_cast<const uint2*>(sm8 + ((size_t)g * 2 + 1) * D + c * VEC);
+        om = make_uint4(e4m3x4_lo_h2(cm.x), e4m3x4_hi_h2(cm.x), e4m3x4_lo_h2(cm.y), e4m3x4_hi_h2(cm.y));
+        oM = make_uint4(e4m3x4_lo_h2(cM.x), e4m3x4_hi_h2(cM.x), e4m3x4_lo_h2(cM.y), e4m3x4_hi_h2(cM.y));
+      } else {
+        om = ld_v4(sm + ((size_t)g * 2 + 0) * D + c * VEC);
+        oM = ld_v4(sm + ((size_t)g * 2 + 1) * D + c * VEC);
+      }
       mn = make_uint4(K::to_key(om.x), K::to_key(om.y), K::to_key(om.z), K::to_key(om.w));
       mx = make_uint4(K::to_key(oM.x), K::to_key(oM.y), K::to_key(oM.z), K::to_key(oM.w));
     }
@@ -119,11 +135,19 @@ append_kernel(const AppendArgs a) {
       mn.z = K::kmin(mn.z, K::to_key(kv.z)); mx.z = K::kmax(mx.z, K::to_key(kv.z));
       mn.w = K::kmin(mn.w, K::to_key(kv.w)); mx.w = K::kmax(mx.w, K::to_key(kv.w));
     }
-    st_v4(sm + ((size_t)g * 2 + 0) * D + c * VEC,
-          make_uint4(K::from_key(mn.x), K::from_key(mn.y), K::from_key(mn.z), K::from_key(mn.w)));
-    st_v4(sm + ((size_t)g * 2 + 1) * D + c * VEC,
-          make_uint4(K::from_key(mx.x), K::from_key(mx.y), K::from_key(mx.z), K::from_key(mx.w)));
+    const uint4 vm = make_uint4(K::from_key(mn.x), K::from_key(mn.y), K::from_key(mn.z), K::from_key(mn.w));
+    const uint4 vM = make_uint4(K::from_key(mx.x), K::from_key(mx.y), K::from_key(mx.z), K::from_key(mx.w));
+    if constexpr (F8) {
+      *reinterpret_cast<uint2*>(sm8 + ((size_t)g * 2 + 0) * D + c * VEC) =
+          make_uint2(e4m3x4_floor_h(vm.x, vm.y, ovf), e4m3x4_floor_h(vm.z, vm.w, ovf));
+      *reinterpret_cast<uint2*>(sm8 + ((size_t)g * 2 + 1) * D + c * VEC) =
+          make_uint2(e4m3x4_ceil_h(vM.x, vM.y, ovf), e4m3x4_ceil_h(vM.z, vM.w, ovf));
+    } else {
+      st_v4(sm + ((size_t)g * 2 + 0) * D + c * VEC, vm);
+      st_v4(sm + ((size_t)g * 2 + 1) * D + c * VEC, vM);
+    }
   }
+  if (F8 && ovf) report(a.err, QUEST_DEVERR_FP8_RANGE);
 }
 
 }  // namespace
@@ -134,12 +158,15 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   // sum_r ceil(n_r / S) < n_new / S + batch, so this bounds the segment count.
   const long long segs = (long long)(a.n_new + a.page_size - 1) / a.page_size + 2LL * a.batch;
   dim3 grid((unsigned)segs);
-  if (a.dtype == QUEST_F16) {
-    if (a.head_dim == 128) append_kernel<__half, 128><<<grid, kAppendThreads, 0, s>>>(a);
-    else append_kernel<__half, 64><<<grid, kAppendThreads, 0, s>>>(a);
+  if (a.dtype == QUEST_F16 && a.summary_fp8) {
+    if (a.head_dim == 128) append_kernel<__half, 128, true><<<grid, kAppendThreads, 0, s>>>(a);
+    else append_kernel<__half, 64, true><<<grid, kAppendThreads, 0, s>>>(a);
+  } else if (a.dtype == QUEST_F16) {
+    if (a.head_dim == 128) append_kernel<__half, 128, false><<<grid, kAppendThreads, 0, s>>>(a);
+    else append_kernel<__half, 64, false><<<grid, kAppendThreads, 0, s>>>(a);
   } else {
-    if (a.head_dim == 128) append_kernel<float, 128><<<grid, kAppendThreads, 0, s>>>(a);
-    else append_kernel<float, 64><<<grid, kAppendThreads, 0, s>>>(a);
+    if (a.head_dim == 128) append_kernel<float, 128, false><<<grid, kAppendThreads, 0, s>>>(a);
+    else append_kernel<float, 64, false><<<grid, kAppendThreads, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

@@ -102,6 +102,16 @@ __device__ __forceinline__ uint4 ld_stream_v4_hint(const void* p, uint64_t pol) 
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p), "l"(pol));
   return r;
 }
+// 8-byte forms of the two above (E4M3 summary halves of 8 dims).
+__device__ __forceinline__ uint2 ld_stream_v2_hint(const void* p, uint64_t pol) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+               : "=r"(r.x), "=r"(r.y) : "l"(p), "l"(pol));
+  return r;
+}
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+  asm volatile("st.global.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
                :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
@@ -157,6 +167,125 @@ template <> __device__ __forceinline__ float bound16<float>(uint4 q, uint4 m, ui
     s = fmaf(qf, xf, s);
   }
   return s;
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 page summaries (Quest page §3, the paragraph on the summary dtype).
+// Format: the OCP 8-bit float without infinities -- sign bit, 4 exponent bits
+// (bias 7), 3 mantissa bits; exponent field 0 is subnormal (m/8 * 2^-6);
+// S.1111.111 is NaN; the largest finite magnitude is 448. The min of a page
+// is rounded toward -inf and the max toward +inf, so the stored box still
+// contains the page's keys and its bound stays an upper bound (eq (4)). A
+// rounded zero is stored as +0 (code 0x00), so codes and values correspond
+// one to one and min/max may be taken on either.
+// ---------------------------------------------------------------------------
+
+// Code of the largest E4M3 value <= x (x finite). Sets `ovf` when x < -448:
+// nothing representable lies below, the code saturates at -448.
+__device__ __forceinline__ uint32_t e4m3_floor(float x, bool& ovf) {
+  const float a = fabsf(x);
+  const bool neg = x < 0.f;
+  float n;   // a in steps of its E4M3 binade
+  int base;  // code of that binade's first value, less the 8 implied steps
+  if (a < 0x1p-6f) {
+    n = a * 512.f;                                   // subnormal step 2^-9
+    base = 0;
+  } else {
+    const int e = (int)((__float_as_uint(a) >> 23) & 0xffu) - 127;   // 2^e <= a
+    n = a * __uint_as_float((uint32_t)(130 - e) << 23);              // a / 2^(e-3) in [8, 16)
+    base = (e + 7) * 8 - 8;
+  }
+  // x >= 0 rounds its magnitude down, x < 0 up; a carry out of the mantissa
+  // lands on the next binade's first code, which is the next value
+  int c = base + (int)(neg ? ceilf(n) : floorf(n));
+  if (c > 0x7e) {
+    ovf = ovf || neg;
+    c = 0x7e;
+  }
+  return c == 0 ? 0u : ((neg ? 0x80u : 0u) | (uint32_t)c);
+}
+
+// Code of the smallest E4M3 value >= x, i.e. -floor(-x). Sets `ovf` when x > 448.
+__device__ __forceinline__ uint32_t e4m3_ceil(float x, bool& ovf) {
+  const uint32_t c = e4m3_floor(-x, ovf);
+  return c == 0 ? 0u : (c ^ 0x80u);
+}
+
+// Two E4M3 codes (bytes lo, hi of `pair`, already placed at bits 8..15 and
+// 24..31) -> the fp16 pair of their values times 2^-8. Moving the 7 magnitude
+// bits down by one puts the exponent field e at fp16 exponent e and the
+// mantissa on top of fp16's, i.e. the value 2^(e-15) (1 + m/8), or m 2^-17
+// for e = 0 (an fp16 subnormal): exactly the E4M3 value times 2^-8.
+__device__ __forceinline__ uint32_t e4m3x2_placed_to_h2_scaled(uint32_t placed) {
+  return ((placed >> 1) & 0x3f803f80u) | (placed & 0x80008000u);
+}
+// Codes 0,1 / 2,3 of a word of four codes, as fp32 values times 2^-8.
+__device__ __forceinline__ float2 e4m3x4_lo_scaled(uint32_t w) {
+  const uint32_t h = e4m3x2_placed_to_h2_scaled(__byte_perm(w, 0u, 0x1404));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+__device__ __forceinline__ float2 e4m3x4_hi_scaled(uint32_t w) {
+  const uint32_t h = e4m3x2_placed_to_h2_scaled(__byte_perm(w, 0u, 0x3424));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+// Codes 0,1 / 2,3 of a word of four codes as an exact fp16 pair (raw bits).
+__device__ __forceinline__ uint32_t e4m3x4_lo_h2(uint32_t w) {
+  uint32_t h = e4m3x2_placed_to_h2_scaled(__byte_perm(w, 0u, 0x1404));
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h), __float2half2_rn(256.f));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t e4m3x4_hi_h2(uint32_t w) {
+  uint32_t h = e4m3x2_placed_to_h2_scaled(__byte_perm(w, 0u, 0x3424));
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h), __float2half2_rn(256.f));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// Per-code select mask of a word of four codes: 0xff where the query of that
+// dim is >= 0 (take the max), from the fp16 query words of dims 0,1 and 2,3.
+__device__ __forceinline__ uint32_t e4m3_qsel(uint32_t q01, uint32_t q23) {
+  const uint32_t hi = __byte_perm(q01, q23, 0x7531);   // the high byte of each half
+  return ((~hi & 0x80808080u) >> 7) * 0xffu;
+}
+// The same mask from per-half masks (0xffff where q >= 0) of dims 0,1 and 2,3.
+__device__ __forceinline__ uint32_t e4m3_qsel_from_masks(uint32_t m01, uint32_t m23) {
+  return __byte_perm(m01, m23, 0x6420);
+}
+// Page-bound contribution (eq (2)) of 4 dims with E4M3 summary words m, M and
+// fp32 queries q[0..3]: sum_j q_j * (q_j >= 0 ? M_j : m_j), times 2^-8 (the
+// caller scales the total by 2^8; every step is exact or scales exactly).
+__device__ __forceinline__ float bound4_e4m3_scaled(const float* q, uint32_t sel, uint32_t m,
+                                                    uint32_t M, float s) {
+  const uint32_t x = (M & sel) | (m & ~sel);
+  const float2 lo = e4m3x4_lo_scaled(x), hi = e4m3x4_hi_scaled(x);
+  s = fmaf(q[0], lo.x, s);
+  s = fmaf(q[1], lo.y, s);
+  s = fmaf(q[2], hi.x, s);
+  s = fmaf(q[3], hi.y, s);
+  return s;
+}
+// eq (2) over 8 dims: fp16 queries (one 16-byte vector) against E4M3 codes
+// of m and M (8 bytes each). Exact up to fp32 rounding of the sum.
+__device__ __forceinline__ float bound8_e4m3(uint4 q, uint2 m, uint2 M) {
+  const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&q.x));
+  const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&q.y));
+  const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(&q.z));
+  const float2 q3 = __half22float2(*reinterpret_cast<const __half2*>(&q.w));
+  const float qa[4] = {q0.x, q0.y, q1.x, q1.y}, qb[4] = {q2.x, q2.y, q3.x, q3.y};
+  float s = bound4_e4m3_scaled(qa, e4m3_qsel(q.x, q.y), m.x, M.x, 0.f);
+  s = bound4_e4m3_scaled(qb, e4m3_qsel(q.z, q.w), m.y, M.y, s);
+  return s * 256.f;
+}
+// Four fp16 keys (two words) -> floor / ceil codes packed in one word.
+__device__ __forceinline__ uint32_t e4m3x4_floor_h(uint32_t k01, uint32_t k23, bool& ovf) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&k01));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&k23));
+  return e4m3_floor(a.x, ovf) | (e4m3_floor(a.y, ovf) << 8) | (e4m3_floor(b.x, ovf) << 16) |
+         (e4m3_floor(b.y, ovf) << 24);
+}
+__device__ __forceinline__ uint32_t e4m3x4_ceil_h(uint32_t k01, uint32_t k23, bool& ovf) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&k01));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&k23));
+  return e4m3_ceil(a.x, ovf) | (e4m3_ceil(a.y, ovf) << 8) | (e4m3_ceil(b.x, ovf) << 16) |
+         (e4m3_ceil(b.y, ovf) << 24);
 }
 
 // ---------------------------------------------------------------------------

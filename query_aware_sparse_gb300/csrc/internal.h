@@ -15,6 +15,7 @@ struct AppendArgs {
   const int32_t* page_indptr; const int32_t* page_indices;
   const int32_t* append_indptr; const int32_t* seq_lens_before;
   int32_t batch, n_new, n_phys, h_kv, page_size, head_dim, dtype;
+  int32_t summary_fp8;                        // summary holds E4M3 codes
   unsigned* err;
 };
 
@@ -23,6 +24,7 @@ struct ScoreArgs {
   const int32_t* page_indptr; const int32_t* page_indices; const int32_t* seq_lens;
   float* scores;
   int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype;
+  int32_t summary_fp8;                        // summary holds E4M3 codes
   unsigned* err;
 };
 
@@ -61,6 +63,7 @@ struct StepArgs {
   unsigned long long* tagged;                 // [h_kv, nnz] score bits | call tag << 32
   float* part_o; float* part_ml;              // [units, group, n_chunks, head_dim | 4 (max, sum, tag, 0)]
   int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype, k;
+  int32_t summary_fp8;                        // summary holds E4M3 codes
   int32_t n_sink, n_local;                    // pages always kept (hybrid budget)
   int32_t n_chunks, chunk_pages;
   float scale_log2;
@@ -97,7 +100,15 @@ struct StepPlan {
 
 cudaError_t launch_step(const StepArgs& a, const StepPlan& p, cudaStream_t s);
 StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int32_t head_dim,
-                   int32_t page_size, int32_t dtype, int32_t k);
+                   int32_t page_size, int32_t dtype, int32_t k, int32_t summary_fp8);
+// Per-variant instantiations of the fused step (step_f32.cu, step_f16.cu,
+// step_e4m3.cu): launch, and shared memory / resident CTAs per SM.
+cudaError_t launch_step_f32(const StepArgs& a, const StepPlan& p, cudaStream_t s);
+cudaError_t launch_step_f16(const StepArgs& a, const StepPlan& p, cudaStream_t s);
+cudaError_t launch_step_e4m3(const StepArgs& a, const StepPlan& p, cudaStream_t s);
+void shape_step_f32(int dev, int head_dim, int page_size, int group, int* smem, int* per_sm);
+void shape_step_f16(int dev, int head_dim, int page_size, int group, int* smem, int* per_sm);
+void shape_step_e4m3(int dev, int head_dim, int page_size, int group, int* smem, int* per_sm);
 
 // Split-K plan of the attention for a problem size on the current device.
 struct AttnPlan {

@@ -39,6 +39,8 @@ quest_status check_cache(const quest_cache* c) {
   if (c->dtype != QUEST_F16 && c->dtype != QUEST_F32) return QUEST_ERR_UNSUPPORTED;
   if (c->head_dim != 64 && c->head_dim != 128) return QUEST_ERR_UNSUPPORTED;
   if (c->page_size != 16 && c->page_size != 32) return QUEST_ERR_UNSUPPORTED;
+  if (c->summary_fp8 != 0 && c->summary_fp8 != 1) return QUEST_ERR_INVALID_ARG;
+  if (c->summary_fp8 && c->dtype != QUEST_F16) return QUEST_ERR_UNSUPPORTED;
   if (!aligned16(c->k_pool) || !aligned16(c->v_pool) || !aligned16(c->summary))
     return QUEST_ERR_INVALID_ARG;
   return QUEST_OK;
@@ -81,6 +83,7 @@ quest_status quest_append_kv(const quest_cache* cache, const quest_pages* pages,
   a.append_indptr = append_indptr; a.seq_lens_before = seq_lens_before;
   a.batch = pages->batch; a.n_new = n_new; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
   a.page_size = cache->page_size; a.head_dim = cache->head_dim; a.dtype = cache->dtype;
+  a.summary_fp8 = cache->summary_fp8;
   a.err = err_ptr();
   if (!a.err) return QUEST_ERR_CUDA;
   return launched(quest::launch_append(a, static_cast<cudaStream_t>(stream)));
@@ -102,7 +105,7 @@ quest_status quest_score_pages(const quest_cache* cache, const quest_pages* page
   a.seq_lens = pages->seq_lens; a.scores = scores;
   a.batch = pages->batch; a.nnz = pages->nnz; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
   a.group = group; a.page_size = cache->page_size; a.head_dim = cache->head_dim;
-  a.dtype = cache->dtype;
+  a.dtype = cache->dtype; a.summary_fp8 = cache->summary_fp8;
   a.err = err_ptr();
   if (!a.err) return QUEST_ERR_CUDA;
   return launched(quest::launch_score(a, static_cast<cudaStream_t>(stream)));
@@ -187,8 +190,14 @@ size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t h_kv, int
   if ((dtype != QUEST_F16 && dtype != QUEST_F32) || (head_dim != 64 && head_dim != 128) ||
       (page_size != 16 && page_size != 32))
     return 0;
-  quest::StepPlan p = quest::plan_step(batch, nnz, h_kv, group, head_dim, page_size, dtype, k);
-  return p.ok ? p.workspace_bytes : 0;
+  // the E4M3-summary variant of the kernel may plan another grid: size for both
+  quest::StepPlan p = quest::plan_step(batch, nnz, h_kv, group, head_dim, page_size, dtype, k, 0);
+  size_t need = p.ok ? p.workspace_bytes : 0;
+  if (dtype == QUEST_F16) {
+    quest::StepPlan p8 = quest::plan_step(batch, nnz, h_kv, group, head_dim, page_size, dtype, k, 1);
+    if (p8.ok && p8.workspace_bytes > need) need = p8.workspace_bytes;
+  }
+  return need;
 }
 
 quest_status quest_decode_step(const quest_cache* cache, const quest_pages* pages,
@@ -210,7 +219,8 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   if ((k_new == nullptr) != (v_new == nullptr)) return QUEST_ERR_INVALID_ARG;
   if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return QUEST_ERR_INVALID_ARG;
   quest::StepPlan plan = quest::plan_step(pages->batch, pages->nnz, cache->h_kv, group,
-                                          cache->head_dim, cache->page_size, cache->dtype, k);
+                                          cache->head_dim, cache->page_size, cache->dtype, k,
+                                          cache->summary_fp8);
   if (!plan.ok) return QUEST_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace))
     return QUEST_ERR_WORKSPACE;
@@ -231,6 +241,7 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   a.batch = pages->batch; a.nnz = pages->nnz; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
   a.group = group; a.page_size = cache->page_size; a.head_dim = cache->head_dim;
   a.dtype = cache->dtype; a.k = k; a.n_chunks = plan.n_chunks; a.chunk_pages = plan.chunk_pages;
+  a.summary_fp8 = cache->summary_fp8;
   a.n_sink = n_sink; a.n_local = n_local;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)cache->head_dim);
   a.scale_log2 = scale * quest::LOG2E;
@@ -253,7 +264,7 @@ quest_status quest_recall_diagnostics(const quest_cache* cache, const quest_page
   quest_status st = check_cache(cache);
   if (st != QUEST_OK) return st;
   if ((st = check_pages(pages, true)) != QUEST_OK) return st;
-  if (!valid_group(group)) return QUEST_ERR_UNSUPPORTED;
+  if (!valid_group(group) || cache->summary_fp8) return QUEST_ERR_UNSUPPORTED;
   if (k < 1 || top_r < 1) return QUEST_ERR_INVALID_ARG;
   if (pages->batch == 0) return QUEST_OK;
   if (!q || !sel_logical || !slack || !eps || !topr || !vmax || !aligned16(q))
@@ -282,7 +293,7 @@ int32_t quest_set_trace(void* device_buffer, int32_t max_ctas, int32_t batch, in
   g_trace = static_cast<unsigned long long*>(device_buffer);
   g_trace_ctas = device_buffer ? max_ctas : 0;
   if (batch <= 0 || h_kv <= 0 || k < 1 || !valid_group(group)) return 0;
-  quest::StepPlan p = quest::plan_step(batch, 0, h_kv, group, head_dim, page_size, dtype, k);
+  quest::StepPlan p = quest::plan_step(batch, 0, h_kv, group, head_dim, page_size, dtype, k, 0);
   return p.ok ? p.grid : 0;
 }
 

@@ -6,7 +6,9 @@
 // summary is 2*d contiguous elements; LPP lanes cover one page with 16-byte
 // loads (min half and max half of the same dims in the same lane), so one
 // warp instruction moves 32 x 16 B and the G query heads of the group reuse
-// the registers. Each lane keeps UNROLL pages of loads in flight.
+// the registers. Each lane keeps UNROLL pages of loads in flight. With E4M3
+// summaries (fp16 queries) a lane reads the codes of the same 8 dims as
+// 8-byte loads of m and of M: half the bytes over the same lanes.
 #include "common.cuh"
 #include "internal.h"
 
@@ -43,9 +45,10 @@ __device__ __forceinline__ void load_q(const ScoreArgs& a, int r, int g, int sub
   for (int gi = 0; gi < G; ++gi) q[gi] = ld_nc_v4(qp + (size_t)gi * D);
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool F8>
 __global__ void __launch_bounds__(kScoreThreads)
 score_kernel(const ScoreArgs a) {
+  static_assert(!F8 || sizeof(T) == 2, "E4M3 summaries take fp16 queries");
   using Sh = ScoreShape<T, D>;
   constexpr int VEC = Sh::VEC, LPP = Sh::LPP, PPW = Sh::PPW;
   __shared__ int s_rfirst, s_rlast;
@@ -86,10 +89,18 @@ score_kernel(const ScoreArgs a) {
       const int pp = __ldg(a.page_indices + e);
       if (lp < valid_pages) {
         if (pp >= 0 && pp < a.n_phys) {
-          const T* sp = static_cast<const T*>(a.summary) +
-                        ((size_t)pp * a.h_kv + g) * 2 * D + sub * VEC;
-          vm[u] = ld_stream_v4_hint(sp, pol);
-          vM[u] = ld_stream_v4_hint(sp + D, pol);
+          if constexpr (F8) {
+            const uint8_t* sp = static_cast<const uint8_t*>(a.summary) +
+                                ((size_t)pp * a.h_kv + g) * 2 * D + sub * VEC;
+            const uint2 cm = ld_stream_v2_hint(sp, pol), cM = ld_stream_v2_hint(sp + D, pol);
+            vm[u] = make_uint4(cm.x, cm.y, 0u, 0u);
+            vM[u] = make_uint4(cM.x, cM.y, 0u, 0u);
+          } else {
+            const T* sp = static_cast<const T*>(a.summary) +
+                          ((size_t)pp * a.h_kv + g) * 2 * D + sub * VEC;
+            vm[u] = ld_stream_v4_hint(sp, pol);
+            vM[u] = ld_stream_v4_hint(sp + D, pol);
+          }
           live[u] = true;
         } else if (sub == 0) {
           report(a.err, QUEST_DEVERR_PAGE_RANGE);
@@ -109,7 +120,13 @@ score_kernel(const ScoreArgs a) {
     float best = -INFINITY;
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) {
-      float s = live[u] ? bound16<T>(q[gi], vm[u], vM[u]) : 0.f;
+      float s = 0.f;
+      if (live[u]) {
+        if constexpr (F8)
+          s = bound8_e4m3(q[gi], make_uint2(vm[u].x, vm[u].y), make_uint2(vM[u].x, vM[u].y));
+        else
+          s = bound16<T>(q[gi], vm[u], vM[u]);
+      }
 #pragma unroll
       for (int o = 1; o < LPP; o <<= 1) s += __shfl_xor_sync(FULL, s, o);
       best = fmaxf(best, s);
@@ -118,15 +135,15 @@ score_kernel(const ScoreArgs a) {
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 cudaError_t launch_td(const ScoreArgs& a, cudaStream_t s) {
   using Sh = ScoreShape<T, D>;
   dim3 grid((a.nnz + Sh::TILE - 1) / Sh::TILE, a.h_kv);
   switch (a.group) {
-    case 1: score_kernel<T, D, 1><<<grid, kScoreThreads, 0, s>>>(a); break;
-    case 2: score_kernel<T, D, 2><<<grid, kScoreThreads, 0, s>>>(a); break;
-    case 4: score_kernel<T, D, 4><<<grid, kScoreThreads, 0, s>>>(a); break;
-    case 8: score_kernel<T, D, 8><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 1: score_kernel<T, D, 1, F8><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 2: score_kernel<T, D, 2, F8><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 4: score_kernel<T, D, 4, F8><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 8: score_kernel<T, D, 8, F8><<<grid, kScoreThreads, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -141,9 +158,11 @@ bool score_supported(int32_t dtype, int32_t head_dim, int32_t group) {
 
 cudaError_t launch_score(const ScoreArgs& a, cudaStream_t s) {
   if (a.nnz == 0 || a.batch == 0) return cudaSuccess;
+  if (a.dtype == QUEST_F16 && a.summary_fp8)
+    return a.head_dim == 128 ? launch_td<__half, 128, true>(a, s) : launch_td<__half, 64, true>(a, s);
   if (a.dtype == QUEST_F16)
-    return a.head_dim == 128 ? launch_td<__half, 128>(a, s) : launch_td<__half, 64>(a, s);
-  return a.head_dim == 128 ? launch_td<float, 128>(a, s) : launch_td<float, 64>(a, s);
+    return a.head_dim == 128 ? launch_td<__half, 128, false>(a, s) : launch_td<__half, 64, false>(a, s);
+  return a.head_dim == 128 ? launch_td<float, 128, false>(a, s) : launch_td<float, 64, false>(a, s);
 }
 
 }  // namespace quest

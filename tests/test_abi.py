@@ -84,6 +84,15 @@ def test_host_validation_rejects_bad_arguments(qlib):
     # attention: missing workspace is reported before any launch
     assert L.quest_sparse_decode_attn(by(good), by(pages), fake, 1, fake, fake, 4, fake, None,
                                       ctypes.c_float(0.0), None, 0, None) in (-3, -4)
+    # E4M3 summaries: fp16 keys only, flag 0 or 1, not for the diagnostics
+    f8_32 = C(fake, fake, fake, 8, 2, 16, 128, qlib.QUEST_F32, 1)
+    assert L.quest_score_pages(by(f8_32), by(pages), fake, 1, fake, None) == -2
+    assert L.quest_append_kv(by(f8_32), by(pages), fake, fake, 1, fake, fake, None) == -2
+    assert L.quest_score_pages(by(C(fake, fake, fake, 8, 2, 16, 128, 1, 2)), by(pages), fake, 1,
+                               fake, None) == -1
+    f8 = C(fake, fake, fake, 8, 2, 16, 128, qlib.QUEST_F16, 1)
+    assert L.quest_recall_diagnostics(by(f8), by(pages), fake, 1, fake, 4, 4, ctypes.c_float(0.0),
+                                      fake, fake, fake, fake, fake, 1 << 20, None) == -2
     # empty batches are valid no-ops
     empty = Pg(None, None, None, 0, 0)
     assert L.quest_select_topk(by(empty), 2, 16, None, 4, 0, 0, None, None, None, None) == 0

@@ -26,7 +26,7 @@ def _prefilled(w, lens, seed, spare=4):
     return table, k_tok, v_tok, ind
 
 
-def _run(w, lens, steps, seed, append=True, n_sink=0, n_local=0):
+def _run(w, lens, steps, seed, append=True, n_sink=0, n_local=0, fp8=False):
     import query_aware_sparse_gb300 as qs
     lens = np.asarray(lens)
     full = lens + (steps if append else 0)
@@ -35,6 +35,8 @@ def _run(w, lens, steps, seed, append=True, n_sink=0, n_local=0):
     start = lens.copy()
     # both sides start from the first `lens` tokens of each request
     kp, vp, sm = wl.empty_pool(table, h, d, w.dtype, device="cuda")
+    if fp8:                                  # E4M3 summary codes instead
+        sm = torch.full(sm.shape, 0x7F, dtype=torch.uint8, device="cuda")
     okp, ovp, osm = (np_of(x) for x in wl.empty_pool(table, h, d, w.dtype))
     rows = np.concatenate([np.arange(ind[r], ind[r] + start[r]) for r in range(B)])
     pre_ind = np.concatenate([[0], np.cumsum(start)]).astype(np.int32)
@@ -73,17 +75,24 @@ def _run(w, lens, steps, seed, append=True, n_sink=0, n_local=0):
         assert cnt[2 + ((s + 1) & 1)] > 0 and cnt[2 + ((s + 2) & 1)] == 0
         assert np.all(cnt[4:4 + B * h] == s + 1) and np.all(cnt[4 + B * h:] == 0)
         gsm = np_of(cache.summary)
+        # the summary the selector reads: exact, or its E4M3 rounding
+        ssm = qo.summary_to_e4m3(osm)[0] if fp8 else osm
         for r in range(B):
             P = -(-int(cur[r]) // S)
             phys = table.page_indices[table.page_indptr[r]:table.page_indptr[r] + P]
-            assert np.array_equal(gsm[phys].view(np.uint8), osm[phys].view(np.uint8))
+            assert np.array_equal(gsm[phys].view(np.uint8), ssm[phys].view(np.uint8))
             if append:
                 pp = table.page_indices[table.page_indptr[r] + (cur[r] - 1) // S]
                 slot = (cur[r] - 1) % S
                 assert np.array_equal(np_of(cache.k_pool[pp, :, slot]).view(np.uint8),
                                       okp[pp, :, slot].view(np.uint8))
-        ref_scores = qo.score_pages(np_of(q), osm, table.page_indptr, table.page_indices, w.group)
-        tol = score_tol(np_of(q), osm, tb, w.group)
+        if fp8:
+            ref_scores = qo.score_pages_e4m3(np_of(q), ssm, table.page_indptr, table.page_indices,
+                                             w.group)
+            tol = score_tol(np_of(q), qo.e4m3_decode(ssm), tb, w.group)
+        else:
+            ref_scores = qo.score_pages(np_of(q), osm, table.page_indptr, table.page_indices, w.group)
+            tol = score_tol(np_of(q), osm, tb, w.group)
         got = np_of(step.scores)
         for r in range(B):
             lo = table.page_indptr[r]
@@ -171,3 +180,19 @@ def test_step_hybrid_budget(n_sink, n_local):
     fused step, with short requests whose window and sinks overlap."""
     _run(_w("hyb", batch=4, h_kv=3, k=16), [40, 1, 300, 700], steps=3, seed=20 + n_local,
          n_sink=n_sink, n_local=n_local)
+
+
+@pytest.mark.parametrize("group,S,d", [(1, 16, 128), (4, 16, 128), (2, 32, 64), (8, 16, 64),
+                                       (1, 32, 128)])
+def test_step_e4m3_summaries(group, S, d):
+    """E4M3 summaries (Quest page §3, summary dtype): the fused append keeps
+    the codes equal to the directed rounding of the exact summary, and the
+    scores, selections and outputs follow the oracle on the rounded box."""
+    w = _w("e4m3", batch=3, h_kv=2, group=group, head_dim=d, page_size=S, k=6)
+    _run(w, [S - 2, 5 * S, 3 * S + 7], 4, 640 + group + S + d, fp8=True)
+
+
+def test_step_e4m3_hybrid_and_many_units():
+    w = _w("e4m3_units", batch=24, h_kv=8, group=1, k=8)
+    _run(w, list(np.random.default_rng(3).integers(20, 400, 24)), 3, 661, n_sink=1, n_local=2,
+         fp8=True)
