@@ -306,7 +306,7 @@ step_kernel(const StepArgs a) {
     set_query(r, g, qr);
   };
 
-  uint4 bm[kPD][VPL], bM[kPD][VPL];
+  uint4 bm[kPD][F8 ? 1 : VPL], bM[kPD][F8 ? 1 : VPL];
   int sl_i[kPD], sl_g[kPD];                  // page (n = none) and head of each slot
 
 #pragma unroll 1
@@ -388,7 +388,7 @@ step_kernel(const StepArgs a) {
           const int g = sl_g[u], i = sl_i[u];
           uint4 vm[VPL], vM[VPL];
 #pragma unroll
-          for (int v = 0; v < VPL; ++v) { vm[v] = bm[u][v]; vM[v] = bM[u][v]; }
+          for (int v = 0; v < (F8 ? 1 : VPL); ++v) { vm[v] = bm[u][v]; vM[v] = bM[u][v]; }
           issue(u, true);                    // refill the slot kPD items ahead
           const int2 md = i < n ? smeta[i] : make_int2(-1, 0);
           const int flags = md.y >> 24;
