@@ -475,6 +475,71 @@ def recall_diagnostics(q, k_pool, v_pool, page_indptr, page_indices, seq_lens,
 
 
 # ---------------------------------------------------------------------------
+# GQA with per-query-head selection and a per-KV-head union (Quest page §2.1,
+# the MHA / GQA / head-sharing paragraphs: each query head picks its own
+# pages, the shared KV head reads the union of the picks once, and each head's
+# attention still runs over its own set only)
+# ---------------------------------------------------------------------------
+
+def score_pages_per_head(q, summary, page_indptr, page_indices, group, requests=None):
+    """Scores [h_q, nnz] (fp64): U_{h,p} of every query head h against the
+    summary of its KV head h // group, with no aggregation over the group."""
+    n_phys, h_kv, _, d = summary.shape
+    batch = len(page_indptr) - 1
+    nnz = int(page_indptr[batch])
+    scores = np.full((h_kv * group, nnz), np.nan, dtype=F64)
+    reqs = range(batch) if requests is None else requests
+    for r in reqs:
+        lo, hi = int(page_indptr[r]), int(page_indptr[r + 1])
+        if hi == lo:
+            continue
+        phys = np.asarray(page_indices[lo:hi], dtype=np.int64)
+        for h in range(h_kv * group):
+            g = h // group
+            scores[h, lo:hi] = page_bound(q[r, h], summary[phys, g, 0, :], summary[phys, g, 1, :])
+    return scores
+
+
+def union_pages(sel_heads):
+    """Union of the page sets of one KV head's query heads.
+
+    sel_heads: [G, K] logical ids (-1 = empty slot). Returns (pages, masks):
+    the distinct ids in increasing order and, per page, the bit set of the
+    heads (bit i = head i of the group) that chose it.
+    """
+    owners = {}
+    for i, row in enumerate(np.asarray(sel_heads)):
+        for lp in row:
+            lp = int(lp)
+            if lp >= 0:
+                owners[lp] = owners.get(lp, 0) | (1 << i)
+    pages = sorted(owners)
+    return np.array(pages, dtype=np.int64), np.array([owners[p] for p in pages], dtype=np.int64)
+
+
+def sparse_attention_per_head(q, k_pool, v_pool, page_indptr, page_indices, seq_lens,
+                              sel_logical, group, sm_scale=None, requests=None):
+    """o [batch, h_q, d] and lse [batch, h_q] with a page set per query head.
+
+    sel_logical is [batch, h_q, K]: query head h attends over the valid tokens
+    of its own pages, read from its KV head h // group (the union only decides
+    which pages are fetched, never which tokens a head weighs).
+    """
+    batch, h_q, d = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    o = np.full((batch, h_q, d), np.nan)
+    lse = np.full((batch, h_q), np.nan)
+    reqs = range(batch) if requests is None else requests
+    for r in reqs:
+        for h in range(h_q):
+            keys, vals = candidate_tokens(k_pool, v_pool, page_indptr, page_indices, seq_lens,
+                                          r, h // group, sel_logical[r, h])
+            o[r, h], lse[r, h] = softmax_attention(q[r, h], keys, vals, sm_scale)
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
 # FP8 (E4M3) page summaries with directed rounding (Quest page §3, the
 # paragraph on the summary dtype: min rounded toward -inf, max toward +inf,
 # so the stored box still contains the page's keys and eq (4) stays a bound)

@@ -706,3 +706,77 @@ def test_score_pages_e4m3_is_score_pages_of_the_decoded_box():
     assert (a >= b - 1e-12).all()
     c = qo.score_pages(q, qo.e4m3_decode(codes), indptr, perm, 2)
     assert np.array_equal(a, c)
+
+
+# ---------------------------------------------------------------------------
+# GQA: per-query-head selection, per-KV-head union (Quest page §2.1, the MHA /
+# GQA / head-sharing paragraphs)
+# ---------------------------------------------------------------------------
+
+def test_per_head_scores_bound_each_heads_dot_products():
+    """U_{h,p} bounds every q_h.k of the page (eq (4) per head, brute force in
+    fp64), and the group max of the per-head rows is the shared score."""
+    lens = [70, 33]
+    kp, vp, indptr, perm, sl, q, toks = _paged_case(12, lens, d=32, h_kv=2, G=4)
+    sm = qo.build_summary(kp, indptr, perm, sl)
+    U = qo.score_pages_per_head(q, sm, indptr, perm, 4)
+    assert U.shape == (8, int(indptr[-1]))
+    for r, (k, _) in enumerate(toks):
+        for h in range(8):
+            for lp in range(-(-lens[r] // 16)):
+                keys = k[lp * 16:(lp + 1) * 16, h // 4].astype(np.float64)
+                assert (keys @ q[r, h].astype(np.float64)).max() <= U[h, indptr[r] + lp] + 1e-12
+    grp = qo.score_pages(q, sm, indptr, perm, 4)
+    assert np.array_equal(U.reshape(2, 4, -1).max(axis=1), grp)
+    # G = 1: the per-head rows are the MHA scores
+    kp1, vp1, ip1, pm1, sl1, q1, _ = _paged_case(13, lens, d=32, h_kv=3, G=1)
+    sm1 = qo.build_summary(kp1, ip1, pm1, sl1)
+    assert np.array_equal(qo.score_pages_per_head(q1, sm1, ip1, pm1, 1),
+                          qo.score_pages(q1, sm1, ip1, pm1, 1))
+
+
+def test_union_pages_brute_force():
+    rng = np.random.default_rng(21)
+    for trial in range(200):
+        G, K, P = int(rng.integers(1, 9)), int(rng.integers(1, 9)), int(rng.integers(1, 40))
+        sel = np.full((G, K), -1, np.int64)
+        for i in range(G):
+            n = int(rng.integers(0, min(K, P) + 1))
+            sel[i, :n] = rng.choice(P, size=n, replace=False)
+        pages, masks = qo.union_pages(sel)
+        want = sorted(set(int(x) for x in sel.ravel() if x >= 0))
+        assert pages.tolist() == want and len(pages) <= G * K
+        for p, m in zip(pages, masks):
+            assert m == sum(1 << i for i in range(G) if p in sel[i])
+    same = np.array([[4, 1, 7]] * 3)
+    pages, masks = qo.union_pages(same)
+    assert pages.tolist() == [1, 4, 7] and masks.tolist() == [7, 7, 7]
+
+
+def test_per_head_attention_against_contiguous_tokens():
+    """Each head's output is dense attention over the contiguous (un-paged)
+    tokens of its own pages; with one set for the whole group it equals the
+    shared-set attention."""
+    rng = np.random.default_rng(23)
+    lens = [90, 17]
+    G, h_kv, K = 4, 2, 3
+    kp, vp, indptr, perm, sl, q, toks = _paged_case(14, lens, d=32, h_kv=h_kv, G=G)
+    sel = np.full((2, h_kv * G, K), -1, np.int32)
+    for r, L in enumerate(lens):
+        P = -(-L // 16)
+        for h in range(h_kv * G):
+            n = int(rng.integers(1, min(K, P) + 1))
+            sel[r, h, :n] = rng.choice(P, size=n, replace=False)
+    o, lse = qo.sparse_attention_per_head(q, kp, vp, indptr, perm, sl, sel, G)
+    for r, (k, v) in enumerate(toks):
+        for h in range(h_kv * G):
+            rows = np.concatenate([np.arange(p * 16, min(lens[r], p * 16 + 16))
+                                   for p in sorted(x for x in sel[r, h] if x >= 0)])
+            od, ld = qo.dense_attention(q[r, h], k[rows, h // G].astype(np.float64),
+                                        v[rows, h // G].astype(np.float64))
+            assert np.allclose(o[r, h], od, rtol=1e-12, atol=1e-12)
+            assert abs(lse[r, h] - ld) < 1e-10
+    shared = sel[:, ::G]                                     # head 0's set for its group
+    o2, _ = qo.sparse_attention_per_head(q, kp, vp, indptr, perm, sl, np.repeat(shared, G, axis=1), G)
+    o3, _ = qo.sparse_attention(q, kp, vp, indptr, perm, sl, shared, G)
+    assert np.array_equal(o2, o3)
