@@ -422,6 +422,8 @@ def main():
                     help="hybrid budget: recent-window tokens kept (whole pages, ceil)")
     ap.add_argument("--diagnostics", type=int, default=0, metavar="R",
                     help="also time quest_recall_diagnostics with top-R = R (0 = off)")
+    ap.add_argument("--gqa-union", action="store_true",
+                    help="also time GQA per-query-head selection with the per-KV-head page union")
     ap.add_argument("--summary", choices=["kv", "e4m3"], default="kv",
                     help="page summaries in the K/V dtype or as E4M3 codes (directed rounding)")
     args = ap.parse_args()
@@ -568,12 +570,68 @@ def main():
         "gpu_launches": K * LayerSetup.KERNELS_PER_STEP,
         "clocks": clk.summary(),
     }
+    if args.gqa_union and w.group > 1:
+        line["gqa_union"] = time_gqa_union(setup, args.stage_reps, pk, stage)
     if args.diagnostics > 0 and not args.summary_fp8:   # the diagnostics read kv-dtype summaries
         line["diagnostics"] = time_diagnostics(setup, args.diagnostics, args.stage_reps, pk)
     if rank == 0:
         if args.cpu_seconds > 0:
             line["cpu_baseline"] = cpu_baseline(setup, args.cpu_heads, args.cpu_seconds)
         print(json.dumps(line))
+
+
+def time_gqa_union(setup, reps, peak_gbs, stage):
+    """GQA with a page set per query head (per-head scores, per-head Top-K,
+    the per-KV-head union read once with head masks), as three calls, against
+    the group-max path's separate calls on the same workload: device time per
+    stage and the algorithmic bytes of each (summaries + K/V of the valid
+    tokens of the pages read + q + o)."""
+    qs, w = setup.qs, setup.w
+    B, h, G, d, S, K = len(setup.lens), w.h_kv, w.group, w.head_dim, w.page_size, setup.K
+    dev = setup.q.device
+    h_q = h * G
+    sc = torch.empty((h_q, setup.table_np.nnz), dtype=torch.float32, device=dev)
+    sel = (torch.empty((B, h_q, K), dtype=torch.int32, device=dev),
+           torch.empty((B, h_q, K), dtype=torch.int32, device=dev),
+           torch.empty((B, h_q), dtype=torch.int32, device=dev))
+    out = torch.empty((B, h_q, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, h_q), dtype=torch.float32, device=dev)
+    un = (torch.empty((B, h, G * K), dtype=torch.int32, device=dev),
+          torch.empty((B, h, G * K), dtype=torch.uint8, device=dev),
+          torch.empty((B, h), dtype=torch.int32, device=dev))
+    ws = torch.empty(max(qs.union_workspace_size(B, h, G, d, S, w.dtype, K), 16),
+                     dtype=torch.uint8, device=dev)
+    score = lambda b: qs.score_pages_per_head(setup.caches[b], setup.table, setup.q, G, sc)
+    select = lambda b: qs.select_topk(setup.table, h_q, S, sc, K, out=sel)
+    attend = lambda b: qs.union_decode_attn(setup.caches[b], setup.table, setup.q, G, sel[0], K,
+                                            out, lse, union=un, workspace=ws)
+    def whole(b):
+        score(b)
+        select(b)
+        attend(b)
+    t = {n: time_stage(f, len(setup.caches), reps) * 1e3
+         for n, f in (("score", score), ("select", select), ("attn", attend), ("path", whole))}
+    whole(0)
+    assert qs.device_error() == 0
+    ul = un[0].cpu().numpy()
+    lens = setup.lens[:, None, None]
+    valid = np.where(ul >= 0, np.clip(lens - ul.astype(np.int64) * S, 0, S), 0)
+    esz = setup.k_dec.element_size()
+    P = -(-setup.lens // S)
+    summ = int(P.sum()) * h * 2 * d * setup.caches[0].summary.element_size()
+    kv = int(valid.sum()) * 2 * d * esz
+    qo_bytes = B * h_q * d * (esz + 4)
+    gm = setup.bytes()
+    total = summ + kv + qo_bytes
+    return {"calls": "quest_score_pages_per_head + quest_select_topk (h_kv * group rows) + "
+                     "quest_union_decode_attn",
+            "us": {k: round(v, 3) for k, v in t.items()},
+            "union_pages_per_unit": round(float(un[2].float().mean()), 1),
+            "pages_per_unit_group_max": K,
+            "bytes": total, "kv_bytes": kv, "GBps": round(total / (t["path"] * 1e-6) / 1e9, 1),
+            "frac": round(total / (t["path"] * 1e-6) / 1e9 / peak_gbs, 4),
+            "group_max_same_calls": {"us": round(stage["unfused_step"] - stage["append"], 3),
+                                     "kv_bytes": gm["kv"]}}
 
 
 def time_diagnostics(setup, R, reps, peak_gbs):

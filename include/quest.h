@@ -153,6 +153,20 @@ QUEST_API quest_status quest_score_pages(const quest_cache* cache, const quest_p
                                void* stream);
 
 /*
+ * quest_score_pages_per_head — the page bounds of quest_score_pages with one
+ * row per query head and no aggregation over the group (Quest page §2.1, the
+ * GQA paragraph: each query head may pick its own pages, the shared KV head
+ * then reads the union of the picks; quest_union_decode_attn).
+ *   scores : device fp32 [h_kv * group, nnz]; row h holds U_{h,p} against the
+ *            summary of KV head h / group; reserved entries get -inf.
+ * Select each head's pages with quest_select_topk(pages, h_kv * group, ...)
+ * on these rows (sel_logical [batch, h_kv * group, k]).
+ */
+QUEST_API quest_status quest_score_pages_per_head(const quest_cache* cache,
+                                                  const quest_pages* pages, const void* q,
+                                                  int32_t group, float* scores, void* stream);
+
+/*
  * quest_select_topk — fixed-budget Top-K pages (Quest page Fig. 1, §1.1 and
  * §2: K pages, token budget K * page_size).
  *
@@ -239,6 +253,43 @@ QUEST_API quest_status quest_sparse_decode_attn_noalloc(const quest_cache* cache
 QUEST_API size_t quest_attn_workspace_size(int32_t batch, int32_t h_kv, int32_t group,
                                  int32_t head_dim, int32_t page_size,
                                  int32_t k);
+
+/*
+ * quest_union_decode_attn — GQA attention with a page set per query head
+ * (Quest page §2.1, the MHA / GQA / head-sharing paragraphs): per (request,
+ * KV head) the union of the pages the group's heads chose is formed, each
+ * page of it is read once, and query head h weighs only the valid tokens of
+ * its own pages (softmax over its own candidate set; an empty set gives o = 0,
+ * lse = -inf). Split-K over the union, then the log-sum-exp merge.
+ *   sel_logical   : device int32 [batch, h_kv * group, k] per-head logical
+ *                   pages (-1 = empty slot), e.g. quest_select_topk on the
+ *                   rows of quest_score_pages_per_head
+ *   out, lse      : device fp32 [batch, h_kv * group, head_dim], [batch,
+ *                   h_kv * group] (lse may be NULL); sm_scale <= 0 selects
+ *                   1 / sqrt(head_dim)
+ *   union_logical : device int32 [batch, h_kv, group * k] (written): the union
+ *                   in increasing page order, -1 padded
+ *   union_mask    : device uint8 [batch, h_kv, group * k] (written): bit i set
+ *                   when head i of the group chose the page
+ *   union_count   : device int32 [batch, h_kv] (written): pages in the union
+ *   workspace     : device, >= quest_union_workspace_size(...) bytes, 16-B
+ *                   aligned
+ * A selected page with no valid token is skipped (QUEST_DEVERR_EMPTY_PAGE);
+ * requests of more than 65536 pages (or more than pages->nnz) are cut there
+ * (QUEST_DEVERR_TABLE_RANGE).
+ */
+QUEST_API quest_status quest_union_decode_attn(const quest_cache* cache, const quest_pages* pages,
+                                               const void* q, int32_t group,
+                                               const int32_t* sel_logical, int32_t k, float* out,
+                                               float* lse, float sm_scale, int32_t* union_logical,
+                                               uint8_t* union_mask, int32_t* union_count,
+                                               void* workspace, size_t workspace_bytes,
+                                               void* stream);
+
+/* Workspace bytes quest_union_decode_attn needs (0 for unsupported shapes). */
+QUEST_API size_t quest_union_workspace_size(int32_t batch, int32_t h_kv, int32_t group,
+                                            int32_t head_dim, int32_t page_size, int32_t dtype,
+                                            int32_t k);
 
 /*
  * quest_decode_step — one decode step of one layer in a single fused launch:

@@ -55,6 +55,12 @@ def lib() -> ctypes.CDLL:
         P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
         L.quest_append_kv.argtypes = [P, P, P, P, I32, P, P, P]
         L.quest_score_pages.argtypes = [P, P, P, I32, P, P]
+        L.quest_score_pages_per_head.argtypes = [P, P, P, I32, P, P]
+        L.quest_union_decode_attn.argtypes = [P, P, P, I32, P, I32, P, P, ctypes.c_float, P, P,
+                                              P, P, SZ, P]
+        L.quest_union_decode_attn.restype = I32
+        L.quest_union_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I32]
+        L.quest_union_workspace_size.restype = SZ
         L.quest_select_topk.argtypes = [P, I32, I32, P, I32, I32, I32, P, P, P, P]
         L.quest_sparse_decode_attn.argtypes = [P, P, P, I32, P, P, I32, P, P,
                                                ctypes.c_float, P, SZ, P]
@@ -86,7 +92,8 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_select_topk",
+EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_score_pages_per_head",
+            "quest_select_topk", "quest_union_decode_attn", "quest_union_workspace_size",
             "quest_sparse_decode_attn", "quest_sparse_decode_attn_noalloc",
             "quest_attn_workspace_size",
             "quest_decode_step", "quest_decode_workspace_size",
@@ -176,6 +183,51 @@ def score_pages(cache: PagedCache, table: PageTable, q, group: int, scores=None,
     _check(lib().quest_score_pages(ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(q),
                                    int(group), _ptr(scores), _stream(stream)))
     return scores
+
+
+def score_pages_per_head(cache: PagedCache, table: PageTable, q, group: int, scores=None,
+                         stream=None):
+    """quest_score_pages_per_head: scores [h_kv * group, nnz] fp32, one row per
+    query head (no group max)."""
+    if scores is None:
+        scores = torch.empty((cache.h_kv * group, table.nnz), dtype=torch.float32, device=q.device)
+    _check(lib().quest_score_pages_per_head(ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(q),
+                                            int(group), _ptr(scores), _stream(stream)))
+    return scores
+
+
+def union_workspace_size(batch, h_kv, group, head_dim, page_size, dtype, k) -> int:
+    return int(lib().quest_union_workspace_size(batch, h_kv, group, head_dim, page_size,
+                                                dtype_code(dtype), k))
+
+
+def union_decode_attn(cache: PagedCache, table: PageTable, q, group: int, sel_logical, k: int,
+                      out=None, lse=None, sm_scale: float = 0.0, union=None, workspace=None,
+                      stream=None):
+    """quest_union_decode_attn: per-query-head page sets sel_logical
+    [B, h_q, k]; returns (out [B, h_q, d], lse [B, h_q], (union_logical
+    [B, h_kv, group * k], union_mask uint8 [B, h_kv, group * k], union_count
+    [B, h_kv]))."""
+    B, h_q, d = q.shape
+    dev = q.device
+    h_kv = cache.h_kv
+    if out is None:
+        out = torch.empty((B, h_q, d), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, h_q), dtype=torch.float32, device=dev)
+    if union is None:
+        union = (torch.empty((B, h_kv, group * k), dtype=torch.int32, device=dev),
+                 torch.empty((B, h_kv, group * k), dtype=torch.uint8, device=dev),
+                 torch.empty((B, h_kv), dtype=torch.int32, device=dev))
+    if workspace is None:
+        n = union_workspace_size(B, h_kv, group, d, cache.page_size, cache.dtype, k)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    ul, um, uc = union
+    _check(lib().quest_union_decode_attn(
+        ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(q), int(group), _ptr(sel_logical),
+        int(k), _ptr(out), _ptr(lse), float(sm_scale), _ptr(ul), _ptr(um), _ptr(uc),
+        _ptr(workspace), int(workspace.numel() * workspace.element_size()), _stream(stream)))
+    return out, lse, union
 
 
 def select_topk(table: PageTable, h_kv: int, page_size: int, scores, k: int,

@@ -12,6 +12,8 @@
 // (o, max, sum) per query head; the combine kernel merges the chunks.
 // Decode attention is a matrix-vector product per query head (G <= 8 rows
 // share a KV head), too thin for a tensor-core tile, so it stays on FMA.
+// With a slot mask (the GQA page union) each page carries the heads that
+// chose it, and the other heads of the group give it no weight.
 #include "attn_dev.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -34,7 +36,7 @@ struct AttnShape {
   static_assert(kNW * G * (D + 2) * 4 <= STAGE_BYTES, "merge buffer must fit in the stage area");
 };
 
-template <typename T, int D, int S, int G>
+template <typename T, int D, int S, int G, bool MASK>
 __global__ void __launch_bounds__(kNW * 32)
 attn_split_kernel(const AttnArgs a) {
   using Sh = AttnShape<T, D, S, G>;
@@ -63,12 +65,13 @@ attn_split_kernel(const AttnArgs a) {
   const int jc1 = min(a.k, jc0 + a.chunk_pages);
   const int j0 = jc0 + w;
   const int nmine = j0 < jc1 ? (jc1 - j0 + kNW - 1) / kNW : 0;
-  int my_pp = -1, my_valid = 0;
+  int my_pp = -1, my_valid = 0, my_heads = 0xff;
   if (lane < nmine) {
     const int j = j0 + lane * kNW;
     const int lp = __ldg(a.sel_logical + sel_base + j);
     const int pp = __ldg(a.sel_phys + sel_base + j);
-    if (lp >= 0) {
+    if constexpr (MASK) my_heads = a.sel_mask[sel_base + j];   // heads that chose the page
+    if (lp >= 0 && my_heads != 0) {
       const int valid = min(S, L - lp * S);
       if (valid <= 0) report(a.err, QUEST_DEVERR_EMPTY_PAGE);
       else if (pp < 0 || pp >= a.n_phys) report(a.err, QUEST_DEVERR_PAGE_RANGE);
@@ -77,7 +80,8 @@ attn_split_kernel(const AttnArgs a) {
   }
   const unsigned vmask = __ballot_sync(FULL, my_valid > 0);
   const int nv = __popc(vmask);
-  if (my_valid > 0) desc[__popc(vmask & ((1u << lane) - 1))] = make_int2(my_pp, my_valid);
+  if (my_valid > 0)
+    desc[__popc(vmask & ((1u << lane) - 1))] = make_int2(my_pp, my_valid | (my_heads << 8));
   if (lane == 0) {
     for (int s = 0; s < kNST; ++s) mbar_init(my_bars + s, 1);
     fence_mbar_init();
@@ -109,7 +113,10 @@ attn_split_kernel(const AttnArgs a) {
       if (lane == 0) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
     } else {
       const T* Kb = my_stage + (size_t)slot * 2 * head_block;
-      st.page(Kb, Kb + head_block, desc[n].y, lg, lane);
+      if constexpr (MASK)
+        st.page(Kb, Kb + head_block, desc[n].y & 0xff, lg, lane, (unsigned)desc[n].y >> 8);
+      else
+        st.page(Kb, Kb + head_block, desc[n].y & 0xff, lg, lane);
     }
     __syncwarp();
     if (lane == 0 && n + kNST < nv) {
@@ -180,13 +187,13 @@ attn_combine_kernel(const AttnArgs a) {
   if (a.lse && lane == 0) a.lse[row] = l > 0.f ? (mx + log2f(l)) * LN2 : -INFINITY;
 }
 
-template <typename T, int D, int S, int G>
+template <typename T, int D, int S, int G, bool MASK>
 cudaError_t launch_split(const AttnArgs& a, cudaStream_t s) {
   using Sh = AttnShape<T, D, S, G>;
-  auto kern = attn_split_kernel<T, D, S, G>;
+  auto kern = attn_split_kernel<T, D, S, G, MASK>;
   int dev = 0;
   cudaGetDevice(&dev);
-  static bool attr_done[64] = {};   // per device; racing setters write the same value
+  static bool attr_done[64] = {};   // per device and instantiation; racing setters agree
   if (dev >= 64 || !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
     if (e != cudaSuccess) return e;
@@ -203,11 +210,14 @@ cudaError_t launch_split(const AttnArgs& a, cudaStream_t s) {
 
 template <typename T, int D, int S>
 cudaError_t launch_g(const AttnArgs& a, cudaStream_t s) {
+  // head masks (GQA page union) only for G > 1: with one head a union page
+  // always belongs to it
+  const bool m = a.sel_mask != nullptr;
   switch (a.group) {
-    case 1: return launch_split<T, D, S, 1>(a, s);
-    case 2: return launch_split<T, D, S, 2>(a, s);
-    case 4: return launch_split<T, D, S, 4>(a, s);
-    case 8: return launch_split<T, D, S, 8>(a, s);
+    case 1: return launch_split<T, D, S, 1, false>(a, s);
+    case 2: return m ? launch_split<T, D, S, 2, true>(a, s) : launch_split<T, D, S, 2, false>(a, s);
+    case 4: return m ? launch_split<T, D, S, 4, true>(a, s) : launch_split<T, D, S, 4, false>(a, s);
+    case 8: return m ? launch_split<T, D, S, 8, true>(a, s) : launch_split<T, D, S, 8, false>(a, s);
   }
   return cudaErrorInvalidValue;
 }

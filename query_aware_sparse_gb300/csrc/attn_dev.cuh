@@ -92,8 +92,10 @@ struct WarpAttn {
   }
 
   // Fold one staged page (K block Kb, V block Vb, `valid` leading tokens) into
-  // the running state. `lg` is this warp's NV-float shared scratch.
-  __device__ __forceinline__ void page(const T* Kb, const T* Vb, int valid, float* lg, int lane) {
+  // the running state. `lg` is this warp's NV-float shared scratch. Heads
+  // whose bit of `hmask` is clear did not choose the page and skip it.
+  __device__ __forceinline__ void page(const T* Kb, const T* Vb, int valid, float* lg, int lane,
+                                       unsigned hmask = ~0u) {
     for (int t0 = 0; t0 < valid; t0 += TT) {
       float part[NV];
 #pragma unroll
@@ -125,6 +127,10 @@ struct WarpAttn {
       __syncwarp();
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
+        if (!((hmask >> gi) & 1u)) {         // not this head's page: weight 0
+          if (lane < TT) lg[gi * TT + lane] = 0.f;
+          continue;
+        }
         const float x = lg[gi * TT + (lane % TT)];
         const float mt = warp_max(x);
         const float m_new = fmaxf(m[gi], mt);

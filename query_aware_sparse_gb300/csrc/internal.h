@@ -22,7 +22,8 @@ struct AppendArgs {
 struct ScoreArgs {
   const void* summary; const void* q;
   const int32_t* page_indptr; const int32_t* page_indices; const int32_t* seq_lens;
-  float* scores;
+  float* scores;                              // [h_kv, nnz], or [h_kv * group, nnz] per head
+  int32_t per_head;                           // one row per query head, no group max
   int32_t batch, nnz, n_phys, h_kv, group, page_size, head_dim, dtype;
   int32_t summary_fp8;                        // summary holds E4M3 codes
   unsigned* err;
@@ -40,6 +41,7 @@ struct SelectArgs {
 struct AttnArgs {
   const void* q; const void* k_pool; const void* v_pool;
   const int32_t* sel_logical; const int32_t* sel_phys; const int32_t* seq_lens;
+  const uint8_t* sel_mask;   // [batch, h_kv, k] heads of the group per slot, or null (all)
   float* out; float* lse;
   float* part_o;     // [batch, h_q, n_chunks, head_dim]
   float* part_ml;    // [batch, h_q, n_chunks, 2]  (running max in log2 units, sum)
@@ -121,6 +123,22 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_score(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
+
+// GQA page union (quest_union_decode_attn): per (request, KV head) the pages
+// chosen by any of the group's query heads, in page order, with the bit set
+// of the heads that chose each.
+struct UnionArgs {
+  const int32_t* sel_logical;                 // [batch, h_kv * group, k]
+  const int32_t* page_indptr; const int32_t* page_indices; const int32_t* seq_lens;
+  int32_t* u_logical; int32_t* u_phys;        // [batch, h_kv, group * k], -1 padded
+  uint8_t* u_mask;                            // [batch, h_kv, group * k]
+  int32_t* u_count;                           // [batch, h_kv]
+  int32_t batch, h_kv, group, k, page_size;
+  int32_t max_pages;                          // shared-memory bytes: pages of one request covered
+  unsigned* err;
+};
+constexpr int32_t kUnionMaxPages = 65536;     // cap of max_pages (64 KiB of page bytes)
+cudaError_t launch_union(const UnionArgs& a, cudaStream_t s);
 AttnPlan plan_attn(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
                    int32_t page_size, int32_t dtype, int32_t k);
 

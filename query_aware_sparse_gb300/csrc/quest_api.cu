@@ -111,6 +111,28 @@ quest_status quest_score_pages(const quest_cache* cache, const quest_pages* page
   return launched(quest::launch_score(a, static_cast<cudaStream_t>(stream)));
 }
 
+quest_status quest_score_pages_per_head(const quest_cache* cache, const quest_pages* pages,
+                                        const void* q, int32_t group, float* scores,
+                                        void* stream) {
+  quest_status st = check_cache(cache);
+  if (st != QUEST_OK) return st;
+  if ((st = check_pages(pages, true)) != QUEST_OK) return st;
+  if (!valid_group(group)) return QUEST_ERR_UNSUPPORTED;
+  if (!quest::score_supported(cache->dtype, cache->head_dim, group)) return QUEST_ERR_UNSUPPORTED;
+  if (pages->batch == 0 || pages->nnz == 0) return QUEST_OK;
+  if (!q || !scores || !aligned16(q)) return QUEST_ERR_INVALID_ARG;
+  quest::ScoreArgs a{};
+  a.summary = cache->summary; a.q = q;
+  a.page_indptr = pages->page_indptr; a.page_indices = pages->page_indices;
+  a.seq_lens = pages->seq_lens; a.scores = scores; a.per_head = 1;
+  a.batch = pages->batch; a.nnz = pages->nnz; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv;
+  a.group = group; a.page_size = cache->page_size; a.head_dim = cache->head_dim;
+  a.dtype = cache->dtype; a.summary_fp8 = cache->summary_fp8;
+  a.err = err_ptr();
+  if (!a.err) return QUEST_ERR_CUDA;
+  return launched(quest::launch_score(a, static_cast<cudaStream_t>(stream)));
+}
+
 quest_status quest_select_topk(const quest_pages* pages, int32_t h_kv,
                                int32_t page_size, const float* scores, int32_t k,
                                int32_t n_sink, int32_t n_local,
@@ -181,6 +203,73 @@ quest_status quest_sparse_decode_attn(const quest_cache* cache,
   a.err = err_ptr();
   if (!a.err) return QUEST_ERR_CUDA;
   return launched(quest::launch_attn(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t quest_union_workspace_size(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
+                                  int32_t page_size, int32_t dtype, int32_t k) {
+  if (batch <= 0 || h_kv <= 0 || k < 1 || !valid_group(group)) return 0;
+  if (!quest::attn_supported(dtype, head_dim, page_size, group)) return 0;
+  const int64_t ku = (int64_t)group * k;
+  if (ku > INT32_MAX) return 0;
+  AttnPlan plan = quest::plan_attn(batch, h_kv, group, head_dim, page_size, dtype, (int32_t)ku);
+  const size_t phys = ((size_t)batch * h_kv * ku * sizeof(int32_t) + 255) & ~(size_t)255;
+  return phys + plan.workspace_bytes;
+}
+
+quest_status quest_union_decode_attn(const quest_cache* cache, const quest_pages* pages,
+                                     const void* q, int32_t group, const int32_t* sel_logical,
+                                     int32_t k, float* out, float* lse, float sm_scale,
+                                     int32_t* union_logical, uint8_t* union_mask,
+                                     int32_t* union_count, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  quest_status st = check_cache(cache);
+  if (st != QUEST_OK) return st;
+  if ((st = check_pages(pages, true)) != QUEST_OK) return st;
+  if (!valid_group(group) || k < 1) return QUEST_ERR_INVALID_ARG;
+  if (!quest::attn_supported(cache->dtype, cache->head_dim, cache->page_size, group))
+    return QUEST_ERR_UNSUPPORTED;
+  if ((int64_t)group * k > INT32_MAX) return QUEST_ERR_INVALID_ARG;
+  if (pages->batch == 0) return QUEST_OK;
+  if (!q || !sel_logical || !out || !union_logical || !union_mask || !union_count ||
+      !aligned16(q))
+    return QUEST_ERR_INVALID_ARG;
+  const int32_t ku = group * k;
+  AttnPlan plan = quest::plan_attn(pages->batch, cache->h_kv, group, cache->head_dim,
+                                   cache->page_size, cache->dtype, ku);
+  const size_t phys_bytes = ((size_t)pages->batch * cache->h_kv * ku * sizeof(int32_t) + 255) &
+                            ~(size_t)255;
+  if (!workspace || workspace_bytes < phys_bytes + plan.workspace_bytes || !aligned16(workspace))
+    return QUEST_ERR_WORKSPACE;
+  unsigned* err = err_ptr();
+  if (!err) return QUEST_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* u_phys = static_cast<int32_t*>(workspace);
+  quest::UnionArgs u{};
+  u.sel_logical = sel_logical;
+  u.page_indptr = pages->page_indptr; u.page_indices = pages->page_indices;
+  u.seq_lens = pages->seq_lens;
+  u.u_logical = union_logical; u.u_phys = u_phys; u.u_mask = union_mask; u.u_count = union_count;
+  u.batch = pages->batch; u.h_kv = cache->h_kv; u.group = group; u.k = k;
+  u.page_size = cache->page_size;
+  u.max_pages = pages->nnz < quest::kUnionMaxPages ? pages->nnz : quest::kUnionMaxPages;
+  u.err = err;
+  cudaError_t e = quest::launch_union(u, s);
+  if (e != cudaSuccess) return QUEST_ERR_CUDA;
+  quest::AttnArgs a{};
+  a.q = q; a.k_pool = cache->k_pool; a.v_pool = cache->v_pool;
+  a.sel_logical = union_logical; a.sel_phys = u_phys; a.sel_mask = union_mask;
+  a.seq_lens = pages->seq_lens;
+  a.out = out; a.lse = lse;
+  const size_t rows = (size_t)pages->batch * cache->h_kv * group * plan.n_chunks;
+  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + phys_bytes);
+  a.part_ml = a.part_o + rows * cache->head_dim;
+  a.batch = pages->batch; a.n_phys = cache->n_phys; a.h_kv = cache->h_kv; a.group = group;
+  a.page_size = cache->page_size; a.head_dim = cache->head_dim; a.dtype = cache->dtype;
+  a.k = ku; a.n_chunks = plan.n_chunks; a.chunk_pages = plan.chunk_pages;
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf((float)cache->head_dim);
+  a.scale_log2 = scale * quest::LOG2E;
+  a.err = err;
+  return launched(quest::launch_attn(a, s));
 }
 
 size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group,

@@ -1,6 +1,7 @@
 // a2: page upper bounds U_p(q) = sum_j max(q_j m_j, q_j M_j)
 // (Quest page §1.1 eq (2)-(3)); GQA groups share one score, the maximum over
-// the group's query heads (Quest page §2.1).
+// the group's query heads (Quest page §2.1), or with `per_head` one row per
+// query head (the per-head selection of the same section's GQA paragraph).
 //
 // HBM-bound stream of the [n_phys, h_kv, 2, d] summary. A (page, KV head)
 // summary is 2*d contiguous elements; LPP lanes cover one page with 16-byte
@@ -45,7 +46,7 @@ __device__ __forceinline__ void load_q(const ScoreArgs& a, int r, int g, int sub
   for (int gi = 0; gi < G; ++gi) q[gi] = ld_nc_v4(qp + (size_t)gi * D);
 }
 
-template <typename T, int D, int G, bool F8>
+template <typename T, int D, int G, bool F8, bool PH>
 __global__ void __launch_bounds__(kScoreThreads)
 score_kernel(const ScoreArgs a) {
   static_assert(!F8 || sizeof(T) == 2, "E4M3 summaries take fp16 queries");
@@ -130,8 +131,11 @@ score_kernel(const ScoreArgs a) {
 #pragma unroll
       for (int o = 1; o < LPP; o <<= 1) s += __shfl_xor_sync(FULL, s, o);
       best = fmaxf(best, s);
+      if (PH && sub == 0 && e < e_end)             // one row per query head
+        a.scores[((size_t)g * G + gi) * a.nnz + e] = live[u] ? s : -INFINITY;
     }
-    if (sub == 0 && e < e_end) a.scores[(size_t)g * a.nnz + e] = live[u] ? best : -INFINITY;
+    if (!PH && sub == 0 && e < e_end)
+      a.scores[(size_t)g * a.nnz + e] = live[u] ? best : -INFINITY;
   }
 }
 
@@ -139,11 +143,22 @@ template <typename T, int D, bool F8>
 cudaError_t launch_td(const ScoreArgs& a, cudaStream_t s) {
   using Sh = ScoreShape<T, D>;
   dim3 grid((a.nnz + Sh::TILE - 1) / Sh::TILE, a.h_kv);
+  // per-head rows only differ from the group max for G > 1
+  const bool ph = a.per_head != 0;
   switch (a.group) {
-    case 1: score_kernel<T, D, 1, F8><<<grid, kScoreThreads, 0, s>>>(a); break;
-    case 2: score_kernel<T, D, 2, F8><<<grid, kScoreThreads, 0, s>>>(a); break;
-    case 4: score_kernel<T, D, 4, F8><<<grid, kScoreThreads, 0, s>>>(a); break;
-    case 8: score_kernel<T, D, 8, F8><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 1: score_kernel<T, D, 1, F8, false><<<grid, kScoreThreads, 0, s>>>(a); break;
+    case 2:
+      if (ph) score_kernel<T, D, 2, F8, true><<<grid, kScoreThreads, 0, s>>>(a);
+      else score_kernel<T, D, 2, F8, false><<<grid, kScoreThreads, 0, s>>>(a);
+      break;
+    case 4:
+      if (ph) score_kernel<T, D, 4, F8, true><<<grid, kScoreThreads, 0, s>>>(a);
+      else score_kernel<T, D, 4, F8, false><<<grid, kScoreThreads, 0, s>>>(a);
+      break;
+    case 8:
+      if (ph) score_kernel<T, D, 8, F8, true><<<grid, kScoreThreads, 0, s>>>(a);
+      else score_kernel<T, D, 8, F8, false><<<grid, kScoreThreads, 0, s>>>(a);
+      break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -93,6 +93,16 @@ def test_host_validation_rejects_bad_arguments(qlib):
     f8 = C(fake, fake, fake, 8, 2, 16, 128, qlib.QUEST_F16, 1)
     assert L.quest_recall_diagnostics(by(f8), by(pages), fake, 1, fake, 4, 4, ctypes.c_float(0.0),
                                       fake, fake, fake, fake, fake, 1 << 20, None) == -2
+    # per-head scores and the GQA union: the same validation as their relatives
+    assert L.quest_score_pages_per_head(by(good), by(pages), fake, 3, fake, None) == -2
+    assert L.quest_score_pages_per_head(by(good), by(pages), fake + 4, 1, fake, None) == -1
+    assert L.quest_union_decode_attn(by(good), by(pages), fake, 4, fake, 0, fake, None,
+                                     ctypes.c_float(0.0), fake, fake, fake, fake, 1 << 20,
+                                     None) == -1
+    assert L.quest_union_decode_attn(by(good), by(pages), fake, 4, None, 8, fake, None,
+                                     ctypes.c_float(0.0), fake, fake, fake, fake, 1 << 20,
+                                     None) == -1
+    assert L.quest_union_workspace_size(1, 2, 3, 128, 16, qlib.QUEST_F16, 8) == 0
     # empty batches are valid no-ops
     empty = Pg(None, None, None, 0, 0)
     assert L.quest_select_topk(by(empty), 2, 16, None, 4, 0, 0, None, None, None, None) == 0
