@@ -403,7 +403,18 @@ class OracleSample:
 # Main
 # ---------------------------------------------------------------------------
 
-def main():
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks of the process group (the job ends with
+    its slowest replica); x itself without a group or with one rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=40000)
@@ -426,13 +437,15 @@ def main():
                     help="also time GQA per-query-head selection with the per-KV-head page union")
     ap.add_argument("--summary", choices=["kv", "e4m3"], default="kv",
                     help="page summaries in the K/V dtype or as E4M3 codes (directed rounding)")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
     ws, rank, local = dist_env()
+    if args.impl == "reference" and rank != 0:
+        return          # the oracle arm runs on rank 0 alone; other ranks do no work
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if ws > 1:
+    if ws > 1 and args.impl != "reference":   # the oracle arm needs no group
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = wl.WORKLOADS[args.workload]
@@ -522,10 +535,7 @@ def main():
     total_ms = t_all[0].elapsed_time(t_all[1])
     steps_us = sorted(a.elapsed_time(b) * 1e3 / nb for a, b in per) or [total_ms * 1e3 / K]
     ms_per_step = total_ms / K
-    if ws > 1:
-        tt = torch.tensor([ms_per_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(tt.item())
+    ms_per_step = max_over_ranks(ms_per_step, dev)
     assert qs.device_error() == 0
 
     # per-stage device time of the unfused four-call path (each stage alone,
