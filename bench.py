@@ -147,7 +147,9 @@ def workload_config(w: wl.Workload):
     dt = "fp16" if w.dtype == torch.float16 else "fp32"
     desc = (f"{w.name}: {B} request{'s' if B > 1 else ''}, {heads}, d_h {w.head_dim}, {ctx}, "
             f"page {w.page_size}, budget {w.k * w.page_size} tokens (K={w.k}), {dt}"
-            + (", RoPE" if w.rope else "") + (", physical pages permuted" if w.permute_pages else ""))
+            + (", RoPE" if w.rope else "") + (", physical pages permuted" if w.permute_pages else "")
+            + (f", {w.layers} layers (first {w.dense_layers} dense, K = P), budget sweep "
+               f"{'/'.join(str(b) for b in w.budgets)} tokens" if w.layers > 1 else ""))
     cfg = {"workload": desc, "n_pages": int((-(-lens // w.page_size)).sum()), "k": w.k,
            "h_kv": w.h_kv, "group": w.group, "head_dim": w.head_dim,
            "page_size": w.page_size, "seq_len": int(lens[0]) if B == 1 else int(lens.sum())}
@@ -472,6 +474,9 @@ def main(argv=None):
 
     import query_aware_sparse_gb300 as qs
     qs.lib()
+    if w.layers > 1:
+        run_model_step(args, w, cfg, dev, ws, rank, local)
+        return
     setup = LayerSetup(w, args.nbuf, dev, sample_heads=args.cpu_heads,
                        n_sink=n_sink, n_local=n_local, summary_fp8=args.summary_fp8)
     cfg["l2"] = (f"rotating {args.nbuf} distinct copies of the layer "
@@ -587,6 +592,116 @@ def main(argv=None):
     if rank == 0:
         if args.cpu_seconds > 0:
             line["cpu_baseline"] = cpu_baseline(setup, args.cpu_heads, args.cpu_seconds)
+        print(json.dumps(line))
+
+
+def run_model_step(args, w, cfg, dev, ws, rank, local):
+    """A whole decode step of a multi-layer model: every layer has its own
+    cache (prefilled through the library) and query; the first dense_layers
+    layers attend over all pages (K = P), the others select with the budget.
+    For each budget of the sweep, one CUDA graph holds the step's layers back
+    to back; it is replayed and timed with events (each layer reads its own
+    cold data: the layers together are far larger than L2). Per-layer times
+    come from graphs of one dense and one sparse layer replayed alike."""
+    import query_aware_sparse_gb300 as qs
+    L = int(w.lengths()[0])
+    S, h, d = w.page_size, w.h_kv, w.head_dim
+    P = -(-L // S)
+    t = wl.make_page_table([L], S, seed=w.seed)
+    i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32), device=dev)
+    table = qs.PageTable(i32(t.page_indptr), i32(t.page_indices), i32([L]))
+    pre = qs.PageTable(table.page_indptr, table.page_indices, i32([L - 1]))
+    layers = []
+    for layer in range(w.layers):
+        k_tok, v_tok = wl.request_tokens(w, 0, L, layer=layer, device=dev)
+        q = wl.queries(w, [L - 1], layer=layer, device=dev)
+        kp, vp, sm = wl.empty_pool(t, h, d, w.dtype, device=dev, poison=False)
+        cache = qs.PagedCache(kp, vp, sm)
+        qs.append_kv(cache, pre, k_tok[:L - 1].contiguous(), v_tok[:L - 1].contiguous(),
+                     i32([0, L - 1]), i32([0]))
+        layers.append((cache, q, k_tok[L - 1:L].contiguous(), v_tok[L - 1:L].contiguous()))
+        del k_tok, v_tok
+    torch.cuda.synchronize()
+    assert qs.device_error() == 0
+    esz = torch.tensor([], dtype=w.dtype).element_size()
+    pk, pk_src = peaks()
+
+    def graph_of(calls):
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for c in calls:
+                    c()
+        return g, s
+
+    def replay_us(g, s, reps):
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    sweep = {}
+    whole_2048 = None
+    for B in w.budgets:
+        Ks = wl.selection_budget(B, S)
+        steps = [qs.DecodeStep(c, table, w.group, P if i < w.dense_layers else Ks)
+                 for i, (c, _, _, _) in enumerate(layers)]
+        calls = [(lambda st=st, c=c, q=q, kn=kn, vn=vn: st(c, table, q, kn, vn))
+                 for st, (c, q, kn, vn) in zip(steps, layers)]
+        for c in calls:          # warm-up (kernel attributes before capture)
+            c()
+        torch.cuda.synchronize()
+        assert qs.device_error() == 0
+        g, s = graph_of(calls)
+        reps = max(3, args.steps // w.layers)
+        whole = replay_us(g, s, reps)
+        nd = w.dense_layers
+        gd, sd = graph_of(calls[:nd])                       # the dense layers
+        dense_us = replay_us(gd, sd, max(3, args.stage_reps)) / max(nd, 1)
+        ns = min(8, w.layers - nd)                          # distinct sparse layers
+        gs_, ss = graph_of(calls[nd:nd + ns])
+        sparse_us = replay_us(gs_, ss, max(3, args.stage_reps)) / ns
+        summ = P * h * 2 * d * esz
+        valid_sel = min(Ks, P) * S - (P * S - L if Ks >= P else 0)
+        by_sparse = step_bytes(P, h, w.group, d, S, Ks, valid_sel, esz)["total"]
+        by_dense = step_bytes(P, h, w.group, d, S, P, L, esz)["total"]
+        by_whole = nd * by_dense + (w.layers - nd) * by_sparse
+        sweep[str(B)] = {"k_pages": Ks, "whole_step_us": round(whole, 2),
+                         "per_layer_us": round(whole / w.layers, 3),
+                         "dense_layer_us": round(dense_us, 3),
+                         "sparse_layer_us": round(sparse_us, 3),
+                         "bytes_per_step": by_whole,
+                         "GBps": round(by_whole / (whole * 1e-6) / 1e9, 1),
+                         "frac": round(by_whole / (whole * 1e-6) / 1e9 / pk, 4),
+                         "dense_summary_bytes_share": round(summ / by_dense, 4)}
+        if B == 2048:
+            whole_2048 = (whole, by_whole, reps)
+        del g, gd, gs_, steps
+    whole, by_whole, reps = whole_2048 if whole_2048 else (
+        sweep[str(w.budgets[0])]["whole_step_us"], sweep[str(w.budgets[0])]["bytes_per_step"], 1)
+    per_layer = max_over_ranks(whole / w.layers, dev)
+    cfg["budget_sweep_tokens"] = list(w.budgets)
+    cfg["value_budget"] = 2048
+    line = {"metric": METRIC, "value": round(per_layer, 3), "unit": UNIT, "n_gpus": ws,
+            "steps": reps * w.layers, "warmup": args.warmup,
+            "ms_per_step": round(per_layer / 1e3, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": data_desc(w),
+            "config": cfg, "whole_step": sweep,
+            "roofline": {"bound": "hbm", "kernel": "step_kernel",
+                         "achieved": round(by_whole / (whole * 1e-6) / 1e9, 1), "peak": pk,
+                         "unit": "GB/s", "frac": round(by_whole / (whole * 1e-6) / 1e9 / pk, 4),
+                         "peak_source": pk_src, "bytes_per_launch": by_whole // w.layers,
+                         "traffic": None},
+            "gpu_launches": reps * w.layers}
+    if rank == 0:
         print(json.dumps(line))
 
 

@@ -107,3 +107,27 @@ def test_union_of_identical_heads_is_one_set():
 
 def test_union_long_rows():
     _run(941, [32768, 9000], 2, 4, 128, 16, F16, k=64)
+
+
+def test_per_head_scores_over_e4m3_summaries():
+    """Per-head rows read E4M3 summaries too: against the oracle's per-head
+    bounds over the decoded box (Quest page §3 summary dtype, §2.1 GQA)."""
+    import query_aware_sparse_gb300 as qs
+    group, S = 4, 16
+    case = random_case(951, [1, 17, 500, 2000], h_kv=2, group=group, d=128, S=S, dtype=F16,
+                       scale=3.0)
+    t = case["table"]
+    exact = qo.build_summary(np_of(case["k_pool"]), t.page_indptr, t.page_indices, t.seq_lens)
+    codes, ovf = qo.summary_to_e4m3(exact)
+    assert not ovf.any()
+    cache = gpu_cache(case["k_pool"], case["v_pool"], torch.from_numpy(codes))
+    q = case["q"]
+    got = np_of(qs.score_pages_per_head(cache, gpu_table(t), q.cuda(), group))
+    assert qs.device_error() == 0
+    box = qo.e4m3_decode(codes)
+    ref = qo.score_pages_per_head(np_of(q), box, t.page_indptr, t.page_indices, group)
+    tol = _per_head_tol(np_of(q), box, t, group)
+    for r in range(t.batch):
+        lo = int(t.page_indptr[r])
+        P = -(-int(t.seq_lens[r]) // S)
+        assert np.all(np.abs(got[:, lo:lo + P] - ref[:, lo:lo + P]) <= tol[:, lo:lo + P])
