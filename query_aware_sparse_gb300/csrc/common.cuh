@@ -219,14 +219,16 @@ __device__ __forceinline__ uint32_t e4m3_ceil(float x, bool& ovf) {
 __device__ __forceinline__ uint32_t e4m3x2_placed_to_h2_scaled(uint32_t placed) {
   return ((placed >> 1) & 0x3f803f80u) | (placed & 0x80008000u);
 }
-// Codes 0,1 / 2,3 of a word of four codes, as fp32 values times 2^-8.
-__device__ __forceinline__ float2 e4m3x4_lo_scaled(uint32_t w) {
-  const uint32_t h = e4m3x2_placed_to_h2_scaled(__byte_perm(w, 0u, 0x1404));
+// Codes 0,1 / 2,3 of a word of four codes, as fp32 values: the hardware
+// conversion of a pair of E4M3 codes to an fp16 pair (exact), then to fp32.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t pair) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(pair));
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
-__device__ __forceinline__ float2 e4m3x4_hi_scaled(uint32_t w) {
-  const uint32_t h = e4m3x2_placed_to_h2_scaled(__byte_perm(w, 0u, 0x3424));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+__device__ __forceinline__ float2 e4m3x4_lo_f2(uint32_t w) { return e4m3x2_to_f2((uint16_t)w); }
+__device__ __forceinline__ float2 e4m3x4_hi_f2(uint32_t w) {
+  return e4m3x2_to_f2((uint16_t)(w >> 16));
 }
 // Codes 0,1 / 2,3 of a word of four codes as an exact fp16 pair (raw bits).
 __device__ __forceinline__ uint32_t e4m3x4_lo_h2(uint32_t w) {
@@ -250,12 +252,11 @@ __device__ __forceinline__ uint32_t e4m3_qsel_from_masks(uint32_t m01, uint32_t 
   return __byte_perm(m01, m23, 0x6420);
 }
 // Page-bound contribution (eq (2)) of 4 dims with E4M3 summary words m, M and
-// fp32 queries q[0..3]: sum_j q_j * (q_j >= 0 ? M_j : m_j), times 2^-8 (the
-// caller scales the total by 2^8; every step is exact or scales exactly).
-__device__ __forceinline__ float bound4_e4m3_scaled(const float* q, uint32_t sel, uint32_t m,
-                                                    uint32_t M, float s) {
+// fp32 queries q[0..3]: sum_j q_j * (q_j >= 0 ? M_j : m_j).
+__device__ __forceinline__ float bound4_e4m3(const float* q, uint32_t sel, uint32_t m,
+                                             uint32_t M, float s) {
   const uint32_t x = (M & sel) | (m & ~sel);
-  const float2 lo = e4m3x4_lo_scaled(x), hi = e4m3x4_hi_scaled(x);
+  const float2 lo = e4m3x4_lo_f2(x), hi = e4m3x4_hi_f2(x);
   s = fmaf(q[0], lo.x, s);
   s = fmaf(q[1], lo.y, s);
   s = fmaf(q[2], hi.x, s);
@@ -270,9 +271,8 @@ __device__ __forceinline__ float bound8_e4m3(uint4 q, uint2 m, uint2 M) {
   const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(&q.z));
   const float2 q3 = __half22float2(*reinterpret_cast<const __half2*>(&q.w));
   const float qa[4] = {q0.x, q0.y, q1.x, q1.y}, qb[4] = {q2.x, q2.y, q3.x, q3.y};
-  float s = bound4_e4m3_scaled(qa, e4m3_qsel(q.x, q.y), m.x, M.x, 0.f);
-  s = bound4_e4m3_scaled(qb, e4m3_qsel(q.z, q.w), m.y, M.y, s);
-  return s * 256.f;
+  float s = bound4_e4m3(qa, e4m3_qsel(q.x, q.y), m.x, M.x, 0.f);
+  return bound4_e4m3(qb, e4m3_qsel(q.z, q.w), m.y, M.y, s);
 }
 // Four fp16 keys (two words) -> floor / ceil codes packed in one word.
 __device__ __forceinline__ uint32_t e4m3x4_floor_h(uint32_t k01, uint32_t k23, bool& ovf) {

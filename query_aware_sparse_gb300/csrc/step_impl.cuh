@@ -467,7 +467,7 @@ step_kernel(const StepArgs a) {
               }
             }
             // sum_j max(q_j m_j, q_j M_j) = sum_j q_j * (q_j >= 0 ? M_j : m_j)
-            if constexpr (F8) {              // codes decoded times 2^-8; total times 2^8
+            if constexpr (F8) {              // codes decoded to fp16 (exact), FMA in fp32
               const uint32_t mw[4] = {vm[0].x, vm[0].y, vm[0].z, vm[0].w};
               const uint32_t Mw[4] = {vM[0].x, vM[0].y, vM[0].z, vM[0].w};
 #pragma unroll
@@ -476,15 +476,13 @@ step_kernel(const StepArgs a) {
                 for (int gi = 0; gi < G; ++gi) {
                   const uint32_t sel = e4m3_qsel_from_masks(qmask[gi][2 * cw], qmask[gi][2 * cw + 1]);
                   const uint32_t xw = (Mw[cw] & sel) | (mw[cw] & ~sel);
-                  const float2 lo = e4m3x4_lo_scaled(xw), hi = e4m3x4_hi_scaled(xw);
+                  const float2 lo = e4m3x4_lo_f2(xw), hi = e4m3x4_hi_f2(xw);
                   sg[gi] = fmaf(qf[gi][4 * cw + 0], lo.x, sg[gi]);
                   sg[gi] = fmaf(qf[gi][4 * cw + 1], lo.y, sg[gi]);
                   sg[gi] = fmaf(qf[gi][4 * cw + 2], hi.x, sg[gi]);
                   sg[gi] = fmaf(qf[gi][4 * cw + 3], hi.y, sg[gi]);
                 }
               }
-#pragma unroll
-              for (int gi = 0; gi < G; ++gi) sg[gi] *= 256.f;
             } else {
 #pragma unroll
               for (int v = 0; v < VPL; ++v) {
