@@ -780,3 +780,60 @@ def test_per_head_attention_against_contiguous_tokens():
     o2, _ = qo.sparse_attention_per_head(q, kp, vp, indptr, perm, sl, np.repeat(shared, G, axis=1), G)
     o3, _ = qo.sparse_attention(q, kp, vp, indptr, perm, sl, shared, G)
     assert np.array_equal(o2, o3)
+
+
+def test_planted_mistakes_in_the_next_rows_are_caught(monkeypatch):
+    """Plausible slips planted in the oracle's E4M3, per-head and union
+    functions each make one of the pins above fail."""
+    real_round, real_vals = qo.e4m3_round, qo.e4m3_values
+    real_union, real_ph_attn = qo.union_pages, qo.sparse_attention_per_head
+
+    def planted(attr, fake, pin, *args):
+        monkeypatch.setattr(qo, attr, fake)
+        with pytest.raises(AssertionError):
+            pin(*args)
+        monkeypatch.undo()
+
+    # rounding toward the wrong side
+    planted("e4m3_round", lambda x, toward: real_round(x, -toward),
+            test_e4m3_directed_rounding_brackets_and_rne)
+
+    # subnormals one binade off
+    def vals_subnormal_slip():
+        v = real_vals().copy()
+        v[0x01:0x08] *= 2
+        v[0x81:0x88] *= 2
+        return v
+    planted("e4m3_values", vals_subnormal_slip, test_e4m3_table_matches_torch_float8)
+
+    # exponent bias 8 instead of 7
+    def vals_bias_slip():
+        v = real_vals().copy()
+        v[0x08:0x7F] /= 2
+        return v
+    planted("e4m3_values", vals_bias_slip, test_e4m3_closed_forms)
+
+    # head bits in the wrong order (a transposed index)
+    planted("union_pages", lambda sel: real_union(np.asarray(sel)[::-1]),
+            test_union_pages_brute_force)
+
+    # every head of a group attending over the first head's pages
+    def shared_set(q, kp, vp, ip, ix, sl, sel, group, sm_scale=None, requests=None):
+        return real_ph_attn(q, kp, vp, ip, ix, sl, np.repeat(sel[:, ::group], group, axis=1),
+                            group, sm_scale, requests)
+    planted("sparse_attention_per_head", shared_set,
+            test_per_head_attention_against_contiguous_tokens)
+
+    # query head h read against KV head h % h_kv instead of h // group
+    def wrong_kv_head(q, summary, indptr, indices, group, requests=None):
+        h_kv = summary.shape[1]
+        out = np.full((h_kv * group, int(indptr[-1])), np.nan)
+        for r in range(len(indptr) - 1):
+            lo, hi = int(indptr[r]), int(indptr[r + 1])
+            phys = np.asarray(indices[lo:hi], dtype=np.int64)
+            for h in range(h_kv * group):
+                g = h % h_kv
+                out[h, lo:hi] = qo.page_bound(q[r, h], summary[phys, g, 0], summary[phys, g, 1])
+        return out
+    planted("score_pages_per_head", wrong_kv_head,
+            test_per_head_scores_bound_each_heads_dot_products)
