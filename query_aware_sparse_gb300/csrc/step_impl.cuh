@@ -582,7 +582,9 @@ step_kernel(const StepArgs a) {
 #pragma unroll
         for (int j = 0; j < PB; ++j) {
           const int i = i0 + j * kNT;
-          for (uint32_t it = 0; (unsigned)(v[j] >> 32) != tag; ++it) {
+          // after one wait has run out the rest take what is there: a stuck
+          // row costs one limit, not one per entry
+          for (uint32_t it = 0; !late && (unsigned)(v[j] >> 32) != tag; ++it) {
             if (it >= WAIT_LIMIT) { late = true; break; }
             __nanosleep(32);
             v[j] = ld_relaxed_u64(row + i);
