@@ -11,7 +11,9 @@
  *  - Every pointer argument marked "device" must point to device memory of the
  *    current CUDA device; the caller allocates and owns all of it (pools,
  *    summaries, page tables, outputs, workspace). The library allocates no
- *    memory. Its only state is a 4-byte device error word per device.
+ *    memory. Its device state lives in its own module memory: a 4-byte error
+ *    word per device, and the fixed 4 MiB buffer of
+ *    quest_sparse_decode_attn_noalloc (see there).
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream). A QUEST_OK return means the work was enqueued.
  *  - Host-side validation runs first; on any error nothing is enqueued and a
@@ -21,8 +23,9 @@
  *    offending item is skipped and a bit is OR-ed into the device error word,
  *    which quest_get_device_error() returns and clears.
  *  - Element types: QUEST_F32 or QUEST_F16 for K, V, summaries and q (all the
- *    same type); outputs are fp32. head_dim in {64, 128}; page_size in
- *    {16, 32}; GQA group in {1, 2, 4, 8}.
+ *    same type), or with fp16 K/V/q, E4M3 summaries (quest_cache.summary_fp8);
+ *    outputs are fp32. head_dim in {64, 128}; page_size in {16, 32}; GQA group
+ *    in {1, 2, 4, 8}.
  *  - Data pointers (pools, summary, q, k_new, v_new) must be 16-byte aligned.
  */
 #ifndef QUEST_H
