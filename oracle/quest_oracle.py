@@ -11,7 +11,8 @@ Sources. "Quest page" is the PaperTrace chapter
 notes page "PageWeaver: KV-Guided Query Unions for Sparse Attention".
 Each function names the section / equation it restates.
 
-Conventions (all readings are listed in DESIGN.md's "Readings" section):
+Conventions (where the pages are silent, the reading taken is stated here or
+in the docstring of the function that takes it):
 
 * Arrays are numpy. Keys/values/queries arrive in their stored dtype (float16
   or float32). Every floating-point *arithmetic* step runs in float64 on the
