@@ -337,7 +337,10 @@ def ncu_traffic(kernel_key, workload):
     e = rec.get(kernel_key)
     if not e or e.get("workload") != workload:
         return None
-    if e.get("source_hash") != source_hash(*e["sources"]):
+    try:
+        if e.get("source_hash") != source_hash(*e["sources"]):
+            return None
+    except OSError:                  # a recorded source no longer exists
         return None
     return e["dram_bytes_per_launch"]
 

@@ -103,14 +103,18 @@ struct StepPlan {
 cudaError_t launch_step(const StepArgs& a, const StepPlan& p, cudaStream_t s);
 StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int32_t head_dim,
                    int32_t page_size, int32_t dtype, int32_t k, int32_t summary_fp8);
-// Per-variant instantiations of the fused step (step_f32.cu, step_f16.cu,
-// step_e4m3.cu): launch, and shared memory / resident CTAs per SM.
-cudaError_t launch_step_f32(const StepArgs& a, const StepPlan& p, cudaStream_t s);
-cudaError_t launch_step_f16(const StepArgs& a, const StepPlan& p, cudaStream_t s);
-cudaError_t launch_step_e4m3(const StepArgs& a, const StepPlan& p, cudaStream_t s);
-void shape_step_f32(int dev, int head_dim, int page_size, int group, int* smem, int* per_sm);
-void shape_step_f16(int dev, int head_dim, int page_size, int group, int* smem, int* per_sm);
-void shape_step_e4m3(int dev, int head_dim, int page_size, int group, int* smem, int* per_sm);
+// Per-variant, per-head-dim instantiations of the fused step
+// (step_<variant>_d<head_dim>.cu): launch, and shared memory / resident CTAs
+// per SM.
+#define QUEST_STEP_VARIANT(name)                                                          \
+  cudaError_t launch_step_##name##_d64(const StepArgs& a, const StepPlan& p, cudaStream_t s);  \
+  cudaError_t launch_step_##name##_d128(const StepArgs& a, const StepPlan& p, cudaStream_t s); \
+  void shape_step_##name##_d64(int dev, int page_size, int group, int* smem, int* per_sm);     \
+  void shape_step_##name##_d128(int dev, int page_size, int group, int* smem, int* per_sm);
+QUEST_STEP_VARIANT(f32)
+QUEST_STEP_VARIANT(f16)
+QUEST_STEP_VARIANT(e4m3)
+#undef QUEST_STEP_VARIANT
 
 // Split-K plan of the attention for a problem size on the current device.
 struct AttnPlan {

@@ -1,6 +1,6 @@
 // Plan and dispatch of the fused decode step (the kernel is in
-// step_impl.cuh; step_f32.cu, step_f16.cu and step_e4m3.cu instantiate it
-// per element type and summary format, so the variants compile in parallel).
+// step_impl.cuh; the step_<variant>_d<head_dim>.cu files instantiate it per
+// element type, summary format and head dim, so they compile in parallel).
 // Including the kernel's header instantiates nothing here: its templates
 // are only instantiated by the variant files.
 #include "step_impl.cuh"
@@ -15,9 +15,17 @@ StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int3
                         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
   cudaGetLastError();
   if (have_dev) {
-    if (dtype == QUEST_F16 && summary_fp8) shape_step_e4m3(dev, head_dim, page_size, group, &smem, &per_sm);
-    else if (dtype == QUEST_F16) shape_step_f16(dev, head_dim, page_size, group, &smem, &per_sm);
-    else shape_step_f32(dev, head_dim, page_size, group, &smem, &per_sm);
+    const bool d128 = head_dim == 128;
+    if (dtype == QUEST_F16 && summary_fp8) {
+      if (d128) shape_step_e4m3_d128(dev, page_size, group, &smem, &per_sm);
+      else shape_step_e4m3_d64(dev, page_size, group, &smem, &per_sm);
+    } else if (dtype == QUEST_F16) {
+      if (d128) shape_step_f16_d128(dev, page_size, group, &smem, &per_sm);
+      else shape_step_f16_d64(dev, page_size, group, &smem, &per_sm);
+    } else {
+      if (d128) shape_step_f32_d128(dev, page_size, group, &smem, &per_sm);
+      else shape_step_f32_d64(dev, page_size, group, &smem, &per_sm);
+    }
   } else {
     per_sm = 1;   // no device (sizing only): one CTA per SM of a default part
   }
@@ -54,9 +62,11 @@ StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int3
 }
 
 cudaError_t launch_step(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
-  if (a.dtype == QUEST_F16 && a.summary_fp8) return launch_step_e4m3(a, p, s);
-  if (a.dtype == QUEST_F16) return launch_step_f16(a, p, s);
-  return launch_step_f32(a, p, s);
+  const bool d128 = a.head_dim == 128;
+  if (a.dtype == QUEST_F16 && a.summary_fp8)
+    return d128 ? launch_step_e4m3_d128(a, p, s) : launch_step_e4m3_d64(a, p, s);
+  if (a.dtype == QUEST_F16) return d128 ? launch_step_f16_d128(a, p, s) : launch_step_f16_d64(a, p, s);
+  return d128 ? launch_step_f32_d128(a, p, s) : launch_step_f32_d64(a, p, s);
 }
 
 }  // namespace quest
