@@ -115,3 +115,28 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(q, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         q.lib()
+
+
+def test_workspace_sizes_host_logic(qlib):
+    """Workspace sizing is host logic (no GPU needed): closed forms and the
+    relations between the calls."""
+    L = qlib.lib()
+    up = lambda b: (b + 255) // 256 * 256
+    # diagnostics: token logits, per-page softmax statistics, per-page |v| maxima
+    for h, G, nnz, S in ((32, 1, 2048, 16), (8, 4, 70000, 16), (2, 8, 5, 32)):
+        want = up(h * G * nnz * S * 4) + up(h * G * nnz * 8) + up(h * nnz * 4)
+        assert L.quest_diag_workspace_size(h, G, nnz, S) == want
+    assert L.quest_diag_workspace_size(2, 3, 5, 16) == 0
+    # union: its physical ids, then the split-K partials of G*k slots
+    for B, h, G, d, S, k in ((16, 8, 4, 128, 16, 256), (1, 2, 2, 64, 32, 7), (3, 4, 8, 128, 16, 9)):
+        ws = L.quest_union_workspace_size(B, h, G, d, S, qlib.QUEST_F16, k)
+        phys = up(B * h * G * k * 4)
+        attn = L.quest_attn_workspace_size(B, h, G, d, S, G * k)
+        assert phys < ws <= phys + attn
+    assert L.quest_union_workspace_size(1, 2, 4, 96, 16, qlib.QUEST_F16, 8) == 0
+    # attention and the fused step: positive for supported shapes, 0 otherwise
+    assert L.quest_attn_workspace_size(1, 32, 1, 128, 16, 128) > 0
+    assert L.quest_attn_workspace_size(1, 32, 3, 128, 16, 128) == 0
+    assert L.quest_decode_workspace_size(1, 2048, 32, 1, 128, 16, qlib.QUEST_F16, 128) > 0
+    assert L.quest_decode_workspace_size(1, 2048, 32, 1, 96, 16, qlib.QUEST_F16, 128) == 0
+    assert L.quest_decode_workspace_size(1, 2048, 32, 1, 128, 24, qlib.QUEST_F16, 128) == 0
