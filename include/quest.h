@@ -385,6 +385,17 @@ QUEST_API int32_t quest_set_trace(void* device_buffer, int32_t max_ctas, int32_t
                                   int32_t h_kv, int32_t group, int32_t head_dim,
                                   int32_t page_size, int32_t dtype, int32_t k);
 
+/* Test hook of quest_decode_step's failure handling (no counterpart on the
+ * pages). mode 0: normal operation. mode 1: later calls of the cluster kernel
+ * (groups 1 and 2) make the first summary slot of each CTA's first unit wait
+ * for bytes no copy delivers, so that wait runs out: the call then sets
+ * QUEST_DEVERR_WAIT_TIMEOUT, stops issuing copies, drains those in flight
+ * and returns with its outputs unspecified. wait_limit: tries of every
+ * bounded in-kernel wait (each up to about 1 us); 0 restores the default
+ * (about 2 s of waiting). Host state only (not thread-safe); returns
+ * QUEST_ERR_INVALID_ARG for other values. */
+QUEST_API int32_t quest_test_step_fault(int32_t mode, int32_t wait_limit);
+
 /* Synchronises `stream`, returns the device error word of the current device
  * (QUEST_DEVERR_* bits) and clears it. Returns -1 if a CUDA call fails. */
 QUEST_API int32_t quest_get_device_error(void* stream);

@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.quest_diag_workspace_size.restype = SZ
         L.quest_set_trace.argtypes = [P, I32, I32, I32, I32, I32, I32, I32, I32]
         L.quest_set_trace.restype = I32
+        L.quest_test_step_fault.argtypes = [I32, I32]
+        L.quest_test_step_fault.restype = I32
         L.quest_get_device_error.argtypes = [P]
         L.quest_get_device_error.restype = I32
         L.quest_status_string.argtypes = [I32]
@@ -98,7 +100,7 @@ EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_score_pages_per_head"
             "quest_attn_workspace_size",
             "quest_decode_step", "quest_decode_workspace_size",
             "quest_recall_diagnostics", "quest_diag_workspace_size", "quest_set_trace",
-            "quest_get_device_error", "quest_status_string")
+            "quest_test_step_fault", "quest_get_device_error", "quest_status_string")
 
 
 def _check(status: int) -> None:
@@ -369,6 +371,13 @@ def sparse_decode_attn_noalloc(cache: PagedCache, table: PageTable, q, group: in
         ctypes.byref(cache.c), ctypes.byref(table.c), _ptr(q), int(group), _ptr(sel_logical),
         _ptr(sel_phys), int(k), _ptr(out), _ptr(lse), float(sm_scale), _stream(stream)))
     return out, lse
+
+
+def test_step_fault(mode: int, wait_limit: int = 0) -> None:
+    """quest_test_step_fault: mode 1 makes later decode steps (groups 1, 2)
+    wait for a copy that never comes, under `wait_limit` tries per wait (0 =
+    default); mode 0 restores normal operation."""
+    _check(lib().quest_test_step_fault(int(mode), int(wait_limit)))
 
 
 def device_error(stream=None) -> int:

@@ -20,9 +20,12 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libquest.so")
 SOURCES = ["quest_api.cu", "append.cu", "score.cu", "select.cu", "attn.cu", "step.cu",
            "step_f32_d64.cu", "step_f32_d128.cu", "step_f16_d64.cu", "step_f16_d128.cu",
-           "step_e4m3_d64.cu", "step_e4m3_d128.cu", "noalloc.cu", "diag.cu", "union.cu"]
+           "step_e4m3_d64.cu", "step_e4m3_d128.cu", "noalloc.cu", "diag.cu", "union.cu",
+           "cstep_f32_d64.cu", "cstep_f32_d128.cu", "cstep_f16_d64.cu", "cstep_f16_d128.cu",
+           "cstep_e4m3_d64.cu", "cstep_e4m3_d128.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.h", "topk.cuh", "attn_dev.cuh",
-                                           "attn_mma.cuh", "step_impl.cuh")] + [
+                                           "attn_mma.cuh", "step_impl.cuh",
+                                           "cstep_impl.cuh")] + [
            os.path.join(ROOT, "include", "quest.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -160,6 +160,72 @@ struct WarpAttn {
     }
   }
 
+  // page() in two halves, for pages of one tile (TT == S): qk() folds the
+  // logits of the K block into the running max and sum and leaves the
+  // probabilities in `lg`; av() then accumulates the V block with them. The
+  // K block is not read after qk() returns, so its buffer may be refilled
+  // while av() runs.
+  __device__ __forceinline__ void qk(const T* Kb, int valid, float* lg, int lane) {
+    static_assert(TT == S, "one tile per page");
+    float part[NV];
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      float kr[VD];
+      lds_row<T, VD>(Kb + (size_t)tt * D + lane * VD, kr);
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        float s = 0.f;
+#pragma unroll
+        for (int v = 0; v < VD; ++v) s = fmaf(q[gi][v], kr[v], s);
+        part[gi * TT + tt] = s;
+      }
+    }
+    transpose_reduce<NV>(part, lane);
+    if constexpr (NV >= 32) {
+#pragma unroll
+      for (int i = 0; i < NV / 32; ++i) {
+        const int vi = lane * (NV / 32) + i;
+        lg[vi] = (vi % TT < valid) ? part[i] : -INFINITY;
+      }
+    } else {
+      constexpr int SH = 5 - ILog2<NV>::value;
+      if ((lane & ((1 << SH) - 1)) == 0) {
+        const int vi = lane >> SH;
+        lg[vi] = (vi % TT < valid) ? part[0] : -INFINITY;
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      const float x = lg[gi * TT + (lane % TT)];
+      const float mt = warp_max(x);
+      const float m_new = fmaxf(m[gi], mt);
+      const float alpha = exp2f(m[gi] - m_new);
+      const float p = exp2f(x - m_new);
+      const float psum = warp_sum(lane < TT ? p : 0.f);
+      l[gi] = l[gi] * alpha + psum;
+      m[gi] = m_new;
+#pragma unroll
+      for (int v = 0; v < VD; ++v) acc[gi][v] *= alpha;
+      __syncwarp();
+      if (lane < TT) lg[gi * TT + lane] = p;
+    }
+    __syncwarp();
+  }
+  __device__ __forceinline__ void av(const T* Vb, int valid, const float* lg, int lane) {
+    for (int tt = 0; tt < valid; ++tt) {
+      float vr[VD];
+      lds_row<T, VD>(Vb + (size_t)tt * D + lane * VD, vr);
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        const float p = lg[gi * TT + tt];
+#pragma unroll
+        for (int v = 0; v < VD; ++v) acc[gi][v] = fmaf(p, vr[v], acc[gi][v]);
+      }
+    }
+    __syncwarp();
+  }
+
   // Store this warp's state in shared memory: mo[w][gi][D], ml[w][gi][2].
   __device__ __forceinline__ void stash(float* mo, float* ml, int w, int lane) const {
 #pragma unroll

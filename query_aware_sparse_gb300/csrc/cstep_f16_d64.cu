@@ -1,0 +1,16 @@
+// Cluster decode step instantiated for fp16 K/V/q with fp16 summaries, head dim 64
+// (page sizes 16 and 32, GQA groups 1 and 2; one file per variant and head
+// dim, so the instantiations compile in parallel).
+#include "cstep_impl.cuh"
+
+namespace quest {
+
+cudaError_t launch_cstep_f16_d64(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
+  return cstep_launch_sg<__half, 64, false>(a, p, s);
+}
+
+int clusters_cstep_f16_d64(int dev, int page_size, int group) {
+  return cstep_clusters_sg<__half, 64, false>(dev, page_size, group);
+}
+
+}  // namespace quest

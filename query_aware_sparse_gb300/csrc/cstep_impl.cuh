@@ -1,0 +1,1041 @@
+// Fused decode step of one layer on thread-block clusters: every (request,
+// KV head) unit is scored, selected and attended inside ONE cluster of kCL
+// CTAs (one per SM), so no step of the path waits on another cluster:
+//   a1 append of the new token (Quest page §1.2 eq (8)) folded into the
+//      scoring of its page,
+//   a2 page upper bounds U_p (Quest page §1.1 eq (2)-(3); GQA group max §2.1),
+//   a3 Top-K pages, ties to the lower page index (Quest page Fig. 1, §2),
+//   a4 attention over the selected pages (Quest page Fig. 1, §2.1), and
+//   a5 the log-sum-exp merge of the partial results (Quest page §2.1).
+//
+// Each cluster takes a list of units (one, or several in a snake order over
+// the requests sorted by length) and works through them in the order
+// S(0), S(1), A(0), S(2), A(1), ..., A(n-1): the selection of a unit runs
+// while the next unit's summaries stream. Warps of a CTA have fixed roles:
+//   * consumer warps feed themselves. In S(t) warp w scores the CTA's
+//     chunks w, w + NCW, ... of the unit's pages (chunk c of CHUNK pages
+//     belongs to CTA c % kCL): it copies their summaries into its own buffer
+//     with cp.async (16 bytes per lane, one page summary per warp copy, two
+//     chunks in flight) and writes each score as an order-preserving key into
+//     the row buffer of every CTA of the cluster (distributed shared memory).
+//     In A(t) it streams its share of the CTA's selected pages with 1-D bulk
+//     copies, the next page's K block loading while the current V block is
+//     folded into the warp's online softmax; the state is stashed per unit.
+//   * select warps wait until every CTA has delivered the unit's keys, run
+//     the block Top-K (every CTA computes the same set), look up the
+//     selected pages' physical ids, release the unit to the consumers, then
+//     merge the consumers' states into the CTA's partial and send it to the
+//     unit's owner CTA, which combines the kCL partials into the output row.
+// Hand-offs are mbarrier phases (bulk-copy completion, local and remote
+// arrivals); every wait is bounded and sets QUEST_DEVERR_WAIT_TIMEOUT rather
+// than hanging, after which the CTA stops issuing and drains its copies.
+// The launch needs no workspace and no grid-wide synchronisation.
+#pragma once
+
+#include <cstdlib>
+
+#include "attn_dev.cuh"
+#include "common.cuh"
+#include "internal.h"
+#include "topk.cuh"
+
+namespace quest {
+namespace {
+
+constexpr int kCL = 4;                       // CTAs per cluster
+constexpr int kCSW = 4;                      // select warps (the last ones)
+constexpr int kCSelT = kCSW * 32;
+constexpr int kCMaxCW = 12;                  // consumer warps at most
+constexpr int kCMaxU = 64;                   // units per cluster
+constexpr int kCRowCap = 8192;               // keys of a row held in shared memory
+constexpr int kCKCap = 512;                  // selected pages listed in shared memory
+constexpr int kCSmemMax = 227 * 1024;
+constexpr int kCTrace = 16;
+
+struct CUnit {
+  int r, g, lo, P;       // request, KV head, first table entry, scored pages
+  int L, nsel, app, tp;  // valid tokens, selected pages, appends (1/0), table pages
+};
+
+template <typename T, int D, int S, int G, bool F8>
+struct CShape {
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int ESS = F8 ? 1 : ES;           // summary element bytes
+  static constexpr int RB = D * ESS;                // one summary row (m or M)
+  static constexpr int SUMB = 2 * RB;               // summary of one (page, head)
+  static constexpr int BLK = S * D * ES;            // K (or V) block of one (page, head)
+  static constexpr int HALF = BLK < 4096 ? BLK : 4096;   // a K (or V) sub-block
+  static constexpr int NSB = BLK / HALF;            // sub-blocks per block
+  static constexpr int TB = HALF / (D * ES);        // tokens per sub-block
+  static constexpr int SLOT = 2 * HALF;             // a warp's buffer: K | V, or two chunks
+  using W = WarpAttn<T, D, TB, G>;                  // one sub-block = one attention tile
+  static constexpr int CHUNK = HALF / SUMB < 32 ? HALF / SUMB : 32;   // pages per scoring chunk
+  static constexpr int CPI = 512 / SUMB > 0 ? 512 / SUMB : 1;        // pages per warp copy
+  static constexpr int NCPY = CHUNK * SUMB / 512;   // warp copies (16 B per lane) per chunk
+  static constexpr int LPP = RB / 16 < 8 ? RB / 16 : 8;   // lanes per page when scoring
+  static constexpr int VPL = RB / (16 * LPP);       // 16-byte vectors of m per lane
+  static constexpr int PPR = 32 / LPP;              // pages per round
+  static constexpr int NR = CHUNK / PPR;            // rounds per chunk
+  static constexpr int VECS = 16 / ESS;             // summary elements per vector
+  static constexpr int NV = NR * G;                 // partial bounds per lane
+  static constexpr int LGN = W::NV > CHUNK * G ? W::NV : CHUNK * G;
+  static_assert(CHUNK % PPR == 0 && LPP * VPL * 16 == RB && NCPY >= 1, "scoring layout");
+  static_assert(CHUNK * SUMB % 512 == 0, "a chunk is whole warp copies");
+
+  static constexpr int al(int x, int a) { return (x + a - 1) / a * a; }
+  // consumer warps: as many 2 * BLK buffers as fit, at most kCMaxCW
+  static constexpr int FIXED_EST = 2 * kCRowCap * 4 + 4 * kCKCap * 4 + 2 * kCMaxCW * G * (D + 2) * 4 +
+                                   kCL * G * (D + 2) * 4 + kCMaxU * 32 + 256 + kCMaxCW * 64 * 4 +
+                                   (int)sizeof(TopkSmem<kCMaxCW * 32 + kCSelT>) + 1024;
+  static constexpr int NCW_FIT = (kCSmemMax - FIXED_EST) / SLOT;
+  static constexpr int NCW = NCW_FIT < kCMaxCW ? NCW_FIT : kCMaxCW;
+  static_assert(NCW == kCMaxCW, "twelve consumer warps: 512 threads, a power of two for the Top-K");
+  static constexpr int NT = (NCW + kCSW) * 32;
+  static constexpr int SEL0 = NCW * 32;             // first select thread
+  using SelGrp = BarGrp<2, NCW * 32, kCSelT>;      // the select warps
+  using AllGrp = BarGrp<3, 0, NT>;                 // every warp (a cluster with one unit)
+
+  static constexpr int ROWS_OFF = 0;                                  // [2][kCRowCap] keys
+  static constexpr int SELL_OFF = ROWS_OFF + 2 * kCRowCap * 4;       // [2][kCKCap] logical ids
+  static constexpr int SELP_OFF = SELL_OFF + 2 * kCKCap * 4;         // [2][kCKCap] physical ids
+  static constexpr int STO_OFF = SELP_OFF + 2 * kCKCap * 4;          // [2][NCW][G][D]
+  static constexpr int STML_OFF = STO_OFF + 2 * NCW * G * D * 4;     // [2][NCW][G][2]
+  static constexpr int PART_OFF = STML_OFF + 2 * NCW * G * 2 * 4;    // [kCL][G][D]
+  static constexpr int PARTML_OFF = PART_OFF + kCL * G * D * 4;      // [kCL][G][2]
+  static constexpr int UNITS_OFF = PARTML_OFF + kCL * G * 2 * 4;     // [kCMaxU] CUnit
+  static constexpr int ORDER_OFF = UNITS_OFF + kCMaxU * (int)sizeof(CUnit);   // [64] requests
+  static constexpr int LG_OFF = ORDER_OFF + 64 * 4;                  // [NCW][LGN]
+  static constexpr int TOPK_OFF = al(LG_OFF + NCW * LGN * 4, 16);
+  static constexpr int BAR_OFF = al(TOPK_OFF + (int)sizeof(TopkSmem<NT>), 8);
+  // kv[NCW][2] (K and V halves of each consumer's buffer), row_full[2],
+  // row_free[2], sel_ready[2], attn_done[2], stash_free[2], part_full
+  static constexpr int NBAR = 2 * NCW + 11;
+  static constexpr int FLAG_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int BUF_OFF = al(FLAG_OFF + 64, 128);              // [NCW][SLOT]
+  static constexpr int SMEM = BUF_OFF + NCW * SLOT;
+  static_assert(SMEM <= kCSmemMax, "shared memory");
+};
+
+// ---------------------------------------------------------------------------
+// Cluster helpers (PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cl_u32(uint32_t caddr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(caddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cl_f32(uint32_t caddr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(caddr), "f"(v) : "memory");
+}
+// arrive on an mbarrier of CTA `rank` of the cluster, releasing this
+// thread's prior writes at cluster scope
+__device__ __forceinline__ void arrive_cl(const uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+               :: "r"(cl_map(smem_u32(bar), rank)) : "memory");
+}
+__device__ __forceinline__ void arrive_local(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool try_wait_cl(const uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(1000u) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void red_cl_min(uint32_t caddr, uint32_t v) {
+  asm volatile("red.shared::cluster.min.u32 [%0], %1;" :: "r"(caddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_cl_max(uint32_t caddr, uint32_t v) {
+  asm volatile("red.shared::cluster.max.u32 [%0], %1;" :: "r"(caddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_grp() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_grp() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Whole-warp bounded wait for phase `parity` of a CTA-local mbarrier (its
+// completion may come from TMA, local or remote arrivals). Returns false if
+// the CTA is aborting or the limit runs out (then the CTA aborts and the
+// error word says so). Warp-uniform.
+__device__ __forceinline__ bool cwait_warp(const uint64_t* bar, uint32_t parity,
+                                           volatile int* abort, unsigned* err, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    const bool ok = try_wait_cl(bar, parity);
+    if (__all_sync(FULL, ok)) return true;
+    if (__any_sync(FULL, *abort != 0)) return false;
+  }
+  if ((threadIdx.x & 31) == 0) {
+    *abort = 1;
+    report(err, QUEST_DEVERR_WAIT_TIMEOUT);
+  }
+  __syncwarp();
+  return false;
+}
+// Single-thread form of the same wait.
+__device__ __forceinline__ bool cwait_one(const uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned* err, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (try_wait_cl(bar, parity)) return true;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  report(err, QUEST_DEVERR_WAIT_TIMEOUT);
+  return false;
+}
+
+// Sums N per-lane values over aligned groups of 2*O lanes, halving the
+// values each step (transposed butterfly); afterwards a lane holds values
+// [sub_base(lane), sub_base(lane) + max(1, N / (2*O))).
+template <int N, int O>
+__device__ __forceinline__ void sub_reduce(float* v, int lane) {
+  if constexpr (O >= 1) {
+    if constexpr (N >= 2) {
+      tr_step<N>(v, lane, O);
+      sub_reduce<N / 2, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(FULL, v[0], O);
+      sub_reduce<1, O / 2>(v, lane);
+    }
+  }
+}
+template <int N, int O>
+__device__ __forceinline__ int sub_base(int lane) {
+  if constexpr (O >= 1 && N >= 2) return ((lane & O) ? N / 2 : 0) + sub_base<N / 2, O / 2>(lane);
+  else return 0;
+}
+
+template <typename T, int D, int S, int G, bool F8>
+__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(CShape<T, D, S, G, F8>::NT, 1)
+cstep_kernel(const StepArgs a) {
+  static_assert(!F8 || sizeof(T) == 2, "E4M3 summaries take fp16 keys");
+  using Sh = CShape<T, D, S, G, F8>;
+  using W = typename Sh::W;
+  using KO = KeyOps<T>;
+  using SelGrp = typename Sh::SelGrp;
+  constexpr int NCW = Sh::NCW, NT = Sh::NT;
+  constexpr int CHUNK = Sh::CHUNK, LPP = Sh::LPP, VPL = Sh::VPL, PPR = Sh::PPR, NR = Sh::NR;
+  constexpr int VECS = Sh::VECS, SLOT = Sh::SLOT, SUMB = Sh::SUMB, RB = Sh::RB, BLK = Sh::BLK;
+  constexpr int NCPY = Sh::NCPY, HALF = Sh::HALF;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cl_rank();
+  const int cid = (int)(blockIdx.x / kCL), ncl = (int)(gridDim.x / kCL);
+  const int h_q = a.h_kv * G;
+  const int K = a.k;
+  const uint32_t lim = a.wait_limit;
+
+  uint32_t* rows = reinterpret_cast<uint32_t*>(smem + Sh::ROWS_OFF);
+  int32_t* sell = reinterpret_cast<int32_t*>(smem + Sh::SELL_OFF);
+  int32_t* selp = reinterpret_cast<int32_t*>(smem + Sh::SELP_OFF);
+  float* sto = reinterpret_cast<float*>(smem + Sh::STO_OFF);
+  float* stml = reinterpret_cast<float*>(smem + Sh::STML_OFF);
+  float* part = reinterpret_cast<float*>(smem + Sh::PART_OFF);
+  float* partml = reinterpret_cast<float*>(smem + Sh::PARTML_OFF);
+  CUnit* units = reinterpret_cast<CUnit*>(smem + Sh::UNITS_OFF);
+  int32_t* order = reinterpret_cast<int32_t*>(smem + Sh::ORDER_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::BAR_OFF);
+  uint64_t* kvb = bars;                        // [NCW][2] K and V halves of each consumer
+  uint64_t* row_full = bars + 2 * NCW;         // [2] every CTA's keys of the unit delivered
+  uint64_t* row_free = row_full + 2;           // [2] every CTA done reading the row
+  uint64_t* sel_ready = row_full + 4;          // [2] this CTA's selection published
+  uint64_t* attn_done = row_full + 6;          // [2] consumer states of the unit stashed
+  uint64_t* stash_free = row_full + 8;         // [2] stash merged
+  uint64_t* part_full = row_full + 10;         // partials of an owned unit delivered
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Sh::FLAG_OFF);
+  volatile int* s_n = s_abort + 1;             // units of this cluster
+  volatile int* s_ok = s_abort + 2;            // select group's wait result
+  volatile int* s_ok_all = s_abort + 3;        // the all-warp group's wait result
+  uint32_t* kmm = reinterpret_cast<uint32_t*>(smem + Sh::FLAG_OFF) + 4;   // [2][2] key min, max
+  unsigned char* bufs = smem + Sh::BUF_OFF;
+
+  unsigned long long* trace = a.trace ? a.trace + (size_t)blockIdx.x * kCTrace : nullptr;
+  auto stamp = [&](int i) { if (trace) trace[i] = global_ns(); };
+  if (tid == 0) stamp(0);
+
+  if (tid == 0) {
+    for (int w = 0; w < NCW; ++w) { mbar_init(kvb + 2 * w, 1); mbar_init(kvb + 2 * w + 1, 1); }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(row_full + b, kCL * NCW);
+      mbar_init(row_free + b, kCL);
+      mbar_init(sel_ready + b, 1);
+      mbar_init(attn_done + b, NCW);
+      mbar_init(stash_free + b, 1);
+    }
+    mbar_init(part_full, kCL);
+    *s_abort = 0;
+    for (int b = 0; b < 2; ++b) { kmm[2 * b] = 0xffffffffu; kmm[2 * b + 1] = 0u; }
+    fence_mbar_init();
+  }
+  // the next kernel on the stream may be scheduled now; this grid waits for
+  // the previous one (and its writes) before touching global memory
+  pdl_launch_dependents();
+  cluster_sync_all();                          // barriers of every CTA initialised
+  pdl_wait();
+
+  // ---------------------- unit list (first select warp) ----------------------
+  if (warp == NCW) {
+    const int B = a.batch, H = a.h_kv, U = B * H;
+    // requests by decreasing length (ties to the lower index), for B <= 64;
+    // longer batches keep their order
+    const bool sorted = U > ncl && B <= 64;
+    if (sorted) {
+      int Pl[2];
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        Pl[h] = r < B ? (__ldg(a.seq_lens + r) + S - 1) / S : -1;
+      }
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        int rk = 0;
+        for (int x = 0; x < B; ++x) {
+          const int px = __shfl_sync(FULL, Pl[x >> 5], x & 31);
+          rk += (px > Pl[h]) || (px == Pl[h] && x < r);
+        }
+        if (r < B) order[rk] = r;
+      }
+      __syncwarp();
+    }
+    // snake over the clusters: pass p gives cluster c the unit p*ncl + c
+    // (even p) or p*ncl + ncl-1-c (odd p)
+    int n = 0;
+    if (U <= ncl) {
+      n = cid < U ? 1 : 0;
+    } else {
+      for (int p = 0; p * ncl < U; ++p)
+        if (p * ncl + ((p & 1) ? ncl - 1 - cid : cid) < U) ++n;
+    }
+    if (n > kCMaxU) {                        // the host keeps units per cluster within the cap
+      n = kCMaxU;
+      if (lane == 0) report(a.err, QUEST_DEVERR_TABLE_RANGE);
+    }
+    for (int i = lane; i < n; i += 32) {
+      int k = cid;
+      if (U > ncl) {                         // the i-th unit of this cluster in pass order
+        int cnt = -1;
+        for (int p = 0; p * ncl < U; ++p) {
+          const int kk = p * ncl + ((p & 1) ? ncl - 1 - cid : cid);
+          if (kk < U && ++cnt == i) { k = kk; break; }
+        }
+      }
+      const int r = sorted ? order[k / H] : k / H, g = k % H;
+      CUnit un;
+      un.r = r; un.g = g;
+      un.lo = __ldg(a.page_indptr + r);
+      un.tp = __ldg(a.page_indptr + r + 1) - un.lo;
+      un.L = __ldg(a.seq_lens + r);
+      int P = (un.L + S - 1) / S;
+      un.app = (a.k_new != nullptr && P >= 1 && P <= un.tp) ? 1 : 0;
+      if (P > un.tp) {
+        report(a.err, QUEST_DEVERR_TABLE_RANGE);
+        P = un.tp;
+      }
+      un.P = P;
+      un.nsel = P < K ? P : K;
+      units[i] = un;
+    }
+    if (lane == 0) *s_n = n;
+    __syncwarp();
+  }
+  asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory");
+  const int n = *s_n;
+
+
+  // this CTA's chunks of the unit's pages (CTA r takes chunks
+  // [nch r / kCL, nch (r+1) / kCL)) and its share of the selection (winner
+  // w belongs to CTA w % kCL)
+  auto c_lo = [&](const CUnit& un, int r) {
+    return (int)((long long)((un.P + CHUNK - 1) / CHUNK) * r / kCL);
+  };
+  auto n_at = [&](const CUnit& un) {
+    return un.nsel > (int)rank ? (un.nsel - (int)rank + kCL - 1) / kCL : 0;
+  };
+
+  // A cluster with a single unit has nothing to stream while it selects:
+  // then every warp of the CTA runs the select (AllGrp), else the select
+  // warps do (SelGrp) while the consumers stream the next unit.
+  const bool all_hands = n == 1;
+
+  // T(u) on thread group Grp: wait for every CTA's keys of unit u, Top-K,
+  // the selected pages' physical ids. Returns false if the CTA aborts.
+  auto select_core = [&](auto grp, int u) -> bool {
+    using Grp = decltype(grp);
+    constexpr int NTH = Grp::kN;
+    const int gt = Grp::tid(), gw = gt >> 5;
+    TopkSmem<NTH>& tsm = *reinterpret_cast<TopkSmem<NTH>*>(smem + Sh::TOPK_OFF);
+    volatile int* okf = NTH == kCSelT ? s_ok : s_ok_all;
+    const int b = u & 1;
+    const CUnit un = units[u];
+    if (gt == 0) *okf = cwait_one(row_full + b, (u >> 1) & 1, s_abort, a.err, lim) ? 1 : 0;
+    Grp::sync();
+    if (!*okf) return false;
+    if (u == 0 && gt == 0) stamp(5);
+    const int P = un.P, nsel = un.nsel;
+    const bool owner = (int)rank == u % kCL;
+    const bool listed = nsel <= kCKCap;
+    int32_t* ol = a.sel_logical + ((size_t)un.r * a.h_kv + un.g) * K;
+    int32_t* sl = sell + b * kCKCap;
+    int32_t* sp = selp + b * kCKCap;
+    const int f_lo = min(a.n_sink, P), f_hi = max(f_lo, P - a.n_local);
+    auto forced = [f_lo, f_hi](int i) { return i < f_lo || i >= f_hi; };
+    auto emit = [&](int pos, int i) {   // (the owner writes the outputs afterwards)
+      if (listed) sl[pos] = i;
+      else ol[pos] = i;
+    };
+    uint32_t* keys = rows + b * kCRowCap;
+    if (P <= kCRowCap && P <= 32 * NTH) {
+      // min and max of the competing keys, folded in by the consumers
+      const uint32_t kmin = kmm[2 * b], kmax = kmm[2 * b + 1];
+      (void)gw;
+      block_topk_smem<NTH, decltype(emit), decltype(forced), Grp>(P, K, keys, kmin, kmax, tsm, emit,
+                                                                  forced, f_lo + (P - f_hi));
+    } else if (P <= kCRowCap) {
+      auto key_at = [keys, forced](int i) { return forced(i) ? 0xffffffffu : keys[i]; };
+      block_topk_keys<NTH, decltype(key_at), decltype(emit), Grp>(P, K, key_at, tsm, emit);
+    } else {                                      // keys of long rows from the scores in L2
+      const float* sc = a.scores + (size_t)un.g * a.nnz + un.lo;
+      auto key_at = [sc, forced](int i) { return forced(i) ? 0xffffffffu : score_key(__ldcg(sc + i)); };
+      block_topk_keys<NTH, decltype(key_at), decltype(emit), Grp>(P, K, key_at, tsm, emit);
+    }
+    Grp::sync();
+    if (u == 0 && gt == 0) stamp(10);
+    if (listed && P > K) {                        // physical pages of the listed selection
+      for (int pos = gt; pos < nsel; pos += NTH) {
+        const int lp = sl[pos];
+        sp[pos] = (lp >= 0 && lp < P) ? __ldg(a.page_indices + un.lo + lp) : -1;
+      }
+      Grp::sync();
+    }
+    if (u == 0 && gt == 0) stamp(11);
+    return true;
+  };
+
+  if (warp < NCW) {
+    // ================================ consumers ================================
+    // Warp cw takes the CTA's chunks and pages cw, cw + NCW, ...: it loads
+    // them itself into its own buffer (two chunks in flight, or the K and V
+    // halves of a page) and folds them in.
+    const int cw = warp;
+    float* lg = reinterpret_cast<float*>(smem + Sh::LG_OFF) + cw * Sh::LGN;
+    unsigned char* buf = bufs + (size_t)cw * SLOT;
+    uint64_t* kbar = kvb + 2 * cw;
+    uint64_t* vbar = kbar + 1;
+    uint32_t kph = 0, vph = 0;               // completed phases of kbar, vbar
+    bool kpend = false, vpend = false;       // a copy issued and not yet waited for
+    const uint64_t pol = evict_first_policy();
+    const int pg = lane / LPP, sub = lane % LPP;
+    bool dead = false;
+    for (int t = 0; t <= n && !dead; ++t) {
+      if (t < n) {
+        // ------------------------------ S(t) ------------------------------
+        const CUnit un = units[t];
+        const int b = t & 1;
+        // my chunks: a contiguous run [mc0, mc0 + nm) of the CTA's chunks
+        const int cc0 = c_lo(un, (int)rank), ncc = c_lo(un, (int)rank + 1) - cc0;
+        const int mc0 = cc0 + ncc * cw / NCW;
+        const int nm = cc0 + ncc * (cw + 1) / NCW - mc0;
+        // query of the unit for the bound: per 32-bit word a select mask
+        // (take M where q >= 0) and the values as fp32
+        constexpr int QW = VPL * (F8 ? 8 : 4);
+        constexpr int QV = F8 ? VPL * 16 : (Sh::ES == 2 ? QW * 2 : QW);
+        uint32_t qmask[G][QW];
+        float qf[G][QV];
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+          const T* qp = static_cast<const T*>(a.q) + ((size_t)un.r * h_q + (size_t)un.g * G + gi) * D;
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) {
+            const int d0 = (v * LPP + sub) * VECS;
+#pragma unroll
+            for (int h = 0; h < (F8 ? 2 : 1); ++h) {
+              const uint4 qv = ld_nc_v4(qp + d0 + h * 8);
+              const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int wi = (v * (F8 ? 2 : 1) + h) * 4 + j;
+                if constexpr (Sh::ES == 2) {
+                  qmask[gi][wi] = ((~w4[j] & 0x80008000u) >> 15) * 0xffffu;
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
+                  qf[gi][wi * 2] = f.x;
+                  qf[gi][wi * 2 + 1] = f.y;
+                } else {
+                  qmask[gi][wi] = (w4[j] & 0x80000000u) ? 0u : 0xffffffffu;
+                  qf[gi][wi] = __uint_as_float(w4[j]);
+                }
+              }
+            }
+          }
+        }
+        // the appended token: its key dims of this lane, if this warp scores
+        // the tail page
+        const int ct = (un.P - 1) / CHUNK;                  // chunk of the tail page
+        const int pin = (un.P - 1) - ct * CHUNK;
+        const int m_tail = ct - mc0;
+        const bool tail_mine = un.app && m_tail >= 0 && m_tail < nm && pg == pin % PPR;
+        const int ro_t = pin / PPR;
+        constexpr int KNV = F8 ? 2 * VPL : VPL;             // 16-byte vectors of k per lane
+        uint4 kn[KNV];
+        if (tail_mine) {
+          const T* kp = static_cast<const T*>(a.k_new) + ((size_t)un.r * a.h_kv + un.g) * D;
+#pragma unroll
+          for (int v = 0; v < VPL; ++v)
+#pragma unroll
+            for (int h = 0; h < (F8 ? 2 : 1); ++h)
+              kn[v * (F8 ? 2 : 1) + h] = ld_nc_v4(kp + (v * LPP + sub) * VECS + h * 8);
+        }
+        // keys of unit t go to row buffer b of every CTA: it must be free
+        if (t >= 2 && !cwait_warp(row_free + b, ((t >> 1) - 1) & 1, s_abort, a.err, lim)) {
+          dead = true;
+          break;
+        }
+        const bool cached = un.P <= kCRowCap;
+        const int f_lo = min(a.n_sink, un.P), f_hi = max(f_lo, un.P - a.n_local);
+        uint32_t kmn = 0xffffffffu, kmx = 0u;        // over my competing pages' keys
+        // the physical pages of my run, 64 table entries per window (two per
+        // lane): the current window and the next one are held in registers
+        const int pb = mc0 * CHUNK, pe = min(un.P, (mc0 + nm) * CHUNK);
+        const int32_t* idx = a.page_indices + un.lo;
+        auto ldwin = [&](int k, int& w0, int& w1) {
+          const int p = pb + 64 * k + lane;
+          w0 = p < pe ? __ldg(idx + p) : -1;
+          w1 = p + 32 < pe ? __ldg(idx + p + 32) : -1;
+        };
+        int cw0, cw1, nw0, nw1, kcur = 0;
+        ldwin(0, cw0, cw1);
+        ldwin(1, nw0, nw1);
+        // lane j < CHUNK: physical page of page j of my chunk m (a chunk lies
+        // in one half of one window), -1 past the row
+        auto tbl = [&](int m) -> int {
+          if (m >= nm) return -1;
+          const int o = m * CHUNK, k = o >> 6, h = (o >> 5) & 1;
+          const int src = k == kcur ? (h ? cw1 : cw0) : (h ? nw1 : nw0);
+          const int v = __shfl_sync(FULL, src, (o & 31) + (lane & (CHUNK - 1)));
+          return lane < CHUNK ? v : -1;
+        };
+        // 16 bytes per lane per copy: copy k holds bytes [512k, 512k + 512) of the chunk
+        auto issue = [&](int m, int ph) {
+          if (m < nm) {
+            unsigned char* dst = buf + (m & 1) * HALF;
+#pragma unroll
+            for (int k = 0; k < NCPY; ++k) {
+              const int byte = k * 512 + lane * 16;
+              const int j = byte / SUMB;
+              const int phj = __shfl_sync(FULL, ph, j);
+              if (phj >= 0 && phj < a.n_phys)
+                cp_async16(dst + byte, static_cast<const unsigned char*>(a.summary) +
+                                           ((size_t)phj * a.h_kv + un.g) * SUMB + byte % SUMB);
+            }
+          }
+          cp_async_commit_grp();
+        };
+        issue(0, tbl(0));
+        for (int m = 0; m < nm; ++m) {
+          if (((m + 1) * CHUNK) >> 6 > kcur + 1) {      // chunk m + 1 is past the next window
+            ++kcur;
+            cw0 = nw0; cw1 = nw1;
+            ldwin(kcur + 1, nw0, nw1);
+          }
+          issue(m + 1, tbl(m + 1));          // the next chunk streams while this one is scored
+          const int phm = tbl(m);
+          cp_async_wait_grp<1>();
+          __syncwarp();
+          const int p0 = (mc0 + m) * CHUNK;
+          const int np = min(CHUNK, un.P - p0);
+          const unsigned bad = __ballot_sync(FULL, lane < np && !(phm >= 0 && phm < a.n_phys));
+          if (bad && lane == 0) report(a.err, QUEST_DEVERR_PAGE_RANGE);
+          const unsigned char* sb = buf + (m & 1) * HALF;
+          float vals[Sh::NV];
+#pragma unroll
+          for (int ro = 0; ro < NR; ++ro) {
+            const int p = ro * PPR + pg;
+            uint4 vm[VPL], vM[VPL];
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+              vm[v] = *reinterpret_cast<const uint4*>(sb + p * SUMB + (v * LPP + sub) * 16);
+              vM[v] = *reinterpret_cast<const uint4*>(sb + p * SUMB + RB + (v * LPP + sub) * 16);
+            }
+            if (tail_mine && ro == ro_t && m == m_tail) {
+              // append (eq (8)): the new token's K/V into the pool, the summary
+              // of its page folded with the key (a fresh page starts from it)
+              const int slot = (un.L - 1) % S;
+              const int pp = __ldg(a.page_indices + un.lo + un.P - 1);
+              if (pp >= 0 && pp < a.n_phys) {
+                const T* vp = static_cast<const T*>(a.v_new) + ((size_t)un.r * a.h_kv + un.g) * D;
+                T* kd = static_cast<T*>(a.k_pool) + (((size_t)pp * a.h_kv + un.g) * S + slot) * D;
+                T* vd = static_cast<T*>(a.v_pool) + (((size_t)pp * a.h_kv + un.g) * S + slot) * D;
+                bool ovf = false;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) {
+                  const int d0 = (v * LPP + sub) * VECS;
+#pragma unroll
+                  for (int h = 0; h < (F8 ? 2 : 1); ++h) {
+                    st_v4(kd + d0 + h * 8, kn[v * (F8 ? 2 : 1) + h]);
+                    st_v4(vd + d0 + h * 8, ld_nc_v4(vp + d0 + h * 8));
+                  }
+                  if constexpr (F8) {
+                    // the old codes decode exactly to fp16; fold the key in,
+                    // round out again (min down, max up)
+                    const uint32_t om[4] = {vm[v].x, vm[v].y, vm[v].z, vm[v].w};
+                    const uint32_t oM[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
+                    const uint32_t kw[8] = {kn[2 * v].x, kn[2 * v].y, kn[2 * v].z, kn[2 * v].w,
+                                            kn[2 * v + 1].x, kn[2 * v + 1].y, kn[2 * v + 1].z,
+                                            kn[2 * v + 1].w};
+                    uint32_t c8m[4], c8M[4];
+#pragma unroll
+                    for (int cw4 = 0; cw4 < 4; ++cw4) {
+                      uint32_t m01 = KO::to_key(kw[2 * cw4]), m23 = KO::to_key(kw[2 * cw4 + 1]);
+                      uint32_t M01 = m01, M23 = m23;
+                      if (slot != 0) {
+                        m01 = KO::kmin(KO::to_key(e4m3x4_lo_h2(om[cw4])), m01);
+                        m23 = KO::kmin(KO::to_key(e4m3x4_hi_h2(om[cw4])), m23);
+                        M01 = KO::kmax(KO::to_key(e4m3x4_lo_h2(oM[cw4])), M01);
+                        M23 = KO::kmax(KO::to_key(e4m3x4_hi_h2(oM[cw4])), M23);
+                      }
+                      c8m[cw4] = e4m3x4_floor_h(KO::from_key(m01), KO::from_key(m23), ovf);
+                      c8M[cw4] = e4m3x4_ceil_h(KO::from_key(M01), KO::from_key(M23), ovf);
+                    }
+                    vm[v] = make_uint4(c8m[0], c8m[1], c8m[2], c8m[3]);
+                    vM[v] = make_uint4(c8M[0], c8M[1], c8M[2], c8M[3]);
+                  } else {
+                    const uint4 k4 = kn[v];
+                    uint4 mn, mx;
+                    if (slot == 0) {
+                      mn = make_uint4(KO::to_key(k4.x), KO::to_key(k4.y), KO::to_key(k4.z), KO::to_key(k4.w));
+                      mx = mn;
+                    } else {
+                      mn = make_uint4(KO::kmin(KO::to_key(vm[v].x), KO::to_key(k4.x)),
+                                      KO::kmin(KO::to_key(vm[v].y), KO::to_key(k4.y)),
+                                      KO::kmin(KO::to_key(vm[v].z), KO::to_key(k4.z)),
+                                      KO::kmin(KO::to_key(vm[v].w), KO::to_key(k4.w)));
+                      mx = make_uint4(KO::kmax(KO::to_key(vM[v].x), KO::to_key(k4.x)),
+                                      KO::kmax(KO::to_key(vM[v].y), KO::to_key(k4.y)),
+                                      KO::kmax(KO::to_key(vM[v].z), KO::to_key(k4.z)),
+                                      KO::kmax(KO::to_key(vM[v].w), KO::to_key(k4.w)));
+                    }
+                    vm[v] = make_uint4(KO::from_key(mn.x), KO::from_key(mn.y), KO::from_key(mn.z), KO::from_key(mn.w));
+                    vM[v] = make_uint4(KO::from_key(mx.x), KO::from_key(mx.y), KO::from_key(mx.z), KO::from_key(mx.w));
+                  }
+                  unsigned char* sp = static_cast<unsigned char*>(a.summary) +
+                                      ((size_t)pp * a.h_kv + un.g) * SUMB + (v * LPP + sub) * 16;
+                  st_v4(sp, vm[v]);
+                  st_v4(sp + RB, vM[v]);
+                }
+                if (F8 && ovf) report(a.err, QUEST_DEVERR_FP8_RANGE);
+              }
+            }
+            // sum_j max(q_j m_j, q_j M_j) = sum_j q_j * (q_j >= 0 ? M_j : m_j)
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+              float sg = 0.f;
+#pragma unroll
+              for (int v = 0; v < VPL; ++v) {
+                const uint32_t mw[4] = {vm[v].x, vm[v].y, vm[v].z, vm[v].w};
+                const uint32_t Mw[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  if constexpr (F8) {              // codes decoded to fp16 (exact), fp32 FMA
+                    const int wi = v * 8 + 2 * j;
+                    const uint32_t sel = e4m3_qsel_from_masks(qmask[gi][wi], qmask[gi][wi + 1]);
+                    const uint32_t xw = (Mw[j] & sel) | (mw[j] & ~sel);
+                    const float2 lo = e4m3x4_lo_f2(xw), hi = e4m3x4_hi_f2(xw);
+                    sg = fmaf(qf[gi][wi * 2 + 0], lo.x, sg);
+                    sg = fmaf(qf[gi][wi * 2 + 1], lo.y, sg);
+                    sg = fmaf(qf[gi][wi * 2 + 2], hi.x, sg);
+                    sg = fmaf(qf[gi][wi * 2 + 3], hi.y, sg);
+                  } else if constexpr (Sh::ES == 2) {
+                    const uint32_t mk = qmask[gi][v * 4 + j];
+                    const uint32_t xw = (Mw[j] & mk) | (mw[j] & ~mk);
+                    const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xw));
+                    sg = fmaf(qf[gi][(v * 4 + j) * 2 + 0], xf.x, sg);
+                    sg = fmaf(qf[gi][(v * 4 + j) * 2 + 1], xf.y, sg);
+                  } else {
+                    const uint32_t mk = qmask[gi][v * 4 + j];
+                    const uint32_t xw = (Mw[j] & mk) | (mw[j] & ~mk);
+                    sg = fmaf(qf[gi][v * 4 + j], __uint_as_float(xw), sg);
+                  }
+                }
+              }
+              vals[gi * NR + ro] = sg;
+            }
+          }
+          // sums over the LPP lanes of each page, then the group max
+          sub_reduce<Sh::NV, LPP / 2>(vals, lane);
+          {
+            constexpr int NF = Sh::NV / LPP > 1 ? Sh::NV / LPP : 1;
+            const int base = sub_base<Sh::NV, LPP / 2>(lane);
+#pragma unroll
+            for (int i = 0; i < NF; ++i) lg[(base + i) * PPR + pg] = vals[i];
+          }
+          __syncwarp();
+          if (lane < np) {
+            float sc = -INFINITY;
+            if (!((bad >> lane) & 1u)) {
+              sc = lg[lane];
+#pragma unroll
+              for (int gi = 1; gi < G; ++gi) sc = fmaxf(sc, lg[gi * NR * PPR + lane]);
+            }
+            if (cached) {
+              const uint32_t key = score_key(sc);
+              const uint32_t ra = smem_u32(rows + b * kCRowCap + p0 + lane);
+#pragma unroll
+              for (int c = 0; c < kCL; ++c) st_cl_u32(cl_map(ra, c), key);
+              if (p0 + lane >= f_lo && p0 + lane < f_hi) {
+                kmn = min(kmn, key);
+                kmx = max(kmx, key);
+              }
+            } else {                         // long rows: the select reads the scores
+              a.scores[(size_t)un.g * a.nnz + un.lo + p0 + lane] = sc;
+            }
+          }
+          __syncwarp();                      // buffer half (m & 1) may be refilled
+        }
+        cp_async_wait_grp<0>();
+        kmn = warp_min_u32(kmn);
+        kmx = warp_max_u32(kmx);
+        if (lane < kCL && cached && nm > 0) {   // into every CTA's min and max of row b
+          red_cl_min(cl_map(smem_u32(kmm + 2 * b), lane), kmn);
+          red_cl_max(cl_map(smem_u32(kmm + 2 * b + 1), lane), kmx);
+        }
+        // this warp's keys (and appended rows) of unit t are out: tell every
+        // CTA (the lanes' stores are ordered before the release by the warp
+        // barrier)
+        __syncwarp();
+        if (lane < kCL) arrive_cl(row_full + b, lane);
+        if (cached) {
+          // the scores output, from the keys (after the release, which then
+          // does not wait for these stores; row b holds them until the
+          // select of unit t has released it)
+          float* so = a.scores + (size_t)un.g * a.nnz + un.lo;
+          for (int p = pb + lane; p < pe; p += 32) so[p] = __uint_as_float(key_to_f32(rows[b * kCRowCap + p]));
+        }
+      }
+      if (t >= 1) {
+        // ------------------------------ A(t-1) ------------------------------
+        const int u = t - 1, b = u & 1;
+        const CUnit un = units[u];
+        const int nal = n_at(un);
+        const int na = nal > cw ? (nal - cw + NCW - 1) / NCW : 0;   // my pages
+        W st;
+        st.init(static_cast<const T*>(a.q) + ((size_t)un.r * h_q + (size_t)un.g * G) * D,
+                a.scale_log2, lane);
+        if (all_hands) {
+          if (!select_core(typename Sh::AllGrp{}, u)) { dead = true; break; }
+        } else if (!cwait_warp(sel_ready + b, (u >> 1) & 1, s_abort, a.err, lim)) {
+          dead = true;
+          break;
+        }
+        const bool ident = un.P <= K;        // every page is selected, in page order
+        const bool listed = un.nsel <= kCKCap;
+        const int32_t* gl = a.sel_logical + ((size_t)un.r * a.h_kv + un.g) * K;
+        // the appended rows were acquired through sel_ready: order them
+        // before the bulk copies that read the pool
+        if (lane == 0 && na > 0) fence_proxy_async_global();
+        __syncwarp();
+        for (int i0 = 0; i0 < na && !dead; i0 += 32) {
+          const int i = i0 + lane;
+          int lp = -1, ph = -1;
+          if (i < na) {
+            const int wi = (int)rank + kCL * (cw + NCW * i);    // place in the selection
+            if (ident) lp = wi;
+            else lp = listed ? sell[b * kCKCap + wi] : __ldcg(gl + wi);
+            if (lp >= 0 && lp < un.P) ph = (listed && !ident) ? selp[b * kCKCap + wi]
+                                                               : __ldg(a.page_indices + un.lo + lp);
+          }
+          const int valid = (lp >= 0 && lp < un.P) ? min(S, un.L - lp * S) : 0;
+          const bool ok = i < na && valid > 0 && ph >= 0 && ph < a.n_phys;
+          if (i < na && !ok) {
+            if (lp < 0 || lp >= un.P) report(a.err, QUEST_DEVERR_TABLE_RANGE);
+            else if (valid <= 0) report(a.err, QUEST_DEVERR_EMPTY_PAGE);
+            else report(a.err, QUEST_DEVERR_PAGE_RANGE);
+          }
+          // items: (page li, sub-block sb) with valid tokens, in order; each
+          // is one attention tile of up to TB tokens
+          unsigned rem = __ballot_sync(FULL, ok);
+          int li = rem ? __ffs(rem) - 1 : -1, sb = 0;
+          auto next_item = [&](int& l, int& s) {   // the item after (l, s), l = -1 at the end
+            const int vl = __shfl_sync(FULL, valid, l);
+            if (s + 1 < Sh::NSB && (s + 1) * Sh::TB < vl) { ++s; return; }
+            const unsigned r = rem & ~((2u << l) - 1u);
+            l = r ? __ffs(r) - 1 : -1;
+            s = 0;
+          };
+          auto issue_half = [&](int l, int s, int half) {   // K (half 0) or V (half 1) of an item
+            const int pk = __shfl_sync(FULL, ph, l);
+            if (lane == 0) {
+              uint64_t* bar = half ? vbar : kbar;
+              mbar_arrive_tx(bar, HALF);
+              bulk_g2s_hint(buf + half * HALF,
+                            static_cast<const unsigned char*>(half ? a.v_pool : a.k_pool) +
+                                ((size_t)pk * a.h_kv + un.g) * BLK + (size_t)s * HALF,
+                            HALF, bar, pol);
+            }
+            if (half) vpend = true; else kpend = true;
+          };
+          if (li >= 0) {
+            issue_half(li, 0, 0);
+            issue_half(li, 0, 1);
+          }
+          while (li >= 0) {
+            const int vk = min(Sh::TB, __shfl_sync(FULL, valid, li) - sb * Sh::TB);
+            int l1 = li, s1 = sb;
+            next_item(l1, s1);
+            if (!cwait_warp(kbar, kph & 1, s_abort, a.err, lim)) { dead = true; break; }
+            ++kph;
+            kpend = false;
+            st.qk(reinterpret_cast<const T*>(buf), vk, lg, lane);
+            if (l1 >= 0) issue_half(l1, s1, 0);          // the next K while this V is folded
+            if (!cwait_warp(vbar, vph & 1, s_abort, a.err, lim)) { dead = true; break; }
+            ++vph;
+            vpend = false;
+            st.av(reinterpret_cast<const T*>(buf + HALF), vk, lg, lane);
+            if (l1 >= 0) issue_half(l1, s1, 1);
+            if (u == 0 && cw == 0 && lane == 0 && i0 == 0 && vph == 1) stamp(4);
+            li = l1;
+            sb = s1;
+          }
+        }
+        if (dead) break;
+        if (u >= 2 && !cwait_warp(stash_free + b, ((u >> 1) - 1) & 1, s_abort, a.err, lim)) {
+          dead = true;
+          break;
+        }
+        st.stash(sto + (size_t)b * NCW * G * D, stml + (size_t)b * NCW * G * 2, cw, lane);
+        __syncwarp();
+        if (lane == 0) arrive_local(attn_done + b);
+      }
+    }
+    // nothing may still be copying into this warp's buffer when the CTA exits
+    cp_async_wait_grp<0>();
+    for (uint32_t i = 0; kpend && i < lim; ++i) kpend = !__all_sync(FULL, try_wait_cl(kbar, kph & 1));
+    for (uint32_t i = 0; vpend && i < lim; ++i) vpend = !__all_sync(FULL, try_wait_cl(vbar, vph & 1));
+  } else {
+    // ============================ select group ============================
+    const int gt = tid - Sh::SEL0;
+    {
+      TopkSmem<NT>& tsm = *reinterpret_cast<TopkSmem<NT>*>(smem + Sh::TOPK_OFF);
+      for (int i = gt; i < kTopkBins; i += kCSelT) tsm.hist[i] = 0;   // kept zero by the Top-K
+    }
+    SelGrp::sync();
+    bool dead = false;
+    // one thread waits, the group follows its verdict
+    auto gwait = [&](const uint64_t* bar, uint32_t parity) {
+      if (gt == 0) *s_ok = cwait_one(bar, parity, s_abort, a.err, lim) ? 1 : 0;
+      SelGrp::sync();
+      const bool ok = *s_ok != 0;
+      SelGrp::sync();
+      return ok;
+    };
+    for (int t = 0; t <= n && !dead; ++t) {
+      if (t < n) {
+        // ------------------------------ T(t) ------------------------------
+        const int u = t, b = u & 1;
+        const CUnit un = units[u];
+        const bool ok = all_hands ? select_core(typename Sh::AllGrp{}, u)
+                                  : select_core(SelGrp{}, u);
+        if (!ok) { dead = true; break; }
+        SelGrp::sync();
+        const int P = un.P, nsel = un.nsel;
+        const bool owner = (int)rank == u % kCL;
+        const bool listed = nsel <= kCKCap;
+        const size_t ug = (size_t)un.r * a.h_kv + un.g;
+        int32_t* ol = a.sel_logical + ug * K;
+        int32_t* sl = sell + b * kCKCap;
+        int32_t* sp = selp + b * kCKCap;
+        if (gt == 0) {                           // (the group's reads precede it by the barrier)
+          kmm[2 * b] = 0xffffffffu;              // ready for unit u + 2
+          kmm[2 * b + 1] = 0u;
+          arrive_local(sel_ready + b);           // the consumers may stream the pages
+#pragma unroll
+          for (int c = 0; c < kCL; ++c) arrive_cl(row_free + b, c);   // row b may be refilled
+        }
+        if (u == 0 && gt == 0) stamp(6);
+        if (owner) {                             // the call's selection outputs
+          int32_t* op = a.sel_phys + ug * K;
+          for (int pos = nsel + gt; pos < K; pos += kCSelT) { ol[pos] = -1; op[pos] = -1; }
+          if (gt == 0) a.sel_count[ug] = nsel;
+          for (int pos = gt; pos < nsel; pos += kCSelT) {
+            if (listed) ol[pos] = sl[pos];
+            if (listed && P > K) {
+              op[pos] = sp[pos];
+            } else {
+              const int lp = listed ? sl[pos] : __ldcg(ol + pos);
+              op[pos] = (lp >= 0 && lp < P) ? __ldg(a.page_indices + un.lo + lp) : -1;
+            }
+          }
+          for (int i = P + gt; i < un.tp; i += kCSelT)
+            a.scores[(size_t)un.g * a.nnz + un.lo + i] = -INFINITY;
+        }
+      }
+      if (t >= 1) {
+        // ------------------------------ M(t-1) ------------------------------
+        const int u = t - 1, b = u & 1;
+        const CUnit un = units[u];
+        const int owner = u % kCL;
+        if (!gwait(attn_done + b, (u >> 1) & 1)) { dead = true; break; }
+        const float* mo = sto + (size_t)b * NCW * G * D;
+        const float* ml = stml + (size_t)b * NCW * G * 2;
+        const uint32_t po = cl_map(smem_u32(part), owner);
+        const uint32_t pm = cl_map(smem_u32(partml), owner);
+        for (int idx = gt; idx < G * D; idx += kCSelT) {
+          const int gi = idx / D, col = idx % D;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < NCW; ++w) mx = fmaxf(mx, ml[(w * G + gi) * 2]);
+          float o = 0.f, l = 0.f;
+          if (mx != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) {
+              const float sc = exp2f(ml[(w * G + gi) * 2] - mx);
+              o = fmaf(sc, mo[(w * G + gi) * D + col], o);
+              l = fmaf(sc, ml[(w * G + gi) * 2 + 1], l);
+            }
+          }
+          st_cl_f32(po + (uint32_t)((rank * G + gi) * D + col) * 4u, o);
+          if (col == 0) {
+            st_cl_f32(pm + (uint32_t)((rank * G + gi) * 2) * 4u, mx);
+            st_cl_f32(pm + (uint32_t)((rank * G + gi) * 2 + 1) * 4u, l);
+          }
+        }
+        SelGrp::sync();                           // the group's stores precede the release
+        if (gt == 0) {
+          arrive_cl(part_full, owner);
+          arrive_local(stash_free + b);          // the consumers may stash unit u + 2
+        }
+        if ((int)rank == owner) {
+          if (!gwait(part_full, (u / kCL) & 1)) { dead = true; break; }
+          for (int idx = gt; idx < G * D; idx += kCSelT) {
+            const int gi = idx / D, col = idx % D;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kCL; ++c) mx = fmaxf(mx, partml[(c * G + gi) * 2]);
+            float o = 0.f, l = 0.f;
+            if (mx != -INFINITY) {
+#pragma unroll
+              for (int c = 0; c < kCL; ++c) {
+                const float w = exp2f(partml[(c * G + gi) * 2] - mx);
+                o = fmaf(w, part[(c * G + gi) * D + col], o);
+                l = fmaf(w, partml[(c * G + gi) * 2 + 1], l);
+              }
+            }
+            const size_t orow = (size_t)un.r * h_q + (size_t)un.g * G + gi;
+            a.out[orow * D + col] = l > 0.f ? o / l : 0.f;
+            if (col == 0 && a.lse) a.lse[orow] = l > 0.f ? (mx + log2f(l)) * LN2 : -INFINITY;
+          }
+          SelGrp::sync();                         // part read before the next owned unit
+        }
+        if (u == n - 1 && gt == 0) stamp(7);
+      }
+    }
+  }
+  // no CTA leaves while another may still write into its shared memory
+  cluster_sync_all();
+  if (tid == 0) stamp(9);
+}
+
+template <typename T, int D, int S, int G, bool F8>
+int cstep_clusters(int dev) {
+  static int cached[64] = {};
+  using Sh = CShape<T, D, S, G, F8>;
+  if (dev >= 0 && dev < 64 && cached[dev] != 0) return cached[dev];
+  int n = 0;
+  if (cudaFuncSetAttribute(cstep_kernel<T, D, S, G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Sh::SMEM) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCL * 64);
+    cfg.blockDim = dim3(Sh::NT);
+    cfg.dynamicSmemBytes = Sh::SMEM;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)cstep_kernel<T, D, S, G, F8>, &cfg) != cudaSuccess)
+      n = 0;
+  }
+  cudaGetLastError();
+  if (n <= 0) n = -1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+template <typename T, int D, int S, int G, bool F8>
+cudaError_t cstep_launch(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
+  using Sh = CShape<T, D, S, G, F8>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(Sh::NT);
+  cfg.dynamicSmemBytes = Sh::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  // the launch may overlap the previous kernel's tail (the kernel waits for
+  // it with griddepcontrol.wait before touching global memory)
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  static int pdl_ok = getenv("QUEST_NO_PDL") ? 0 : -1;   // -1 untried, 0 off, 1 on
+  cfg.numAttrs = pdl_ok == 0 ? 0 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, cstep_kernel<T, D, S, G, F8>, a);
+  if (e != cudaSuccess && cfg.numAttrs == 1 && pdl_ok == -1) {
+    cudaGetLastError();
+    pdl_ok = 0;
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, cstep_kernel<T, D, S, G, F8>, a);
+  } else if (e == cudaSuccess && cfg.numAttrs == 1) {
+    pdl_ok = 1;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <typename T, int D, bool F8>
+cudaError_t cstep_launch_sg(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
+  if (a.page_size == 16) {
+    if (a.group == 1) return cstep_launch<T, D, 16, 1, F8>(a, p, s);
+    if (a.group == 2) return cstep_launch<T, D, 16, 2, F8>(a, p, s);
+  } else {
+    if (a.group == 1) return cstep_launch<T, D, 32, 1, F8>(a, p, s);
+    if (a.group == 2) return cstep_launch<T, D, 32, 2, F8>(a, p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename T, int D, bool F8>
+int cstep_clusters_sg(int dev, int page_size, int group) {
+  if (page_size == 16) {
+    if (group == 1) return cstep_clusters<T, D, 16, 1, F8>(dev);
+    if (group == 2) return cstep_clusters<T, D, 16, 2, F8>(dev);
+  } else if (page_size == 32) {
+    if (group == 1) return cstep_clusters<T, D, 32, 1, F8>(dev);
+    if (group == 2) return cstep_clusters<T, D, 32, 2, F8>(dev);
+  }
+  return -1;
+}
+
+}  // namespace
+}  // namespace quest

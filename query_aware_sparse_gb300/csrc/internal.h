@@ -71,6 +71,8 @@ struct StepArgs {
   float scale_log2;
   unsigned long long* trace;                  // [grid, 16] phase stamps, or null
   unsigned* err;
+  uint32_t wait_limit;                        // tries of every bounded wait (cluster step)
+  int32_t test_fault;                         // 0; 1 = a slot whose copy never arrives (tests)
 };
 
 // Recall diagnostics (quest_recall_diagnostics): per query head, against
@@ -96,6 +98,7 @@ void diag_carve(DiagArgs& a, void* workspace);
 
 struct StepPlan {
   bool ok;
+  bool cluster;                               // the cluster kernel (cstep_impl.cuh)
   int32_t grid, n_chunks, chunk_pages, smem;
   size_t counters_bytes, tagged_bytes, workspace_bytes;
 };
@@ -115,6 +118,20 @@ QUEST_STEP_VARIANT(f32)
 QUEST_STEP_VARIANT(f16)
 QUEST_STEP_VARIANT(e4m3)
 #undef QUEST_STEP_VARIANT
+// The same for the cluster kernel (cstep_<variant>_d<head_dim>.cu): launch,
+// and clusters of it the current device keeps resident (<= 0: the shape is
+// not built or does not fit).
+#define QUEST_CSTEP_VARIANT(name)                                                           \
+  cudaError_t launch_cstep_##name##_d64(const StepArgs& a, const StepPlan& p, cudaStream_t s);  \
+  cudaError_t launch_cstep_##name##_d128(const StepArgs& a, const StepPlan& p, cudaStream_t s); \
+  int clusters_cstep_##name##_d64(int dev, int page_size, int group);                        \
+  int clusters_cstep_##name##_d128(int dev, int page_size, int group);
+QUEST_CSTEP_VARIANT(f32)
+QUEST_CSTEP_VARIANT(f16)
+QUEST_CSTEP_VARIANT(e4m3)
+#undef QUEST_CSTEP_VARIANT
+constexpr int32_t kCStepUnitsPerCluster = 64;   // units one cluster of the cluster kernel takes
+constexpr uint32_t kStepWaitLimit = 1u << 21;    // tries (up to ~1 us each) of a bounded wait
 
 // Split-K plan of the attention for a problem size on the current device.
 struct AttnPlan {

@@ -58,6 +58,9 @@ bool valid_group(int32_t g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
 unsigned long long* g_trace = nullptr;      // quest_set_trace buffer (device)
 int32_t g_trace_ctas = 0;
+// quest_test_step_fault: fault mode and wait limit of later decode steps
+int32_t g_test_fault = 0;
+uint32_t g_wait_limit = quest::kStepWaitLimit;
 
 quest_status launched(cudaError_t e) { return e == cudaSuccess ? QUEST_OK : QUEST_ERR_CUDA; }
 
@@ -337,6 +340,8 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   a.trace = (g_trace && plan.grid <= g_trace_ctas) ? g_trace : nullptr;
   a.err = err_ptr();
   if (!a.err) return QUEST_ERR_CUDA;
+  a.wait_limit = g_wait_limit;
+  a.test_fault = g_test_fault;
   return launched(quest::launch_step(a, plan, static_cast<cudaStream_t>(stream)));
 }
 
@@ -407,6 +412,13 @@ const char* quest_status_string(int32_t status) {
     case QUEST_ERR_CUDA: return "QUEST_ERR_CUDA: a CUDA call or kernel launch failed";
   }
   return "unknown quest_status";
+}
+
+int32_t quest_test_step_fault(int32_t mode, int32_t wait_limit) {
+  if (mode < 0 || mode > 1 || wait_limit < 0) return QUEST_ERR_INVALID_ARG;
+  g_test_fault = mode;
+  g_wait_limit = wait_limit > 0 ? (uint32_t)wait_limit : quest::kStepWaitLimit;
+  return QUEST_OK;
 }
 
 }  // extern "C"

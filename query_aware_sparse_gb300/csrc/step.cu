@@ -3,12 +3,59 @@
 // element type, summary format and head dim, so they compile in parallel).
 // Including the kernel's header instantiates nothing here: its templates
 // are only instantiated by the variant files.
+#include <cstdlib>
+
 #include "step_impl.cuh"
 
 namespace quest {
 
+namespace {
+
+// The cluster kernel (cstep_impl.cuh) for shapes it is built for: units of
+// the batch spread evenly over the clusters the device keeps resident. It
+// uses no workspace (the size returned is a token 256 bytes).
+StepPlan plan_cstep(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
+                    int32_t page_size, int32_t dtype, int32_t summary_fp8) {
+  StepPlan p{};
+  if (group > 2 || (head_dim != 64 && head_dim != 128) || (page_size != 16 && page_size != 32))
+    return p;
+  if (summary_fp8 && dtype != QUEST_F16) return p;
+  if (getenv("QUEST_STEP_LEGACY")) return p;     // the grid-wide kernel instead (comparisons)
+  int dev = 0, maxc = 32;                         // no device (sizing only): a default part
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    const bool d128 = head_dim == 128;
+    if (dtype == QUEST_F16 && summary_fp8)
+      maxc = d128 ? clusters_cstep_e4m3_d128(dev, page_size, group) : clusters_cstep_e4m3_d64(dev, page_size, group);
+    else if (dtype == QUEST_F16)
+      maxc = d128 ? clusters_cstep_f16_d128(dev, page_size, group) : clusters_cstep_f16_d64(dev, page_size, group);
+    else
+      maxc = d128 ? clusters_cstep_f32_d128(dev, page_size, group) : clusters_cstep_f32_d64(dev, page_size, group);
+  }
+  cudaGetLastError();
+  if (maxc <= 0) return p;
+  const long long units = (long long)batch * h_kv;
+  const long long per = (units + maxc - 1) / maxc;
+  if (per > kCStepUnitsPerCluster) return p;
+  long long nc = per > 0 ? (units + per - 1) / per : 1;
+  if (const char* e = getenv("QUEST_STEP_CLUSTERS")) {   // cluster count override (experiments)
+    const long long want = atoll(e);
+    if (want > 0 && want <= maxc && (units + want - 1) / want <= kCStepUnitsPerCluster) nc = want;
+  }
+  p.ok = true;
+  p.cluster = true;
+  p.grid = (int32_t)(nc * 4);
+  p.workspace_bytes = 256;
+  return p;
+}
+
+}  // namespace
+
 StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int32_t head_dim,
                    int32_t page_size, int32_t dtype, int32_t k, int32_t summary_fp8) {
+  {
+    StepPlan c = plan_cstep(batch, h_kv, group, head_dim, page_size, dtype, summary_fp8);
+    if (c.ok) return c;
+  }
   StepPlan p{};
   int smem = 0, per_sm = 0, dev = 0, sms = 148;
   const bool have_dev = cudaGetDevice(&dev) == cudaSuccess &&
@@ -63,6 +110,12 @@ StepPlan plan_step(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group, int3
 
 cudaError_t launch_step(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
   const bool d128 = a.head_dim == 128;
+  if (p.cluster) {
+    if (a.dtype == QUEST_F16 && a.summary_fp8)
+      return d128 ? launch_cstep_e4m3_d128(a, p, s) : launch_cstep_e4m3_d64(a, p, s);
+    if (a.dtype == QUEST_F16) return d128 ? launch_cstep_f16_d128(a, p, s) : launch_cstep_f16_d64(a, p, s);
+    return d128 ? launch_cstep_f32_d128(a, p, s) : launch_cstep_f32_d64(a, p, s);
+  }
   if (a.dtype == QUEST_F16 && a.summary_fp8)
     return d128 ? launch_step_e4m3_d128(a, p, s) : launch_step_e4m3_d64(a, p, s);
   if (a.dtype == QUEST_F16) return d128 ? launch_step_f16_d128(a, p, s) : launch_step_f16_d64(a, p, s);

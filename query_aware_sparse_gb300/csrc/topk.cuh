@@ -25,6 +25,30 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return x ^ ((x & 0x80000000u) ? 0xffffffffu : 0x80000000u);
 }
 
+// Thread groups the routines below run on: the whole CTA (__syncthreads),
+// or NTH threads starting at thread BASE (a multiple of 32) that meet at
+// named barrier ID.
+struct CtaGrp {
+  __device__ __forceinline__ static int tid() { return threadIdx.x; }
+  __device__ __forceinline__ static void sync() { __syncthreads(); }
+};
+template <int ID, int BASE, int NTH>
+struct BarGrp {
+  static_assert(BASE % 32 == 0 && NTH % 32 == 0, "groups are whole warps");
+  static constexpr int kN = NTH;
+  __device__ __forceinline__ static int tid() { return (int)threadIdx.x - BASE; }
+  __device__ __forceinline__ static void sync() {
+    asm volatile("bar.sync %0, %1;" :: "n"(ID), "n"(NTH) : "memory");
+  }
+};
+
+// Hook told about pages that are certain to be selected as soon as the first
+// radix digit is known (before the boundary bucket is resolved): the caller
+// may start fetching them early. The default does nothing.
+struct NoEarly {
+  __device__ __forceinline__ void operator()(int) const {}
+};
+
 constexpr int kTopkBits = 11;                 // radix digit width
 constexpr int kTopkBins = 1 << kTopkBits;
 
@@ -37,15 +61,16 @@ struct TopkSmem {
   unsigned long long scan[NT / 32];
   alignas(16) uint32_t gkey[kTopkGather];
   alignas(16) int32_t gidx[kTopkGather];
+  uint32_t gmark[kTopkGather];
   uint32_t digit, krem, done, bcnt, gcount;
 };
 
 // Exclusive block scan of a 64-bit value.
-template <int NT>
+template <int NT, class Grp = CtaGrp>
 __device__ __forceinline__ unsigned long long topk_excl_scan(unsigned long long v,
                                                              TopkSmem<NT>& sm) {
   constexpr int NWP = NT / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = Grp::tid() & 31, warp = Grp::tid() >> 5;
   unsigned long long incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -53,7 +78,7 @@ __device__ __forceinline__ unsigned long long topk_excl_scan(unsigned long long 
     if (lane >= o) incl += t;
   }
   if (lane == 31) sm.scan[warp] = incl;
-  __syncthreads();
+  Grp::sync();
   if (warp == 0) {
     unsigned long long w = lane < NWP ? sm.scan[lane] : 0ull;
     unsigned long long wi = w;
@@ -64,9 +89,9 @@ __device__ __forceinline__ unsigned long long topk_excl_scan(unsigned long long 
     }
     if (lane < NWP) sm.scan[lane] = wi - w;
   }
-  __syncthreads();
+  Grp::sync();
   const unsigned long long r = sm.scan[warp] + incl - v;
-  __syncthreads();   // scan[] may be reused right after
+  Grp::sync();   // scan[] may be reused right after
   return r;
 }
 
@@ -74,9 +99,9 @@ __device__ __forceinline__ unsigned long long topk_excl_scan(unsigned long long 
 // global): emit(pos, i) is called once for each of the min(P, K) selected
 // pages i, pos being its place in ascending page order. All NT threads of
 // the block must call it (it synchronises the block).
-template <int NT, typename KeyAt, typename Emit>
+template <int NT, typename KeyAt, typename Emit, class Grp = CtaGrp>
 __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Emit emit) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = Grp::tid(), lane = tid & 31, warp = tid >> 5;
   constexpr int NWP = NT / 32;
 
   if (P <= K) {                     // every scored page is selected
@@ -96,7 +121,7 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Em
   }
   if (lane == 0) { sm.red[0][warp] = kmin; sm.red[1][warp] = kmax; }
   for (int i = tid; i < kTopkBins; i += NT) sm.hist[i] = 0;
-  __syncthreads();
+  Grp::sync();
   kmin = sm.red[0][0];
   kmax = sm.red[1][0];
 #pragma unroll
@@ -124,7 +149,7 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Em
         const uint32_t k = key_at(i);
         if ((k & hi_mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
       }
-      __syncthreads();
+      Grp::sync();
       // thread t owns bins [t*BPT, t*BPT + BPT); count of keys in higher bins
       uint32_t h[BPT], tot = 0;
 #pragma unroll
@@ -136,7 +161,7 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Em
         if (lane + o < 32) incl += t;
       }
       if (lane == 0) sm.red[0][warp] = incl;       // warp totals
-      __syncthreads();
+      Grp::sync();
       uint32_t above = incl - tot;
       for (int w = warp + 1; w < NWP; ++w) above += sm.red[0][w];
       uint32_t cum = above;
@@ -151,7 +176,7 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Em
       }
 #pragma unroll
       for (int j = 0; j < BPT; ++j) sm.hist[tid * BPT + j] = 0;   // ready for the next pass
-      __syncthreads();
+      Grp::sync();
       prefix |= sm.digit << shift;
       krem = sm.krem;
       if (sm.done || shift == 0) {
@@ -162,7 +187,7 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Em
       }
       hi = shift - 1;
     }
-    __syncthreads();   // everyone has read sm.digit/krem/done
+    Grp::sync();   // everyone has read sm.digit/krem/done
   }
 
   // Stable compaction in page order.
@@ -174,7 +199,7 @@ __device__ void block_topk_keys(int P, int K, KeyAt key_at, TopkSmem<NT>& sm, Em
     if (ge_mode) gt += k >= T;
     else { gt += k > T; eq += k == T; }
   }
-  const unsigned long long ex = topk_excl_scan<NT>(((unsigned long long)gt << 32) | eq, sm);
+  const unsigned long long ex = topk_excl_scan<NT, Grp>(((unsigned long long)gt << 32) | eq, sm);
   uint32_t gt_b = (uint32_t)(ex >> 32), eq_b = (uint32_t)ex;
   for (int i = c0; i < c1; ++i) {
     const uint32_t k = key_at(i);
@@ -202,7 +227,7 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
                            int32_t* out_count, PhysOf phys_of, Forced forced, int nforced);
 
 // Top-K of P <= 32 * NT keys held in shared memory (`keys`, P rounded up to
-// a multiple of 4 * NT readable, 16-byte aligned; overwritten), whose
+// a multiple of 4 * NT readable, 16-byte aligned; only read), whose
 // block-wide min and max the caller has already reduced. Same result as
 // block_topk_keys. Pages with forced(i) (nforced of them, at most K) are kept
 // outright and the other pages compete for the remaining K - nforced;
@@ -214,13 +239,16 @@ __device__ void block_topk(const float* __restrict__ sc, int P, int K, uint32_t*
 // registers. After the first radix digit, a boundary bucket of at most
 // kTopkGather keys is ranked directly (key, then lower index) instead of
 // taking more digits: its winners are marked with the top key and its
-// losers with 0, so one threshold then selects exactly K keys. The page-
+// losers with 0 (through the gather slot each thread remembers for its
+// bucket keys), so one threshold then selects exactly K keys. The page-
 // order compaction packs (greater, equal) counts into 32 bits (P < 65536).
-template <int NT, int KPT, typename Emit, typename Forced>
+template <int NT, int KPT, typename Emit, typename Forced, class Grp = CtaGrp,
+          typename Early = NoEarly>
 __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
-                          TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced) {
+                          TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced,
+                          Early early = Early()) {
   static_assert(KPT % 4 == 0 && KPT <= 32, "keys per thread: a multiple of 4, at most 32");
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = Grp::tid(), lane = tid & 31, warp = tid >> 5;
   constexpr int NWP = NT / 32;
   constexpr int BPT = kTopkBins / NT;            // bins per thread in the digit search
   static_assert(BPT % 4 == 0, "bins are read as 16-byte vectors");
@@ -254,6 +282,7 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
     int hi = 31 - __clz(kmin ^ kmax);           // highest differing bit
     uint32_t prefix = kmin & ~((hi == 31) ? 0xffffffffu : ((2u << hi) - 1u));
     uint32_t krem = Kq;
+    bool first = true;
     while (true) {
       const int shift = max(hi - (kTopkBits - 1), 0);
       const int nbits = hi - shift + 1;
@@ -264,7 +293,7 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
         if (((comp >> j) & 1u) && (kr[j] & hi_mask) == prefix)
           atomicAdd(&sm.hist[(kr[j] >> shift) & dmask], 1u);
       if (tid == 0) sm.gcount = 0;
-      __syncthreads();
+      Grp::sync();
       // thread t owns bins [t*BPT, t*BPT + BPT); count of keys in higher bins
       uint32_t h[BPT], tot = 0;
 #pragma unroll
@@ -281,7 +310,7 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
         if (lane + o < 32) incl += t;
       }
       if (lane == 0) sm.red[0][warp] = incl;       // warp totals
-      __syncthreads();
+      Grp::sync();
       uint32_t cum = incl - tot;
 #pragma unroll
       for (int w = 0; w < NWP; ++w)
@@ -296,10 +325,21 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
         }
         cum += h[j];
       }
-      __syncthreads();
+      Grp::sync();
       prefix |= sm.digit << shift;
       krem = sm.krem;
       const uint32_t bcnt = sm.bcnt;
+      if (first) {
+        // keys above the boundary bucket (or in it, when it is taken whole)
+        // and the forced pages are selected whatever the rest of the select
+        // decides
+        first = false;
+        const unsigned long long thr =
+            (sm.done || shift == 0) ? prefix : (unsigned long long)prefix + (1ull << shift);
+#pragma unroll
+        for (int j = 0; j < KPT; ++j)
+          if ((((comp >> j) & 1u) && kr[j] >= thr) || (((inr & ~comp) >> j) & 1u)) early(c0 + j);
+      }
       if (sm.done || shift == 0) {
         T = prefix;
         need = krem;
@@ -310,6 +350,9 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
         // rank the bucket [prefix, prefix + 2^shift) directly
         const uint32_t span = (1u << shift) - 1u;
         uint32_t inb = 0;                          // bit j: key c0 + j is in the bucket
+        uint32_t slots[KPT / 4];                   // byte j % 4 of word j / 4: its gather slot
+#pragma unroll
+        for (int j = 0; j < KPT / 4; ++j) slots[j] = 0u;
 #pragma unroll
         for (int j = 0; j < KPT; ++j) {
           if (((comp >> j) & 1u) && (kr[j] & ~span) == prefix) {
@@ -317,9 +360,10 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
             const uint32_t at = atomicAdd(&sm.gcount, 1u);
             sm.gkey[at] = kr[j];
             sm.gidx[at] = c0 + j;
+            slots[j / 4] |= (at & 0xffu) << (8 * (j % 4));
           }
         }
-        __syncthreads();
+        Grp::sync();
         if (tid < (int)bcnt) {
           const uint32_t mk = sm.gkey[tid];
           const int mi = sm.gidx[tid];
@@ -338,12 +382,12 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
             const uint32_t kj = sm.gkey[j];
             r4[0] += (kj > mk) || (kj == mk && sm.gidx[j] < mi);
           }
-          keys[mi] = (r4[0] + r4[1] + r4[2] + r4[3]) < krem ? 0xffffffffu : 0u;
+          sm.gmark[tid] = (r4[0] + r4[1] + r4[2] + r4[3]) < krem ? 0xffffffffu : 0u;
         }
-        __syncthreads();
+        Grp::sync();
 #pragma unroll
         for (int j = 0; j < KPT; ++j)               // take the marks back
-          if ((inb >> j) & 1u) kr[j] = keys[c0 + j];
+          if ((inb >> j) & 1u) kr[j] = sm.gmark[(slots[j / 4] >> (8 * (j % 4))) & 0xffu];
         const unsigned long long top = (unsigned long long)prefix + (1ull << shift);
         T = top > 0xffffffffull ? 0xffffffffu : (uint32_t)top;
         need = 0;
@@ -352,7 +396,7 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
       }
       hi = shift - 1;
     }
-    __syncthreads();   // sm.digit/krem/done/bcnt read by all before any reuse
+    Grp::sync();   // sm.digit/krem/done/bcnt read by all before any reuse
   }
 
   // Stable compaction in page order over the register keys (branch-free:
@@ -377,7 +421,7 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
     if (lane >= o) incl += t;
   }
   if (lane == 31) sm.red[1][warp] = incl;
-  __syncthreads();
+  Grp::sync();
   uint32_t ex = incl - cnt;
 #pragma unroll
   for (int w = 0; w < NWP; ++w)
@@ -399,16 +443,20 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
 
 // Top-K of P <= 32 * NT keys in shared memory (see topk_regs): picks the
 // register footprint for the row length.
-template <int NT, typename Emit, typename Forced>
+template <int NT, typename Emit, typename Forced, class Grp = CtaGrp, typename Early = NoEarly>
 __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
-                                TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced) {
+                                TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced,
+                                Early early = Early()) {
   if (P <= K) {                     // every scored page is selected
-    for (int i = threadIdx.x; i < P; i += NT) emit(i, i);
+    for (int i = Grp::tid(); i < P; i += NT) emit(i, i);
     return;
   }
-  if (P <= 8 * NT) topk_regs<NT, 8>(P, K, keys, kmin, kmax, sm, emit, forced, nforced);
-  else if (P <= 16 * NT) topk_regs<NT, 16>(P, K, keys, kmin, kmax, sm, emit, forced, nforced);
-  else topk_regs<NT, 32>(P, K, keys, kmin, kmax, sm, emit, forced, nforced);
+  if (P <= 8 * NT)
+    topk_regs<NT, 8, Emit, Forced, Grp, Early>(P, K, keys, kmin, kmax, sm, emit, forced, nforced, early);
+  else if (P <= 16 * NT)
+    topk_regs<NT, 16, Emit, Forced, Grp, Early>(P, K, keys, kmin, kmax, sm, emit, forced, nforced, early);
+  else
+    topk_regs<NT, 32, Emit, Forced, Grp, Early>(P, K, keys, kmin, kmax, sm, emit, forced, nforced, early);
 }
 
 template <int NT, typename PhysOf, typename Forced>

@@ -66,14 +66,16 @@ def _run(w, lens, steps, seed, append=True, n_sink=0, n_local=0, fp8=False):
         else:
             step(cache, gtab, q.cuda())
         assert qs.device_error() == 0
-        # after every call: the call tag and the ready flags hold the number
-        # of calls made so far, the per-unit slot counters are back at zero,
-        # this call's counted-in bank (tag parity) holds every CTA and the
-        # next call's bank is clear
-        cnt = step.workspace[:(4 + 2 * B * h) * 4].view(torch.int32).cpu().numpy()
-        assert cnt[0] == s + 1 and cnt[1] == 0
-        assert cnt[2 + ((s + 1) & 1)] > 0 and cnt[2 + ((s + 2) & 1)] == 0
-        assert np.all(cnt[4:4 + B * h] == s + 1) and np.all(cnt[4 + B * h:] == 0)
+        if step.workspace.numel() > 256:
+            # the grid-wide kernel: after every call the call tag and the
+            # ready flags hold the number of calls made so far, the per-unit
+            # slot counters are back at zero, this call's counted-in bank (tag
+            # parity) holds every CTA and the next call's bank is clear (the
+            # cluster kernel uses no workspace)
+            cnt = step.workspace[:(4 + 2 * B * h) * 4].view(torch.int32).cpu().numpy()
+            assert cnt[0] == s + 1 and cnt[1] == 0
+            assert cnt[2 + ((s + 1) & 1)] > 0 and cnt[2 + ((s + 2) & 1)] == 0
+            assert np.all(cnt[4:4 + B * h] == s + 1) and np.all(cnt[4 + B * h:] == 0)
         gsm = np_of(cache.summary)
         # the summary the selector reads: exact, or its E4M3 rounding
         ssm = qo.summary_to_e4m3(osm)[0] if fp8 else osm
@@ -124,7 +126,16 @@ def _w(name, **kw):
     return wl.Workload(name, **base)
 
 
-def test_step_mha_crosses_page_boundaries():
+@pytest.fixture(params=["cluster", "grid"])
+def kernel(request, monkeypatch):
+    """Groups 1 and 2 run on the cluster kernel; QUEST_STEP_LEGACY selects
+    the grid-wide kernel (the one groups 4 and 8 always take) instead."""
+    if request.param == "grid":
+        monkeypatch.setenv("QUEST_STEP_LEGACY", "1")
+    return request.param
+
+
+def test_step_mha_crosses_page_boundaries(kernel):
     # 30 -> 31, 32 (page full), 33 (fresh page: slot 0), 34
     _run(_w("mha", batch=3, h_kv=4), [30, 1, 200], steps=4, seed=1)
 
@@ -148,7 +159,7 @@ def test_step_without_append_and_k_above_pages():
     _run(_w("noapp", batch=3, h_kv=2, k=40), [100, 700, 5], steps=2, seed=9, append=False)
 
 
-def test_step_many_units():
+def test_step_many_units(kernel):
     # more (request, head) units than select workers and CTAs per head
     _run(_w("many", batch=24, h_kv=8, group=1, k=8, head_dim=64), list(range(10, 250, 10)),
          steps=1, seed=10)
@@ -161,7 +172,8 @@ def test_step_units_above_grid():
          [17 + 13 * i for i in range(20)], steps=2, seed=11)
 
 
-@pytest.mark.parametrize("group,lens", [(1, [70000, 900]), (4, [140000, 3000])])
+@pytest.mark.parametrize("group,lens", [(1, [70000, 900]), (1, [140000, 3000]),
+                                        (4, [140000, 3000])])
 def test_step_long_rows(group, lens):
     # rows above the 4096 and 8192 keys the selecting CTA caches in shared
     # memory (the second reads its keys from L2)
