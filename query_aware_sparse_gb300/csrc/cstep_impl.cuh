@@ -12,12 +12,14 @@
 // the requests sorted by length) and works through them in the order
 // S(0), S(1), A(0), S(2), A(1), ..., A(n-1): the selection of a unit runs
 // while the next unit's summaries stream. Warps of a CTA have fixed roles:
-//   * consumer warps feed themselves. In S(t) warp w scores the CTA's
-//     chunks w, w + NCW, ... of the unit's pages (chunk c of CHUNK pages
-//     belongs to CTA c % kCL): it copies their summaries into its own buffer
-//     with cp.async (16 bytes per lane, one page summary per warp copy, two
-//     chunks in flight) and writes each score as an order-preserving key into
-//     the row buffer of every CTA of the cluster (distributed shared memory).
+//   * consumer warps feed themselves. In S(t) the unit's pages are split
+//     into kCL contiguous ranges (one per CTA) and each range into NCW
+//     contiguous runs (one per consumer warp); a warp copies its run's
+//     summaries, CHUNK pages at a time, into its own buffer with cp.async (16
+//     bytes per lane, one page summary per warp copy, one chunk in flight
+//     while one is scored) and writes each score as an order-preserving key
+//     into the row buffer of every CTA of the cluster (distributed shared
+//     memory).
 //     In A(t) it streams its share of the CTA's selected pages with 1-D bulk
 //     copies, the next page's K block loading while the current V block is
 //     folded into the warp's online softmax; the state is stashed per unit.
@@ -69,7 +71,13 @@ struct CShape {
   static constexpr int TB = HALF / (D * ES);        // tokens per sub-block
   static constexpr int SLOT = 2 * HALF;             // a warp's buffer: K | V, or two chunks
   using W = WarpAttn<T, D, TB, G>;                  // one sub-block = one attention tile
-  static constexpr int CHUNK = HALF / SUMB < 32 ? HALF / SUMB : 32;   // pages per scoring chunk
+  // scoring chunks: half of a warp's buffer (at least one round of PPR
+  // pages), so that one streams while the other is scored (finer chunks,
+  // more in flight, measured slower: the per-chunk reduction dominates)
+  static constexpr int CHB0 = HALF, CHBR = (32 / (RB / 16 < 8 ? RB / 16 : 8)) * SUMB;
+  static constexpr int CHB = CHB0 >= CHBR ? CHB0 : CHBR;   // bytes of a chunk
+  static constexpr int NQ = SLOT / CHB;                    // chunks a warp's buffer holds
+  static constexpr int CHUNK = CHB / SUMB < 32 ? CHB / SUMB : 32;   // pages per chunk
   static constexpr int CPI = 512 / SUMB > 0 ? 512 / SUMB : 1;        // pages per warp copy
   static constexpr int NCPY = CHUNK * SUMB / 512;   // warp copies (16 B per lane) per chunk
   static constexpr int LPP = RB / 16 < 8 ? RB / 16 : 8;   // lanes per page when scoring
@@ -80,7 +88,7 @@ struct CShape {
   static constexpr int NV = NR * G;                 // partial bounds per lane
   static constexpr int LGN = W::NV > CHUNK * G ? W::NV : CHUNK * G;
   static_assert(CHUNK % PPR == 0 && LPP * VPL * 16 == RB && NCPY >= 1, "scoring layout");
-  static_assert(CHUNK * SUMB % 512 == 0, "a chunk is whole warp copies");
+  static_assert(CHUNK * SUMB % 512 == 0 && NQ >= 2 && 32 % CHUNK == 0, "chunks");
 
   static constexpr int al(int x, int a) { return (x + a - 1) / a * a; }
   // consumer warps: as many 2 * BLK buffers as fit, at most kCMaxCW
@@ -93,7 +101,8 @@ struct CShape {
   static constexpr int NT = (NCW + kCSW) * 32;
   static constexpr int SEL0 = NCW * 32;             // first select thread
   using SelGrp = BarGrp<2, NCW * 32, kCSelT>;      // the select warps
-  using AllGrp = BarGrp<3, 0, NT>;                 // every warp (a cluster with one unit)
+  static constexpr int HANDS = 8;                  // consumer warps that select a lone unit
+  using AllGrp = BarGrp<3, 0, HANDS * 32>;
 
   static constexpr int ROWS_OFF = 0;                                  // [2][kCRowCap] keys
   static constexpr int SELL_OFF = ROWS_OFF + 2 * kCRowCap * 4;       // [2][kCKCap] logical ids
@@ -246,7 +255,7 @@ cstep_kernel(const StepArgs a) {
   constexpr int NCW = Sh::NCW, NT = Sh::NT;
   constexpr int CHUNK = Sh::CHUNK, LPP = Sh::LPP, VPL = Sh::VPL, PPR = Sh::PPR, NR = Sh::NR;
   constexpr int VECS = Sh::VECS, SLOT = Sh::SLOT, SUMB = Sh::SUMB, RB = Sh::RB, BLK = Sh::BLK;
-  constexpr int NCPY = Sh::NCPY, HALF = Sh::HALF;
+  constexpr int NCPY = Sh::NCPY, HALF = Sh::HALF, NQ = Sh::NQ, CHB = Sh::CHB;
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -303,6 +312,7 @@ cstep_kernel(const StepArgs a) {
   pdl_launch_dependents();
   cluster_sync_all();                          // barriers of every CTA initialised
   pdl_wait();
+  if (tid == 0) stamp(1);
 
   // ---------------------- unit list (first select warp) ----------------------
   if (warp == NCW) {
@@ -368,6 +378,54 @@ cstep_kernel(const StepArgs a) {
     if (lane == 0) *s_n = n;
     __syncwarp();
   }
+  // one request: the consumers' first page-table windows, before the list
+  int pw[4] = {-1, -1, -1, -1};
+  constexpr int QLD = Sh::VPL * (F8 ? 2 : 1);       // 16-byte query vectors per lane and head
+  uint4 qpre[G][QLD];                               // the scoring query, fetched early
+  const bool pre = a.batch == 1 && warp < NCW && cid < a.h_kv;
+  if (pre) {
+    const int sub0 = lane % Sh::LPP;
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      const T* qp = static_cast<const T*>(a.q) + ((size_t)cid * G + gi) * D;
+#pragma unroll
+      for (int v = 0; v < Sh::VPL; ++v)
+#pragma unroll
+        for (int h = 0; h < (F8 ? 2 : 1); ++h)
+          qpre[gi][v * (F8 ? 2 : 1) + h] = ld_nc_v4(qp + (v * Sh::LPP + sub0) * Sh::VECS + h * 8);
+    }
+    const int span = a.nnz, nch = (span + CHUNK - 1) / CHUNK;
+    const int cc0 = (int)((long long)nch * (int)rank / kCL);
+    const int ncc = (int)((long long)nch * ((int)rank + 1) / kCL) - cc0;
+    const int pb = (cc0 + ncc * warp / NCW) * CHUNK;
+    const int pe = min(span, (cc0 + ncc * (warp + 1) / NCW) * CHUNK);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int p = pb + 32 * k + lane;
+      pw[k] = p < pe ? __ldg(a.page_indices + p) : -1;
+    }
+    // ... and the first NQ - 1 chunks of the warp's run start streaming
+    // (unit = cluster: KV head cid of the request)
+    const int nm0 = (cc0 + ncc * (warp + 1) / NCW) - (cc0 + ncc * warp / NCW);
+    unsigned char* buf0 = smem + Sh::BUF_OFF + (size_t)warp * SLOT;
+#pragma unroll
+    for (int m = 0; m < NQ - 1; ++m) {
+      if (m < nm0) {
+        const int o = m * CHUNK;
+        const int srcw = ((o >> 5) & 1) ? pw[1] : pw[0];
+        const int ph = __shfl_sync(FULL, srcw, (o & 31) + (lane & (CHUNK - 1)));
+#pragma unroll
+        for (int k = 0; k < NCPY; ++k) {
+          const int byte = k * 512 + lane * 16;
+          const int phj = __shfl_sync(FULL, ph, byte / SUMB);
+          if (phj >= 0 && phj < a.n_phys)
+            cp_async16(buf0 + m * CHB + byte, static_cast<const unsigned char*>(a.summary) +
+                                                   ((size_t)phj * a.h_kv + cid) * SUMB + byte % SUMB);
+        }
+      }
+      cp_async_commit_grp();
+    }
+  }
   asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory");
   const int n = *s_n;
 
@@ -375,16 +433,21 @@ cstep_kernel(const StepArgs a) {
   // this CTA's chunks of the unit's pages (CTA r takes chunks
   // [nch r / kCL, nch (r+1) / kCL)) and its share of the selection (winner
   // w belongs to CTA w % kCL)
+  // (one request: over its table pages, known before any load, so that the
+  // consumers can fetch their page-table windows while the unit list forms)
   auto c_lo = [&](const CUnit& un, int r) {
-    return (int)((long long)((un.P + CHUNK - 1) / CHUNK) * r / kCL);
+    const int span = a.batch == 1 ? un.tp : un.P;
+    return (int)((long long)((span + CHUNK - 1) / CHUNK) * r / kCL);
   };
   auto n_at = [&](const CUnit& un) {
     return un.nsel > (int)rank ? (un.nsel - (int)rank + kCL - 1) / kCL : 0;
   };
 
   // A cluster with a single unit has nothing to stream while it selects:
-  // then every warp of the CTA runs the select (AllGrp), else the select
-  // warps do (SelGrp) while the consumers stream the next unit.
+  // then the first HANDS consumer warps run the select (AllGrp; more
+  // threads would only add barrier latency) and publish it through
+  // sel_ready, else the select warps do (SelGrp) while the consumers stream
+  // the next unit.
   const bool all_hands = n == 1;
 
   // T(u) on thread group Grp: wait for every CTA's keys of unit u, Top-K,
@@ -465,6 +528,57 @@ cstep_kernel(const StepArgs a) {
         const int cc0 = c_lo(un, (int)rank), ncc = c_lo(un, (int)rank + 1) - cc0;
         const int mc0 = cc0 + ncc * cw / NCW;
         const int nm = cc0 + ncc * (cw + 1) / NCW - mc0;
+        const bool cached = un.P <= kCRowCap;
+        const int f_lo = min(a.n_sink, un.P), f_hi = max(f_lo, un.P - a.n_local);
+        uint32_t kmn = 0xffffffffu, kmx = 0u;        // over my competing pages' keys
+        // the physical pages of my run, 64 table entries per window (two per
+        // lane): the current window and the next one are held in registers
+        const int pb = mc0 * CHUNK, pe = min(un.P, (mc0 + nm) * CHUNK);
+        const int32_t* idx = a.page_indices + un.lo;
+        auto ldwin = [&](int k, int& w0, int& w1) {
+          const int p = pb + 64 * k + lane;
+          w0 = p < pe ? __ldg(idx + p) : -1;
+          w1 = p + 32 < pe ? __ldg(idx + p + 32) : -1;
+        };
+        int cw0, cw1, nw0, nw1, kcur = 0;
+        if (t == 0 && pre && un.lo == 0 && un.tp == a.nnz) {   // fetched before the list
+          cw0 = pw[0]; cw1 = pw[1]; nw0 = pw[2]; nw1 = pw[3];
+        } else {
+          ldwin(0, cw0, cw1);
+          ldwin(1, nw0, nw1);
+        }
+        // lane j < CHUNK: physical page of page j of my chunk m (a chunk lies
+        // in one half of one window), -1 past the row
+        auto tbl = [&](int m) -> int {
+          if (m >= nm) return -1;
+          const int o = m * CHUNK, k = o >> 6, h = (o >> 5) & 1;
+          const int src = k == kcur ? (h ? cw1 : cw0) : (h ? nw1 : nw0);
+          const int v = __shfl_sync(FULL, src, (o & 31) + (lane & (CHUNK - 1)));
+          return lane < CHUNK ? v : -1;
+        };
+        // 16 bytes per lane per copy: copy k holds bytes [512k, 512k + 512) of the chunk
+        auto issue = [&](int m, int ph) {
+          if (m < nm) {
+            unsigned char* dst = buf + (m % NQ) * CHB;
+#pragma unroll
+            for (int k = 0; k < NCPY; ++k) {
+              const int byte = k * 512 + lane * 16;
+              const int j = byte / SUMB;
+              const int phj = __shfl_sync(FULL, ph, j);
+              if (phj >= 0 && phj < a.n_phys)
+                cp_async16(dst + byte, static_cast<const unsigned char*>(a.summary) +
+                                           ((size_t)phj * a.h_kv + un.g) * SUMB + byte % SUMB);
+            }
+          }
+          cp_async_commit_grp();
+        };
+        // the first NQ - 1 chunks (one request: issued before the unit list)
+        const bool preissued = t == 0 && pre && un.lo == 0 && un.tp == a.nnz;
+        if (!preissued) {
+          cp_async_wait_grp<0>();            // (none pending but a stale early issue)
+#pragma unroll
+          for (int m = 0; m < NQ - 1; ++m) issue(m, tbl(m));
+        }
         // query of the unit for the bound: per 32-bit word a select mask
         // (take M where q >= 0) and the values as fp32
         constexpr int QW = VPL * (F8 ? 8 : 4);
@@ -479,7 +593,8 @@ cstep_kernel(const StepArgs a) {
             const int d0 = (v * LPP + sub) * VECS;
 #pragma unroll
             for (int h = 0; h < (F8 ? 2 : 1); ++h) {
-              const uint4 qv = ld_nc_v4(qp + d0 + h * 8);
+              const uint4 qv = (t == 0 && pre && un.g == cid) ? qpre[gi][v * (F8 ? 2 : 1) + h]
+                                                               : ld_nc_v4(qp + d0 + h * 8);
               const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
@@ -519,62 +634,21 @@ cstep_kernel(const StepArgs a) {
           dead = true;
           break;
         }
-        const bool cached = un.P <= kCRowCap;
-        const int f_lo = min(a.n_sink, un.P), f_hi = max(f_lo, un.P - a.n_local);
-        uint32_t kmn = 0xffffffffu, kmx = 0u;        // over my competing pages' keys
-        // the physical pages of my run, 64 table entries per window (two per
-        // lane): the current window and the next one are held in registers
-        const int pb = mc0 * CHUNK, pe = min(un.P, (mc0 + nm) * CHUNK);
-        const int32_t* idx = a.page_indices + un.lo;
-        auto ldwin = [&](int k, int& w0, int& w1) {
-          const int p = pb + 64 * k + lane;
-          w0 = p < pe ? __ldg(idx + p) : -1;
-          w1 = p + 32 < pe ? __ldg(idx + p + 32) : -1;
-        };
-        int cw0, cw1, nw0, nw1, kcur = 0;
-        ldwin(0, cw0, cw1);
-        ldwin(1, nw0, nw1);
-        // lane j < CHUNK: physical page of page j of my chunk m (a chunk lies
-        // in one half of one window), -1 past the row
-        auto tbl = [&](int m) -> int {
-          if (m >= nm) return -1;
-          const int o = m * CHUNK, k = o >> 6, h = (o >> 5) & 1;
-          const int src = k == kcur ? (h ? cw1 : cw0) : (h ? nw1 : nw0);
-          const int v = __shfl_sync(FULL, src, (o & 31) + (lane & (CHUNK - 1)));
-          return lane < CHUNK ? v : -1;
-        };
-        // 16 bytes per lane per copy: copy k holds bytes [512k, 512k + 512) of the chunk
-        auto issue = [&](int m, int ph) {
-          if (m < nm) {
-            unsigned char* dst = buf + (m & 1) * HALF;
-#pragma unroll
-            for (int k = 0; k < NCPY; ++k) {
-              const int byte = k * 512 + lane * 16;
-              const int j = byte / SUMB;
-              const int phj = __shfl_sync(FULL, ph, j);
-              if (phj >= 0 && phj < a.n_phys)
-                cp_async16(dst + byte, static_cast<const unsigned char*>(a.summary) +
-                                           ((size_t)phj * a.h_kv + un.g) * SUMB + byte % SUMB);
-            }
-          }
-          cp_async_commit_grp();
-        };
-        issue(0, tbl(0));
         for (int m = 0; m < nm; ++m) {
-          if (((m + 1) * CHUNK) >> 6 > kcur + 1) {      // chunk m + 1 is past the next window
+          if (((m + NQ - 1) * CHUNK) >> 6 > kcur + 1) {   // past the next window
             ++kcur;
             cw0 = nw0; cw1 = nw1;
             ldwin(kcur + 1, nw0, nw1);
           }
-          issue(m + 1, tbl(m + 1));          // the next chunk streams while this one is scored
+          issue(m + NQ - 1, tbl(m + NQ - 1));   // streams while chunk m is scored
           const int phm = tbl(m);
-          cp_async_wait_grp<1>();
+          cp_async_wait_grp<NQ - 1>();
           __syncwarp();
           const int p0 = (mc0 + m) * CHUNK;
           const int np = min(CHUNK, un.P - p0);
           const unsigned bad = __ballot_sync(FULL, lane < np && !(phm >= 0 && phm < a.n_phys));
           if (bad && lane == 0) report(a.err, QUEST_DEVERR_PAGE_RANGE);
-          const unsigned char* sb = buf + (m & 1) * HALF;
+          const unsigned char* sb = buf + (m % NQ) * CHB;
           float vals[Sh::NV];
 #pragma unroll
           for (int ro = 0; ro < NR; ++ro) {
@@ -718,7 +792,7 @@ cstep_kernel(const StepArgs a) {
               a.scores[(size_t)un.g * a.nnz + un.lo + p0 + lane] = sc;
             }
           }
-          __syncwarp();                      // buffer half (m & 1) may be refilled
+          __syncwarp();                      // chunk slot m % NQ may be refilled
         }
         cp_async_wait_grp<0>();
         kmn = warp_min_u32(kmn);
@@ -747,10 +821,11 @@ cstep_kernel(const StepArgs a) {
         const int nal = n_at(un);
         const int na = nal > cw ? (nal - cw + NCW - 1) / NCW : 0;   // my pages
         W st;
-        st.init(static_cast<const T*>(a.q) + ((size_t)un.r * h_q + (size_t)un.g * G) * D,
-                a.scale_log2, lane);
-        if (all_hands) {
+        bool inited = false;                 // q loads once the first copies are out
+        const T* qrow = static_cast<const T*>(a.q) + ((size_t)un.r * h_q + (size_t)un.g * G) * D;
+        if (all_hands && cw < Sh::HANDS) {
           if (!select_core(typename Sh::AllGrp{}, u)) { dead = true; break; }
+          if (cw == 0 && lane == 0) arrive_local(sel_ready + b);   // the group synced: all of it
         } else if (!cwait_warp(sel_ready + b, (u >> 1) & 1, s_abort, a.err, lim)) {
           dead = true;
           break;
@@ -806,6 +881,10 @@ cstep_kernel(const StepArgs a) {
             issue_half(li, 0, 0);
             issue_half(li, 0, 1);
           }
+          if (!inited) {
+            st.init(qrow, a.scale_log2, lane);
+            inited = true;
+          }
           while (li >= 0) {
             const int vk = min(Sh::TB, __shfl_sync(FULL, valid, li) - sb * Sh::TB);
             int l1 = li, s1 = sb;
@@ -826,6 +905,7 @@ cstep_kernel(const StepArgs a) {
           }
         }
         if (dead) break;
+        if (!inited) st.init(qrow, a.scale_log2, lane);   // no pages: the empty state
         if (u >= 2 && !cwait_warp(stash_free + b, ((u >> 1) - 1) & 1, s_abort, a.err, lim)) {
           dead = true;
           break;
@@ -861,8 +941,7 @@ cstep_kernel(const StepArgs a) {
         // ------------------------------ T(t) ------------------------------
         const int u = t, b = u & 1;
         const CUnit un = units[u];
-        const bool ok = all_hands ? select_core(typename Sh::AllGrp{}, u)
-                                  : select_core(SelGrp{}, u);
+        const bool ok = all_hands ? gwait(sel_ready + b, (u >> 1) & 1) : select_core(SelGrp{}, u);
         if (!ok) { dead = true; break; }
         SelGrp::sync();
         const int P = un.P, nsel = un.nsel;
@@ -872,7 +951,7 @@ cstep_kernel(const StepArgs a) {
         int32_t* ol = a.sel_logical + ug * K;
         int32_t* sl = sell + b * kCKCap;
         int32_t* sp = selp + b * kCKCap;
-        if (gt == 0) {                           // (the group's reads precede it by the barrier)
+        if (gt == 0 && !all_hands) {             // (the group's reads precede it by the barrier)
           kmm[2 * b] = 0xffffffffu;              // ready for unit u + 2
           kmm[2 * b + 1] = 0u;
           arrive_local(sel_ready + b);           // the consumers may stream the pages
