@@ -143,7 +143,6 @@ struct WarpAttnMma {
       acc[mt][0] *= alpha[0]; acc[mt][1] *= alpha[1];
       acc[mt][2] *= alpha[0]; acc[mt][3] *= alpha[1];
     }
-    __syncwarp();
     // B = P^T: P[head gid][tokens 2t, 2t+1] and [2t+8, 2t+9]
     const uint32_t* pw = reinterpret_cast<const uint32_t*>(ps);
     const uint32_t b0 = pw[gid * 8 + t], b1 = pw[gid * 8 + 4 + t];
@@ -177,6 +176,152 @@ struct WarpAttnMma {
         const int d = 64 * (mt >> 2) + 8 * gid + 2 * (mt & 3);
         mo[(size_t)(w * G + gi) * D + d] = acc[mt][h];
         mo[(size_t)(w * G + gi) * D + d + 1] = acc[mt][h + 2];
+      }
+      if (gid == 0) {
+        ml[(w * G + gi) * 2 + 0] = m[h];
+        ml[(w * G + gi) * 2 + 1] = l[h];
+      }
+    }
+  }
+};
+
+}  // namespace quest
+
+namespace quest {
+
+// The same attention for the G >= 4 query heads of a KV head, with the K and
+// V blocks of 16-token tiles staged in shared memory in rows of D halves whose
+// 16-byte units are XOR-swizzled by the row (unit u of row r at u ^ (r & 7)),
+// so that ldmatrix reads eight rows without bank conflicts:
+//   S^T = K Q^T   A = K tile (ldmatrix.x4), B = the group's queries
+//                 (registers; head gid, the rest of the 8 columns zero)
+//   O^T += V^T P^T   A = V tile transposed (ldmatrix.x4.trans), B = P^T
+//                 staged through a 256-byte warp scratch
+// Accumulators: acc[mt] = O^T[16 mt + gid][2t], [..][2t+1], [16 mt + gid + 8][2t], [..][2t+1].
+template <int D, int G>
+struct WarpAttnMmaS {
+  static_assert(G >= 1 && G <= 8 && D % 64 == 0, "at most 8 heads, D a multiple of 64");
+  static constexpr int KT = D / 16;         // k-steps of QK; m-tiles of AV
+  static constexpr int RB = D * 2;          // bytes of a K or V row
+
+  uint32_t qb[KT][2];                       // B fragments of Q^T
+  float m[2], l[2];                         // heads 2t, 2t+1 (base-2 logits)
+  float acc[KT][4];
+  float scale_log2;
+
+  __device__ __forceinline__ static int sw(int row, int unit) {
+    return row * RB + (((unit ^ (row & 7)) & (RB / 16 - 1)) << 4);
+  }
+
+  __device__ __forceinline__ void init(const __half* qrows, float sl2, int lane) {
+    const int gid = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      if (gid < G) {
+        qb[kk][0] = *reinterpret_cast<const uint32_t*>(qrows + (size_t)gid * D + 16 * kk + 2 * t);
+        qb[kk][1] = *reinterpret_cast<const uint32_t*>(qrows + (size_t)gid * D + 16 * kk + 2 * t + 8);
+      } else {
+        qb[kk][0] = 0u;
+        qb[kk][1] = 0u;
+      }
+    }
+    scale_log2 = sl2;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) { m[h] = -INFINITY; l[h] = 0.f; }
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[mt][c] = 0.f;
+  }
+
+  // One tile of 16 tokens (`valid` of them real), in two halves: qk() folds
+  // the K tile (shared-memory byte address kb, swizzled rows) into the running
+  // max and sum and leaves P in ps (this warp's 256-byte scratch); av() then
+  // accumulates the V tile (vb). The K tile is not read after qk() returns.
+  __device__ __forceinline__ void qk(uint32_t kb, int valid, __half* ps, int lane) {
+    const int gid = lane >> 2, t = lane & 3;
+    const int q4 = lane >> 3, r8 = lane & 7;  // ldmatrix: matrix q4, row r8 of this lane's address
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      // matrices: (tokens 0-7, dims 16kk..+7), (8-15, same), (0-7, +8..+15), (8-15, +8..+15)
+      const int row = r8 + 8 * (q4 & 1), unit = 2 * kk + (q4 >> 1);
+      uint32_t a0, a1, a2, a3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(kb + sw(row, unit)));
+      if (kk & 1) mma_f16_16816(s1, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      else mma_f16_16816(s0, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+    }
+    // tokens gid (s: head 2t, 2t+1) and gid + 8
+    const bool v0 = gid < valid, v1 = gid + 8 < valid;
+    const float x[4] = {v0 ? (s0[0] + s1[0]) * scale_log2 : -INFINITY,
+                        v0 ? (s0[1] + s1[1]) * scale_log2 : -INFINITY,
+                        v1 ? (s0[2] + s1[2]) * scale_log2 : -INFINITY,
+                        v1 ? (s0[3] + s1[3]) * scale_log2 : -INFINITY};
+    float alpha[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float mx = fmaxf(x[h], x[h + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
+      const float mn = fmaxf(m[h], mx);
+      alpha[h] = mn == -INFINITY ? 1.f : exp2f(m[h] - mn);
+      m[h] = mn;
+      // p rounded to fp16 (the MMA's input); the sum takes the rounded values
+      const __half pa = __float2half_rn(mn == -INFINITY ? 0.f : exp2f(x[h] - mn));
+      const __half pb = __float2half_rn(mn == -INFINITY ? 0.f : exp2f(x[h + 2] - mn));
+      float sum = __half2float(pa) + __half2float(pb);
+      sum += __shfl_xor_sync(FULL, sum, 4);
+      sum += __shfl_xor_sync(FULL, sum, 8);
+      sum += __shfl_xor_sync(FULL, sum, 16);
+      l[h] = l[h] * alpha[h] + sum;
+      ps[(2 * t + h) * 16 + gid] = pa;       // P[head][token]
+      ps[(2 * t + h) * 16 + gid + 8] = pb;
+    }
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      acc[mt][0] *= alpha[0]; acc[mt][1] *= alpha[1];
+      acc[mt][2] *= alpha[0]; acc[mt][3] *= alpha[1];
+    }
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ void av(uint32_t vb, int valid, const __half* ps, int lane) {
+    const int gid = lane >> 2, t = lane & 3;
+    const int q4 = lane >> 3, r8 = lane & 7;
+    // B = P^T: P[head gid][tokens 2t, 2t+1] and [2t+8, 2t+9]
+    const uint32_t* pw = reinterpret_cast<const uint32_t*>(ps);
+    const uint32_t b0 = pw[gid * 8 + t], b1 = pw[gid * 8 + 4 + t];
+    __syncwarp();                                        // scratch free for the next tile
+    // tokens past `valid` may hold anything (a NaN times p = 0 is NaN): their
+    // V entries are zeroed. A = V^T: a0 (dims gid, tokens 2t, 2t+1), a1 (dims
+    // gid + 8, same), a2 (dims gid, tokens 2t+8, 2t+9), a3 (dims gid + 8, same)
+    const uint32_t z02 = (2 * t < valid ? 0xffffu : 0u) | (2 * t + 1 < valid ? 0xffff0000u : 0u);
+    const uint32_t z13 = (2 * t + 8 < valid ? 0xffffu : 0u) | (2 * t + 9 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      // matrices (transposed): (tokens 0-7, dims 16mt..+7), (tokens 0-7, +8..+15),
+      // (tokens 8-15, dims 16mt..+7), (tokens 8-15, +8..+15)
+      const int row = r8 + 8 * (q4 >> 1), unit = 2 * mt + (q4 & 1);
+      uint32_t a0, a1, a2, a3;
+      asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(vb + sw(row, unit)));
+      mma_f16_16816(acc[mt], a0 & z02, a1 & z02, a2 & z13, a3 & z13, b0, b1);
+    }
+  }
+
+  // Store this warp's state for the CTA merge: mo[w][gi][D], ml[w][gi][2].
+  __device__ __forceinline__ void stash(float* mo, float* ml, int w, int lane) const {
+    const int gid = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int gi = 2 * t + h;
+      if (gi >= G) continue;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        mo[(size_t)(w * G + gi) * D + 16 * mt + gid] = acc[mt][h];
+        mo[(size_t)(w * G + gi) * D + 16 * mt + gid + 8] = acc[mt][h + 2];
       }
       if (gid == 0) {
         ml[(w * G + gi) * 2 + 0] = m[h];

@@ -1,5 +1,5 @@
 // Cluster decode step instantiated for fp16 K/V/q with fp16 summaries, head dim 128
-// (page sizes 16 and 32, GQA groups 1 and 2; one file per variant and head
+// (page sizes 16 and 32, GQA groups 1, 2, 4 and 8; one file per variant and head
 // dim, so the instantiations compile in parallel).
 #include "cstep_impl.cuh"
 

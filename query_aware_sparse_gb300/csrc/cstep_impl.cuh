@@ -35,8 +35,10 @@
 #pragma once
 
 #include <cstdlib>
+#include <type_traits>
 
 #include "attn_dev.cuh"
+#include "attn_mma.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "topk.cuh"
@@ -70,7 +72,11 @@ struct CShape {
   static constexpr int NSB = BLK / HALF;            // sub-blocks per block
   static constexpr int TB = HALF / (D * ES);        // tokens per sub-block
   static constexpr int SLOT = 2 * HALF;             // a warp's buffer: K | V, or two chunks
-  using W = WarpAttn<T, D, TB, G>;                  // one sub-block = one attention tile
+  // fp16 groups of 4 or 8: QK and AV on the warp MMA, from tiles of 16 tokens
+  // staged swizzled by cp.async; otherwise FMA from bulk-copied sub-blocks
+  static constexpr bool MMAA = ES == 2 && G >= 4;
+  using W = std::conditional_t<MMAA, WarpAttnMmaS<D, G>, WarpAttn<T, D, TB, G>>;
+  static constexpr int WNV = MMAA ? 64 : WarpAttn<T, D, TB, G>::NV;   // warp scratch floats
   // scoring chunks: half of a warp's buffer (at least one round of PPR
   // pages), so that one streams while the other is scored (finer chunks,
   // more in flight, measured slower: the per-chunk reduction dominates)
@@ -85,19 +91,24 @@ struct CShape {
   static constexpr int PPR = 32 / LPP;              // pages per round
   static constexpr int NR = CHUNK / PPR;            // rounds per chunk
   static constexpr int VECS = 16 / ESS;             // summary elements per vector
-  static constexpr int NV = NR * G;                 // partial bounds per lane
-  static constexpr int LGN = W::NV > CHUNK * G ? W::NV : CHUNK * G;
+  static constexpr int NV = NR * G;                 // partial bounds per lane (FMA bound)
+  // fp16 keys and groups of 4 or 8: the bound on the warp MMA,
+  // U = [m | M] . [q- ; q+] over the 2D summary elements (k), 8 pages per
+  // n-tile, the group's heads as A rows (for one or two heads the FMA bound
+  // is faster: measured)
+  static constexpr bool MMAS = ES == 2 && G >= 4;
+  static constexpr int KT = 2 * D / 16;             // k-steps of 16 summary elements
+  static constexpr int NT8 = CHUNK / 8;             // n-tiles of 8 pages per chunk
+  static constexpr int LGN = WNV > CHUNK * G ? WNV : CHUNK * G;
   static_assert(CHUNK % PPR == 0 && LPP * VPL * 16 == RB && NCPY >= 1, "scoring layout");
   static_assert(CHUNK * SUMB % 512 == 0 && NQ >= 2 && 32 % CHUNK == 0, "chunks");
+  static_assert(!MMAS || (CHUNK % 8 == 0 && G <= 8), "MMA bound: whole n-tiles, at most 8 heads");
 
   static constexpr int al(int x, int a) { return (x + a - 1) / a * a; }
-  // consumer warps: as many 2 * BLK buffers as fit, at most kCMaxCW
-  static constexpr int FIXED_EST = 2 * kCRowCap * 4 + 4 * kCKCap * 4 + 2 * kCMaxCW * G * (D + 2) * 4 +
-                                   kCL * G * (D + 2) * 4 + kCMaxU * 32 + 256 + kCMaxCW * 64 * 4 +
-                                   (int)sizeof(TopkSmem<kCMaxCW * 32 + kCSelT>) + 1024;
-  static constexpr int NCW_FIT = (kCSmemMax - FIXED_EST) / SLOT;
-  static constexpr int NCW = NCW_FIT < kCMaxCW ? NCW_FIT : kCMaxCW;
-  static_assert(NCW == kCMaxCW, "twelve consumer warps: 512 threads, a power of two for the Top-K");
+  // consumer warps: twelve, or eight for groups of 4 or 8 (their per-warp
+  // states take the room); one stash buffer for groups of 8
+  static constexpr int NCW = G >= 4 ? 8 : kCMaxCW;
+  static constexpr int NSTASH = G >= 8 ? 1 : 2;
   static constexpr int NT = (NCW + kCSW) * 32;
   static constexpr int SEL0 = NCW * 32;             // first select thread
   using SelGrp = BarGrp<2, NCW * 32, kCSelT>;      // the select warps
@@ -107,9 +118,9 @@ struct CShape {
   static constexpr int ROWS_OFF = 0;                                  // [2][kCRowCap] keys
   static constexpr int SELL_OFF = ROWS_OFF + 2 * kCRowCap * 4;       // [2][kCKCap] logical ids
   static constexpr int SELP_OFF = SELL_OFF + 2 * kCKCap * 4;         // [2][kCKCap] physical ids
-  static constexpr int STO_OFF = SELP_OFF + 2 * kCKCap * 4;          // [2][NCW][G][D]
-  static constexpr int STML_OFF = STO_OFF + 2 * NCW * G * D * 4;     // [2][NCW][G][2]
-  static constexpr int PART_OFF = STML_OFF + 2 * NCW * G * 2 * 4;    // [kCL][G][D]
+  static constexpr int STO_OFF = SELP_OFF + 2 * kCKCap * 4;          // [NSTASH][NCW][G][D]
+  static constexpr int STML_OFF = STO_OFF + NSTASH * NCW * G * D * 4;   // [NSTASH][NCW][G][2]
+  static constexpr int PART_OFF = STML_OFF + NSTASH * NCW * G * 2 * 4;  // [kCL][G][D]
   static constexpr int PARTML_OFF = PART_OFF + kCL * G * D * 4;      // [kCL][G][2]
   static constexpr int UNITS_OFF = PARTML_OFF + kCL * G * 2 * 4;     // [kCMaxU] CUnit
   static constexpr int ORDER_OFF = UNITS_OFF + kCMaxU * (int)sizeof(CUnit);   // [64] requests
@@ -238,6 +249,14 @@ __device__ __forceinline__ void sub_reduce(float* v, int lane) {
     }
   }
 }
+// Byte offset of byte `byte` of page row p in a chunk staged for the MMA
+// bound: 16-byte units XOR-swizzled by the row (so that the eight rows of an
+// n-tile, SUMB apart, fall in different banks).
+template <int SUMB>
+__device__ __forceinline__ int sw_off(int p, int byte) {
+  return p * SUMB + ((((byte >> 4) ^ (p & 7)) << 4) | (byte & 15));
+}
+
 template <int N, int O>
 __device__ __forceinline__ int sub_base(int lane) {
   if constexpr (O >= 1 && N >= 2) return ((lane & O) ? N / 2 : 0) + sub_base<N / 2, O / 2>(lane);
@@ -380,19 +399,28 @@ cstep_kernel(const StepArgs a) {
   }
   // one request: the consumers' first page-table windows, before the list
   int pw[4] = {-1, -1, -1, -1};
-  constexpr int QLD = Sh::VPL * (F8 ? 2 : 1);       // 16-byte query vectors per lane and head
-  uint4 qpre[G][QLD];                               // the scoring query, fetched early
+  constexpr int QLD = Sh::MMAS ? 1 : Sh::VPL * (F8 ? 2 : 1);   // 16-byte query vectors per lane, head
+  constexpr int QL8 = Sh::MMAS ? D / 16 : 1;                   // 8-byte pieces (MMA layout)
+  uint4 qpre[Sh::MMAS ? 1 : G][QLD];                // the scoring query, fetched early
+  uint2 qpre8[QL8];
   const bool pre = a.batch == 1 && warp < NCW && cid < a.h_kv;
   if (pre) {
-    const int sub0 = lane % Sh::LPP;
+    if constexpr (Sh::MMAS) {                       // head gid's dims 16j + 4t .. + 3
+      const int gid = lane >> 2, tq = lane & 3;
+      const T* qh = static_cast<const T*>(a.q) + ((size_t)cid * G + (gid < G ? gid : 0)) * D;
 #pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-      const T* qp = static_cast<const T*>(a.q) + ((size_t)cid * G + gi) * D;
+      for (int j = 0; j < QL8; ++j) qpre8[j] = *reinterpret_cast<const uint2*>(qh + 16 * j + 4 * tq);
+    } else {
+      const int sub0 = lane % Sh::LPP;
 #pragma unroll
-      for (int v = 0; v < Sh::VPL; ++v)
+      for (int gi = 0; gi < G; ++gi) {
+        const T* qp = static_cast<const T*>(a.q) + ((size_t)cid * G + gi) * D;
 #pragma unroll
-        for (int h = 0; h < (F8 ? 2 : 1); ++h)
-          qpre[gi][v * (F8 ? 2 : 1) + h] = ld_nc_v4(qp + (v * Sh::LPP + sub0) * Sh::VECS + h * 8);
+        for (int v = 0; v < Sh::VPL; ++v)
+#pragma unroll
+          for (int h = 0; h < (F8 ? 2 : 1); ++h)
+            qpre[gi][v * (F8 ? 2 : 1) + h] = ld_nc_v4(qp + (v * Sh::LPP + sub0) * Sh::VECS + h * 8);
+      }
     }
     const int span = a.nnz, nch = (span + CHUNK - 1) / CHUNK;
     const int cc0 = (int)((long long)nch * (int)rank / kCL);
@@ -418,8 +446,9 @@ cstep_kernel(const StepArgs a) {
         for (int k = 0; k < NCPY; ++k) {
           const int byte = k * 512 + lane * 16;
           const int phj = __shfl_sync(FULL, ph, byte / SUMB);
+          const int dsto = Sh::MMAS ? sw_off<SUMB>(byte / SUMB, byte % SUMB) : byte;
           if (phj >= 0 && phj < a.n_phys)
-            cp_async16(buf0 + m * CHB + byte, static_cast<const unsigned char*>(a.summary) +
+            cp_async16(buf0 + m * CHB + dsto, static_cast<const unsigned char*>(a.summary) +
                                                    ((size_t)phj * a.h_kv + cid) * SUMB + byte % SUMB);
         }
       }
@@ -465,7 +494,6 @@ cstep_kernel(const StepArgs a) {
     if (!*okf) return false;
     if (u == 0 && gt == 0) stamp(5);
     const int P = un.P, nsel = un.nsel;
-    const bool owner = (int)rank == u % kCL;
     const bool listed = nsel <= kCKCap;
     int32_t* ol = a.sel_logical + ((size_t)un.r * a.h_kv + un.g) * K;
     int32_t* sl = sell + b * kCKCap;
@@ -565,8 +593,9 @@ cstep_kernel(const StepArgs a) {
               const int byte = k * 512 + lane * 16;
               const int j = byte / SUMB;
               const int phj = __shfl_sync(FULL, ph, j);
+              const int dsto = Sh::MMAS ? sw_off<SUMB>(j, byte % SUMB) : byte;
               if (phj >= 0 && phj < a.n_phys)
-                cp_async16(dst + byte, static_cast<const unsigned char*>(a.summary) +
+                cp_async16(dst + dsto, static_cast<const unsigned char*>(a.summary) +
                                            ((size_t)phj * a.h_kv + un.g) * SUMB + byte % SUMB);
             }
           }
@@ -579,34 +608,58 @@ cstep_kernel(const StepArgs a) {
 #pragma unroll
           for (int m = 0; m < NQ - 1; ++m) issue(m, tbl(m));
         }
-        // query of the unit for the bound: per 32-bit word a select mask
-        // (take M where q >= 0) and the values as fp32
-        constexpr int QW = VPL * (F8 ? 8 : 4);
-        constexpr int QV = F8 ? VPL * 16 : (Sh::ES == 2 ? QW * 2 : QW);
+        // query of the unit for the bound. FMA bound: per 32-bit word a select
+        // mask (take M where q >= 0) and the values as fp32. MMA bound: A
+        // fragments of [q- ; q+] (k-step kk < D/16: q- against m, else q+
+        // against M), head gid's elements 16 kk + 4t .. + 3 of the k order
+        // that the staged summaries are read in.
+        constexpr int QW = Sh::MMAS ? 1 : VPL * (F8 ? 8 : 4);
+        constexpr int QV = Sh::MMAS ? 1 : (F8 ? VPL * 16 : (Sh::ES == 2 ? QW * 2 : QW));
         uint32_t qmask[G][QW];
         float qf[G][QV];
+        constexpr int KQ = Sh::MMAS ? Sh::KT : 1;
+        uint32_t qa[KQ], qb[KQ];
+        if constexpr (Sh::MMAS) {
+          const int gid = lane >> 2, tq = lane & 3;
+          const bool hv = gid < G;
+          const T* qh = static_cast<const T*>(a.q) + ((size_t)un.r * h_q + (size_t)un.g * G + (hv ? gid : 0)) * D;
+          const __half2 z2 = __float2half2_rn(0.f);
 #pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-          const T* qp = static_cast<const T*>(a.q) + ((size_t)un.r * h_q + (size_t)un.g * G + gi) * D;
+          for (int j = 0; j < D / 16; ++j) {
+            uint2 w = (t == 0 && pre && un.g == cid) ? qpre8[j]
+                                                       : *reinterpret_cast<const uint2*>(qh + 16 * j + 4 * tq);
+            if (!hv) w = make_uint2(0u, 0u);
+            const __half2 x = *reinterpret_cast<const __half2*>(&w.x), y = *reinterpret_cast<const __half2*>(&w.y);
+            const __half2 xn = __hmin2(x, z2), yn = __hmin2(y, z2), xp = __hmax2(x, z2), yp = __hmax2(y, z2);
+            qa[j] = *reinterpret_cast<const uint32_t*>(&xn);
+            qb[j] = *reinterpret_cast<const uint32_t*>(&yn);
+            qa[j + D / 16] = *reinterpret_cast<const uint32_t*>(&xp);
+            qb[j + D / 16] = *reinterpret_cast<const uint32_t*>(&yp);
+          }
+        } else {
 #pragma unroll
-          for (int v = 0; v < VPL; ++v) {
-            const int d0 = (v * LPP + sub) * VECS;
+          for (int gi = 0; gi < G; ++gi) {
+            const T* qp = static_cast<const T*>(a.q) + ((size_t)un.r * h_q + (size_t)un.g * G + gi) * D;
 #pragma unroll
-            for (int h = 0; h < (F8 ? 2 : 1); ++h) {
-              const uint4 qv = (t == 0 && pre && un.g == cid) ? qpre[gi][v * (F8 ? 2 : 1) + h]
-                                                               : ld_nc_v4(qp + d0 + h * 8);
-              const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+            for (int v = 0; v < VPL; ++v) {
+              const int d0 = (v * LPP + sub) * VECS;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int wi = (v * (F8 ? 2 : 1) + h) * 4 + j;
-                if constexpr (Sh::ES == 2) {
-                  qmask[gi][wi] = ((~w4[j] & 0x80008000u) >> 15) * 0xffffu;
-                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
-                  qf[gi][wi * 2] = f.x;
-                  qf[gi][wi * 2 + 1] = f.y;
-                } else {
-                  qmask[gi][wi] = (w4[j] & 0x80000000u) ? 0u : 0xffffffffu;
-                  qf[gi][wi] = __uint_as_float(w4[j]);
+              for (int h = 0; h < (F8 ? 2 : 1); ++h) {
+                const uint4 qv = (t == 0 && pre && un.g == cid) ? qpre[gi][v * (F8 ? 2 : 1) + h]
+                                                                 : ld_nc_v4(qp + d0 + h * 8);
+                const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int wi = (v * (F8 ? 2 : 1) + h) * 4 + j;
+                  if constexpr (Sh::ES == 2) {
+                    qmask[gi][wi] = ((~w4[j] & 0x80008000u) >> 15) * 0xffffu;
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
+                    qf[gi][wi * 2] = f.x;
+                    qf[gi][wi * 2 + 1] = f.y;
+                  } else {
+                    qmask[gi][wi] = (w4[j] & 0x80000000u) ? 0u : 0xffffffffu;
+                    qf[gi][wi] = __uint_as_float(w4[j]);
+                  }
                 }
               }
             }
@@ -617,11 +670,16 @@ cstep_kernel(const StepArgs a) {
         const int ct = (un.P - 1) / CHUNK;                  // chunk of the tail page
         const int pin = (un.P - 1) - ct * CHUNK;
         const int m_tail = ct - mc0;
-        const bool tail_mine = un.app && m_tail >= 0 && m_tail < nm && pg == pin % PPR;
+        const bool tail_warp = un.app && m_tail >= 0 && m_tail < nm;
+        const bool tail_mine = tail_warp && pg == pin % PPR;
         const int ro_t = pin / PPR;
         constexpr int KNV = F8 ? 2 * VPL : VPL;             // 16-byte vectors of k per lane
         uint4 kn[KNV];
-        if (tail_mine) {
+        uint2 kq = make_uint2(0u, 0u);                      // MMA bound: dims 4 lane .. + 3
+        if (Sh::MMAS && tail_warp && lane < D / 4)
+          kq = *reinterpret_cast<const uint2*>(static_cast<const T*>(a.k_new) +
+                                               ((size_t)un.r * a.h_kv + un.g) * D + 4 * lane);
+        if (!Sh::MMAS && tail_mine) {
           const T* kp = static_cast<const T*>(a.k_new) + ((size_t)un.r * a.h_kv + un.g) * D;
 #pragma unroll
           for (int v = 0; v < VPL; ++v)
@@ -649,135 +707,230 @@ cstep_kernel(const StepArgs a) {
           const unsigned bad = __ballot_sync(FULL, lane < np && !(phm >= 0 && phm < a.n_phys));
           if (bad && lane == 0) report(a.err, QUEST_DEVERR_PAGE_RANGE);
           const unsigned char* sb = buf + (m % NQ) * CHB;
-          float vals[Sh::NV];
-#pragma unroll
-          for (int ro = 0; ro < NR; ++ro) {
-            const int p = ro * PPR + pg;
-            uint4 vm[VPL], vM[VPL];
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) {
-              vm[v] = *reinterpret_cast<const uint4*>(sb + p * SUMB + (v * LPP + sub) * 16);
-              vM[v] = *reinterpret_cast<const uint4*>(sb + p * SUMB + RB + (v * LPP + sub) * 16);
-            }
-            if (tail_mine && ro == ro_t && m == m_tail) {
-              // append (eq (8)): the new token's K/V into the pool, the summary
-              // of its page folded with the key (a fresh page starts from it)
+          if constexpr (Sh::MMAS) {
+            unsigned char* sbw = buf + (m % NQ) * CHB;
+            if (tail_warp && m == m_tail) {
+              // append (eq (8)): the new token's K/V into the pool, and the
+              // staged summary of its page folded with the key (a fresh page
+              // starts from it), written back to the cache; lane l takes dims
+              // 4l .. 4l + 3
               const int slot = (un.L - 1) % S;
               const int pp = __ldg(a.page_indices + un.lo + un.P - 1);
-              if (pp >= 0 && pp < a.n_phys) {
-                const T* vp = static_cast<const T*>(a.v_new) + ((size_t)un.r * a.h_kv + un.g) * D;
-                T* kd = static_cast<T*>(a.k_pool) + (((size_t)pp * a.h_kv + un.g) * S + slot) * D;
-                T* vd = static_cast<T*>(a.v_pool) + (((size_t)pp * a.h_kv + un.g) * S + slot) * D;
-                bool ovf = false;
-#pragma unroll
-                for (int v = 0; v < VPL; ++v) {
-                  const int d0 = (v * LPP + sub) * VECS;
-#pragma unroll
-                  for (int h = 0; h < (F8 ? 2 : 1); ++h) {
-                    st_v4(kd + d0 + h * 8, kn[v * (F8 ? 2 : 1) + h]);
-                    st_v4(vd + d0 + h * 8, ld_nc_v4(vp + d0 + h * 8));
+              if (pp >= 0 && pp < a.n_phys && lane < D / 4) {
+                const size_t row = ((size_t)pp * a.h_kv + un.g) * S + slot;
+                *reinterpret_cast<uint2*>(static_cast<T*>(a.k_pool) + row * D + 4 * lane) = kq;
+                *reinterpret_cast<uint2*>(static_cast<T*>(a.v_pool) + row * D + 4 * lane) =
+                    *reinterpret_cast<const uint2*>(static_cast<const T*>(a.v_new) +
+                                                    ((size_t)un.r * a.h_kv + un.g) * D + 4 * lane);
+                unsigned char* gs = static_cast<unsigned char*>(a.summary) + ((size_t)pp * a.h_kv + un.g) * SUMB;
+                if constexpr (F8) {
+                  const int bm = 4 * lane, bM = D + 4 * lane;   // code bytes of m, M
+                  uint32_t* sm_m = reinterpret_cast<uint32_t*>(sbw + sw_off<SUMB>(pin, bm));
+                  uint32_t* sm_M = reinterpret_cast<uint32_t*>(sbw + sw_off<SUMB>(pin, bM));
+                  uint32_t m01 = KO::to_key(kq.x), m23 = KO::to_key(kq.y);
+                  uint32_t M01 = m01, M23 = m23;
+                  if (slot != 0) {
+                    m01 = KO::kmin(KO::to_key(e4m3x4_lo_h2(*sm_m)), m01);
+                    m23 = KO::kmin(KO::to_key(e4m3x4_hi_h2(*sm_m)), m23);
+                    M01 = KO::kmax(KO::to_key(e4m3x4_lo_h2(*sm_M)), M01);
+                    M23 = KO::kmax(KO::to_key(e4m3x4_hi_h2(*sm_M)), M23);
                   }
-                  if constexpr (F8) {
-                    // the old codes decode exactly to fp16; fold the key in,
-                    // round out again (min down, max up)
-                    const uint32_t om[4] = {vm[v].x, vm[v].y, vm[v].z, vm[v].w};
-                    const uint32_t oM[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
-                    const uint32_t kw[8] = {kn[2 * v].x, kn[2 * v].y, kn[2 * v].z, kn[2 * v].w,
-                                            kn[2 * v + 1].x, kn[2 * v + 1].y, kn[2 * v + 1].z,
-                                            kn[2 * v + 1].w};
-                    uint32_t c8m[4], c8M[4];
-#pragma unroll
-                    for (int cw4 = 0; cw4 < 4; ++cw4) {
-                      uint32_t m01 = KO::to_key(kw[2 * cw4]), m23 = KO::to_key(kw[2 * cw4 + 1]);
-                      uint32_t M01 = m01, M23 = m23;
-                      if (slot != 0) {
-                        m01 = KO::kmin(KO::to_key(e4m3x4_lo_h2(om[cw4])), m01);
-                        m23 = KO::kmin(KO::to_key(e4m3x4_hi_h2(om[cw4])), m23);
-                        M01 = KO::kmax(KO::to_key(e4m3x4_lo_h2(oM[cw4])), M01);
-                        M23 = KO::kmax(KO::to_key(e4m3x4_hi_h2(oM[cw4])), M23);
-                      }
-                      c8m[cw4] = e4m3x4_floor_h(KO::from_key(m01), KO::from_key(m23), ovf);
-                      c8M[cw4] = e4m3x4_ceil_h(KO::from_key(M01), KO::from_key(M23), ovf);
-                    }
-                    vm[v] = make_uint4(c8m[0], c8m[1], c8m[2], c8m[3]);
-                    vM[v] = make_uint4(c8M[0], c8M[1], c8M[2], c8M[3]);
-                  } else {
-                    const uint4 k4 = kn[v];
-                    uint4 mn, mx;
-                    if (slot == 0) {
-                      mn = make_uint4(KO::to_key(k4.x), KO::to_key(k4.y), KO::to_key(k4.z), KO::to_key(k4.w));
-                      mx = mn;
-                    } else {
-                      mn = make_uint4(KO::kmin(KO::to_key(vm[v].x), KO::to_key(k4.x)),
-                                      KO::kmin(KO::to_key(vm[v].y), KO::to_key(k4.y)),
-                                      KO::kmin(KO::to_key(vm[v].z), KO::to_key(k4.z)),
-                                      KO::kmin(KO::to_key(vm[v].w), KO::to_key(k4.w)));
-                      mx = make_uint4(KO::kmax(KO::to_key(vM[v].x), KO::to_key(k4.x)),
-                                      KO::kmax(KO::to_key(vM[v].y), KO::to_key(k4.y)),
-                                      KO::kmax(KO::to_key(vM[v].z), KO::to_key(k4.z)),
-                                      KO::kmax(KO::to_key(vM[v].w), KO::to_key(k4.w)));
-                    }
-                    vm[v] = make_uint4(KO::from_key(mn.x), KO::from_key(mn.y), KO::from_key(mn.z), KO::from_key(mn.w));
-                    vM[v] = make_uint4(KO::from_key(mx.x), KO::from_key(mx.y), KO::from_key(mx.z), KO::from_key(mx.w));
+                  bool ovf = false;
+                  const uint32_t cm = e4m3x4_floor_h(KO::from_key(m01), KO::from_key(m23), ovf);
+                  const uint32_t cM = e4m3x4_ceil_h(KO::from_key(M01), KO::from_key(M23), ovf);
+                  *sm_m = cm;
+                  *sm_M = cM;
+                  *reinterpret_cast<uint32_t*>(gs + bm) = cm;
+                  *reinterpret_cast<uint32_t*>(gs + bM) = cM;
+                  if (ovf) report(a.err, QUEST_DEVERR_FP8_RANGE);
+                } else {
+                  const int bm = 8 * lane, bM = 2 * D + 8 * lane;   // bytes of m, M dims
+                  uint2* sm_m = reinterpret_cast<uint2*>(sbw + sw_off<SUMB>(pin, bm));
+                  uint2* sm_M = reinterpret_cast<uint2*>(sbw + sw_off<SUMB>(pin, bM));
+                  uint2 mn = make_uint2(KO::to_key(kq.x), KO::to_key(kq.y)), mx = mn;
+                  if (slot != 0) {
+                    const uint2 om = *sm_m, oM = *sm_M;
+                    mn = make_uint2(KO::kmin(KO::to_key(om.x), mn.x), KO::kmin(KO::to_key(om.y), mn.y));
+                    mx = make_uint2(KO::kmax(KO::to_key(oM.x), mx.x), KO::kmax(KO::to_key(oM.y), mx.y));
                   }
-                  unsigned char* sp = static_cast<unsigned char*>(a.summary) +
-                                      ((size_t)pp * a.h_kv + un.g) * SUMB + (v * LPP + sub) * 16;
-                  st_v4(sp, vm[v]);
-                  st_v4(sp + RB, vM[v]);
+                  const uint2 nm2 = make_uint2(KO::from_key(mn.x), KO::from_key(mn.y));
+                  const uint2 nM2 = make_uint2(KO::from_key(mx.x), KO::from_key(mx.y));
+                  *sm_m = nm2;
+                  *sm_M = nM2;
+                  *reinterpret_cast<uint2*>(gs + bm) = nm2;
+                  *reinterpret_cast<uint2*>(gs + bM) = nM2;
                 }
-                if (F8 && ovf) report(a.err, QUEST_DEVERR_FP8_RANGE);
+              }
+              __syncwarp();
+            }
+            // U for the chunk's pages, n-tile by n-tile: C[head][page] over
+            // the 2D summary elements, then the max over the group's heads
+            const int gid = lane >> 2, tq = lane & 3;
+#pragma unroll
+            for (int nt = 0; nt < Sh::NT8; ++nt) {
+              const int pr = nt * 8 + gid;                   // this lane's page of the tile
+              float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int kk = 0; kk < Sh::KT; ++kk) {
+                uint32_t b0, b1;
+                if constexpr (F8) {                          // 4 codes, decoded to fp16 pairs
+                  const uint32_t c = *reinterpret_cast<const uint32_t*>(sb + sw_off<SUMB>(pr, 16 * kk + 4 * tq));
+                  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b0) : "h"((uint16_t)c));
+                  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(b1) : "h"((uint16_t)(c >> 16)));
+                } else {
+                  const uint2 c = *reinterpret_cast<const uint2*>(sb + sw_off<SUMB>(pr, 32 * kk + 8 * tq));
+                  b0 = c.x;
+                  b1 = c.y;
+                }
+                if (kk & 1) mma_f16_16816(c1, qa[kk], 0u, qb[kk], 0u, b0, b1);
+                else mma_f16_16816(c0, qa[kk], 0u, qb[kk], 0u, b0, b1);
+              }
+              // rows gid < G are the heads (the rest of the 16 rows are zero)
+              float v0 = gid < G ? c0[0] + c1[0] : -INFINITY;
+              float v1 = gid < G ? c0[1] + c1[1] : -INFINITY;
+#pragma unroll
+              for (int o = 4; o < 32; o <<= 1) {
+                v0 = fmaxf(v0, __shfl_xor_sync(FULL, v0, o));
+                v1 = fmaxf(v1, __shfl_xor_sync(FULL, v1, o));
+              }
+              if (gid == 0) {
+                lg[nt * 8 + 2 * tq] = v0;
+                lg[nt * 8 + 2 * tq + 1] = v1;
               }
             }
-            // sum_j max(q_j m_j, q_j M_j) = sum_j q_j * (q_j >= 0 ? M_j : m_j)
+          } else {
+            float vals[Sh::NV];
 #pragma unroll
-            for (int gi = 0; gi < G; ++gi) {
-              float sg = 0.f;
+            for (int ro = 0; ro < NR; ++ro) {
+              const int p = ro * PPR + pg;
+              uint4 vm[VPL], vM[VPL];
 #pragma unroll
               for (int v = 0; v < VPL; ++v) {
-                const uint32_t mw[4] = {vm[v].x, vm[v].y, vm[v].z, vm[v].w};
-                const uint32_t Mw[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
+                vm[v] = *reinterpret_cast<const uint4*>(sb + p * SUMB + (v * LPP + sub) * 16);
+                vM[v] = *reinterpret_cast<const uint4*>(sb + p * SUMB + RB + (v * LPP + sub) * 16);
+              }
+              if (tail_mine && ro == ro_t && m == m_tail) {
+                // append (eq (8)): the new token's K/V into the pool, the summary
+                // of its page folded with the key (a fresh page starts from it)
+                const int slot = (un.L - 1) % S;
+                const int pp = __ldg(a.page_indices + un.lo + un.P - 1);
+                if (pp >= 0 && pp < a.n_phys) {
+                  const T* vp = static_cast<const T*>(a.v_new) + ((size_t)un.r * a.h_kv + un.g) * D;
+                  T* kd = static_cast<T*>(a.k_pool) + (((size_t)pp * a.h_kv + un.g) * S + slot) * D;
+                  T* vd = static_cast<T*>(a.v_pool) + (((size_t)pp * a.h_kv + un.g) * S + slot) * D;
+                  bool ovf = false;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  if constexpr (F8) {              // codes decoded to fp16 (exact), fp32 FMA
-                    const int wi = v * 8 + 2 * j;
-                    const uint32_t sel = e4m3_qsel_from_masks(qmask[gi][wi], qmask[gi][wi + 1]);
-                    const uint32_t xw = (Mw[j] & sel) | (mw[j] & ~sel);
-                    const float2 lo = e4m3x4_lo_f2(xw), hi = e4m3x4_hi_f2(xw);
-                    sg = fmaf(qf[gi][wi * 2 + 0], lo.x, sg);
-                    sg = fmaf(qf[gi][wi * 2 + 1], lo.y, sg);
-                    sg = fmaf(qf[gi][wi * 2 + 2], hi.x, sg);
-                    sg = fmaf(qf[gi][wi * 2 + 3], hi.y, sg);
-                  } else if constexpr (Sh::ES == 2) {
-                    const uint32_t mk = qmask[gi][v * 4 + j];
-                    const uint32_t xw = (Mw[j] & mk) | (mw[j] & ~mk);
-                    const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xw));
-                    sg = fmaf(qf[gi][(v * 4 + j) * 2 + 0], xf.x, sg);
-                    sg = fmaf(qf[gi][(v * 4 + j) * 2 + 1], xf.y, sg);
-                  } else {
-                    const uint32_t mk = qmask[gi][v * 4 + j];
-                    const uint32_t xw = (Mw[j] & mk) | (mw[j] & ~mk);
-                    sg = fmaf(qf[gi][v * 4 + j], __uint_as_float(xw), sg);
+                  for (int v = 0; v < VPL; ++v) {
+                    const int d0 = (v * LPP + sub) * VECS;
+#pragma unroll
+                    for (int h = 0; h < (F8 ? 2 : 1); ++h) {
+                      st_v4(kd + d0 + h * 8, kn[v * (F8 ? 2 : 1) + h]);
+                      st_v4(vd + d0 + h * 8, ld_nc_v4(vp + d0 + h * 8));
+                    }
+                    if constexpr (F8) {
+                      // the old codes decode exactly to fp16; fold the key in,
+                      // round out again (min down, max up)
+                      const uint32_t om[4] = {vm[v].x, vm[v].y, vm[v].z, vm[v].w};
+                      const uint32_t oM[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
+                      const uint32_t kw[8] = {kn[2 * v].x, kn[2 * v].y, kn[2 * v].z, kn[2 * v].w,
+                                              kn[2 * v + 1].x, kn[2 * v + 1].y, kn[2 * v + 1].z,
+                                              kn[2 * v + 1].w};
+                      uint32_t c8m[4], c8M[4];
+#pragma unroll
+                      for (int cw4 = 0; cw4 < 4; ++cw4) {
+                        uint32_t m01 = KO::to_key(kw[2 * cw4]), m23 = KO::to_key(kw[2 * cw4 + 1]);
+                        uint32_t M01 = m01, M23 = m23;
+                        if (slot != 0) {
+                          m01 = KO::kmin(KO::to_key(e4m3x4_lo_h2(om[cw4])), m01);
+                          m23 = KO::kmin(KO::to_key(e4m3x4_hi_h2(om[cw4])), m23);
+                          M01 = KO::kmax(KO::to_key(e4m3x4_lo_h2(oM[cw4])), M01);
+                          M23 = KO::kmax(KO::to_key(e4m3x4_hi_h2(oM[cw4])), M23);
+                        }
+                        c8m[cw4] = e4m3x4_floor_h(KO::from_key(m01), KO::from_key(m23), ovf);
+                        c8M[cw4] = e4m3x4_ceil_h(KO::from_key(M01), KO::from_key(M23), ovf);
+                      }
+                      vm[v] = make_uint4(c8m[0], c8m[1], c8m[2], c8m[3]);
+                      vM[v] = make_uint4(c8M[0], c8M[1], c8M[2], c8M[3]);
+                    } else {
+                      const uint4 k4 = kn[v];
+                      uint4 mn, mx;
+                      if (slot == 0) {
+                        mn = make_uint4(KO::to_key(k4.x), KO::to_key(k4.y), KO::to_key(k4.z), KO::to_key(k4.w));
+                        mx = mn;
+                      } else {
+                        mn = make_uint4(KO::kmin(KO::to_key(vm[v].x), KO::to_key(k4.x)),
+                                        KO::kmin(KO::to_key(vm[v].y), KO::to_key(k4.y)),
+                                        KO::kmin(KO::to_key(vm[v].z), KO::to_key(k4.z)),
+                                        KO::kmin(KO::to_key(vm[v].w), KO::to_key(k4.w)));
+                        mx = make_uint4(KO::kmax(KO::to_key(vM[v].x), KO::to_key(k4.x)),
+                                        KO::kmax(KO::to_key(vM[v].y), KO::to_key(k4.y)),
+                                        KO::kmax(KO::to_key(vM[v].z), KO::to_key(k4.z)),
+                                        KO::kmax(KO::to_key(vM[v].w), KO::to_key(k4.w)));
+                      }
+                      vm[v] = make_uint4(KO::from_key(mn.x), KO::from_key(mn.y), KO::from_key(mn.z), KO::from_key(mn.w));
+                      vM[v] = make_uint4(KO::from_key(mx.x), KO::from_key(mx.y), KO::from_key(mx.z), KO::from_key(mx.w));
+                    }
+                    unsigned char* sp = static_cast<unsigned char*>(a.summary) +
+                                        ((size_t)pp * a.h_kv + un.g) * SUMB + (v * LPP + sub) * 16;
+                    st_v4(sp, vm[v]);
+                    st_v4(sp + RB, vM[v]);
                   }
+                  if (F8 && ovf) report(a.err, QUEST_DEVERR_FP8_RANGE);
                 }
               }
-              vals[gi * NR + ro] = sg;
-            }
-          }
-          // sums over the LPP lanes of each page, then the group max
-          sub_reduce<Sh::NV, LPP / 2>(vals, lane);
-          {
-            constexpr int NF = Sh::NV / LPP > 1 ? Sh::NV / LPP : 1;
-            const int base = sub_base<Sh::NV, LPP / 2>(lane);
+              // sum_j max(q_j m_j, q_j M_j) = sum_j q_j * (q_j >= 0 ? M_j : m_j)
 #pragma unroll
-            for (int i = 0; i < NF; ++i) lg[(base + i) * PPR + pg] = vals[i];
+              for (int gi = 0; gi < G; ++gi) {
+                float sg = 0.f;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) {
+                  const uint32_t mw[4] = {vm[v].x, vm[v].y, vm[v].z, vm[v].w};
+                  const uint32_t Mw[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    if constexpr (F8) {              // codes decoded to fp16 (exact), fp32 FMA
+                      const int wi = v * 8 + 2 * j;
+                      const uint32_t sel = e4m3_qsel_from_masks(qmask[gi][wi], qmask[gi][wi + 1]);
+                      const uint32_t xw = (Mw[j] & sel) | (mw[j] & ~sel);
+                      const float2 lo = e4m3x4_lo_f2(xw), hi = e4m3x4_hi_f2(xw);
+                      sg = fmaf(qf[gi][wi * 2 + 0], lo.x, sg);
+                      sg = fmaf(qf[gi][wi * 2 + 1], lo.y, sg);
+                      sg = fmaf(qf[gi][wi * 2 + 2], hi.x, sg);
+                      sg = fmaf(qf[gi][wi * 2 + 3], hi.y, sg);
+                    } else if constexpr (Sh::ES == 2) {
+                      const uint32_t mk = qmask[gi][v * 4 + j];
+                      const uint32_t xw = (Mw[j] & mk) | (mw[j] & ~mk);
+                      const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xw));
+                      sg = fmaf(qf[gi][(v * 4 + j) * 2 + 0], xf.x, sg);
+                      sg = fmaf(qf[gi][(v * 4 + j) * 2 + 1], xf.y, sg);
+                    } else {
+                      const uint32_t mk = qmask[gi][v * 4 + j];
+                      const uint32_t xw = (Mw[j] & mk) | (mw[j] & ~mk);
+                      sg = fmaf(qf[gi][v * 4 + j], __uint_as_float(xw), sg);
+                    }
+                  }
+                }
+                vals[gi * NR + ro] = sg;
+              }
+            }
+            // sums over the LPP lanes of each page, then the group max
+            sub_reduce<Sh::NV, LPP / 2>(vals, lane);
+            {
+              constexpr int NF = Sh::NV / LPP > 1 ? Sh::NV / LPP : 1;
+              const int base = sub_base<Sh::NV, LPP / 2>(lane);
+#pragma unroll
+              for (int i = 0; i < NF; ++i) lg[(base + i) * PPR + pg] = vals[i];
+            }
           }
           __syncwarp();
           if (lane < np) {
             float sc = -INFINITY;
             if (!((bad >> lane) & 1u)) {
               sc = lg[lane];
+              if constexpr (!Sh::MMAS) {
 #pragma unroll
-              for (int gi = 1; gi < G; ++gi) sc = fmaxf(sc, lg[gi * NR * PPR + lane]);
+                for (int gi = 1; gi < G; ++gi) sc = fmaxf(sc, lg[gi * NR * PPR + lane]);
+              }
             }
             if (cached) {
               const uint32_t key = score_key(sc);
@@ -865,54 +1018,118 @@ cstep_kernel(const StepArgs a) {
             l = r ? __ffs(r) - 1 : -1;
             s = 0;
           };
-          auto issue_half = [&](int l, int s, int half) {   // K (half 0) or V (half 1) of an item
-            const int pk = __shfl_sync(FULL, ph, l);
-            if (lane == 0) {
-              uint64_t* bar = half ? vbar : kbar;
-              mbar_arrive_tx(bar, HALF);
-              bulk_g2s_hint(buf + half * HALF,
-                            static_cast<const unsigned char*>(half ? a.v_pool : a.k_pool) +
-                                ((size_t)pk * a.h_kv + un.g) * BLK + (size_t)s * HALF,
-                            HALF, bar, pol);
+          if constexpr (Sh::MMAA) {
+            // 16-byte pieces by cp.async into swizzled rows (conflict-free
+            // ldmatrix); one commit group per half, K and V of an item
+            constexpr int KRB = D * Sh::ES;                  // bytes of a K (V) row
+            auto issue_half = [&](int l, int s, int half) {
+              const int pk = __shfl_sync(FULL, ph, l);
+              const unsigned char* src = static_cast<const unsigned char*>(half ? a.v_pool : a.k_pool) +
+                                         ((size_t)pk * a.h_kv + un.g) * BLK + (size_t)s * HALF;
+              unsigned char* dst = buf + half * HALF;
+#pragma unroll
+              for (int k = 0; k < HALF / 512; ++k) {
+                const int pc = k * 32 + lane;               // 16-byte piece of the sub-block
+                cp_async16(dst + W::sw(pc / (KRB / 16), pc % (KRB / 16)), src + (size_t)pc * 16);
+              }
+              cp_async_commit_grp();
+            };
+            if (li >= 0) {
+              issue_half(li, 0, 0);
+              issue_half(li, 0, 1);
             }
-            if (half) vpend = true; else kpend = true;
-          };
-          if (li >= 0) {
-            issue_half(li, 0, 0);
-            issue_half(li, 0, 1);
-          }
-          if (!inited) {
-            st.init(qrow, a.scale_log2, lane);
-            inited = true;
-          }
-          while (li >= 0) {
-            const int vk = min(Sh::TB, __shfl_sync(FULL, valid, li) - sb * Sh::TB);
-            int l1 = li, s1 = sb;
-            next_item(l1, s1);
-            if (!cwait_warp(kbar, kph & 1, s_abort, a.err, lim)) { dead = true; break; }
-            ++kph;
-            kpend = false;
-            st.qk(reinterpret_cast<const T*>(buf), vk, lg, lane);
-            if (l1 >= 0) issue_half(l1, s1, 0);          // the next K while this V is folded
-            if (!cwait_warp(vbar, vph & 1, s_abort, a.err, lim)) { dead = true; break; }
-            ++vph;
-            vpend = false;
-            st.av(reinterpret_cast<const T*>(buf + HALF), vk, lg, lane);
-            if (l1 >= 0) issue_half(l1, s1, 1);
-            if (u == 0 && cw == 0 && lane == 0 && i0 == 0 && vph == 1) stamp(4);
-            li = l1;
-            sb = s1;
+            if (!inited) {
+              st.init(qrow, a.scale_log2, lane);
+              inited = true;
+            }
+            __half* ps = reinterpret_cast<__half*>(lg);
+            const uint32_t kb = smem_u32(buf), vb = smem_u32(buf + HALF);
+            while (li >= 0) {
+              const int vk = min(Sh::TB, __shfl_sync(FULL, valid, li) - sb * Sh::TB);
+              int l1 = li, s1 = sb;
+              next_item(l1, s1);
+              if constexpr (Sh::TB == 16) {
+                cp_async_wait_grp<1>();                     // this K (its V may still stream)
+                __syncwarp();
+                st.qk(kb, vk, ps, lane);
+                if (l1 >= 0) {
+                  issue_half(l1, s1, 0);                    // the next K while this V is folded
+                  cp_async_wait_grp<1>();
+                } else {
+                  cp_async_wait_grp<0>();
+                }
+                __syncwarp();
+                st.av(vb, vk, ps, lane);
+                __syncwarp();
+                if (l1 >= 0) issue_half(l1, s1, 1);
+              } else {                                      // several tiles: each folds whole
+                cp_async_wait_grp<0>();
+                __syncwarp();
+                for (int j = 0; j * 16 < vk; ++j) {
+                  st.qk(kb + j * 16 * KRB, vk - j * 16, ps, lane);
+                  st.av(vb + j * 16 * KRB, vk - j * 16, ps, lane);
+                }
+                __syncwarp();
+                if (l1 >= 0) {
+                  issue_half(l1, s1, 0);
+                  issue_half(l1, s1, 1);
+                }
+              }
+              if (u == 0 && cw == 0 && lane == 0 && i0 == 0 && li == __ffs(rem) - 1 && sb == 0) stamp(4);
+              li = l1;
+              sb = s1;
+            }
+          } else {
+            auto issue_half = [&](int l, int s, int half) {   // K (half 0) or V (half 1) of an item
+              const int pk = __shfl_sync(FULL, ph, l);
+              if (lane == 0) {
+                uint64_t* bar = half ? vbar : kbar;
+                mbar_arrive_tx(bar, HALF);
+                bulk_g2s_hint(buf + half * HALF,
+                              static_cast<const unsigned char*>(half ? a.v_pool : a.k_pool) +
+                                  ((size_t)pk * a.h_kv + un.g) * BLK + (size_t)s * HALF,
+                              HALF, bar, pol);
+              }
+              if (half) vpend = true; else kpend = true;
+            };
+            if (li >= 0) {
+              issue_half(li, 0, 0);
+              issue_half(li, 0, 1);
+            }
+            if (!inited) {
+              st.init(qrow, a.scale_log2, lane);
+              inited = true;
+            }
+            while (li >= 0) {
+              const int vk = min(Sh::TB, __shfl_sync(FULL, valid, li) - sb * Sh::TB);
+              int l1 = li, s1 = sb;
+              next_item(l1, s1);
+              if (!cwait_warp(kbar, kph & 1, s_abort, a.err, lim)) { dead = true; break; }
+              ++kph;
+              kpend = false;
+              st.qk(reinterpret_cast<const T*>(buf), vk, lg, lane);
+              if (l1 >= 0) issue_half(l1, s1, 0);          // the next K while this V is folded
+              if (!cwait_warp(vbar, vph & 1, s_abort, a.err, lim)) { dead = true; break; }
+              ++vph;
+              vpend = false;
+              st.av(reinterpret_cast<const T*>(buf + HALF), vk, lg, lane);
+              if (l1 >= 0) issue_half(l1, s1, 1);
+              if (u == 0 && cw == 0 && lane == 0 && i0 == 0 && vph == 1) stamp(4);
+              li = l1;
+              sb = s1;
+            }
           }
         }
         if (dead) break;
         if (!inited) st.init(qrow, a.scale_log2, lane);   // no pages: the empty state
-        if (u >= 2 && !cwait_warp(stash_free + b, ((u >> 1) - 1) & 1, s_abort, a.err, lim)) {
+        const int sbf = u % Sh::NSTASH, ku = u / Sh::NSTASH;   // stash slot, its use number
+        if (ku >= 1 && !cwait_warp(stash_free + sbf, (ku - 1) & 1, s_abort, a.err, lim)) {
           dead = true;
           break;
         }
-        st.stash(sto + (size_t)b * NCW * G * D, stml + (size_t)b * NCW * G * 2, cw, lane);
+        st.stash(sto + (size_t)sbf * NCW * G * D, stml + (size_t)sbf * NCW * G * 2, cw, lane);
         __syncwarp();
-        if (lane == 0) arrive_local(attn_done + b);
+        if (lane == 0) arrive_local(attn_done + sbf);
       }
     }
     // nothing may still be copying into this warp's buffer when the CTA exits
@@ -981,9 +1198,10 @@ cstep_kernel(const StepArgs a) {
         const int u = t - 1, b = u & 1;
         const CUnit un = units[u];
         const int owner = u % kCL;
-        if (!gwait(attn_done + b, (u >> 1) & 1)) { dead = true; break; }
-        const float* mo = sto + (size_t)b * NCW * G * D;
-        const float* ml = stml + (size_t)b * NCW * G * 2;
+        const int sbf = u % Sh::NSTASH;          // stash slot of the unit
+        if (!gwait(attn_done + sbf, (u / Sh::NSTASH) & 1)) { dead = true; break; }
+        const float* mo = sto + (size_t)sbf * NCW * G * D;
+        const float* ml = stml + (size_t)sbf * NCW * G * 2;
         const uint32_t po = cl_map(smem_u32(part), owner);
         const uint32_t pm = cl_map(smem_u32(partml), owner);
         for (int idx = gt; idx < G * D; idx += kCSelT) {
@@ -1009,7 +1227,7 @@ cstep_kernel(const StepArgs a) {
         SelGrp::sync();                           // the group's stores precede the release
         if (gt == 0) {
           arrive_cl(part_full, owner);
-          arrive_local(stash_free + b);          // the consumers may stash unit u + 2
+          arrive_local(stash_free + sbf);        // the consumers may stash unit u + NSTASH
         }
         if ((int)rank == owner) {
           if (!gwait(part_full, (u / kCL) & 1)) { dead = true; break; }
@@ -1097,9 +1315,17 @@ cudaError_t cstep_launch_sg(const StepArgs& a, const StepPlan& p, cudaStream_t s
   if (a.page_size == 16) {
     if (a.group == 1) return cstep_launch<T, D, 16, 1, F8>(a, p, s);
     if (a.group == 2) return cstep_launch<T, D, 16, 2, F8>(a, p, s);
+    if constexpr (sizeof(T) == 2) {          // groups of 4 and 8: fp16 K/V (the warp MMA)
+      if (a.group == 4) return cstep_launch<T, D, 16, 4, F8>(a, p, s);
+      if (a.group == 8) return cstep_launch<T, D, 16, 8, F8>(a, p, s);
+    }
   } else {
     if (a.group == 1) return cstep_launch<T, D, 32, 1, F8>(a, p, s);
     if (a.group == 2) return cstep_launch<T, D, 32, 2, F8>(a, p, s);
+    if constexpr (sizeof(T) == 2) {
+      if (a.group == 4) return cstep_launch<T, D, 32, 4, F8>(a, p, s);
+      if (a.group == 8) return cstep_launch<T, D, 32, 8, F8>(a, p, s);
+    }
   }
   return cudaErrorInvalidValue;
 }
@@ -1109,9 +1335,17 @@ int cstep_clusters_sg(int dev, int page_size, int group) {
   if (page_size == 16) {
     if (group == 1) return cstep_clusters<T, D, 16, 1, F8>(dev);
     if (group == 2) return cstep_clusters<T, D, 16, 2, F8>(dev);
+    if constexpr (sizeof(T) == 2) {
+      if (group == 4) return cstep_clusters<T, D, 16, 4, F8>(dev);
+      if (group == 8) return cstep_clusters<T, D, 16, 8, F8>(dev);
+    }
   } else if (page_size == 32) {
     if (group == 1) return cstep_clusters<T, D, 32, 1, F8>(dev);
     if (group == 2) return cstep_clusters<T, D, 32, 2, F8>(dev);
+    if constexpr (sizeof(T) == 2) {
+      if (group == 4) return cstep_clusters<T, D, 32, 4, F8>(dev);
+      if (group == 8) return cstep_clusters<T, D, 32, 8, F8>(dev);
+    }
   }
   return -1;
 }

@@ -17,7 +17,9 @@ namespace {
 StepPlan plan_cstep(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
                     int32_t page_size, int32_t dtype, int32_t summary_fp8) {
   StepPlan p{};
-  if (group > 2 || (head_dim != 64 && head_dim != 128) || (page_size != 16 && page_size != 32))
+  // groups of 4 and 8 only with fp16 K/V (their attention runs on the warp MMA)
+  const bool g_ok = group == 1 || group == 2 || ((group == 4 || group == 8) && dtype == QUEST_F16);
+  if (!g_ok || (head_dim != 64 && head_dim != 128) || (page_size != 16 && page_size != 32))
     return p;
   if (summary_fp8 && dtype != QUEST_F16) return p;
   if (getenv("QUEST_STEP_LEGACY")) return p;     // the grid-wide kernel instead (comparisons)

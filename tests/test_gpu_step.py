@@ -128,8 +128,8 @@ def _w(name, **kw):
 
 @pytest.fixture(params=["cluster", "grid"])
 def kernel(request, monkeypatch):
-    """Groups 1 and 2 run on the cluster kernel; QUEST_STEP_LEGACY selects
-    the grid-wide kernel (the one groups 4 and 8 always take) instead."""
+    """The cluster kernel runs groups 1 and 2 (and 4 and 8 with fp16 K/V);
+    QUEST_STEP_LEGACY selects the grid-wide kernel instead."""
     if request.param == "grid":
         monkeypatch.setenv("QUEST_STEP_LEGACY", "1")
     return request.param
@@ -141,13 +141,21 @@ def test_step_mha_crosses_page_boundaries(kernel):
 
 
 @pytest.mark.parametrize("group", [2, 4, 8])
-def test_step_gqa_ragged(group):
+def test_step_gqa_ragged(group, kernel):
     _run(_w("gqa", batch=5, h_kv=2, group=group, k=24), [1, 15, 16, 17, 900], steps=2,
          seed=2 + group)
 
 
 def test_step_page32_fp16():
     _run(_w("p32", batch=2, h_kv=3, page_size=32, k=8), [31, 500], steps=3, seed=7)
+
+
+@pytest.mark.parametrize("group,S,d", [(4, 32, 64), (8, 32, 128), (4, 16, 64), (8, 32, 64)])
+def test_step_gqa_tiles(group, S, d, kernel):
+    """Groups of 4 and 8 over every page size and head dim: sub-blocks of one
+    and of two 16-token attention tiles, ragged last pages."""
+    _run(_w("gqa_t", batch=3, h_kv=2, group=group, head_dim=d, page_size=S, k=12),
+         [S + 3, 7 * S - 5, 40 * S + 1], steps=2, seed=30 + group + S + d)
 
 
 def test_step_fp32_d64():
@@ -165,7 +173,7 @@ def test_step_many_units(kernel):
          steps=1, seed=10)
 
 
-def test_step_units_above_grid():
+def test_step_units_above_grid(kernel):
     # more units than CTAs (one per SM at G = 4): CTAs select several units
     # each after scoring
     _run(_w("above", batch=20, h_kv=8, group=4, k=4, head_dim=64),
@@ -174,7 +182,7 @@ def test_step_units_above_grid():
 
 @pytest.mark.parametrize("group,lens", [(1, [70000, 900]), (1, [140000, 3000]),
                                         (4, [140000, 3000])])
-def test_step_long_rows(group, lens):
+def test_step_long_rows(group, lens, kernel):
     # rows above the 4096 and 8192 keys the selecting CTA caches in shared
     # memory (the second reads its keys from L2)
     _run(_w("long", batch=2, h_kv=2, group=group, k=64, head_dim=64), lens, steps=2,
@@ -196,7 +204,7 @@ def test_step_hybrid_budget(n_sink, n_local):
 
 @pytest.mark.parametrize("group,S,d", [(1, 16, 128), (4, 16, 128), (2, 32, 64), (8, 16, 64),
                                        (1, 32, 128)])
-def test_step_e4m3_summaries(group, S, d):
+def test_step_e4m3_summaries(group, S, d, kernel):
     """E4M3 summaries (Quest page §3, summary dtype): the fused append keeps
     the codes equal to the directed rounding of the exact summary, and the
     scores, selections and outputs follow the oracle on the rounded box."""
