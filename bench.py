@@ -199,10 +199,9 @@ class LayerSetup:
         self.table_np = t
         k_tok, v_tok, ind = wl.tokens_for_table(w, t, device=dev)
         self.q = wl.queries(w, lens - 1, device=dev)
-        # host copies of a few heads of request 0's inputs, for the oracle
+        # host copies of request 0's inputs (every head), for the oracle
         L0 = int(lens[0])
-        self.sample = (k_tok[:L0, :sample_heads].cpu(), v_tok[:L0, :sample_heads].cpu(),
-                       self.q[:1, :sample_heads * w.group].cpu())
+        self.sample = (k_tok[:L0].cpu(), v_tok[:L0].cpu(), self.q[:1].cpu())
         i32 = lambda a: torch.as_tensor(np.asarray(a, dtype=np.int32), device=dev)
         self.table = qs.PageTable(i32(t.page_indptr), i32(t.page_indices), i32(lens))
         kp, vp, sm = wl.empty_pool(t, h, d, w.dtype, device=dev, poison=False)
@@ -334,8 +333,8 @@ def ncu_traffic(kernel_key, workload):
         return None
     with open(p) as f:
         rec = json.load(f)
-    e = rec.get(kernel_key)
-    if not e or e.get("workload") != workload:
+    e = rec.get(f"{kernel_key}@{workload}")      # one record per kernel and workload
+    if not e:
         return None
     try:
         if e.get("source_hash") != source_hash(*e["sources"]):
@@ -354,13 +353,14 @@ class OracleSample:
     built from the generated inputs (never from the device path's results)."""
 
     def __init__(self, w: wl.Workload, k_tok, v_tok, q, heads: int, n_sink=0, n_local=0,
-                 summary_fp8=False):
+                 summary_fp8=False, k=None):
         from oracle import quest_oracle as qo
         self.qo = qo
         self.summary_fp8 = summary_fp8
         self.n_sink, self.n_local = n_sink, n_local
         self.heads = heads
         self.w = w
+        self.k = w.k if k is None else k          # pages selected (K = P: dense)
         L = int(w.lengths()[0])
         self.L = L
         t = wl.make_page_table([L], w.page_size, seed=w.seed)
@@ -387,7 +387,7 @@ class OracleSample:
         else:
             sc = qo.score_pages(self.q, self.sm, t.page_indptr, t.page_indices, w.group)
         sel, _, _ = qo.select_hybrid(sc, t.page_indptr, t.page_indices, np.array([self.L]),
-                                     w.page_size, w.k, self.n_sink, self.n_local)
+                                     w.page_size, self.k, self.n_sink, self.n_local)
         qo.sparse_attention(self.q, self.kp, self.vp, t.page_indptr, t.page_indices,
                             np.array([self.L], np.int32), sel, w.group)
 
@@ -398,10 +398,95 @@ class OracleSample:
             self.step()
             ts.append(time.perf_counter() - t0)
         # µs per full layer: all KV heads, all requests (by their pages)
-        lens = self.w.lengths().astype(np.int64)
-        pages = -(-lens // self.w.page_size)
-        scale = self.w.h_kv / self.heads * float(pages.sum()) / float(pages[0])
-        return [x * 1e6 * scale for x in ts]
+        return [x * 1e6 * self.w.h_kv / self.heads * pages_scale(self.w) for x in ts]
+
+
+def pages_scale(w: wl.Workload) -> float:
+    """All requests' pages over request 0's: the oracle samples request 0."""
+    lens = w.lengths().astype(np.int64)
+    pages = -(-lens // w.page_size)
+    return float(pages.sum()) / float(pages[0])
+
+
+def _oracle_proc(conn, barrier):
+    """A worker of OraclePool (a spawned process on one core): builds oracle
+    samples when asked, and times rounds over them, starting together with
+    the other workers at a barrier."""
+    torch.set_num_threads(1)
+    samples = []
+    while True:
+        msg = conn.recv()
+        if msg[0] == "build":
+            samples.append(OracleSample(*msg[1], **msg[2]))
+            conn.send(None)
+        elif msg[0] == "clear":
+            samples = []
+            conn.send(None)
+        elif msg[0] == "time":
+            for o in samples:                       # warm
+                o.step()
+            barrier.wait(timeout=600)
+            t0 = time.perf_counter()
+            for _ in range(msg[1]):
+                for o in samples:
+                    o.step()
+            conn.send((t0, time.perf_counter()))
+        else:
+            return
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OraclePool:
+    """The oracle on several host cores at once: one spawned single-threaded
+    process per core, each over its own (layer, KV head) units of request 0
+    (independent work), timed from a common start to the last finish."""
+
+    def __init__(self, n: int):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.n = n
+        self.barrier = ctx.Barrier(n)
+        self.conns, self.procs = [], []
+        for _ in range(n):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_proc, args=(b, self.barrier), daemon=True)
+            p.start()
+            self.conns.append(a)
+            self.procs.append(p)
+
+    def build(self, w, k_tok, v_tok, q, k=None, n_sink=0, n_local=0, summary_fp8=False):
+        """Worker i takes KV heads [i h_kv / n, (i + 1) h_kv / n) of these
+        inputs (request 0, one layer; all heads)."""
+        h, G = w.h_kv, w.group
+        for c in self.conns:
+            c.send(("clear",))
+            c.recv()
+        for i, c in enumerate(self.conns):
+            h0, h1 = i * h // self.n, (i + 1) * h // self.n
+            c.send(("build", (w, k_tok[:, h0:h1].contiguous(), v_tok[:, h0:h1].contiguous(),
+                              q[:, h0 * G:h1 * G].contiguous(), h1 - h0, n_sink, n_local),
+                    {"summary_fp8": summary_fp8, "k": k}))
+        for c in self.conns:
+            c.recv()
+
+    def time(self, rounds: int) -> float:
+        """Seconds per round of every worker's units."""
+        for c in self.conns:
+            c.send(("time", rounds))
+        res = [c.recv() for c in self.conns]
+        return (max(r[1] for r in res) - min(r[0] for r in res)) / rounds
+
+    def close(self):
+        for c in self.conns:
+            c.send(("stop",))
+        for p in self.procs:
+            p.join(timeout=30)
 
 
 # ---------------------------------------------------------------------------
@@ -561,12 +646,15 @@ def main(argv=None):
     pk, pk_src = peaks()
     value = ms_per_step * 1e3
     path_gbs = by["total"] / (value * 1e-6) / 1e9
-    # the dominant (only) kernel of the timed step is the fused step kernel
-    # the timed region launches only step_kernel, back to back on the replay
-    # stream: its average launch duration is the region's time per step
+    # the timed region launches only the fused step kernel (the cluster
+    # kernel or the grid-wide one, as the library plans this shape), back to
+    # back on the replay stream: its average launch duration is the region's
+    # time per step
+    kname = qs.decode_step_kernel(len(setup.lens), w.h_kv, w.group, w.head_dim, w.page_size,
+                                  w.dtype, setup.K, args.summary_fp8)
     dom_bytes = by["total"]
     dom_gbs = dom_bytes / (value * 1e-6) / 1e9
-    traffic = ncu_traffic("step_kernel", w.name)
+    traffic = ncu_traffic(kname, w.name + ("_e4m3" if args.summary_fp8 else ""))
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
@@ -579,7 +667,7 @@ def main(argv=None):
         "stage_us": {k: round(v, 3) for k, v in stage.items()},
         "path": {"bytes": by["total"], "GBps": round(path_gbs, 1),
                  "frac": round(path_gbs / pk, 4), "frac_of_8TBps": round(path_gbs / 8000, 4)},
-        "roofline": {"bound": "hbm", "kernel": "step_kernel", "achieved": round(dom_gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(dom_gbs, 1),
                      "peak": pk, "unit": "GB/s", "frac": round(dom_gbs / pk, 4),
                      "peak_source": pk_src, "bytes_per_launch": dom_bytes,
                      "traffic": traffic},
@@ -705,6 +793,17 @@ def run_model_step(args, w, cfg, dev, ws, rank, local):
                          "traffic": None},
             "gpu_launches": reps * w.layers}
     if rank == 0:
+        if args.cpu_seconds > 0:
+            v, v1, n, per = model_oracle(w, args.cpu_heads, args.cpu_seconds)
+            line["cpu_baseline"] = {
+                "value": round(v, 1), "unit": UNIT, "cores": n, "cores_1": round(v1, 1),
+                "kind": "oracle", "layers_us": per,
+                "sample": f"fp64 numpy oracle over layers {sorted(int(x) for x in per)} of the "
+                          f"{w.layers} (dense: K = P; sparse: the 2048-token budget), every KV "
+                          f"head on {n} single-threaded processes; the step is the dense layers' "
+                          f"time plus the sparse layers' mean times {w.layers - w.dense_layers}, "
+                          f"over {w.layers} layers; cores_1: {args.cpu_heads} heads on one core, "
+                          f"scaled"}
         print(json.dumps(line))
 
 
@@ -837,46 +936,138 @@ def run_e2e(setup, graphs, nb, n):
                       "step, 2 downloads to pinned memory; host waits on each step"}
 
 
-def cpu_baseline(setup, heads, seconds):
-    o = OracleSample(setup.w, *setup.sample, heads, setup.n_sink, setup.n_local,
-                     summary_fp8=setup.summary_fp8)
-    o.time_steps(1)
+def oracle_timings(w, k_tok, v_tok, q, heads, seconds, n_sink=0, n_local=0, summary_fp8=False,
+                   k=None, steps=None):
+    """The oracle's decode step of one layer (request 0's inputs, every head),
+    µs per layer (scaled to every request by pages): on one core over `heads`
+    heads (scaled to all heads), and on every host core (one process per core,
+    the KV heads split among them; at most one core per head). Each part takes
+    about `seconds` (and at most `steps` samples, at least 3). Returns
+    (one-core samples, all-core samples, cores used)."""
+    def more(ts, t0):
+        return len(ts) < 3 or (time.perf_counter() - t0 < seconds and
+                               (steps is None or len(ts) < steps))
+
+    h = min(heads, w.h_kv)
+    one = OracleSample(w, k_tok[:, :h], v_tok[:, :h], q[:, :h * w.group], h, n_sink, n_local,
+                       summary_fp8=summary_fp8, k=k)
+    one.time_steps(1)
     t0 = time.perf_counter()
-    ts = []
-    while time.perf_counter() - t0 < seconds or len(ts) < 3:
-        ts += o.time_steps(1)
-    return {"value": round(statistics.median(ts), 1), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": f"fp64 numpy oracle decode step (append, score, select, attention) on "
-                      f"{heads} of {setup.w.h_kv} heads of request 0 of the same layer, scaled "
-                      f"to every head and request by pages; {len(ts)} steps"}
+    ts1 = []
+    while more(ts1, t0):
+        ts1 += one.time_steps(1)
+    del one
+    n = min(host_cores(), w.h_kv)
+    pool = OraclePool(n)
+    try:
+        pool.build(w, k_tok, v_tok, q, k=k, n_sink=n_sink, n_local=n_local,
+                   summary_fp8=summary_fp8)
+        # a round (every head once) on n cores, from the one-core figure
+        est = statistics.median(ts1) * 1e-6 / pages_scale(w) / n
+        per = max(1, int(0.1 / est)) if est > 0 else 1       # rounds per sample (~0.1 s)
+        tsn, t0 = [], time.perf_counter()
+        while more(tsn, t0):
+            tsn.append(pool.time(per) * 1e6 * pages_scale(w))
+    finally:
+        pool.close()
+    return ts1, tsn, n
+
+
+def model_oracle(w, heads, seconds, layers=None):
+    """The oracle's whole decode step of a multi-layer model, as µs per layer
+    (the step over its layer count), from a stated subset of its layers:
+    every dense layer of the subset (K = P) and its sparse layers (K of the
+    2048-token budget) timed on every host core, each over all its KV heads
+    and inputs regenerated from the layer's seed; the step is the dense
+    layers' sum plus the sparse layers' mean times their count. On one core:
+    `heads` heads of the first dense and first sparse layer, scaled."""
+    L = int(w.lengths()[0])
+    S = w.page_size
+    P = -(-L // S)
+    Ks = wl.selection_budget(2048, S)
+    if layers is None:
+        layers = sorted({0, w.dense_layers - 1, w.dense_layers, w.layers - 1} - {-1})
+    n = min(host_cores(), w.h_kv)
+    per, one = {}, {}
+    pool = OraclePool(n)
+    try:
+        for layer in layers:
+            k_tok, v_tok = wl.request_tokens(w, 0, L, layer=layer)
+            q = wl.queries(w, [L - 1], layer=layer)[:1]
+            dense = layer < w.dense_layers
+            K = P if dense else Ks
+            pool.build(w, k_tok, v_tok, q, k=K)
+            ts, t0 = [], time.perf_counter()
+            while len(ts) < 3 or time.perf_counter() - t0 < seconds / (2 * len(layers)):
+                ts.append(pool.time(1) * 1e6)
+            per[layer] = statistics.median(ts)
+            if dense not in one:             # one core: a few heads of this kind of layer
+                o = OracleSample(w, k_tok[:, :heads], v_tok[:, :heads], q[:, :heads * w.group],
+                                 heads, k=K)
+                o.time_steps(1)
+                ts1, t0 = [], time.perf_counter()
+                while len(ts1) < 3 or time.perf_counter() - t0 < seconds / 4:
+                    ts1 += o.time_steps(1)
+                one[dense] = statistics.median(ts1)
+                del o
+            del k_tok, v_tok
+    finally:
+        pool.close()
+    dl = [per[x] for x in layers if x < w.dense_layers]
+    sl = [per[x] for x in layers if x >= w.dense_layers]
+    nd = w.dense_layers
+    whole = (sum(dl) / max(len(dl), 1)) * nd + (sum(sl) / max(len(sl), 1)) * (w.layers - nd)
+    whole1 = one.get(True, 0.0) * nd + one.get(False, 0.0) * (w.layers - nd)
+    return whole / w.layers, whole1 / w.layers, n, {str(x): round(per[x], 1) for x in layers}
+
+
+def cpu_baseline(setup, heads, seconds):
+    ts1, tsn, n = oracle_timings(setup.w, *setup.sample, heads, seconds / 2, setup.n_sink,
+                                 setup.n_local, summary_fp8=setup.summary_fp8)
+    return {"value": round(statistics.median(tsn), 1), "unit": UNIT, "cores": n,
+            "cores_1": round(statistics.median(ts1), 1), "kind": "oracle",
+            "sample": f"fp64 numpy oracle decode step (append, score, select, attention) of "
+                      f"request 0 of the same layer, scaled to every request by pages: on "
+                      f"{n} cores ({n} single-threaded processes over the {setup.w.h_kv} KV "
+                      f"heads, {len(tsn)} samples); cores_1: {heads} of the heads on one core, "
+                      f"scaled to all ({len(ts1)} steps)"}
 
 
 def run_reference(args, w, cfg, dev, ws):
-    """The oracle as the reference arm: same workload, metric and unit."""
+    """The oracle as the reference arm: same workload, metric and unit, on
+    every host core (and on one, reported beside it)."""
+    if w.layers > 1:
+        v, v1, n, per = model_oracle(w, args.cpu_heads, 60.0)
+        print(json.dumps({
+            "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": ws, "steps": 1,
+            "warmup": args.warmup, "ms_per_step": round(v * w.layers / 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": cfg, "impl": "reference",
+            "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": n,
+                             "cores_1": round(v1, 1), "kind": "oracle", "layers_us": per,
+                             "sample": f"layers {sorted(int(x) for x in per)}, every KV head, "
+                                       f"on {n} single-threaded processes; per layer of the "
+                                       f"{w.layers}-layer step"},
+            "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
     L = int(w.lengths()[0])
-    k_tok, v_tok = wl.request_tokens(w, 0, L, device=dev)
-    q = wl.queries(w, [L - 1], device=dev)
-    h = args.cpu_heads
-    o = OracleSample(w, k_tok[:, :h].cpu(), v_tok[:, :h].cpu(), q[:, :h * w.group].cpu(), h,
-                     args.n_sink, args.n_local, summary_fp8=args.summary_fp8)
-    del k_tok, v_tok
-    for _ in range(args.warmup):
-        o.time_steps(1)
-    # bounded: at most ~2 minutes of oracle work however many steps are asked
-    t0 = time.perf_counter()
-    ts = []
-    for _ in range(args.steps):
-        ts += o.time_steps(1)
-        if time.perf_counter() - t0 > 120:
-            break
-    v = statistics.median(ts)
+    k_tok, v_tok = wl.request_tokens(w, 0, L)
+    q = wl.queries(w, [L - 1])[:1]
+    # bounded: about a minute per part however many steps are asked
+    ts1, tsn, n = oracle_timings(w, k_tok, v_tok, q, args.cpu_heads, 60.0, args.n_sink,
+                                 args.n_local, summary_fp8=args.summary_fp8, steps=args.steps)
+    v = statistics.median(tsn)
     line = {"metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": ws,
-            "steps": len(ts), "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
+            "steps": len(tsn), "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "config": cfg, "impl": "reference",
-            "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{args.cpu_heads} of {w.h_kv} heads per step, scaled"},
+            "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": n,
+                             "cores_1": round(statistics.median(ts1), 1), "kind": "oracle",
+                             "sample": f"request 0 of the layer, every KV head, on {n} "
+                                       f"single-threaded processes, scaled to every request by "
+                                       f"pages; cores_1: {args.cpu_heads} heads on one core, "
+                                       f"scaled"},
             "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))

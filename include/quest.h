@@ -234,9 +234,12 @@ QUEST_API quest_status quest_sparse_decode_attn(const quest_cache* cache,
  * not call cudaMalloc (which can synchronise the device) once it is running.
  * The split-K partials go to a fixed 4 MiB buffer inside the library's own
  * module memory (one per device that loads the library, kept until the
- * process exits); the call allocates nothing. A problem whose partials need
- * more than 4 MiB (quest_attn_workspace_size(...) > 4 MiB) is rejected with
- * QUEST_ERR_WORKSPACE before anything is launched. The first call on a device
+ * process exits); the call allocates nothing. A problem whose partials, as
+ * planned for the cache's element type on the current device, need more than
+ * 4 MiB is rejected with QUEST_ERR_WORKSPACE before anything is launched.
+ * quest_attn_workspace_size(...) covers both element types, so a problem it
+ * sizes at 4 MiB or less is always accepted (an fp16 one somewhat above may
+ * be too). The first call on a device
  * looks up the buffer's device address (cudaGetSymbolAddress, with that device
  * current); make that first call before any stream capture. Every call shares
  * the one buffer and leaves its contents behind; no part of it needs to start
@@ -298,8 +301,7 @@ QUEST_API size_t quest_union_workspace_size(int32_t batch, int32_t h_kv, int32_t
  * quest_decode_step — one decode step of one layer in a single fused launch:
  * the append of one new token per request (optional), page scoring, Top-K
  * selection and sparse attention with its log-sum-exp merge (the four calls
- * above, Quest page Fig. 1 and §1.2/§2.1, in one persistent cooperative
- * kernel). Results equal those of quest_append_kv (one token per request at
+ * above, Quest page Fig. 1 and §1.2/§2.1, in one kernel). Results equal those of quest_append_kv (one token per request at
  * position seq_lens[r] - 1) followed by quest_score_pages, quest_select_topk
  * and quest_sparse_decode_attn on the same arguments.
  *   pages->seq_lens : lengths INCLUDING the new token
@@ -315,9 +317,13 @@ QUEST_API size_t quest_union_workspace_size(int32_t batch, int32_t h_kv, int32_t
  *                     that completes leaves its counters at zero again (after
  *                     a QUEST_DEVERR_WAIT_TIMEOUT, zero it again). Calls that
  *                     share a workspace must not overlap on the GPU.
- * Needs a device that can keep one 256-thread CTA per SM resident (the launch
- * is cooperative); returns QUEST_ERR_UNSUPPORTED for shapes whose shared
- * memory does not fit.
+ * Two kernels serve it (quest_decode_step_kernel tells which one a shape
+ * gets): a kernel on clusters of four CTAs, one cluster per group of
+ * (request, KV head) units, with the units' keys and partials exchanged in
+ * distributed shared memory (no workspace use beyond the size check); and a
+ * persistent cooperative kernel (one or two CTAs per SM, hand-offs through
+ * the workspace) for the shapes the first one does not take. Returns
+ * QUEST_ERR_UNSUPPORTED for shapes neither fits.
  */
 QUEST_API quest_status quest_decode_step(const quest_cache* cache, const quest_pages* pages,
                                          const void* k_new, const void* v_new,
@@ -334,6 +340,14 @@ QUEST_API quest_status quest_decode_step(const quest_cache* cache, const quest_p
 QUEST_API size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t h_kv, int32_t group,
                                              int32_t head_dim, int32_t page_size,
                                              int32_t dtype, int32_t k);
+
+/* Which kernel quest_decode_step launches for these sizes on the current
+ * device: 2 the cluster kernel (cstep_kernel), 1 the cooperative grid-wide
+ * kernel (step_kernel), 0 the shape is unsupported. summary_fp8 as in
+ * quest_cache. */
+QUEST_API int32_t quest_decode_step_kernel(int32_t batch, int32_t h_kv, int32_t group,
+                                           int32_t head_dim, int32_t page_size, int32_t dtype,
+                                           int32_t k, int32_t summary_fp8);
 
 /*
  * quest_recall_diagnostics — how well a selection covers dense attention, per
@@ -374,26 +388,36 @@ QUEST_API size_t quest_diag_workspace_size(int32_t h_kv, int32_t group, int32_t 
 
 /* Phase trace of quest_decode_step (profiling aid, off by default): with a
  * device buffer of at least 16 * max_ctas uint64 set, each later call whose
- * grid has at most max_ctas CTAs writes, per CTA, 16 %globaltimer stamps (ns):
- * [0] start, [1] scoring done, [2] selection done, [3..5] attention start /
- * pages done / merged, [6..7] first select started / last select done (CTAs
- * that select), [9] exit; [10..15] on CTAs that only select: polled / done of
- * their 1st..3rd select; on the others: descriptors loaded, first page done,
- * partials merged, final merges. NULL turns it off. Returns the grid size the
- * current device uses for these shapes (0 if the shape is unsupported). */
+ * grid has at most max_ctas CTAs writes, per CTA, 16 %globaltimer stamps (ns;
+ * a stamp a CTA does not reach stays as it was).
+ * Cluster kernel: [0] start, [1] the previous kernel on the stream waited
+ * for, [5] every CTA's keys of the first unit in, [10] its Top-K done, [11]
+ * its physical ids looked up, [6] its selection published, [4] the first
+ * attention tile of warp 0 done, [7] the last unit merged (owning CTA), [9]
+ * exit.
+ * Grid-wide kernel: [0] start, [1] scoring done, [2] selection done, [3..5]
+ * attention start / pages done / merged, [6..7] first select started / last
+ * select done (CTAs that select), [9] exit; [10..15] on CTAs that only
+ * select: polled / done of their 1st..3rd select; on the others: descriptors
+ * loaded, first page done, partials merged, final merges.
+ * NULL turns it off. Returns the grid size the current device uses for these
+ * shapes (0 if the shape is unsupported). */
 QUEST_API int32_t quest_set_trace(void* device_buffer, int32_t max_ctas, int32_t batch,
                                   int32_t h_kv, int32_t group, int32_t head_dim,
                                   int32_t page_size, int32_t dtype, int32_t k);
 
-/* Test hook of quest_decode_step's failure handling (no counterpart on the
- * pages). mode 0: normal operation. mode 1: later calls of the cluster kernel
- * (groups 1 and 2) make the first summary slot of each CTA's first unit wait
- * for bytes no copy delivers, so that wait runs out: the call then sets
- * QUEST_DEVERR_WAIT_TIMEOUT, stops issuing copies, drains those in flight
- * and returns with its outputs unspecified. wait_limit: tries of every
- * bounded in-kernel wait (each up to about 1 us); 0 restores the default
- * (about 2 s of waiting). Host state only (not thread-safe); returns
- * QUEST_ERR_INVALID_ARG for other values. */
+/* Test hook of the kernels' failure handling (no counterpart on the pages).
+ * mode 0: normal operation. mode 1: in later quest_decode_step calls that
+ * take the cluster kernel, warp 0 of the first CTA of each cluster first
+ * waits on a barrier nothing arrives on. mode 2: in later
+ * quest_sparse_decode_attn(_noalloc) and quest_union_decode_attn calls, the
+ * first copy slot of warp 0 of the first CTA expects 16 bytes more than its
+ * copies bring. Either way that wait runs out: the kernel sets
+ * QUEST_DEVERR_WAIT_TIMEOUT, issues no further copies, waits (bounded) for
+ * those in flight and returns, its outputs unspecified; the device stays
+ * usable. wait_limit: tries of every bounded in-kernel wait of those calls
+ * (each up to about 1 us); 0 restores the default (about 2 s). Process-wide
+ * host state; returns QUEST_ERR_INVALID_ARG for other values. */
 QUEST_API int32_t quest_test_step_fault(int32_t mode, int32_t wait_limit);
 
 /* Synchronises `stream`, returns the device error word of the current device

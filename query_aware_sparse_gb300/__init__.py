@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.quest_decode_step.restype = I32
         L.quest_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32]
         L.quest_decode_workspace_size.restype = SZ
+        L.quest_decode_step_kernel.argtypes = [I32, I32, I32, I32, I32, I32, I32, I32]
+        L.quest_decode_step_kernel.restype = I32
         L.quest_recall_diagnostics.argtypes = [P, P, P, I32, P, I32, I32, ctypes.c_float, P, P,
                                                P, P, P, SZ, P]
         L.quest_recall_diagnostics.restype = I32
@@ -98,7 +100,7 @@ EXPORTED = ("quest_append_kv", "quest_score_pages", "quest_score_pages_per_head"
             "quest_select_topk", "quest_union_decode_attn", "quest_union_workspace_size",
             "quest_sparse_decode_attn", "quest_sparse_decode_attn_noalloc",
             "quest_attn_workspace_size",
-            "quest_decode_step", "quest_decode_workspace_size",
+            "quest_decode_step", "quest_decode_workspace_size", "quest_decode_step_kernel",
             "quest_recall_diagnostics", "quest_diag_workspace_size", "quest_set_trace",
             "quest_test_step_fault", "quest_get_device_error", "quest_status_string")
 
@@ -336,6 +338,16 @@ class DecodeStep:
         return self.out, self.lse
 
 
+def decode_step_kernel(batch, h_kv, group, head_dim, page_size, dtype, k, summary_fp8=False) -> str:
+    """quest_decode_step_kernel: the kernel quest_decode_step launches for
+    these sizes on the current device ("cstep_kernel", "step_kernel", or ""
+    if unsupported)."""
+    r = int(lib().quest_decode_step_kernel(int(batch), int(h_kv), int(group), int(head_dim),
+                                           int(page_size), dtype_code(dtype), int(k),
+                                           int(bool(summary_fp8))))
+    return {2: "cstep_kernel", 1: "step_kernel"}.get(r, "")
+
+
 TRACE_NAMES = ("start", "scored", "selected", "att_start", "att_pages", "att_merged",
                "sel_begin", "sel_end", "", "exit",
                "sel0_polled | desc0", "sel0_done | page0", "sel1_polled | merged",
@@ -344,6 +356,10 @@ TRACE_NAMES = ("start", "scored", "selected", "att_start", "att_pages", "att_mer
 # select's end, on every CTA that selects; slots 10-15 depend on the CTA's
 # role: select stamps on dedicated selectors (the CTAs whose "scored" stamp
 # precedes any scoring), attention and final-merge stamps on the others
+
+# the cluster kernel's slots (unused ones empty)
+CTRACE_NAMES = ("start", "prev_waited", "", "", "att_tile0", "keys_in", "sel_published",
+                "merged_last", "", "exit", "topk_done", "phys_done", "", "", "", "")
 
 
 def set_trace(buffer, max_ctas=0, batch=0, h_kv=0, group=1, head_dim=128, page_size=16,
@@ -374,9 +390,10 @@ def sparse_decode_attn_noalloc(cache: PagedCache, table: PageTable, q, group: in
 
 
 def test_step_fault(mode: int, wait_limit: int = 0) -> None:
-    """quest_test_step_fault: mode 1 makes later decode steps (groups 1, 2)
-    wait for a copy that never comes, under `wait_limit` tries per wait (0 =
-    default); mode 0 restores normal operation."""
+    """quest_test_step_fault: mode 1 makes a wait of later decode steps on the
+    cluster kernel run out, mode 2 one of later attention calls; under
+    `wait_limit` tries per wait (0 = default). Mode 0 restores normal
+    operation."""
     _check(lib().quest_test_step_fault(int(mode), int(wait_limit)))
 
 

@@ -93,11 +93,14 @@ attn_split_kernel(const AttnArgs a) {
   const T* vbase = static_cast<const T*>(a.v_pool) + (size_t)g * head_block;
   const size_t page_stride = (size_t)a.h_kv * head_block;
 
+  // the failure-handling test: warp 0 of CTA 0 expects 16 bytes more in its
+  // first slot than the copies bring, so that slot's wait runs out
+  const uint32_t extra = (a.test_fault == 2 && blockIdx.x == 0 && w == 0) ? 16u : 0u;
   auto issue = [&](int n) {
     const int slot = n % kNST;
     const int pp = desc[n].x;
     T* dst = my_stage + (size_t)slot * 2 * head_block;
-    mbar_expect_tx(my_bars + slot, 2 * W::BLOCK_BYTES);
+    mbar_expect_tx(my_bars + slot, 2 * W::BLOCK_BYTES + (n == 0 ? extra : 0u));
     bulk_g2s_hint(dst, kbase + (size_t)pp * page_stride, W::BLOCK_BYTES, my_bars + slot, pol);
     bulk_g2s_hint(dst + head_block, vbase + (size_t)pp * page_stride, W::BLOCK_BYTES, my_bars + slot, pol);
   };
@@ -107,17 +110,24 @@ attn_split_kernel(const AttnArgs a) {
   W st;
   st.init(static_cast<const T*>(a.q) + ((size_t)r * h_q + g * G) * D, a.scale_log2, lane);
 
+  // a wait that runs out ends this warp's pages: no more copies are issued,
+  // the other slots' copies in flight are waited for (bounded), and the CTA
+  // writes an empty partial instead of merging through the stage area
+  bool dead = false;
   for (int n = 0; n < nv; ++n) {
     const int slot = n % kNST;
-    if (!mbar_wait_bounded(my_bars + slot, (n / kNST) & 1)) {
+    if (!warp_wait_bounded(my_bars + slot, (n / kNST) & 1, a.wait_limit)) {
       if (lane == 0) report(a.err, QUEST_DEVERR_WAIT_TIMEOUT);
-    } else {
-      const T* Kb = my_stage + (size_t)slot * 2 * head_block;
-      if constexpr (MASK)
-        st.page(Kb, Kb + head_block, desc[n].y & 0xff, lg, lane, (unsigned)desc[n].y >> 8);
-      else
-        st.page(Kb, Kb + head_block, desc[n].y & 0xff, lg, lane);
+      dead = true;
+      for (int m = n + 1; m < min(n + kNST, nv); ++m)
+        warp_wait_bounded(my_bars + m % kNST, (m / kNST) & 1, a.wait_limit);
+      break;
     }
+    const T* Kb = my_stage + (size_t)slot * 2 * head_block;
+    if constexpr (MASK)
+      st.page(Kb, Kb + head_block, desc[n].y & 0xff, lg, lane, (unsigned)desc[n].y >> 8);
+    else
+      st.page(Kb, Kb + head_block, desc[n].y & 0xff, lg, lane);
     __syncwarp();
     if (lane == 0 && n + kNST < nv) {
       fence_proxy_async_smem();
@@ -125,13 +135,22 @@ attn_split_kernel(const AttnArgs a) {
     }
   }
 
+  const size_t row0 = ((size_t)r * h_q + g * G) * a.n_chunks + c;
+  if (__syncthreads_or(dead)) {
+    for (int gi = w; gi < G; gi += kNW) {
+      for (int col = lane; col < D; col += 32) a.part_o[(row0 + (size_t)gi * a.n_chunks) * D + col] = 0.f;
+      if (lane == 0) {
+        a.part_ml[(row0 + (size_t)gi * a.n_chunks) * 2 + 0] = -INFINITY;
+        a.part_ml[(row0 + (size_t)gi * a.n_chunks) * 2 + 1] = 0.f;
+      }
+    }
+    return;
+  }
   // Merge the warps of this CTA (stage area reused once every warp is done).
-  __syncthreads();
   float* mo = reinterpret_cast<float*>(smem);                 // [NW][G][D]
   float* ml = mo + kNW * G * D;                               // [NW][G][2]
   st.stash(mo, ml, w, lane);
   __syncthreads();
-  const size_t row0 = ((size_t)r * h_q + g * G) * a.n_chunks + c;
   merge_warps<D, G, kNW, kNW * 32>(
       mo, ml,
       [&](int gi, int col, float o) { a.part_o[(row0 + (size_t)gi * a.n_chunks) * D + col] = o; },
@@ -193,11 +212,11 @@ cudaError_t launch_split(const AttnArgs& a, cudaStream_t s) {
   auto kern = attn_split_kernel<T, D, S, G, MASK>;
   int dev = 0;
   cudaGetDevice(&dev);
-  static bool attr_done[64] = {};   // per device and instantiation; racing setters agree
-  if (dev >= 64 || !attr_done[dev]) {
+  static std::atomic<bool> attr_done[64];   // per device and instantiation
+  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
   }
   const unsigned grid = (unsigned)a.batch * a.h_kv * a.n_chunks;
   kern<<<grid, kNW * 32, Sh::SMEM, s>>>(a);
@@ -267,8 +286,11 @@ AttnPlan plan_attn(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
   return p;
 }
 
-cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
-  if (a.batch == 0 || a.h_kv == 0) return cudaSuccess;
+cudaError_t launch_attn(const AttnArgs& args, cudaStream_t s) {
+  if (args.batch == 0 || args.h_kv == 0) return cudaSuccess;
+  AttnArgs a = args;
+  a.wait_limit = wait_limit();
+  a.test_fault = test_fault_mode() == 2 ? 2 : 0;
   if (a.dtype == QUEST_F16)
     return a.head_dim == 128 ? launch_s<__half, 128>(a, s) : launch_s<__half, 64>(a, s);
   return a.head_dim == 128 ? launch_s<float, 128>(a, s) : launch_s<float, 64>(a, s);

@@ -335,6 +335,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Warp-uniform form: every lane polls and the warp agrees on the outcome;
+// false once `limit` tries (up to about 1 us each) pass without the phase.
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, 1000u))) return true;
+  return false;
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

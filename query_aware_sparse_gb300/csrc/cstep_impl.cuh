@@ -113,6 +113,9 @@ struct CShape {
   static constexpr int SEL0 = NCW * 32;             // first select thread
   using SelGrp = BarGrp<2, NCW * 32, kCSelT>;      // the select warps
   static constexpr int HANDS = 8;                  // consumer warps that select a lone unit
+  // ... for groups of 1 and 2 only (with the larger groups' code, the hands'
+  // select and its failure path measured slower on every unit, lone or not)
+  static constexpr bool HANDSOK = G <= 2;
   using AllGrp = BarGrp<3, 0, HANDS * 32>;
 
   static constexpr int ROWS_OFF = 0;                                  // [2][kCRowCap] keys
@@ -128,8 +131,8 @@ struct CShape {
   static constexpr int TOPK_OFF = al(LG_OFF + NCW * LGN * 4, 16);
   static constexpr int BAR_OFF = al(TOPK_OFF + (int)sizeof(TopkSmem<NT>), 8);
   // kv[NCW][2] (K and V halves of each consumer's buffer), row_full[2],
-  // row_free[2], sel_ready[2], attn_done[2], stash_free[2], part_full
-  static constexpr int NBAR = 2 * NCW + 11;
+  // row_free[2], sel_ready[2], attn_done[2], stash_free[2], part_full, never
+  static constexpr int NBAR = 2 * NCW + 12;
   static constexpr int FLAG_OFF = BAR_OFF + NBAR * 8;
   static constexpr int BUF_OFF = al(FLAG_OFF + 64, 128);              // [NCW][SLOT]
   static constexpr int SMEM = BUF_OFF + NCW * SLOT;
@@ -301,6 +304,7 @@ cstep_kernel(const StepArgs a) {
   uint64_t* attn_done = row_full + 6;          // [2] consumer states of the unit stashed
   uint64_t* stash_free = row_full + 8;         // [2] stash merged
   uint64_t* part_full = row_full + 10;         // partials of an owned unit delivered
+  uint64_t* never = row_full + 11;             // nothing arrives (the failure-handling test)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Sh::FLAG_OFF);
   volatile int* s_n = s_abort + 1;             // units of this cluster
   volatile int* s_ok = s_abort + 2;            // select group's wait result
@@ -322,6 +326,7 @@ cstep_kernel(const StepArgs a) {
       mbar_init(stash_free + b, 1);
     }
     mbar_init(part_full, kCL);
+    mbar_init(never, 1);
     *s_abort = 0;
     for (int b = 0; b < 2; ++b) { kmm[2 * b] = 0xffffffffu; kmm[2 * b + 1] = 0u; }
     fence_mbar_init();
@@ -397,15 +402,24 @@ cstep_kernel(const StepArgs a) {
     if (lane == 0) *s_n = n;
     __syncwarp();
   }
-  // one request: the consumers' first page-table windows, before the list
-  int pw[4] = {-1, -1, -1, -1};
+  // one request: the consumers' first page-table windows and scoring
+  // query, fetched before the list. They wait in the second chunk slot of the
+  // warp's buffer (untouched until the first unit's chunk loop), not in
+  // registers, which would stay allocated across the whole unit loop.
   constexpr int QLD = Sh::MMAS ? 1 : Sh::VPL * (F8 ? 2 : 1);   // 16-byte query vectors per lane, head
   constexpr int QL8 = Sh::MMAS ? D / 16 : 1;                   // 8-byte pieces (MMA layout)
-  uint4 qpre[Sh::MMAS ? 1 : G][QLD];                // the scoring query, fetched early
-  uint2 qpre8[QL8];
+  constexpr int QB0 = Sh::MMAS ? QL8 * 8 : G * QLD * 16;       // query bytes per lane
+  constexpr bool EARLYQ = 32 * (QB0 + 16) <= CHB;               // (not for fp32 head dim 128)
+  constexpr int QB = EARLYQ ? QB0 : 0;
+  static_assert(32 * (QB + 16) <= CHB && QB % 16 == 0, "early values fit the second chunk slot");
   const bool pre = a.batch == 1 && warp < NCW && cid < a.h_kv;
   if (pre) {
-    if constexpr (Sh::MMAS) {                       // head gid's dims 16j + 4t .. + 3
+    int pw[4] = {-1, -1, -1, -1};
+    uint4 qpre[Sh::MMAS ? 1 : G][QLD];
+    uint2 qpre8[QL8];
+    unsigned char* early = smem + Sh::BUF_OFF + (size_t)warp * SLOT + CHB;
+    if constexpr (!EARLYQ) {
+    } else if constexpr (Sh::MMAS) {                // head gid's dims 16j + 4t .. + 3
       const int gid = lane >> 2, tq = lane & 3;
       const T* qh = static_cast<const T*>(a.q) + ((size_t)cid * G + (gid < G ? gid : 0)) * D;
 #pragma unroll
@@ -454,6 +468,18 @@ cstep_kernel(const StepArgs a) {
       }
       cp_async_commit_grp();
     }
+    if constexpr (!EARLYQ) {
+    } else if constexpr (Sh::MMAS) {
+#pragma unroll
+      for (int j = 0; j < QL8; ++j) *reinterpret_cast<uint2*>(early + lane * QB + 8 * j) = qpre8[j];
+    } else {
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+        for (int j = 0; j < QLD; ++j)
+          *reinterpret_cast<uint4*>(early + lane * QB + 16 * (gi * QLD + j)) = qpre[gi][j];
+    }
+    *reinterpret_cast<int4*>(early + 32 * QB + lane * 16) = make_int4(pw[0], pw[1], pw[2], pw[3]);
   }
   asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory");
   const int n = *s_n;
@@ -477,7 +503,7 @@ cstep_kernel(const StepArgs a) {
   // threads would only add barrier latency) and publish it through
   // sel_ready, else the select warps do (SelGrp) while the consumers stream
   // the next unit.
-  const bool all_hands = n == 1;
+  const bool all_hands = Sh::HANDSOK && n == 1;
 
   // T(u) on thread group Grp: wait for every CTA's keys of unit u, Top-K,
   // the selected pages' physical ids. Returns false if the CTA aborts.
@@ -547,9 +573,15 @@ cstep_kernel(const StepArgs a) {
     const uint64_t pol = evict_first_policy();
     const int pg = lane / LPP, sub = lane % LPP;
     bool dead = false;
+    bool joined = false;                     // took part in the all-hands select
     for (int t = 0; t <= n && !dead; ++t) {
       if (t < n) {
         // ------------------------------ S(t) ------------------------------
+        if (a.test_fault == 1 && t == 0 && rank == 0 && cw == 0 &&
+            !cwait_warp(never, 0, s_abort, a.err, lim)) {   // runs out: the test's failure
+          dead = true;
+          break;
+        }
         const CUnit un = units[t];
         const int b = t & 1;
         // my chunks: a contiguous run [mc0, mc0 + nm) of the CTA's chunks
@@ -569,8 +601,10 @@ cstep_kernel(const StepArgs a) {
           w1 = p + 32 < pe ? __ldg(idx + p + 32) : -1;
         };
         int cw0, cw1, nw0, nw1, kcur = 0;
-        if (t == 0 && pre && un.lo == 0 && un.tp == a.nnz) {   // fetched before the list
-          cw0 = pw[0]; cw1 = pw[1]; nw0 = pw[2]; nw1 = pw[3];
+        const unsigned char* early = buf + CHB;         // the values fetched before the list
+        if (t == 0 && pre && un.lo == 0 && un.tp == a.nnz) {
+          const int4 p4 = *reinterpret_cast<const int4*>(early + 32 * QB + lane * 16);
+          cw0 = p4.x; cw1 = p4.y; nw0 = p4.z; nw1 = p4.w;
         } else {
           ldwin(0, cw0, cw1);
           ldwin(1, nw0, nw1);
@@ -626,7 +660,7 @@ cstep_kernel(const StepArgs a) {
           const __half2 z2 = __float2half2_rn(0.f);
 #pragma unroll
           for (int j = 0; j < D / 16; ++j) {
-            uint2 w = (t == 0 && pre && un.g == cid) ? qpre8[j]
+            uint2 w = (EARLYQ && t == 0 && pre && un.g == cid) ? *reinterpret_cast<const uint2*>(early + lane * QB + 8 * j)
                                                        : *reinterpret_cast<const uint2*>(qh + 16 * j + 4 * tq);
             if (!hv) w = make_uint2(0u, 0u);
             const __half2 x = *reinterpret_cast<const __half2*>(&w.x), y = *reinterpret_cast<const __half2*>(&w.y);
@@ -645,7 +679,9 @@ cstep_kernel(const StepArgs a) {
               const int d0 = (v * LPP + sub) * VECS;
 #pragma unroll
               for (int h = 0; h < (F8 ? 2 : 1); ++h) {
-                const uint4 qv = (t == 0 && pre && un.g == cid) ? qpre[gi][v * (F8 ? 2 : 1) + h]
+                const uint4 qv = (EARLYQ && t == 0 && pre && un.g == cid)
+                                     ? *reinterpret_cast<const uint4*>(early + lane * QB +
+                                                                       16 * (gi * QLD + v * (F8 ? 2 : 1) + h))
                                                                  : ld_nc_v4(qp + d0 + h * 8);
                 const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
@@ -687,6 +723,7 @@ cstep_kernel(const StepArgs a) {
             for (int h = 0; h < (F8 ? 2 : 1); ++h)
               kn[v * (F8 ? 2 : 1) + h] = ld_nc_v4(kp + (v * LPP + sub) * VECS + h * 8);
         }
+        __syncwarp();                        // every lane's early values read: slot 1 may refill
         // keys of unit t go to row buffer b of every CTA: it must be free
         if (t >= 2 && !cwait_warp(row_free + b, ((t >> 1) - 1) & 1, s_abort, a.err, lim)) {
           dead = true;
@@ -977,6 +1014,7 @@ cstep_kernel(const StepArgs a) {
         bool inited = false;                 // q loads once the first copies are out
         const T* qrow = static_cast<const T*>(a.q) + ((size_t)un.r * h_q + (size_t)un.g * G) * D;
         if (all_hands && cw < Sh::HANDS) {
+          joined = true;
           if (!select_core(typename Sh::AllGrp{}, u)) { dead = true; break; }
           if (cw == 0 && lane == 0) arrive_local(sel_ready + b);   // the group synced: all of it
         } else if (!cwait_warp(sel_ready + b, (u >> 1) & 1, s_abort, a.err, lim)) {
@@ -1132,6 +1170,16 @@ cstep_kernel(const StepArgs a) {
         if (lane == 0) arrive_local(attn_done + sbf);
       }
     }
+    // a hand that gave up before the lone unit's select (so before its
+    // arrival on the unit's row_full, which therefore never completes) still
+    // meets the group's one barrier of a failing select: the select's verdict
+    // is "failed" whoever writes it
+    if constexpr (Sh::HANDSOK) {
+      if (dead && all_hands && cw < Sh::HANDS && !joined) {
+        if (lane == 0) *s_ok_all = 0;
+        Sh::AllGrp::sync();
+      }
+    }
     // nothing may still be copying into this warp's buffer when the CTA exits
     cp_async_wait_grp<0>();
     for (uint32_t i = 0; kpend && i < lim; ++i) kpend = !__all_sync(FULL, try_wait_cl(kbar, kph & 1));
@@ -1195,7 +1243,7 @@ cstep_kernel(const StepArgs a) {
       }
       if (t >= 1) {
         // ------------------------------ M(t-1) ------------------------------
-        const int u = t - 1, b = u & 1;
+        const int u = t - 1;
         const CUnit un = units[u];
         const int owner = u % kCL;
         const int sbf = u % Sh::NSTASH;          // stash slot of the unit
@@ -1262,9 +1310,12 @@ cstep_kernel(const StepArgs a) {
 
 template <typename T, int D, int S, int G, bool F8>
 int cstep_clusters(int dev) {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];   // per device: 0 untried
   using Sh = CShape<T, D, S, G, F8>;
-  if (dev >= 0 && dev < 64 && cached[dev] != 0) return cached[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_acquire);
+    if (c != 0) return c;
+  }
   int n = 0;
   if (cudaFuncSetAttribute(cstep_kernel<T, D, S, G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Sh::SMEM) == cudaSuccess) {
@@ -1277,7 +1328,7 @@ int cstep_clusters(int dev) {
   }
   cudaGetLastError();
   if (n <= 0) n = -1;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_release);
   return n;
 }
 
@@ -1295,10 +1346,10 @@ cudaError_t cstep_launch(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  static int pdl_ok = getenv("QUEST_NO_PDL") ? 0 : -1;   // -1 untried, 0 off, 1 on
-  cfg.numAttrs = pdl_ok == 0 ? 0 : 1;
+  static std::atomic<int> pdl_ok{getenv("QUEST_NO_PDL") ? 0 : -1};   // -1 untried, 0 off, 1 on
+  cfg.numAttrs = pdl_ok.load() == 0 ? 0 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, cstep_kernel<T, D, S, G, F8>, a);
-  if (e != cudaSuccess && cfg.numAttrs == 1 && pdl_ok == -1) {
+  if (e != cudaSuccess && cfg.numAttrs == 1 && pdl_ok.load() == -1) {
     cudaGetLastError();
     pdl_ok = 0;
     cfg.numAttrs = 0;

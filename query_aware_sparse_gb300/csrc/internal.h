@@ -3,11 +3,45 @@
 
 #include <cuda_runtime.h>
 #include <stddef.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include "../../include/quest.h"
 
 namespace quest {
+
+// Argument checks shared by the entry points (quest_api.cu, noalloc.cu).
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline quest_status check_cache(const quest_cache* c) {
+  if (!c || !c->k_pool || !c->v_pool || !c->summary) return QUEST_ERR_INVALID_ARG;
+  if (c->n_phys <= 0 || c->h_kv <= 0) return QUEST_ERR_INVALID_ARG;
+  if (c->dtype != QUEST_F16 && c->dtype != QUEST_F32) return QUEST_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return QUEST_ERR_UNSUPPORTED;
+  if (c->page_size != 16 && c->page_size != 32) return QUEST_ERR_UNSUPPORTED;
+  if (c->summary_fp8 != 0 && c->summary_fp8 != 1) return QUEST_ERR_INVALID_ARG;
+  if (c->summary_fp8 && c->dtype != QUEST_F16) return QUEST_ERR_UNSUPPORTED;
+  if (!aligned16(c->k_pool) || !aligned16(c->v_pool) || !aligned16(c->summary))
+    return QUEST_ERR_INVALID_ARG;
+  return QUEST_OK;
+}
+
+inline quest_status check_pages(const quest_pages* p, bool need_seq_lens) {
+  if (!p || p->batch < 0 || p->nnz < 0) return QUEST_ERR_INVALID_ARG;
+  if (p->batch == 0) return QUEST_OK;
+  if (!p->page_indptr || (p->nnz > 0 && !p->page_indices)) return QUEST_ERR_INVALID_ARG;
+  if (need_seq_lens && !p->seq_lens) return QUEST_ERR_INVALID_ARG;
+  return QUEST_OK;
+}
+
+inline bool valid_group(int32_t g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+// quest_test_step_fault's state: the fault mode (0 none, 1 a wait of the
+// cluster step runs out, 2 a wait of the attention split kernel runs out)
+// and the tries of every bounded in-kernel wait.
+int32_t test_fault_mode();
+uint32_t wait_limit();
 
 struct AppendArgs {
   void* k_pool; void* v_pool; void* summary;
@@ -49,6 +83,8 @@ struct AttnArgs {
   int32_t n_chunks, chunk_pages;
   float scale_log2;  // sm_scale * log2(e)
   unsigned* err;
+  uint32_t wait_limit;   // tries of each bounded wait (set by launch_attn)
+  int32_t test_fault;    // 2: a copy slot of CTA 0 never completes (tests; set by launch_attn)
 };
 
 // Fused decode step: append (optional, one token per request) + score +

@@ -37,29 +37,21 @@ float* scratch_ptr() {
   return g_scratch_ptr[dev];
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" QUEST_API quest_status quest_sparse_decode_attn_noalloc(
     const quest_cache* cache, const quest_pages* pages, const void* q, int32_t group,
     const int32_t* sel_logical, const int32_t* sel_phys, int32_t k, float* out, float* lse,
     float sm_scale, void* stream) {
-  if (!cache || !cache->k_pool || !cache->v_pool || !cache->summary || cache->n_phys <= 0 ||
-      cache->h_kv <= 0)
-    return QUEST_ERR_INVALID_ARG;
-  if (cache->dtype != QUEST_F16 && cache->dtype != QUEST_F32) return QUEST_ERR_UNSUPPORTED;
-  if (cache->head_dim != 64 && cache->head_dim != 128) return QUEST_ERR_UNSUPPORTED;
-  if (cache->page_size != 16 && cache->page_size != 32) return QUEST_ERR_UNSUPPORTED;
-  if (!aligned16(cache->k_pool) || !aligned16(cache->v_pool)) return QUEST_ERR_INVALID_ARG;
-  if (!pages || pages->batch < 0 || pages->nnz < 0) return QUEST_ERR_INVALID_ARG;
-  if (group != 1 && group != 2 && group != 4 && group != 8) return QUEST_ERR_INVALID_ARG;
-  if (k < 1) return QUEST_ERR_INVALID_ARG;
+  // the same checks, in the same order, as quest_sparse_decode_attn
+  quest_status st = quest::check_cache(cache);
+  if (st != QUEST_OK) return st;
+  if ((st = quest::check_pages(pages, true)) != QUEST_OK) return st;
+  if (!quest::valid_group(group) || k < 1) return QUEST_ERR_INVALID_ARG;
   if (!quest::attn_supported(cache->dtype, cache->head_dim, cache->page_size, group))
     return QUEST_ERR_UNSUPPORTED;
   if (pages->batch == 0) return QUEST_OK;
-  if (!pages->seq_lens || !q || !sel_logical || !sel_phys || !out || !aligned16(q))
-    return QUEST_ERR_INVALID_ARG;
+  if (!q || !sel_logical || !sel_phys || !out || !quest::aligned16(q)) return QUEST_ERR_INVALID_ARG;
   const quest::AttnPlan plan = quest::plan_attn(pages->batch, cache->h_kv, group,
                                                 cache->head_dim, cache->page_size, cache->dtype, k);
   if (plan.workspace_bytes > kNoAllocScratchBytes) return QUEST_ERR_WORKSPACE;   // too large

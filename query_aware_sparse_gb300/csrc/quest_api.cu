@@ -1,5 +1,6 @@
 // C ABI of libquest: host-side validation, the device error word and the
 // dispatch to the kernel files. No torch types, no allocation.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -31,36 +32,16 @@ unsigned* err_ptr() {
   return g_err_ptr[dev];
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-quest_status check_cache(const quest_cache* c) {
-  if (!c || !c->k_pool || !c->v_pool || !c->summary) return QUEST_ERR_INVALID_ARG;
-  if (c->n_phys <= 0 || c->h_kv <= 0) return QUEST_ERR_INVALID_ARG;
-  if (c->dtype != QUEST_F16 && c->dtype != QUEST_F32) return QUEST_ERR_UNSUPPORTED;
-  if (c->head_dim != 64 && c->head_dim != 128) return QUEST_ERR_UNSUPPORTED;
-  if (c->page_size != 16 && c->page_size != 32) return QUEST_ERR_UNSUPPORTED;
-  if (c->summary_fp8 != 0 && c->summary_fp8 != 1) return QUEST_ERR_INVALID_ARG;
-  if (c->summary_fp8 && c->dtype != QUEST_F16) return QUEST_ERR_UNSUPPORTED;
-  if (!aligned16(c->k_pool) || !aligned16(c->v_pool) || !aligned16(c->summary))
-    return QUEST_ERR_INVALID_ARG;
-  return QUEST_OK;
-}
-
-quest_status check_pages(const quest_pages* p, bool need_seq_lens) {
-  if (!p || p->batch < 0 || p->nnz < 0) return QUEST_ERR_INVALID_ARG;
-  if (p->batch == 0) return QUEST_OK;
-  if (!p->page_indptr || (p->nnz > 0 && !p->page_indices)) return QUEST_ERR_INVALID_ARG;
-  if (need_seq_lens && !p->seq_lens) return QUEST_ERR_INVALID_ARG;
-  return QUEST_OK;
-}
-
-bool valid_group(int32_t g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+using quest::aligned16;
+using quest::check_cache;
+using quest::check_pages;
+using quest::valid_group;
 
 unsigned long long* g_trace = nullptr;      // quest_set_trace buffer (device)
 int32_t g_trace_ctas = 0;
-// quest_test_step_fault: fault mode and wait limit of later decode steps
-int32_t g_test_fault = 0;
-uint32_t g_wait_limit = quest::kStepWaitLimit;
+// quest_test_step_fault: fault mode and wait limit of later calls
+std::atomic<int32_t> g_test_fault{0};
+std::atomic<uint32_t> g_wait_limit{quest::kStepWaitLimit};
 
 quest_status launched(cudaError_t e) { return e == cudaSuccess ? QUEST_OK : QUEST_ERR_CUDA; }
 
@@ -292,6 +273,18 @@ size_t quest_decode_workspace_size(int32_t batch, int32_t nnz, int32_t h_kv, int
   return need;
 }
 
+int32_t quest_decode_step_kernel(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim,
+                                 int32_t page_size, int32_t dtype, int32_t k, int32_t summary_fp8) {
+  if (batch <= 0 || h_kv <= 0 || k < 1 || !valid_group(group)) return 0;
+  if ((dtype != QUEST_F16 && dtype != QUEST_F32) || (head_dim != 64 && head_dim != 128) ||
+      (page_size != 16 && page_size != 32) || (summary_fp8 != 0 && summary_fp8 != 1) ||
+      (summary_fp8 && dtype != QUEST_F16))
+    return 0;
+  quest::StepPlan p = quest::plan_step(batch, 0, h_kv, group, head_dim, page_size, dtype, k,
+                                       summary_fp8);
+  return p.ok ? (p.cluster ? 2 : 1) : 0;
+}
+
 quest_status quest_decode_step(const quest_cache* cache, const quest_pages* pages,
                                const void* k_new, const void* v_new, const void* q,
                                int32_t group, int32_t k, int32_t n_sink, int32_t n_local,
@@ -340,8 +333,8 @@ quest_status quest_decode_step(const quest_cache* cache, const quest_pages* page
   a.trace = (g_trace && plan.grid <= g_trace_ctas) ? g_trace : nullptr;
   a.err = err_ptr();
   if (!a.err) return QUEST_ERR_CUDA;
-  a.wait_limit = g_wait_limit;
-  a.test_fault = g_test_fault;
+  a.wait_limit = g_wait_limit.load();
+  a.test_fault = g_test_fault.load() == 1 ? 1 : 0;
   return launched(quest::launch_step(a, plan, static_cast<cudaStream_t>(stream)));
 }
 
@@ -415,7 +408,7 @@ const char* quest_status_string(int32_t status) {
 }
 
 int32_t quest_test_step_fault(int32_t mode, int32_t wait_limit) {
-  if (mode < 0 || mode > 1 || wait_limit < 0) return QUEST_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 2 || wait_limit < 0) return QUEST_ERR_INVALID_ARG;
   g_test_fault = mode;
   g_wait_limit = wait_limit > 0 ? (uint32_t)wait_limit : quest::kStepWaitLimit;
   return QUEST_OK;
@@ -425,4 +418,6 @@ int32_t quest_test_step_fault(int32_t mode, int32_t wait_limit) {
 
 namespace quest {
 unsigned* error_word_ptr() { return err_ptr(); }
+int32_t test_fault_mode() { return g_test_fault.load(); }
+uint32_t wait_limit() { return g_wait_limit.load(); }
 }  // namespace quest

@@ -46,12 +46,12 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
   const size_t smem = kSelSmemKeys * sizeof(uint32_t);
   int dev = 0;
   cudaGetDevice(&dev);
-  static bool attr_done[64] = {};   // per device; racing setters write the same value
-  if (dev >= 64 || !attr_done[dev]) {
+  static std::atomic<bool> attr_done[64];   // per device
+  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
   }
   select_kernel<<<(unsigned)a.batch * a.h_kv, kSelThreads, smem, s>>>(a);
   return cudaGetLastError();

@@ -38,7 +38,10 @@ StepPlan plan_cstep(int32_t batch, int32_t h_kv, int32_t group, int32_t head_dim
   const long long units = (long long)batch * h_kv;
   const long long per = (units + maxc - 1) / maxc;
   if (per > kCStepUnitsPerCluster) return p;
-  long long nc = per > 0 ? (units + per - 1) / per : 1;
+  // every resident cluster takes units (their counts differ by at most one;
+  // the kernel deals them out longest request first)
+  long long nc = units < maxc ? units : maxc;
+  if (nc < 1) nc = 1;
   if (const char* e = getenv("QUEST_STEP_CLUSTERS")) {   // cluster count override (experiments)
     const long long want = atoll(e);
     if (want > 0 && want <= maxc && (units + want - 1) / want <= kCStepUnitsPerCluster) nc = want;

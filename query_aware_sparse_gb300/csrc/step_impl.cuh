@@ -940,16 +940,19 @@ bool set_attr() {
 // device; the large shared-memory opt-in is set before the query).
 template <typename T, int D, int S, int G, bool F8>
 void shape_of(int dev, int* smem, int* per_sm) {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];   // per device: 0 unknown
   *smem = StepShape<T, D, S, G>::SMEM;
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) { *per_sm = cached[dev]; return; }
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_acquire);
+    if (c > 0) { *per_sm = c; return; }
+  }
   int n = 0;
   if (!set_attr<T, D, S, G, F8>() ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, D, S, G, F8>, kNT, *smem) !=
           cudaSuccess)
     n = 0;
   cudaGetLastError();
-  if (dev >= 0 && dev < 64 && n > 0) cached[dev] = n;
+  if (dev >= 0 && dev < 64 && n > 0) cached[dev].store(n, std::memory_order_release);
   *per_sm = n;
 }
 
@@ -970,16 +973,16 @@ cudaError_t launch_t(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   // -1 untried, 0 refused (or QUEST_NO_PDL set in the environment), 1 accepted
-  static int pdl_ok = getenv("QUEST_NO_PDL") ? 0 : -1;
-  cfg.numAttrs = pdl_ok == 0 ? 1 : 2;
+  static std::atomic<int> pdl_ok{getenv("QUEST_NO_PDL") ? 0 : -1};
+  cfg.numAttrs = pdl_ok.load() == 0 ? 1 : 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, step_kernel<T, D, S, G, F8>, a);
-  if (e != cudaSuccess && cfg.numAttrs == 2 && pdl_ok == -1) {   // not with this launch: plain
+  if (e != cudaSuccess && cfg.numAttrs == 2 && pdl_ok.load() == -1) {   // not with this launch: plain
     cudaGetLastError();
     pdl_ok = 0;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, step_kernel<T, D, S, G, F8>, a);
   } else if (e == cudaSuccess) {
-    pdl_ok = cfg.numAttrs == 2 ? 1 : pdl_ok;
+    if (cfg.numAttrs == 2) pdl_ok = 1;
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

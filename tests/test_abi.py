@@ -140,3 +140,25 @@ def test_workspace_sizes_host_logic(qlib):
     assert L.quest_decode_workspace_size(1, 2048, 32, 1, 128, 16, qlib.QUEST_F16, 128) > 0
     assert L.quest_decode_workspace_size(1, 2048, 32, 1, 96, 16, qlib.QUEST_F16, 128) == 0
     assert L.quest_decode_workspace_size(1, 2048, 32, 1, 128, 24, qlib.QUEST_F16, 128) == 0
+
+
+def test_decode_step_kernel_choice_host_logic(qlib):
+    """Which kernel quest_decode_step takes is host logic: the cluster kernel
+    for groups 1 and 2 (and 4 and 8 with fp16 K/V) while the (request, KV
+    head) units fit 64 per cluster, the grid-wide kernel otherwise, 0 for
+    unsupported shapes. With no device the plan assumes 32 resident
+    clusters."""
+    L = qlib.lib()
+    F16, F32 = qlib.QUEST_F16, qlib.QUEST_F32
+    assert L.quest_decode_step_kernel(1, 32, 1, 128, 16, F16, 128, 0) == 2
+    assert L.quest_decode_step_kernel(16, 8, 4, 128, 16, F16, 256, 0) == 2
+    assert L.quest_decode_step_kernel(3, 2, 8, 64, 32, F16, 8, 1) == 2
+    assert L.quest_decode_step_kernel(2, 4, 2, 64, 16, F32, 8, 0) == 2
+    assert L.quest_decode_step_kernel(2, 4, 4, 64, 16, F32, 8, 0) == 1    # fp32 GQA of 4
+    assert L.quest_decode_step_kernel(64 * 32, 1, 1, 64, 16, F16, 8, 0) == 2   # 64 per cluster
+    assert L.quest_decode_step_kernel(64 * 32 + 1, 1, 1, 64, 16, F16, 8, 0) == 1
+    assert L.quest_decode_step_kernel(1, 32, 3, 128, 16, F16, 128, 0) == 0
+    assert L.quest_decode_step_kernel(1, 32, 1, 96, 16, F16, 128, 0) == 0
+    assert L.quest_decode_step_kernel(1, 32, 1, 128, 16, F32, 128, 1) == 0  # E4M3 needs fp16
+    # the cluster kernel keeps everything in shared memory: a nominal workspace
+    assert L.quest_decode_workspace_size(1, 2048, 32, 1, 128, 16, F16, 128) == 256
