@@ -185,7 +185,7 @@ class LayerSetup:
     request's decode token and query."""
 
     def __init__(self, w: wl.Workload, nbuf: int, dev, sample_heads=4, n_sink=0, n_local=0,
-                 summary_fp8=False):
+                 summary_fp8=False, prefill_reps=5):
         import query_aware_sparse_gb300 as qs
         self.qs = qs
         self.w = w
@@ -216,15 +216,25 @@ class LayerSetup:
         kpre, vpre = k_tok[rows].contiguous(), v_tok[rows].contiguous()
         pre_ind = np.concatenate([[0], np.cumsum(lens - 1)])
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        qs.append_kv(self.caches[0], pre, kpre, vpre, i32(pre_ind), i32(np.zeros(B)))
-        e1.record()
-        torch.cuda.synchronize()
-        pre_ms = e0.elapsed_time(e1)
+        # the first call, then repeats (each page starts over from its slot 0,
+        # so a repeat rewrites the same pool and summaries): the median of the
+        # repeats is the prefill's time, the first call is reported beside it
+        ind_d, zero_d = i32(pre_ind), i32(np.zeros(B))
+        pre_ms = []
+        for _ in range(1 + prefill_reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            qs.append_kv(self.caches[0], pre, kpre, vpre, ind_d, zero_d)
+            e1.record()
+            torch.cuda.synchronize()
+            pre_ms.append(e0.elapsed_time(e1))
         n_pre = int(pre_ind[-1])
-        pre_bytes = n_pre * h * d * k_tok.element_size() * 4 + t.nnz * h * 2 * d * sm.element_size()
-        self.prefill = {"tokens": n_pre, "ms": pre_ms, "GBps": pre_bytes / pre_ms / 1e6}
+        # read K and V rows, write them into the pool, write every page's summary
+        pre_bytes = (n_pre * h * d * k_tok.element_size() * 4 +
+                     int(-(-(lens - 1) // S).sum()) * h * 2 * d * sm.element_size())
+        med = statistics.median(pre_ms[1:]) if prefill_reps else pre_ms[0]
+        self.prefill = {"tokens": n_pre, "bytes": pre_bytes, "ms": med, "GBps": pre_bytes / med / 1e6,
+                        "first_call_ms": pre_ms[0], "reps": prefill_reps}
         assert qs.device_error() == 0
         for _ in range(nbuf - 1):   # distinct copies: each step reads cold memory
             c = self.caches[0]
@@ -572,7 +582,7 @@ def main(argv=None):
                  " so every step reads memory not touched in the previous "
                  f"{args.nbuf - 1} steps (> the 129 MB L2)")
     cfg["launch"] = (f"CUDA graphs of {args.nbuf} back-to-back steps (one per cache copy); "
-                     "p50/p95 are per graph / steps in it")
+                     "p50/p95: single-step graphs each between two events, >= 200 samples")
     nb = args.nbuf
 
     # warm-up (also sets per-device kernel attributes before capture)
@@ -607,8 +617,6 @@ def main(argv=None):
     # timed region: exactly K steps
     K = args.steps
     reps, rem = divmod(K, nb)
-    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(reps)]
     t_all = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     if ws > 1:
         torch.distributed.barrier()
@@ -616,9 +624,7 @@ def main(argv=None):
     with ClockSampler(local) as clk:
         t_all[0].record()
         for i in range(reps):
-            per[i][0].record()
             g_run.replay()
-            per[i][1].record()
         for i in range(rem):
             graphs[i].replay()
         t_all[1].record()
@@ -626,10 +632,24 @@ def main(argv=None):
     if ws > 1:
         torch.distributed.barrier()
     total_ms = t_all[0].elapsed_time(t_all[1])
-    steps_us = sorted(a.elapsed_time(b) * 1e3 / nb for a, b in per) or [total_ms * 1e3 / K]
     ms_per_step = total_ms / K
     ms_per_step = max_over_ranks(ms_per_step, dev)
     assert qs.device_error() == 0
+
+    # the step-time distribution (after the timed region, not part of
+    # `value`): each step alone between events, single-step graphs over the
+    # rotating copies, at least 200 samples whatever --steps is
+    n_dist = max(200, min(K, 4000))
+    dist_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_dist)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(n_dist):
+            dist_ev[i][0].record(s)
+            graphs[i % nb].replay()
+            dist_ev[i][1].record(s)
+    torch.cuda.synchronize()
+    steps_us = sorted(a.elapsed_time(b) * 1e3 for a, b in dist_ev)
 
     # per-stage device time of the unfused four-call path (each stage alone,
     # rotating copies, events); informational
@@ -671,7 +691,8 @@ def main(argv=None):
                      "peak": pk, "unit": "GB/s", "frac": round(dom_gbs / pk, 4),
                      "peak_source": pk_src, "bytes_per_launch": dom_bytes,
                      "traffic": traffic},
-        "append_prefill": {k: round(v, 3) for k, v in setup.prefill.items()},
+        "append_prefill": {**{k: round(v, 3) for k, v in setup.prefill.items()},
+                           "frac": round(setup.prefill["GBps"] / pk, 4)},
         "e2e": e2e,
         "gpu_launches": K * LayerSetup.KERNELS_PER_STEP,
         "clocks": clk.summary(),

@@ -707,22 +707,102 @@ cstep_kernel(const StepArgs a) {
         const int pin = (un.P - 1) - ct * CHUNK;
         const int m_tail = ct - mc0;
         const bool tail_warp = un.app && m_tail >= 0 && m_tail < nm;
-        const bool tail_mine = tail_warp && pg == pin % PPR;
-        const int ro_t = pin / PPR;
-        constexpr int KNV = F8 ? 2 * VPL : VPL;             // 16-byte vectors of k per lane
-        uint4 kn[KNV];
-        uint2 kq = make_uint2(0u, 0u);                      // MMA bound: dims 4 lane .. + 3
-        if (Sh::MMAS && tail_warp && lane < D / 4)
-          kq = *reinterpret_cast<const uint2*>(static_cast<const T*>(a.k_new) +
-                                               ((size_t)un.r * a.h_kv + un.g) * D + 4 * lane);
-        if (!Sh::MMAS && tail_mine) {
-          const T* kp = static_cast<const T*>(a.k_new) + ((size_t)un.r * a.h_kv + un.g) * D;
-#pragma unroll
-          for (int v = 0; v < VPL; ++v)
-#pragma unroll
-            for (int h = 0; h < (F8 ? 2 : 1); ++h)
-              kn[v * (F8 ? 2 : 1) + h] = ld_nc_v4(kp + (v * LPP + sub) * VECS + h * 8);
+        // lane l < D/4 takes dims 4l .. 4l + 3 of the new token's key and value
+        // (fetched now, used when the tail page's chunk is scored)
+        constexpr int NB4 = 4 * Sh::ES;                     // bytes of 4 dims
+        uint4 kq = make_uint4(0u, 0u, 0u, 0u), vq = make_uint4(0u, 0u, 0u, 0u);
+        if (tail_warp && lane < D / 4) {
+          const unsigned char* kp = static_cast<const unsigned char*>(a.k_new) +
+                                    ((size_t)un.r * a.h_kv + un.g) * D * Sh::ES + (size_t)lane * NB4;
+          const unsigned char* vp = static_cast<const unsigned char*>(a.v_new) +
+                                    ((size_t)un.r * a.h_kv + un.g) * D * Sh::ES + (size_t)lane * NB4;
+          if constexpr (NB4 == 16) {
+            kq = ld_nc_v4(kp);
+            vq = ld_nc_v4(vp);
+          } else {
+            const uint2 k2 = *reinterpret_cast<const uint2*>(kp), v2 = *reinterpret_cast<const uint2*>(vp);
+            kq = make_uint4(k2.x, k2.y, 0u, 0u);
+            vq = make_uint4(v2.x, v2.y, 0u, 0u);
+          }
         }
+        // append (eq (8)): the new token's K/V into the pool, and the staged
+        // summary of its page (row pin of the chunk at sbw) folded with the
+        // key (a fresh page starts from it), written back to the cache too
+        auto tail_patch = [&](unsigned char* sbw) {
+          const int slot = (un.L - 1) % S;
+          const int pp = __ldg(a.page_indices + un.lo + un.P - 1);
+          if (pp >= 0 && pp < a.n_phys && lane < D / 4) {
+            const size_t row = ((size_t)pp * a.h_kv + un.g) * S + slot;
+            unsigned char* kd = static_cast<unsigned char*>(a.k_pool) + row * D * Sh::ES + (size_t)lane * NB4;
+            unsigned char* vd = static_cast<unsigned char*>(a.v_pool) + row * D * Sh::ES + (size_t)lane * NB4;
+            unsigned char* gs = static_cast<unsigned char*>(a.summary) + ((size_t)pp * a.h_kv + un.g) * SUMB;
+            auto at = [&](int byte) { return sbw + (Sh::MMAS ? sw_off<SUMB>(pin, byte) : pin * SUMB + byte); };
+            if constexpr (NB4 == 16) {                     // fp32: 4 keys per lane
+              st_v4(kd, kq);
+              st_v4(vd, vq);
+              const int bm = 16 * lane, bM = RB + 16 * lane;
+              uint4* sm_m = reinterpret_cast<uint4*>(at(bm));
+              uint4* sm_M = reinterpret_cast<uint4*>(at(bM));
+              const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+              const uint4 om = *sm_m, oM = *sm_M;
+              const uint32_t omw[4] = {om.x, om.y, om.z, om.w}, oMw[4] = {oM.x, oM.y, oM.z, oM.w};
+              uint32_t nmw[4], nMw[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t kk = KO::to_key(kw[j]);
+                nmw[j] = KO::from_key(slot != 0 ? KO::kmin(KO::to_key(omw[j]), kk) : kk);
+                nMw[j] = KO::from_key(slot != 0 ? KO::kmax(KO::to_key(oMw[j]), kk) : kk);
+              }
+              const uint4 nm4 = make_uint4(nmw[0], nmw[1], nmw[2], nmw[3]);
+              const uint4 nM4 = make_uint4(nMw[0], nMw[1], nMw[2], nMw[3]);
+              *sm_m = nm4;
+              *sm_M = nM4;
+              st_v4(gs + bm, nm4);
+              st_v4(gs + bM, nM4);
+            } else {
+              *reinterpret_cast<uint2*>(kd) = make_uint2(kq.x, kq.y);
+              *reinterpret_cast<uint2*>(vd) = make_uint2(vq.x, vq.y);
+              if constexpr (F8) {
+                const int bm = 4 * lane, bM = D + 4 * lane;   // code bytes of m, M
+                uint32_t* sm_m = reinterpret_cast<uint32_t*>(at(bm));
+                uint32_t* sm_M = reinterpret_cast<uint32_t*>(at(bM));
+                uint32_t m01 = KO::to_key(kq.x), m23 = KO::to_key(kq.y);
+                uint32_t M01 = m01, M23 = m23;
+                if (slot != 0) {
+                  m01 = KO::kmin(KO::to_key(e4m3x4_lo_h2(*sm_m)), m01);
+                  m23 = KO::kmin(KO::to_key(e4m3x4_hi_h2(*sm_m)), m23);
+                  M01 = KO::kmax(KO::to_key(e4m3x4_lo_h2(*sm_M)), M01);
+                  M23 = KO::kmax(KO::to_key(e4m3x4_hi_h2(*sm_M)), M23);
+                }
+                bool ovf = false;
+                const uint32_t cm = e4m3x4_floor_h(KO::from_key(m01), KO::from_key(m23), ovf);
+                const uint32_t cM = e4m3x4_ceil_h(KO::from_key(M01), KO::from_key(M23), ovf);
+                *sm_m = cm;
+                *sm_M = cM;
+                *reinterpret_cast<uint32_t*>(gs + bm) = cm;
+                *reinterpret_cast<uint32_t*>(gs + bM) = cM;
+                if (ovf) report(a.err, QUEST_DEVERR_FP8_RANGE);
+              } else {
+                const int bm = 8 * lane, bM = RB + 8 * lane;   // bytes of m, M dims
+                uint2* sm_m = reinterpret_cast<uint2*>(at(bm));
+                uint2* sm_M = reinterpret_cast<uint2*>(at(bM));
+                uint2 mn = make_uint2(KO::to_key(kq.x), KO::to_key(kq.y)), mx = mn;
+                if (slot != 0) {
+                  const uint2 om = *sm_m, oM = *sm_M;
+                  mn = make_uint2(KO::kmin(KO::to_key(om.x), mn.x), KO::kmin(KO::to_key(om.y), mn.y));
+                  mx = make_uint2(KO::kmax(KO::to_key(oM.x), mx.x), KO::kmax(KO::to_key(oM.y), mx.y));
+                }
+                const uint2 nm2 = make_uint2(KO::from_key(mn.x), KO::from_key(mn.y));
+                const uint2 nM2 = make_uint2(KO::from_key(mx.x), KO::from_key(mx.y));
+                *sm_m = nm2;
+                *sm_M = nM2;
+                *reinterpret_cast<uint2*>(gs + bm) = nm2;
+                *reinterpret_cast<uint2*>(gs + bM) = nM2;
+              }
+            }
+          }
+          __syncwarp();
+        };
         __syncwarp();                        // every lane's early values read: slot 1 may refill
         // keys of unit t go to row buffer b of every CTA: it must be free
         if (t >= 2 && !cwait_warp(row_free + b, ((t >> 1) - 1) & 1, s_abort, a.err, lim)) {
@@ -744,62 +824,8 @@ cstep_kernel(const StepArgs a) {
           const unsigned bad = __ballot_sync(FULL, lane < np && !(phm >= 0 && phm < a.n_phys));
           if (bad && lane == 0) report(a.err, QUEST_DEVERR_PAGE_RANGE);
           const unsigned char* sb = buf + (m % NQ) * CHB;
+          if (tail_warp && m == m_tail) tail_patch(buf + (m % NQ) * CHB);
           if constexpr (Sh::MMAS) {
-            unsigned char* sbw = buf + (m % NQ) * CHB;
-            if (tail_warp && m == m_tail) {
-              // append (eq (8)): the new token's K/V into the pool, and the
-              // staged summary of its page folded with the key (a fresh page
-              // starts from it), written back to the cache; lane l takes dims
-              // 4l .. 4l + 3
-              const int slot = (un.L - 1) % S;
-              const int pp = __ldg(a.page_indices + un.lo + un.P - 1);
-              if (pp >= 0 && pp < a.n_phys && lane < D / 4) {
-                const size_t row = ((size_t)pp * a.h_kv + un.g) * S + slot;
-                *reinterpret_cast<uint2*>(static_cast<T*>(a.k_pool) + row * D + 4 * lane) = kq;
-                *reinterpret_cast<uint2*>(static_cast<T*>(a.v_pool) + row * D + 4 * lane) =
-                    *reinterpret_cast<const uint2*>(static_cast<const T*>(a.v_new) +
-                                                    ((size_t)un.r * a.h_kv + un.g) * D + 4 * lane);
-                unsigned char* gs = static_cast<unsigned char*>(a.summary) + ((size_t)pp * a.h_kv + un.g) * SUMB;
-                if constexpr (F8) {
-                  const int bm = 4 * lane, bM = D + 4 * lane;   // code bytes of m, M
-                  uint32_t* sm_m = reinterpret_cast<uint32_t*>(sbw + sw_off<SUMB>(pin, bm));
-                  uint32_t* sm_M = reinterpret_cast<uint32_t*>(sbw + sw_off<SUMB>(pin, bM));
-                  uint32_t m01 = KO::to_key(kq.x), m23 = KO::to_key(kq.y);
-                  uint32_t M01 = m01, M23 = m23;
-                  if (slot != 0) {
-                    m01 = KO::kmin(KO::to_key(e4m3x4_lo_h2(*sm_m)), m01);
-                    m23 = KO::kmin(KO::to_key(e4m3x4_hi_h2(*sm_m)), m23);
-                    M01 = KO::kmax(KO::to_key(e4m3x4_lo_h2(*sm_M)), M01);
-                    M23 = KO::kmax(KO::to_key(e4m3x4_hi_h2(*sm_M)), M23);
-                  }
-                  bool ovf = false;
-                  const uint32_t cm = e4m3x4_floor_h(KO::from_key(m01), KO::from_key(m23), ovf);
-                  const uint32_t cM = e4m3x4_ceil_h(KO::from_key(M01), KO::from_key(M23), ovf);
-                  *sm_m = cm;
-                  *sm_M = cM;
-                  *reinterpret_cast<uint32_t*>(gs + bm) = cm;
-                  *reinterpret_cast<uint32_t*>(gs + bM) = cM;
-                  if (ovf) report(a.err, QUEST_DEVERR_FP8_RANGE);
-                } else {
-                  const int bm = 8 * lane, bM = 2 * D + 8 * lane;   // bytes of m, M dims
-                  uint2* sm_m = reinterpret_cast<uint2*>(sbw + sw_off<SUMB>(pin, bm));
-                  uint2* sm_M = reinterpret_cast<uint2*>(sbw + sw_off<SUMB>(pin, bM));
-                  uint2 mn = make_uint2(KO::to_key(kq.x), KO::to_key(kq.y)), mx = mn;
-                  if (slot != 0) {
-                    const uint2 om = *sm_m, oM = *sm_M;
-                    mn = make_uint2(KO::kmin(KO::to_key(om.x), mn.x), KO::kmin(KO::to_key(om.y), mn.y));
-                    mx = make_uint2(KO::kmax(KO::to_key(oM.x), mx.x), KO::kmax(KO::to_key(oM.y), mx.y));
-                  }
-                  const uint2 nm2 = make_uint2(KO::from_key(mn.x), KO::from_key(mn.y));
-                  const uint2 nM2 = make_uint2(KO::from_key(mx.x), KO::from_key(mx.y));
-                  *sm_m = nm2;
-                  *sm_M = nM2;
-                  *reinterpret_cast<uint2*>(gs + bm) = nm2;
-                  *reinterpret_cast<uint2*>(gs + bM) = nM2;
-                }
-              }
-              __syncwarp();
-            }
             // U for the chunk's pages, n-tile by n-tile: C[head][page] over
             // the 2D summary elements, then the max over the group's heads
             const int gid = lane >> 2, tq = lane & 3;
@@ -845,75 +871,6 @@ cstep_kernel(const StepArgs a) {
               for (int v = 0; v < VPL; ++v) {
                 vm[v] = *reinterpret_cast<const uint4*>(sb + p * SUMB + (v * LPP + sub) * 16);
                 vM[v] = *reinterpret_cast<const uint4*>(sb + p * SUMB + RB + (v * LPP + sub) * 16);
-              }
-              if (tail_mine && ro == ro_t && m == m_tail) {
-                // append (eq (8)): the new token's K/V into the pool, the summary
-                // of its page folded with the key (a fresh page starts from it)
-                const int slot = (un.L - 1) % S;
-                const int pp = __ldg(a.page_indices + un.lo + un.P - 1);
-                if (pp >= 0 && pp < a.n_phys) {
-                  const T* vp = static_cast<const T*>(a.v_new) + ((size_t)un.r * a.h_kv + un.g) * D;
-                  T* kd = static_cast<T*>(a.k_pool) + (((size_t)pp * a.h_kv + un.g) * S + slot) * D;
-                  T* vd = static_cast<T*>(a.v_pool) + (((size_t)pp * a.h_kv + un.g) * S + slot) * D;
-                  bool ovf = false;
-#pragma unroll
-                  for (int v = 0; v < VPL; ++v) {
-                    const int d0 = (v * LPP + sub) * VECS;
-#pragma unroll
-                    for (int h = 0; h < (F8 ? 2 : 1); ++h) {
-                      st_v4(kd + d0 + h * 8, kn[v * (F8 ? 2 : 1) + h]);
-                      st_v4(vd + d0 + h * 8, ld_nc_v4(vp + d0 + h * 8));
-                    }
-                    if constexpr (F8) {
-                      // the old codes decode exactly to fp16; fold the key in,
-                      // round out again (min down, max up)
-                      const uint32_t om[4] = {vm[v].x, vm[v].y, vm[v].z, vm[v].w};
-                      const uint32_t oM[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
-                      const uint32_t kw[8] = {kn[2 * v].x, kn[2 * v].y, kn[2 * v].z, kn[2 * v].w,
-                                              kn[2 * v + 1].x, kn[2 * v + 1].y, kn[2 * v + 1].z,
-                                              kn[2 * v + 1].w};
-                      uint32_t c8m[4], c8M[4];
-#pragma unroll
-                      for (int cw4 = 0; cw4 < 4; ++cw4) {
-                        uint32_t m01 = KO::to_key(kw[2 * cw4]), m23 = KO::to_key(kw[2 * cw4 + 1]);
-                        uint32_t M01 = m01, M23 = m23;
-                        if (slot != 0) {
-                          m01 = KO::kmin(KO::to_key(e4m3x4_lo_h2(om[cw4])), m01);
-                          m23 = KO::kmin(KO::to_key(e4m3x4_hi_h2(om[cw4])), m23);
-                          M01 = KO::kmax(KO::to_key(e4m3x4_lo_h2(oM[cw4])), M01);
-                          M23 = KO::kmax(KO::to_key(e4m3x4_hi_h2(oM[cw4])), M23);
-                        }
-                        c8m[cw4] = e4m3x4_floor_h(KO::from_key(m01), KO::from_key(m23), ovf);
-                        c8M[cw4] = e4m3x4_ceil_h(KO::from_key(M01), KO::from_key(M23), ovf);
-                      }
-                      vm[v] = make_uint4(c8m[0], c8m[1], c8m[2], c8m[3]);
-                      vM[v] = make_uint4(c8M[0], c8M[1], c8M[2], c8M[3]);
-                    } else {
-                      const uint4 k4 = kn[v];
-                      uint4 mn, mx;
-                      if (slot == 0) {
-                        mn = make_uint4(KO::to_key(k4.x), KO::to_key(k4.y), KO::to_key(k4.z), KO::to_key(k4.w));
-                        mx = mn;
-                      } else {
-                        mn = make_uint4(KO::kmin(KO::to_key(vm[v].x), KO::to_key(k4.x)),
-                                        KO::kmin(KO::to_key(vm[v].y), KO::to_key(k4.y)),
-                                        KO::kmin(KO::to_key(vm[v].z), KO::to_key(k4.z)),
-                                        KO::kmin(KO::to_key(vm[v].w), KO::to_key(k4.w)));
-                        mx = make_uint4(KO::kmax(KO::to_key(vM[v].x), KO::to_key(k4.x)),
-                                        KO::kmax(KO::to_key(vM[v].y), KO::to_key(k4.y)),
-                                        KO::kmax(KO::to_key(vM[v].z), KO::to_key(k4.z)),
-                                        KO::kmax(KO::to_key(vM[v].w), KO::to_key(k4.w)));
-                      }
-                      vm[v] = make_uint4(KO::from_key(mn.x), KO::from_key(mn.y), KO::from_key(mn.z), KO::from_key(mn.w));
-                      vM[v] = make_uint4(KO::from_key(mx.x), KO::from_key(mx.y), KO::from_key(mx.z), KO::from_key(mx.w));
-                    }
-                    unsigned char* sp = static_cast<unsigned char*>(a.summary) +
-                                        ((size_t)pp * a.h_kv + un.g) * SUMB + (v * LPP + sub) * 16;
-                    st_v4(sp, vm[v]);
-                    st_v4(sp + RB, vM[v]);
-                  }
-                  if (F8 && ovf) report(a.err, QUEST_DEVERR_FP8_RANGE);
-                }
               }
               // sum_j max(q_j m_j, q_j M_j) = sum_j q_j * (q_j >= 0 ? M_j : m_j)
 #pragma unroll

@@ -1,11 +1,14 @@
-"""Full-size workloads through the CUDA path, checked on sampled outputs.
+"""Full-size workloads through the CUDA path, checked against the oracle.
 
 Each test builds the workload's cache through the library (prefill with
 quest_append_kv), runs decode steps with quest_decode_step (the launch the
-bench times) and, where noted, the unfused four calls, then recomputes a few
+bench times) and, where noted, the unfused four calls, then recomputes
 (request, KV head) units with the oracle from the generated tokens: summaries
 bit-exact, scores within the score tolerance, selections under the near-tie
-rule, attention within 2e-3 of fp64.
+rule, attention within 2e-3 of fp64 (every head of the 32K layer and of three
+of the sixteen GQA requests; two heads of the 128K steps). Every unit's
+selection is also checked exactly against the oracle's Top-K over the GPU's
+own fp32 scores.
 """
 
 import math
@@ -91,6 +94,21 @@ class Unit:
         assert np.allclose(g_lse, rl[0], rtol=1e-4, atol=1e-4)
 
 
+def check_every_selection(scores, sel_logical, sel_count, table, seq_lens, K):
+    """Every (request, KV head) selection equals the oracle's Top-K taken over
+    the GPU's own fp32 scores (the same precision on both sides, so the sets
+    must agree exactly, ties to the lower page)."""
+    S = table.page_size
+    for r in range(len(seq_lens)):
+        lo = int(table.page_indptr[r])
+        P = -(-int(seq_lens[r]) // S)
+        for g in range(scores.shape[0]):
+            want = qo.topk_pages(scores[g, lo:lo + P].astype(np.float64), K)
+            got = [int(x) for x in sel_logical[r, g] if x >= 0]
+            assert int(sel_count[r, g]) == len(got) == min(K, P), (r, g)
+            assert np.array_equal(np.sort(got), want), (r, g)
+
+
 def _q_rows(q, r, heads, G):
     return torch.cat([q[r, h * G:(h + 1) * G] for h in heads]).cpu()
 
@@ -127,12 +145,14 @@ def test_llama_layer_32k_fused_and_unfused():
     twin = qs.PagedCache(cache.k_pool.clone(), cache.v_pool.clone(), cache.summary.clone())
     step = _run_decode(w, table, cache, [L], k_tok[L - 1:L].contiguous(),
                        v_tok[L - 1:L].contiguous(), q, w.k)
-    heads = [0, 13, 31]
+    heads = list(range(w.h_kv))              # every head: summaries, scores, sets, outputs
     unit = Unit(k_tok[:, heads].cpu(), v_tok[:, heads].cpu(), _q_rows(q, 0, heads, 1), heads, 1,
                 w.page_size)
     ref = unit.oracle(L, w.k)
     gsum, gsc, gsel, gcnt, gout, glse = _gather(step, cache, 0, heads, 1)
     unit.check(ref, L, w.k, gsum, gsc[heads], gsel, gcnt, gout, glse, table.page_indices)
+    check_every_selection(np_of(step.scores), np_of(step.sel[0]), np_of(step.sel[2]), table,
+                          [L], w.k)
     # the unfused four calls on the twin cache give the same answer
     gt = _table(table, [L])
     qs.append_kv(twin, gt, k_tok[L - 1:L].contiguous(), v_tok[L - 1:L].contiguous(),
@@ -163,8 +183,10 @@ def test_gqa_batch_16_requests_8k_to_128k():
     v1 = torch.stack([v[-1] for _, v in toks]).contiguous()
     q = wl.queries(w, lens - 1, device="cuda")
     step = _run_decode(w, table, cache, lens, k1, v1, q, w.k)
+    check_every_selection(np_of(step.scores), np_of(step.sel[0]), np_of(step.sel[2]), table,
+                          lens, w.k)
     order = np.argsort(lens)
-    heads = [0, 5]
+    heads = list(range(w.h_kv))              # every KV head of the sampled requests
     for r in (int(order[0]), int(order[len(order) // 2]), int(order[-1])):
         L = int(lens[r])
         k, v = toks[r]
@@ -209,6 +231,8 @@ def test_append_128k_prefill_then_64_decode_steps():
             ref = unit.oracle(L, w.k)
             gsum, gsc, gsel, gcnt, gout, glse = _gather(gt_steps, cache, 0, heads, 1)
             unit.check(ref, L, w.k, gsum, gsc[heads], gsel, gcnt, gout, glse, table.page_indices)
+            check_every_selection(np_of(gt_steps.scores), np_of(gt_steps.sel[0]),
+                                  np_of(gt_steps.sel[2]), table, [L], w.k)
     assert qs.device_error() == 0
 
 
