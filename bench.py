@@ -581,8 +581,7 @@ def main(argv=None):
                  f"({args.nbuf * (setup.caches[0].k_pool.nbytes * 2 + setup.caches[0].summary.nbytes) / 2**30:.1f} GiB)"
                  " so every step reads memory not touched in the previous "
                  f"{args.nbuf - 1} steps (> the 129 MB L2)")
-    cfg["launch"] = (f"CUDA graphs of {args.nbuf} back-to-back steps (one per cache copy); "
-                     "p50/p95: single-step graphs each between two events, >= 200 samples")
+    cfg["launch"] = f"CUDA graphs of {args.nbuf} back-to-back steps (one per cache copy)"
     nb = args.nbuf
 
     # warm-up (also sets per-device kernel attributes before capture)
@@ -637,19 +636,22 @@ def main(argv=None):
     assert qs.device_error() == 0
 
     # the step-time distribution (after the timed region, not part of
-    # `value`): each step alone between events, single-step graphs over the
-    # rotating copies, at least 200 samples whatever --steps is
-    n_dist = max(200, min(K, 4000))
+    # `value`): the timed graph of nb back-to-back steps replayed between
+    # two events, at least 200 times whatever --steps is; a sample is the
+    # graph's time over nb (events between single steps would cut the
+    # overlap of consecutive launches that the timed loop has)
+    n_dist = max(200, min(reps, 2000))
     dist_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n_dist)]
     torch.cuda.synchronize()
-    with torch.cuda.stream(s):
-        for i in range(n_dist):
-            dist_ev[i][0].record(s)
-            graphs[i % nb].replay()
-            dist_ev[i][1].record(s)
+    for i in range(n_dist):
+        dist_ev[i][0].record()
+        g_run.replay()
+        dist_ev[i][1].record()
     torch.cuda.synchronize()
-    steps_us = sorted(a.elapsed_time(b) * 1e3 for a, b in dist_ev)
+    steps_us = sorted(a.elapsed_time(b) * 1e3 / nb for a, b in dist_ev)
+    cfg["launch"] += f"; p50/p95 over {n_dist} replays of that graph (per step)"
+    assert qs.device_error() == 0
 
     # per-stage device time of the unfused four-call path (each stage alone,
     # rotating copies, events); informational
