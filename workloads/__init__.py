@@ -23,6 +23,8 @@ Workloads (Llama-2-7B-like MHA shapes of the Quest page's intro and §2):
                   heads, d=128, S=16, K=256, random physical page permutation.
 ``append_128k``   1 request, 32 heads, d=128, S=32, prefill 131072 tokens then
                   64 single-token decode steps, budget 4096 tokens (K=128).
+``gqa_small``     ``gqa_batch``'s shapes with 4 requests of U[16384, 32768]
+                  tokens (a small case for profiler captures).
 """
 
 from __future__ import annotations
@@ -85,6 +87,11 @@ WORKLOADS = {
     "append_128k": Workload("append_128k", batch=1, h_kv=32, group=1, head_dim=128,
                             page_size=32, k=128, dtype=torch.float16, seed=1005,
                             seq_lens=(131072,), decode_steps=64),
+    # gqa_batch's shapes at a quarter of its requests and lengths (about 0.4 GB of
+    # K/V, still above the 129 MB L2): the small case the profiler captures
+    "gqa_small": Workload("gqa_small", batch=4, h_kv=8, group=4, head_dim=128,
+                          page_size=16, k=256, dtype=torch.float16, seed=1006,
+                          len_range=(16384, 32768), permute_pages=True),
 }
 
 
