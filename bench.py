@@ -288,7 +288,7 @@ class LayerSetup:
         """The fused decode step: append + score + select + attention in one launch."""
         self.fused(self.caches[b], self.table, self.q, self.k_dec, self.v_dec)
 
-    KERNELS_PER_STEP = 1   # quest_decode_step is one cooperative kernel
+    KERNELS_PER_STEP = 1   # quest_decode_step is one kernel launch
 
     def bytes(self):  # noqa: A003
         """Algorithmic bytes of one step: the summaries of every valid page and
@@ -918,45 +918,70 @@ def time_diagnostics(setup, R, reps, peak_gbs):
 def run_e2e(setup, graphs, nb, n):
     """Same step through the public API with host buffers: each step copies
     q and the new token's k/v from pinned host memory, runs quest_decode_step
-    and reads o and lse back into pinned host memory. The three uploads, the
-    step and the two downloads of one step are captured as one CUDA graph (one
-    per cache copy), so a step is one graph launch and a synchronisation."""
-    h_q = setup.q.cpu().pin_memory()
-    h_k = setup.k_dec.cpu().pin_memory()
-    h_v = setup.v_dec.cpu().pin_memory()
-    h_o = torch.empty(setup.out.shape, dtype=setup.out.dtype).pin_memory()
-    h_l = torch.empty(setup.lse.shape, dtype=setup.lse.dtype).pin_memory()
+    and reads o and lse back into pinned host memory. q, k and v sit in one
+    device buffer (and o and lse in another), so a step moves its inputs in
+    one copy and its results in one; the upload, the step and the download are
+    captured as one CUDA graph (one per cache copy), so a step is one graph
+    launch and a synchronisation."""
+    dev = setup.q.device
+
+    def packed(ts):
+        """One byte buffer holding the tensors back to back (16-B aligned
+        parts) and views of it shaped like them."""
+        sizes = [(t.nbytes + 15) // 16 * 16 for t in ts]
+        buf = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
+        views, off = [], 0
+        for t, sz in zip(ts, sizes):
+            views.append(buf[off:off + t.nbytes].view(t.dtype).view(t.shape))
+            off += sz
+        return buf, views
+
+    d_in, (q, k1, v1) = packed([setup.q, setup.k_dec, setup.v_dec])
+    q.copy_(setup.q)
+    k1.copy_(setup.k_dec)
+    v1.copy_(setup.v_dec)
+    d_out, (o, lse) = packed([setup.fused.out, setup.fused.lse])
+    h_in = d_in.cpu().pin_memory()
+    h_out = torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory()
+    fused = setup.fused
+    saved = (fused.out, fused.lse)
+    fused.out, fused.lse = o, lse            # the call writes its results into d_out
     s = torch.cuda.Stream()
     e2e = []
-    with torch.cuda.stream(s):
-        for b in range(nb):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                setup.q.copy_(h_q, non_blocking=True)
-                setup.k_dec.copy_(h_k, non_blocking=True)
-                setup.v_dec.copy_(h_v, non_blocking=True)
-                setup.step(b)
-                h_o.copy_(setup.out, non_blocking=True)
-                h_l.copy_(setup.lse, non_blocking=True)
-            e2e.append(g)
-    torch.cuda.synchronize()
-    ts = []
-    with torch.cuda.stream(s):               # replays go to s, the stream waited on
-        for i in range(n + 10):
-            t0 = time.perf_counter()
-            e2e[i % nb].replay()
-            s.synchronize()
-            if i >= 10:
-                ts.append(time.perf_counter() - t0)
-    ts.sort()
-    assert torch.equal(h_o, setup.out.cpu()) and torch.equal(h_l, setup.lse.cpu())
-    bi = h_q.nbytes + h_k.nbytes + h_v.nbytes
-    bo = h_o.nbytes + h_l.nbytes
+    try:
+        with torch.cuda.stream(s):
+            for b in range(nb):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    d_in.copy_(h_in, non_blocking=True)
+                    fused(setup.caches[b], setup.table, q, k1, v1)
+                    h_out.copy_(d_out, non_blocking=True)
+                e2e.append(g)
+        torch.cuda.synchronize()
+        ts = []
+        with torch.cuda.stream(s):               # replays go to s, the stream waited on
+            for i in range(n + 10):
+                t0 = time.perf_counter()
+                e2e[i % nb].replay()
+                s.synchronize()
+                if i >= 10:
+                    ts.append(time.perf_counter() - t0)
+        ts.sort()
+        assert torch.equal(h_out, d_out.cpu())
+        hv = h_out[:o.nbytes].view(o.dtype).view(o.shape)
+        setup.step(0)                            # the library's own buffers, same inputs
+        torch.cuda.synchronize()
+        assert torch.equal(hv, saved[0].cpu())
+    finally:
+        fused.out, fused.lse = saved
+    bi = setup.q.nbytes + setup.k_dec.nbytes + setup.v_dec.nbytes
+    bo = o.nbytes + lse.nbytes
     return {"value": round(statistics.median(ts) * 1e6, 3), "unit": UNIT,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "p95": round(ts[int(len(ts) * 0.95)] * 1e6, 3),
-            "launch": "one CUDA graph per step: 3 uploads from pinned memory, the fused "
-                      "step, 2 downloads to pinned memory; host waits on each step"}
+            "launch": "one CUDA graph per step: one upload of q, k and v from pinned memory, "
+                      "the fused step, one download of o and lse to pinned memory; host waits "
+                      "on each step"}
 
 
 def oracle_timings(w, k_tok, v_tok, q, heads, seconds, n_sink=0, n_local=0, summary_fp8=False,

@@ -49,7 +49,7 @@ namespace {
 constexpr int kCL = 4;                       // CTAs per cluster
 constexpr int kCSW = 4;                      // select warps (the last ones)
 constexpr int kCSelT = kCSW * 32;
-constexpr int kCMaxCW = 12;                  // consumer warps at most
+constexpr int kCMaxCW = 11;                  // consumer warps at most
 constexpr int kCMaxU = 64;                   // units per cluster
 constexpr int kCRowCap = 8192;               // keys of a row held in shared memory
 constexpr int kCKCap = 512;                  // selected pages listed in shared memory
@@ -105,7 +105,7 @@ struct CShape {
   static_assert(!MMAS || (CHUNK % 8 == 0 && G <= 8), "MMA bound: whole n-tiles, at most 8 heads");
 
   static constexpr int al(int x, int a) { return (x + a - 1) / a * a; }
-  // consumer warps: twelve, or eight for groups of 4 or 8 (their per-warp
+  // consumer warps: eleven (measured best of 10-12), or eight for groups of 4 or 8 (their per-warp
   // states take the room); one stash buffer for groups of 8
   static constexpr int NCW = G >= 4 ? 8 : kCMaxCW;
   static constexpr int NSTASH = G >= 8 ? 1 : 2;
