@@ -237,9 +237,9 @@ QUEST_API quest_status quest_sparse_decode_attn(const quest_cache* cache,
  * process exits); the call allocates nothing. A problem whose partials, as
  * planned for the cache's element type on the current device, need more than
  * 4 MiB is rejected with QUEST_ERR_WORKSPACE before anything is launched.
- * quest_attn_workspace_size(...) covers both element types, so a problem it
- * sizes at 4 MiB or less is always accepted (an fp16 one somewhat above may
- * be too). The first call on a device
+ * quest_attn_workspace_size(...) is the larger of the two element types'
+ * plans, so a problem it sizes at 4 MiB or less is always accepted; above
+ * that, the cache's own element type decides. The first call on a device
  * looks up the buffer's device address (cudaGetSymbolAddress, with that device
  * current); make that first call before any stream capture. Every call shares
  * the one buffer and leaves its contents behind; no part of it needs to start
