@@ -10,11 +10,14 @@
 // an mbarrier): one (page, head) K block and V block are each S*d contiguous
 // elements of the pool. The CTA merges its warps and writes one partial
 // (o, max, sum) per query head; the combine kernel merges the chunks.
-// Decode attention is a matrix-vector product per query head (G <= 8 rows
-// share a KV head), too thin for a tensor-core tile, so it stays on FMA.
+// Decode attention is a matrix-vector product per query head; groups of 1
+// and 2 stay on FMA. Groups of 4 and 8 with fp16 K/V run QK^T and PV on the
+// warp MMA (attn_mma_kernel): each warp streams its pages with 16-byte
+// cp.async copies into XOR-swizzled 16-token tiles read by ldmatrix.
 // With a slot mask (the GQA page union) each page carries the heads that
 // chose it, and the other heads of the group give it no weight.
 #include "attn_dev.cuh"
+#include "attn_mma.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -160,6 +163,120 @@ attn_split_kernel(const AttnArgs a) {
       });
 }
 
+// Groups of 4 and 8, fp16, no head masks: the same split as attn_split_kernel
+// with QK^T and PV on the warp MMA. Each warp keeps two pages in flight in
+// its own slots (a page's K and V as one cp.async group).
+template <int D, int S>
+struct AttnMmaShape {
+  static constexpr int RB = D * 2;                          // bytes of a K or V row
+  static constexpr int BLK = S * RB;                        // a (page, head) K or V block
+  static constexpr int SLOT = 2 * BLK;                      // K then V
+  static constexpr int STAGE_BYTES = kNW * kNST * SLOT;
+  static constexpr int PS_OFF = STAGE_BYTES;                // [kNW][256 B] P tiles
+  static constexpr int DESC_OFF = PS_OFF + kNW * 256;
+  static constexpr int SMEM = DESC_OFF + kNW * kMaxWarpPages * 8;
+  static_assert(S % 16 == 0, "whole 16-token tiles");
+};
+
+template <int D, int S, int G>
+__global__ void __launch_bounds__(kNW * 32)
+attn_mma_kernel(const AttnArgs a) {
+  using Sh = AttnMmaShape<D, S>;
+  using W = WarpAttnMmaS<D, G>;
+  static_assert(kNW * G * (D + 2) * 4 <= Sh::STAGE_BYTES, "merge buffer must fit in the stage area");
+  extern __shared__ __align__(128) unsigned char smem[];
+  int2* desc_all = reinterpret_cast<int2*>(smem + Sh::DESC_OFF);
+
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = blockIdx.x % a.n_chunks;
+  const int unit = blockIdx.x / a.n_chunks;     // r * h_kv + g
+  const int g = unit % a.h_kv, r = unit / a.h_kv;
+  const int h_q = a.h_kv * G;
+  const int L = a.seq_lens[r];
+  const size_t sel_base = (size_t)unit * a.k;
+  int2* desc = desc_all + w * kMaxWarpPages;
+  unsigned char* stage = smem + (size_t)w * kNST * Sh::SLOT;
+  __half* ps = reinterpret_cast<__half*>(smem + Sh::PS_OFF + w * 256);
+
+  // this warp's pages: j = c*cp + w + NW*i, i < nmine (as attn_split_kernel)
+  const int jc0 = c * a.chunk_pages;
+  const int jc1 = min(a.k, jc0 + a.chunk_pages);
+  const int j0 = jc0 + w;
+  const int nmine = j0 < jc1 ? (jc1 - j0 + kNW - 1) / kNW : 0;
+  int my_pp = -1, my_valid = 0;
+  if (lane < nmine) {
+    const int j = j0 + lane * kNW;
+    const int lp = __ldg(a.sel_logical + sel_base + j);
+    const int pp = __ldg(a.sel_phys + sel_base + j);
+    if (lp >= 0) {
+      const int valid = min(S, L - lp * S);
+      if (valid <= 0) report(a.err, QUEST_DEVERR_EMPTY_PAGE);
+      else if (pp < 0 || pp >= a.n_phys) report(a.err, QUEST_DEVERR_PAGE_RANGE);
+      else { my_pp = pp; my_valid = valid; }
+    }
+  }
+  const unsigned vmask = __ballot_sync(FULL, my_valid > 0);
+  const int nv = __popc(vmask);
+  if (my_valid > 0) desc[__popc(vmask & ((1u << lane) - 1))] = make_int2(my_pp, my_valid);
+  __syncwarp();
+
+  auto issue = [&](int n) {                     // page n's K and V into slot n % kNST
+    const int pp = desc[n].x;
+    unsigned char* dst = stage + (n % kNST) * Sh::SLOT;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const unsigned char* src = static_cast<const unsigned char*>(half ? a.v_pool : a.k_pool) +
+                                 ((size_t)pp * a.h_kv + g) * Sh::BLK;
+#pragma unroll
+      for (int k = 0; k < Sh::BLK / 512; ++k) {
+        const int pc = k * 32 + lane;               // 16-byte piece of the block
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                     :: "r"(smem_u32(dst + half * Sh::BLK + W::sw(pc / (Sh::RB / 16), pc % (Sh::RB / 16)))),
+                        "l"(src + (size_t)pc * 16) : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+#pragma unroll
+  for (int n = 0; n < kNST - 1; ++n) {
+    if (n < nv) issue(n);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+
+  W st;
+  st.init(static_cast<const __half*>(a.q) + ((size_t)r * h_q + g * G) * D, a.scale_log2, lane);
+  static_assert(kNST == 2, "one page streams while the other is folded");
+  for (int n = 0; n < nv; ++n) {
+    if (n + 1 < nv) issue(n + 1);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncwarp();
+    const uint32_t kb = smem_u32(stage + (n % kNST) * Sh::SLOT), vb = kb + Sh::BLK;
+    const int valid = desc[n].y;
+    for (int t = 0; t * 16 < valid; ++t) {
+      st.qk(kb + t * 16 * Sh::RB, valid - t * 16, ps, lane);
+      st.av(vb + t * 16 * Sh::RB, valid - t * 16, ps, lane);
+    }
+    __syncwarp();                                   // slot n % kNST may be refilled
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+  // Merge the warps of this CTA (stage area reused once every warp is done).
+  __syncthreads();
+  float* mo = reinterpret_cast<float*>(smem);                 // [NW][G][D]
+  float* ml = mo + kNW * G * D;                               // [NW][G][2]
+  st.stash(mo, ml, w, lane);
+  __syncthreads();
+  const size_t row0 = ((size_t)r * h_q + g * G) * a.n_chunks + c;
+  merge_warps<D, G, kNW, kNW * 32>(
+      mo, ml,
+      [&](int gi, int col, float o) { a.part_o[(row0 + (size_t)gi * a.n_chunks) * D + col] = o; },
+      [&](int gi, float mx, float l) {
+        a.part_ml[(row0 + (size_t)gi * a.n_chunks) * 2 + 0] = mx;
+        a.part_ml[(row0 + (size_t)gi * a.n_chunks) * 2 + 1] = l;
+      });
+}
+
 // One warp per (request, query head): LSE merge of the chunk partials. The
 // chunk maxima are read lane-parallel; the weighted sum issues its loads
 // independently of each other.
@@ -208,6 +325,26 @@ attn_combine_kernel(const AttnArgs a) {
 
 template <typename T, int D, int S, int G, bool MASK>
 cudaError_t launch_split(const AttnArgs& a, cudaStream_t s) {
+  if constexpr (sizeof(T) == 2 && G >= 4 && !MASK) {
+    if (a.test_fault != 2) {                        // (the failure test takes the bulk-copy path)
+      using Sm = AttnMmaShape<D, S>;
+      auto kern = attn_mma_kernel<D, S, G>;
+      int dev = 0;
+      cudaGetDevice(&dev);
+      static std::atomic<bool> done[64];
+      if (dev < 0 || dev >= 64 || !done[dev].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
+      }
+      kern<<<(unsigned)a.batch * a.h_kv * a.n_chunks, kNW * 32, Sm::SMEM, s>>>(a);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      const unsigned rows = (unsigned)a.batch * a.h_kv * a.group;
+      attn_combine_kernel<D><<<(rows + 3) / 4, 128, 0, s>>>(a);
+      return cudaGetLastError();
+    }
+  }
   using Sh = AttnShape<T, D, S, G>;
   auto kern = attn_split_kernel<T, D, S, G, MASK>;
   int dev = 0;
