@@ -163,7 +163,7 @@ attn_split_kernel(const AttnArgs a) {
       });
 }
 
-// Groups of 4 and 8, fp16, no head masks: the same split as attn_split_kernel
+// Groups of 4 and 8, fp16: the same split as attn_split_kernel (head masks too)
 // with QK^T and PV on the warp MMA. Each warp keeps two pages in flight in
 // its own slots (a page's K and V as one cp.async group).
 template <int D, int S>
@@ -178,7 +178,7 @@ struct AttnMmaShape {
   static_assert(S % 16 == 0, "whole 16-token tiles");
 };
 
-template <int D, int S, int G>
+template <int D, int S, int G, bool MASK>
 __global__ void __launch_bounds__(kNW * 32)
 attn_mma_kernel(const AttnArgs a) {
   using Sh = AttnMmaShape<D, S>;
@@ -203,12 +203,13 @@ attn_mma_kernel(const AttnArgs a) {
   const int jc1 = min(a.k, jc0 + a.chunk_pages);
   const int j0 = jc0 + w;
   const int nmine = j0 < jc1 ? (jc1 - j0 + kNW - 1) / kNW : 0;
-  int my_pp = -1, my_valid = 0;
+  int my_pp = -1, my_valid = 0, my_heads = 0xff;
   if (lane < nmine) {
     const int j = j0 + lane * kNW;
     const int lp = __ldg(a.sel_logical + sel_base + j);
     const int pp = __ldg(a.sel_phys + sel_base + j);
-    if (lp >= 0) {
+    if constexpr (MASK) my_heads = a.sel_mask[sel_base + j];   // heads that chose the page
+    if (lp >= 0 && my_heads != 0) {
       const int valid = min(S, L - lp * S);
       if (valid <= 0) report(a.err, QUEST_DEVERR_EMPTY_PAGE);
       else if (pp < 0 || pp >= a.n_phys) report(a.err, QUEST_DEVERR_PAGE_RANGE);
@@ -217,7 +218,8 @@ attn_mma_kernel(const AttnArgs a) {
   }
   const unsigned vmask = __ballot_sync(FULL, my_valid > 0);
   const int nv = __popc(vmask);
-  if (my_valid > 0) desc[__popc(vmask & ((1u << lane) - 1))] = make_int2(my_pp, my_valid);
+  if (my_valid > 0)
+    desc[__popc(vmask & ((1u << lane) - 1))] = make_int2(my_pp, my_valid | (my_heads << 8));
   __syncwarp();
 
   auto issue = [&](int n) {                     // page n's K and V into slot n % kNST
@@ -252,9 +254,10 @@ attn_mma_kernel(const AttnArgs a) {
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncwarp();
     const uint32_t kb = smem_u32(stage + (n % kNST) * Sh::SLOT), vb = kb + Sh::BLK;
-    const int valid = desc[n].y;
+    const int valid = desc[n].y & 0xff;
+    const unsigned hm = (unsigned)desc[n].y >> 8;
     for (int t = 0; t * 16 < valid; ++t) {
-      st.qk(kb + t * 16 * Sh::RB, valid - t * 16, ps, lane);
+      st.qk(kb + t * 16 * Sh::RB, valid - t * 16, ps, lane, hm);
       st.av(vb + t * 16 * Sh::RB, valid - t * 16, ps, lane);
     }
     __syncwarp();                                   // slot n % kNST may be refilled
@@ -325,10 +328,10 @@ attn_combine_kernel(const AttnArgs a) {
 
 template <typename T, int D, int S, int G, bool MASK>
 cudaError_t launch_split(const AttnArgs& a, cudaStream_t s) {
-  if constexpr (sizeof(T) == 2 && G >= 4 && !MASK) {
+  if constexpr (sizeof(T) == 2 && G >= 4) {
     if (a.test_fault != 2) {                        // (the failure test takes the bulk-copy path)
       using Sm = AttnMmaShape<D, S>;
-      auto kern = attn_mma_kernel<D, S, G>;
+      auto kern = attn_mma_kernel<D, S, G, MASK>;
       int dev = 0;
       cudaGetDevice(&dev);
       static std::atomic<bool> done[64];

@@ -238,7 +238,8 @@ struct WarpAttnMmaS {
   // the K tile (shared-memory byte address kb, swizzled rows) into the running
   // max and sum and leaves P in ps (this warp's 256-byte scratch); av() then
   // accumulates the V tile (vb). The K tile is not read after qk() returns.
-  __device__ __forceinline__ void qk(uint32_t kb, int valid, __half* ps, int lane) {
+  // Heads whose bit of `hmask` is clear did not choose the page: weight 0.
+  __device__ __forceinline__ void qk(uint32_t kb, int valid, __half* ps, int lane, unsigned hmask = ~0u) {
     const int gid = lane >> 2, t = lane & 3;
     const int q4 = lane >> 3, r8 = lane & 7;  // ldmatrix: matrix q4, row r8 of this lane's address
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -254,10 +255,11 @@ struct WarpAttnMmaS {
     }
     // tokens gid (s: head 2t, 2t+1) and gid + 8
     const bool v0 = gid < valid, v1 = gid + 8 < valid;
-    const float x[4] = {v0 ? (s0[0] + s1[0]) * scale_log2 : -INFINITY,
-                        v0 ? (s0[1] + s1[1]) * scale_log2 : -INFINITY,
-                        v1 ? (s0[2] + s1[2]) * scale_log2 : -INFINITY,
-                        v1 ? (s0[3] + s1[3]) * scale_log2 : -INFINITY};
+    const bool ha = (hmask >> (2 * t)) & 1u, hb = (hmask >> (2 * t + 1)) & 1u;
+    const float x[4] = {v0 && ha ? (s0[0] + s1[0]) * scale_log2 : -INFINITY,
+                        v0 && hb ? (s0[1] + s1[1]) * scale_log2 : -INFINITY,
+                        v1 && ha ? (s0[2] + s1[2]) * scale_log2 : -INFINITY,
+                        v1 && hb ? (s0[3] + s1[3]) * scale_log2 : -INFINITY};
     float alpha[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
