@@ -328,10 +328,16 @@ def time_stage(fn, nbuf, reps):
 
 
 def source_hash(*names):
+    """Hash of the kernel sources as compiled: comments and blank space do
+    not count (an edit to a comment leaves recorded counters valid)."""
+    import re
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "query_aware_sparse_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "query_aware_sparse_gb300", "csrc", n)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -16,18 +16,24 @@
 //     into kCL contiguous ranges (one per CTA) and each range into NCW
 //     contiguous runs (one per consumer warp); a warp copies its run's
 //     summaries, CHUNK pages at a time, into its own buffer with cp.async (16
-//     bytes per lane, one page summary per warp copy, one chunk in flight
-//     while one is scored) and writes each score as an order-preserving key
-//     into the row buffer of every CTA of the cluster (distributed shared
-//     memory).
-//     In A(t) it streams its share of the CTA's selected pages with 1-D bulk
-//     copies, the next page's K block loading while the current V block is
-//     folded into the warp's online softmax; the state is stashed per unit.
+//     bytes per lane, one chunk in flight while one is scored), bounds them
+//     (sign-select and FMA for groups of 1 and 2; for groups of 4 and 8 a
+//     contraction on the warp MMA over XOR-swizzled chunks), folds the new
+//     token into its page's staged summary, and writes each score as an
+//     order-preserving key into the row buffer of every CTA of the cluster
+//     (distributed shared memory).
+//     In A(t) it streams its share of the CTA's selected pages, the next
+//     page's K block loading while the current V block is folded into the
+//     warp's online softmax: 1-D bulk copies and FMA for groups of 1 and 2,
+//     16-byte cp.async pieces into swizzled 16-token tiles and the warp MMA
+//     for groups of 4 and 8; the state is stashed per unit.
 //   * select warps wait until every CTA has delivered the unit's keys, run
 //     the block Top-K (every CTA computes the same set), look up the
 //     selected pages' physical ids, release the unit to the consumers, then
 //     merge the consumers' states into the CTA's partial and send it to the
 //     unit's owner CTA, which combines the kCL partials into the output row.
+//     (A cluster with a single unit of groups 1 or 2 has eight consumer
+//     warps run its Top-K instead: nothing else would run meanwhile.)
 // Hand-offs are mbarrier phases (bulk-copy completion, local and remote
 // arrivals); every wait is bounded and sets QUEST_DEVERR_WAIT_TIMEOUT rather
 // than hanging, after which the CTA stops issuing and drains its copies.
