@@ -1083,8 +1083,8 @@ def cpu_baseline(setup, heads, seconds):
             "sample": f"fp64 numpy oracle decode step (append, score, select, attention) of "
                       f"request 0 of the same layer, scaled to every request by pages: on "
                       f"{n} cores ({n} single-threaded processes over the {setup.w.h_kv} KV "
-                      f"heads, {len(tsn)} samples); cores_1: {heads} of the heads on one core, "
-                      f"scaled to all ({len(ts1)} steps)"}
+                      f"heads, {len(tsn)} samples); cores_1: {min(heads, setup.w.h_kv)} of the heads "
+                      f"on one core, scaled to all ({len(ts1)} steps)"}
 
 
 def run_reference(args, w, cfg, dev, ws):
