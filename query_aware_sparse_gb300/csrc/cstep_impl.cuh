@@ -272,7 +272,13 @@ __device__ __forceinline__ int sub_base(int lane) {
   else return 0;
 }
 
-template <typename T, int D, int S, int G, bool F8>
+// LR: rows longer than the register-resident Top-K takes (32 keys per select
+// thread) may occur. Tables of at most kCShortRows entries cannot hold one,
+// and their launches take the LR = false instance, which leaves the long-row
+// Top-K out of the kernel (measured: llama_layer 20.23 -> 19.94 us).
+constexpr int kCShortRows = 32 * kCSelT;
+
+template <typename T, int D, int S, int G, bool F8, bool LR>
 __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(CShape<T, D, S, G, F8>::NT, 1)
 cstep_kernel(const StepArgs a) {
   static_assert(!F8 || sizeof(T) == 2, "E4M3 summaries take fp16 keys");
@@ -543,13 +549,17 @@ cstep_kernel(const StepArgs a) {
       (void)gw;
       block_topk_smem<NTH, decltype(emit), decltype(forced), Grp>(P, K, keys, kmin, kmax, tsm, emit,
                                                                   forced, f_lo + (P - f_hi));
-    } else if (P <= kCRowCap) {
-      auto key_at = [keys, forced](int i) { return forced(i) ? 0xffffffffu : keys[i]; };
-      block_topk_keys<NTH, decltype(key_at), decltype(emit), Grp>(P, K, key_at, tsm, emit);
-    } else {                                      // keys of long rows from the scores in L2
-      const float* sc = a.scores + (size_t)un.g * a.nnz + un.lo;
-      auto key_at = [sc, forced](int i) { return forced(i) ? 0xffffffffu : score_key(__ldcg(sc + i)); };
-      block_topk_keys<NTH, decltype(key_at), decltype(emit), Grp>(P, K, key_at, tsm, emit);
+    } else if constexpr (LR) {
+      if (P <= kCRowCap) {
+        auto key_at = [keys, forced](int i) { return forced(i) ? 0xffffffffu : keys[i]; };
+        block_topk_keys<NTH, decltype(key_at), decltype(emit), Grp>(P, K, key_at, tsm, emit);
+      } else {                                    // keys of long rows from the scores in L2
+        const float* sc = a.scores + (size_t)un.g * a.nnz + un.lo;
+        auto key_at = [sc, forced](int i) { return forced(i) ? 0xffffffffu : score_key(__ldcg(sc + i)); };
+        block_topk_keys<NTH, decltype(key_at), decltype(emit), Grp>(P, K, key_at, tsm, emit);
+      }
+    } else if (gt == 0) {                         // (a table of at most kCShortRows entries)
+      report(a.err, QUEST_DEVERR_TABLE_RANGE);
     }
     Grp::sync();
     if (u == 0 && gt == 0) stamp(10);
@@ -1280,13 +1290,13 @@ int cstep_clusters(int dev) {
     if (c != 0) return c;
   }
   int n = 0;
-  if (cudaFuncSetAttribute(cstep_kernel<T, D, S, G, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(cstep_kernel<T, D, S, G, F8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Sh::SMEM) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kCL * 64);
     cfg.blockDim = dim3(Sh::NT);
     cfg.dynamicSmemBytes = Sh::SMEM;
-    if (cudaOccupancyMaxActiveClusters(&n, (void*)cstep_kernel<T, D, S, G, F8>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)cstep_kernel<T, D, S, G, F8, true>, &cfg) != cudaSuccess)
       n = 0;
   }
   cudaGetLastError();
@@ -1311,12 +1321,28 @@ cudaError_t cstep_launch(const StepArgs& a, const StepPlan& p, cudaStream_t s) {
   cfg.attrs = attr;
   static std::atomic<int> pdl_ok{getenv("QUEST_NO_PDL") ? 0 : -1};   // -1 untried, 0 off, 1 on
   cfg.numAttrs = pdl_ok.load() == 0 ? 0 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, cstep_kernel<T, D, S, G, F8>, a);
+  // fp16 tables of at most kCShortRows entries: the instance without the
+  // long-row Top-K (fp32 keeps one instance)
+  auto kern = cstep_kernel<T, D, S, G, F8, true>;
+  if constexpr (sizeof(T) == 2) {
+    if (a.nnz <= kCShortRows) {
+      kern = cstep_kernel<T, D, S, G, F8, false>;
+      int dev = 0;
+      cudaGetDevice(&dev);
+      static std::atomic<bool> attr_done[64];   // per device
+      if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
+        const cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
+        if (ea != cudaSuccess) return ea;
+        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
+      }
+    }
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess && cfg.numAttrs == 1 && pdl_ok.load() == -1) {
     cudaGetLastError();
     pdl_ok = 0;
     cfg.numAttrs = 0;
-    e = cudaLaunchKernelEx(&cfg, cstep_kernel<T, D, S, G, F8>, a);
+    e = cudaLaunchKernelEx(&cfg, kern, a);
   } else if (e == cudaSuccess && cfg.numAttrs == 1) {
     pdl_ok = 1;
   }
