@@ -547,8 +547,9 @@ cstep_kernel(const StepArgs a) {
       // min and max of the competing keys, folded in by the consumers
       const uint32_t kmin = kmm[2 * b], kmax = kmm[2 * b + 1];
       (void)gw;
-      block_topk_smem<NTH, decltype(emit), decltype(forced), Grp>(P, K, keys, kmin, kmax, tsm, emit,
-                                                                  forced, f_lo + (P - f_hi));
+      block_topk_smem<NTH, decltype(emit), decltype(forced), Grp, NoEarly,
+                      LR ? 32 * NTH : (kCShortRows < 32 * NTH ? kCShortRows : 32 * NTH)>(
+          P, K, keys, kmin, kmax, tsm, emit, forced, f_lo + (P - f_hi));
     } else if constexpr (LR) {
       if (P <= kCRowCap) {
         auto key_at = [keys, forced](int i) { return forced(i) ? 0xffffffffu : keys[i]; };

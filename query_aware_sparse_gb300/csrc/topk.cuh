@@ -443,7 +443,10 @@ __device__ void topk_regs(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t 
 
 // Top-K of P <= 32 * NT keys in shared memory (see topk_regs): picks the
 // register footprint for the row length.
-template <int NT, typename Emit, typename Forced, class Grp = CtaGrp, typename Early = NoEarly>
+// MAXP bounds P where the caller knows a smaller bound: the register forms
+// no row can need are left out.
+template <int NT, typename Emit, typename Forced, class Grp = CtaGrp, typename Early = NoEarly,
+          int MAXP = 32 * NT>
 __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uint32_t kmax,
                                 TopkSmem<NT>& sm, Emit emit, Forced forced, int nforced,
                                 Early early = Early()) {
@@ -453,9 +456,9 @@ __device__ void block_topk_smem(int P, int K, uint32_t* keys, uint32_t kmin, uin
   }
   if (P <= 8 * NT)
     topk_regs<NT, 8, Emit, Forced, Grp, Early>(P, K, keys, kmin, kmax, sm, emit, forced, nforced, early);
-  else if (P <= 16 * NT)
+  else if (MAXP <= 16 * NT || P <= 16 * NT)
     topk_regs<NT, 16, Emit, Forced, Grp, Early>(P, K, keys, kmin, kmax, sm, emit, forced, nforced, early);
-  else
+  else if constexpr (MAXP > 16 * NT)
     topk_regs<NT, 32, Emit, Forced, Grp, Early>(P, K, keys, kmin, kmax, sm, emit, forced, nforced, early);
 }
 
