@@ -605,7 +605,7 @@ cstep_kernel(const StepArgs a) {
         const int cc0 = c_lo(un, (int)rank), ncc = c_lo(un, (int)rank + 1) - cc0;
         const int mc0 = cc0 + ncc * cw / NCW;
         const int nm = cc0 + ncc * (cw + 1) / NCW - mc0;
-        const bool cached = un.P <= kCRowCap;
+        const bool cached = !LR || un.P <= kCRowCap;   // (short tables: always)
         const int f_lo = min(a.n_sink, un.P), f_hi = max(f_lo, un.P - a.n_local);
         uint32_t kmn = 0xffffffffu, kmx = 0u;        // over my competing pages' keys
         // the physical pages of my run, 64 table entries per window (two per
