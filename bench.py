@@ -805,6 +805,11 @@ def run_model_step(args, w, cfg, dev, ws, rank, local):
         if B == 2048:
             whole_2048 = (whole, by_whole, reps)
         del g, gd, gs_, steps
+    # the kernels the library plans for the sparse layers (the value's budget)
+    # and for the dense ones (K = P)
+    Kv = wl.selection_budget(2048 if whole_2048 else w.budgets[0], S)
+    kname_sparse = qs.decode_step_kernel(1, h, w.group, d, S, w.dtype, Kv)
+    kname_dense = qs.decode_step_kernel(1, h, w.group, d, S, w.dtype, P)
     whole, by_whole, reps = whole_2048 if whole_2048 else (
         sweep[str(w.budgets[0])]["whole_step_us"], sweep[str(w.budgets[0])]["bytes_per_step"], 1)
     per_layer = max_over_ranks(whole / w.layers, dev)
@@ -815,7 +820,7 @@ def run_model_step(args, w, cfg, dev, ws, rank, local):
             "ms_per_step": round(per_layer / 1e3, 6), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": data_desc(w),
             "config": cfg, "whole_step": sweep,
-            "roofline": {"bound": "hbm", "kernel": "step_kernel",
+            "roofline": {"bound": "hbm", "kernel": kname_sparse, "dense_kernel": kname_dense,
                          "achieved": round(by_whole / (whole * 1e-6) / 1e9, 1), "peak": pk,
                          "unit": "GB/s", "frac": round(by_whole / (whole * 1e-6) / 1e9 / pk, 4),
                          "peak_source": pk_src, "bytes_per_launch": by_whole // w.layers,
