@@ -133,6 +133,18 @@ template <> __device__ __forceinline__ void unpack16<__half>(uint4 v, float* out
   }
 }
 
+// s + a.lo * b.lo + a.hi * b.hi for two packed fp16 pairs, accumulated in
+// fp32 in that order: each product of two fp16 values is exact in fp32, so
+// the mixed-precision FMA (fp16 sources, fp32 addend) rounds exactly as an
+// fp32 FMA of the converted values would, without the conversions.
+__device__ __forceinline__ float fma2_h_f32(uint32_t a2, uint32_t b2, float s) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+      : "+f"(s) : "r"(a2), "r"(b2));
+  return s;
+}
+
 // Page upper-bound contribution of one 16-byte vector of dims (Quest page
 // §1.1 eq (2)): sum_j max(q_j m_j, q_j M_j). Since m_j <= M_j, the larger
 // product is q_j M_j when q_j >= 0 and q_j m_j otherwise, so each dim costs a

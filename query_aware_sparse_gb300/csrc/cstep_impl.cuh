@@ -665,8 +665,13 @@ cstep_kernel(const StepArgs a) {
         // against M), head gid's elements 16 kk + 4t .. + 3 of the k order
         // that the staged summaries are read in.
         constexpr int QW = Sh::MMAS ? 1 : VPL * (F8 ? 8 : 4);
-        constexpr int QV = Sh::MMAS ? 1 : (F8 ? VPL * 16 : (Sh::ES == 2 ? QW * 2 : QW));
+        // E4M3 summaries: the queries stay packed fp16 pairs for the
+        // mixed-precision FMA (measured faster there; with fp16 summaries the
+        // converted fp32 queries measured faster)
+        constexpr bool QH = F8 && !Sh::MMAS;
+        constexpr int QV = (Sh::MMAS || QH) ? 1 : (Sh::ES == 2 ? QW * 2 : QW);
         uint32_t qmask[G][QW];
+        uint32_t qh[G][QH ? QW : 1];
         float qf[G][QV];
         constexpr int KQ = Sh::MMAS ? Sh::KT : 1;
         uint32_t qa[KQ], qb[KQ];
@@ -704,7 +709,10 @@ cstep_kernel(const StepArgs a) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   const int wi = (v * (F8 ? 2 : 1) + h) * 4 + j;
-                  if constexpr (Sh::ES == 2) {
+                  if constexpr (QH) {
+                    qmask[gi][wi] = ((~w4[j] & 0x80008000u) >> 15) * 0xffffu;
+                    qh[gi][wi] = w4[j];
+                  } else if constexpr (Sh::ES == 2) {
                     qmask[gi][wi] = ((~w4[j] & 0x80008000u) >> 15) * 0xffffu;
                     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
                     qf[gi][wi * 2] = f.x;
@@ -899,15 +907,15 @@ cstep_kernel(const StepArgs a) {
                   const uint32_t Mw[4] = {vM[v].x, vM[v].y, vM[v].z, vM[v].w};
 #pragma unroll
                   for (int j = 0; j < 4; ++j) {
-                    if constexpr (F8) {              // codes decoded to fp16 (exact), fp32 FMA
+                    if constexpr (F8) {              // codes decoded to fp16 pairs (exact)
                       const int wi = v * 8 + 2 * j;
                       const uint32_t sel = e4m3_qsel_from_masks(qmask[gi][wi], qmask[gi][wi + 1]);
                       const uint32_t xw = (Mw[j] & sel) | (mw[j] & ~sel);
-                      const float2 lo = e4m3x4_lo_f2(xw), hi = e4m3x4_hi_f2(xw);
-                      sg = fmaf(qf[gi][wi * 2 + 0], lo.x, sg);
-                      sg = fmaf(qf[gi][wi * 2 + 1], lo.y, sg);
-                      sg = fmaf(qf[gi][wi * 2 + 2], hi.x, sg);
-                      sg = fmaf(qf[gi][wi * 2 + 3], hi.y, sg);
+                      uint32_t lo, hi;
+                      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((uint16_t)xw));
+                      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((uint16_t)(xw >> 16)));
+                      sg = fma2_h_f32(qh[gi][wi], lo, sg);
+                      sg = fma2_h_f32(qh[gi][wi + 1], hi, sg);
                     } else if constexpr (Sh::ES == 2) {
                       const uint32_t mk = qmask[gi][v * 4 + j];
                       const uint32_t xw = (Mw[j] & mk) | (mw[j] & ~mk);
