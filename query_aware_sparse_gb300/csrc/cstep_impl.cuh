@@ -493,6 +493,12 @@ cstep_kernel(const StepArgs a) {
     }
     *reinterpret_cast<int4*>(early + 32 * QB + lane * 16) = make_int4(pw[0], pw[1], pw[2], pw[3]);
   }
+  {   // the Top-K's histogram starts at zero (each Top-K leaves it so):
+      // zeroed before the barrier, which orders it before any select,
+      // including a lone unit's select by the consumer warps
+    TopkSmem<NT>& tsm = *reinterpret_cast<TopkSmem<NT>*>(smem + Sh::TOPK_OFF);
+    for (int i = tid; i < kTopkBins; i += NT) tsm.hist[i] = 0;
+  }
   asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory");
   const int n = *s_n;
 
@@ -1169,11 +1175,6 @@ cstep_kernel(const StepArgs a) {
   } else {
     // ============================ select group ============================
     const int gt = tid - Sh::SEL0;
-    {
-      TopkSmem<NT>& tsm = *reinterpret_cast<TopkSmem<NT>*>(smem + Sh::TOPK_OFF);
-      for (int i = gt; i < kTopkBins; i += kCSelT) tsm.hist[i] = 0;   // kept zero by the Top-K
-    }
-    SelGrp::sync();
     bool dead = false;
     // one thread waits, the group follows its verdict
     auto gwait = [&](const uint64_t* bar, uint32_t parity) {
