@@ -108,6 +108,9 @@ struct CShape {
   static constexpr int LGN = WNV > CHUNK * G ? WNV : CHUNK * G;
   static_assert(CHUNK % PPR == 0 && LPP * VPL * 16 == RB && NCPY >= 1, "scoring layout");
   static_assert(CHUNK * SUMB % 512 == 0 && NQ >= 2 && 32 % CHUNK == 0, "chunks");
+  // a warp copy of a chunk: 128-byte slices of four pages (8 lanes each)
+  static constexpr int NPL = CHUNK / 4;              // pages per lane
+  static_assert(CHUNK % 4 == 0 && SUMB % 128 == 0 && NCPY % NPL == 0, "chunk copies");
   static_assert(!MMAS || (CHUNK % 8 == 0 && G <= 8), "MMA bound: whole n-tiles, at most 8 heads");
 
   static constexpr int al(int x, int a) { return (x + a - 1) / a * a; }
@@ -467,15 +470,31 @@ cstep_kernel(const StepArgs a) {
       if (m < nm0) {
         const int o = m * CHUNK;
         const int srcw = ((o >> 5) & 1) ? pw[1] : pw[0];
-        const int ph = __shfl_sync(FULL, srcw, (o & 31) + (lane & (CHUNK - 1)));
+        if constexpr (Sh::MMAS) {                  // copy k: bytes [512k, 512k + 512)
+          const int ph = __shfl_sync(FULL, srcw, (o & 31) + (lane & (CHUNK - 1)));
 #pragma unroll
-        for (int k = 0; k < NCPY; ++k) {
-          const int byte = k * 512 + lane * 16;
-          const int phj = __shfl_sync(FULL, ph, byte / SUMB);
-          const int dsto = Sh::MMAS ? sw_off<SUMB>(byte / SUMB, byte % SUMB) : byte;
-          if (phj >= 0 && phj < a.n_phys)
-            cp_async16(buf0 + m * CHB + dsto, static_cast<const unsigned char*>(a.summary) +
-                                                   ((size_t)phj * a.h_kv + cid) * SUMB + byte % SUMB);
+          for (int k = 0; k < NCPY; ++k) {
+            const int byte = k * 512 + lane * 16;
+            const int phj = __shfl_sync(FULL, ph, byte / SUMB);
+            if (phj >= 0 && phj < a.n_phys)
+              cp_async16(buf0 + m * CHB + sw_off<SUMB>(byte / SUMB, byte % SUMB),
+                         static_cast<const unsigned char*>(a.summary) +
+                             ((size_t)phj * a.h_kv + cid) * SUMB + byte % SUMB);
+          }
+        } else {                                   // copy k: slices of four pages
+          // page j of the chunk: table entry o + j, in lane (o & 31) + j of the window
+          constexpr int NPL = Sh::NPL;
+          int phs[NPL];
+#pragma unroll
+          for (int i = 0; i < NPL; ++i) phs[i] = __shfl_sync(FULL, srcw, (o & 31) + (lane >> 3) + 4 * i);
+#pragma unroll
+          for (int k = 0; k < NCPY; ++k) {
+            const int i = k % NPL, j = (lane >> 3) + 4 * i;        // page j of the chunk
+            const int byte = (k / NPL) * 128 + (lane & 7) * 16;   // its 16-byte piece
+            if (phs[i] >= 0 && phs[i] < a.n_phys)
+              cp_async16(buf0 + m * CHB + j * SUMB + byte, static_cast<const unsigned char*>(a.summary) +
+                                                                ((size_t)phs[i] * a.h_kv + cid) * SUMB + byte);
+          }
         }
       }
       cp_async_commit_grp();
@@ -641,19 +660,36 @@ cstep_kernel(const StepArgs a) {
           const int v = __shfl_sync(FULL, src, (o & 31) + (lane & (CHUNK - 1)));
           return lane < CHUNK ? v : -1;
         };
-        // 16 bytes per lane per copy: copy k holds bytes [512k, 512k + 512) of the chunk
+        // 16 bytes per lane per copy. MMA bound: copy k holds bytes [512k,
+        // 512k + 512) of the chunk, swizzled. FMA bound: copy k holds a
+        // 128-byte slice of four pages (lanes 8q .. 8q + 7: page q + 4 (k %
+        // NPL)), so a lane fetches the physical ids of its NPL pages only.
         auto issue = [&](int m, int ph) {
           if (m < nm) {
             unsigned char* dst = buf + (m % NQ) * CHB;
+            if constexpr (Sh::MMAS) {
 #pragma unroll
-            for (int k = 0; k < NCPY; ++k) {
-              const int byte = k * 512 + lane * 16;
-              const int j = byte / SUMB;
-              const int phj = __shfl_sync(FULL, ph, j);
-              const int dsto = Sh::MMAS ? sw_off<SUMB>(j, byte % SUMB) : byte;
-              if (phj >= 0 && phj < a.n_phys)
-                cp_async16(dst + dsto, static_cast<const unsigned char*>(a.summary) +
-                                           ((size_t)phj * a.h_kv + un.g) * SUMB + byte % SUMB);
+              for (int k = 0; k < NCPY; ++k) {
+                const int byte = k * 512 + lane * 16;
+                const int j = byte / SUMB;
+                const int phj = __shfl_sync(FULL, ph, j);
+                if (phj >= 0 && phj < a.n_phys)
+                  cp_async16(dst + sw_off<SUMB>(j, byte % SUMB), static_cast<const unsigned char*>(a.summary) +
+                                                                    ((size_t)phj * a.h_kv + un.g) * SUMB + byte % SUMB);
+              }
+            } else {
+              constexpr int NPL = Sh::NPL;
+              int phs[NPL];
+#pragma unroll
+              for (int i = 0; i < NPL; ++i) phs[i] = __shfl_sync(FULL, ph, (lane >> 3) + 4 * i);
+#pragma unroll
+              for (int k = 0; k < NCPY; ++k) {
+                const int i = k % NPL, j = (lane >> 3) + 4 * i;    // page j of the chunk
+                const int byte = (k / NPL) * 128 + (lane & 7) * 16;   // its 16-byte piece
+                if (phs[i] >= 0 && phs[i] < a.n_phys)
+                  cp_async16(dst + j * SUMB + byte, static_cast<const unsigned char*>(a.summary) +
+                                                        ((size_t)phs[i] * a.h_kv + un.g) * SUMB + byte);
+              }
             }
           }
           cp_async_commit_grp();
