@@ -16,7 +16,8 @@
 //     into kCL contiguous ranges (one per CTA) and each range into NCW
 //     contiguous runs (one per consumer warp); a warp copies its run's
 //     summaries, CHUNK pages at a time, into its own buffer with cp.async (16
-//     bytes per lane, one chunk in flight while one is scored), bounds them
+//     bytes per lane, one chunk in flight while one is scored; for the FMA
+//     bound each warp copy takes 128-byte slices of four pages), bounds them
 //     (sign-select and FMA for groups of 1 and 2; for groups of 4 and 8 a
 //     contraction on the warp MMA over XOR-swizzled chunks), folds the new
 //     token into its page's staged summary, and writes each score as an
