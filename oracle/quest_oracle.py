@@ -27,8 +27,10 @@ in the docstring of the function that takes it):
     page_indices    [nnz]         physical page of logical page i of a request
     seq_lens        [batch]       valid tokens of each request
     q               [batch, h_kv * group, head_dim]
-* parity unpinned: ``score_pages`` with group > 1 (the group-max rule is a
-  reading of Quest page §2.1; only its group == 1 reduction is pinned).
+* ``score_pages`` with group > 1 takes the group max that Quest page §2.1
+  prints, U_{g,p} = max_{h in g} U_{h,p} (one of the two aggregations the page
+  weighs; the union is the other). Pinned by brute force on pages where each
+  head's bound is attained by one of the page's keys.
 """
 
 from __future__ import annotations
@@ -170,8 +172,8 @@ def score_pages(q, summary, page_indptr, page_indices, group, requests=None,
 
     For KV head g the score of a page is U of that page under each query head
     h in g*group .. g*group+group-1; with group > 1 the group shares one page
-    set and its score is max_h U_{h,p} (Quest page §2.1, the "group max" of
-    the GQA discussion: a reading, see module docstring). Pages outside the
+    set and its score is max_h U_{h,p} (Quest page §2.1, the group max the
+    GQA discussion prints). Pages outside the
     listed requests / heads are left NaN.
     """
     n_phys, h_kv, _, d = summary.shape

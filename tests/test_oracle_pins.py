@@ -252,6 +252,47 @@ def test_score_pages_group_reduction():
     assert abs(sc[g, i] - want) < 1e-12
 
 
+def test_group_max_is_attained_by_brute_force():
+    """Quest page §2.1 prints the shared score of a GQA group as
+    U_{g,p} = max_{h in g} U_{h,p}. On pages built so that every head's bound
+    is attained by a key of the page (its corner of the page's min/max box,
+    eq (2)-(3)), the group score must equal the brute-force maximum over the
+    group's heads and the page's valid keys of q_h . k in fp64: a
+    characterisation that uses neither the bound's formula nor the group rule,
+    and that a mean, a sum or a wrong head-to-group index breaks."""
+    rng = np.random.default_rng(21)
+    h_kv, G, d, S, P = 2, 4, 8, 16, 5
+    L = P * S - 3                                       # a ragged tail page
+    q = rng.standard_normal((1, h_kv * G, d)).astype(np.float32)
+    perm = rng.permutation(P + 2)[:P].astype(np.int32)
+    kp = np.full((P + 2, h_kv, S, d), np.nan, np.float32)
+    for lp in range(P):
+        n = min(S, L - lp * S)
+        for g in range(h_kv):
+            lo = rng.standard_normal(d).astype(np.float32)
+            hi = (lo + rng.uniform(0.1, 2.0, d)).astype(np.float32)
+            keys = [lo, hi] + [np.where(q[0, h] >= 0, hi, lo) for h in range(g * G, (g + 1) * G)]
+            while len(keys) < n:                        # interior keys: the box is unchanged
+                keys.append((lo + (hi - lo) * rng.uniform(0.05, 0.95, d)).astype(np.float32))
+            kp[perm[lp], g, :n] = np.array(keys[:n])[rng.permutation(n)]
+    indptr = np.array([0, P], np.int32)
+    sm = qo.build_summary(kp, indptr, perm, np.array([L], np.int32))
+    U = qo.score_pages(q, sm, indptr, perm, G)
+    wrong_idx = wrong_mean = 0
+    for lp in range(P):
+        n = min(S, L - lp * S)
+        for g in range(h_kv):
+            keys = kp[perm[lp], g, :n].astype(np.float64)
+            dots = keys @ q[0].astype(np.float64).T                 # [n, h_q]
+            want = dots[:, g * G:(g + 1) * G].max()
+            tol = 1e-12 * (np.abs(keys).max() * np.abs(q[0]).astype(np.float64).sum(axis=1).max())
+            assert abs(U[g, lp] - want) <= tol
+            # the rules a plausible mistake would compute differ here
+            wrong_idx += abs(dots[:, g::h_kv].max() - want) > tol
+            wrong_mean += abs(dots[:, g * G:(g + 1) * G].max(axis=0).mean() - want) > tol
+    assert wrong_idx > 0 and wrong_mean > 0
+
+
 # --------------------------------------------------------------------------
 # Selection: brute-force rank characterisation, ties, K >= P
 # --------------------------------------------------------------------------
